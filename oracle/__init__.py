@@ -1,0 +1,161 @@
+"""CPU oracle for the STOF masked-attention hot path (test infrastructure).
+
+Only the tests, the package's smoke check and the benchmark's CPU-baseline
+leg may import this package.  The library under test never does, and the two
+share no code.  The arithmetic lives in ``stof_oracle.c`` (plain C, fp64,
+direct loops); this module compiles it with gcc on first use and marshals
+numpy arrays in and out.
+
+What each function follows ("Accelerating Sparse Transformer Inference on
+GPU", gist.science technical summary):
+  - ``attention``: masked softmax attention by its definition, fp64, exact
+    masking (Methodology 1, two-level storage format: "exact masking without
+    materialising the sparse matrix"; Problem statement: skipping instead of
+    resetting scores).  A fully masked query row gives 0.
+  - ``encode`` / ``decode``: the two-level format by brute force
+    (Methodology 1: OT classes empty / full / partial, pointer arrays for
+    full and partial OTs, one uint64 per 8x8 IT of a partial OT).
+
+Pins (tests/test_oracle_pins.py) tie every function to something other than
+itself: library dense attention, closed forms, tiny brute force, round trips
+and hand-derived fixtures under tests/golden/.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "stof_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libstof_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile stof_oracle.c into libstof_oracle.so (plain gcc, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+            lib.stof_oracle_attention.argtypes = [i64, i64, i32, dbl, P, P, P, P, P, i32]
+            lib.stof_oracle_attention.restype = i32
+            lib.stof_oracle_encode_count.argtypes = [P, i32, i32, i32, i32, i32, P]
+            lib.stof_oracle_encode_count.restype = i32
+            lib.stof_oracle_encode.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P]
+            lib.stof_oracle_encode.restype = i32
+            lib.stof_oracle_decode.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P]
+            lib.stof_oracle_decode.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def attention(q, k, v, mask, scale: float, n_threads: int | None = None) -> np.ndarray:
+    """One head: q [n_q, d], k/v [lk, d] (float64), mask [n_q, lk] (0/1 bytes)."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    mask = np.ascontiguousarray(mask, dtype=np.uint8)
+    n_q, d = q.shape
+    lk = k.shape[0]
+    assert k.shape == (lk, d) and v.shape == (lk, d) and mask.shape == (n_q, lk)
+    o = np.empty((n_q, d), dtype=np.float64)
+    rc = lib.stof_oracle_attention(n_q, lk, d, float(scale), _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(mask), _ptr(o), n_threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle attention: bad arguments")
+    return o
+
+
+def encode_count(mask, bm: int, bn: int):
+    """(n_full, n_part, nnz) of mask [n_masks, lq, lk]."""
+    lib = _load()
+    mask = np.ascontiguousarray(mask, dtype=np.uint8)
+    n_masks, lq, lk = mask.shape
+    counts = np.zeros(3, dtype=np.int64)
+    if lib.stof_oracle_encode_count(_ptr(mask), n_masks, lq, lk, bm, bn, _ptr(counts)) != 0:
+        raise ValueError("oracle encode: bad shape")
+    return int(counts[0]), int(counts[1]), int(counts[2])
+
+
+def encode(mask, bm: int, bn: int) -> dict:
+    """Brute-force two-level encoding of mask [n_masks, lq, lk]."""
+    lib = _load()
+    mask = np.ascontiguousarray(mask, dtype=np.uint8)
+    n_masks, lq, lk = mask.shape
+    n_full, n_part, nnz = encode_count(mask, bm, bn)
+    n_rows = n_masks * (lq // bm)
+    fmt = dict(
+        n_masks=n_masks, lq=lq, lk=lk, bm=bm, bn=bn, n_tr=lq // bm, n_tc=lk // bn,
+        full_row_ptr=np.zeros(n_rows + 1, dtype=np.int32),
+        full_col_idx=np.zeros(max(n_full, 1), dtype=np.int32),
+        part_row_ptr=np.zeros(n_rows + 1, dtype=np.int32),
+        part_col_idx=np.zeros(max(n_part, 1), dtype=np.int32),
+        bitmaps=np.zeros((max(n_part, 1), bm // 8, bn // 8), dtype=np.uint64),
+        n_full=n_full, n_part=n_part, nnz=nnz)
+    rc = lib.stof_oracle_encode(_ptr(mask), n_masks, lq, lk, bm, bn,
+                                _ptr(fmt["full_row_ptr"]), _ptr(fmt["full_col_idx"]),
+                                _ptr(fmt["part_row_ptr"]), _ptr(fmt["part_col_idx"]),
+                                _ptr(fmt["bitmaps"]))
+    if rc != 0:
+        raise ValueError("oracle encode: bad shape")
+    fmt["full_col_idx"] = fmt["full_col_idx"][:n_full]
+    fmt["part_col_idx"] = fmt["part_col_idx"][:n_part]
+    fmt["bitmaps"] = fmt["bitmaps"][:n_part]
+    return fmt
+
+
+def decode(fmt: dict) -> np.ndarray:
+    """Dense 0/1 mask [n_masks, lq, lk] rebuilt from a format dict."""
+    lib = _load()
+    n_masks, lq, lk, bm, bn = (fmt[x] for x in ("n_masks", "lq", "lk", "bm", "bn"))
+    out = np.empty((n_masks, lq, lk), dtype=np.uint8)
+    arrs = [np.ascontiguousarray(fmt[x], dtype=t) for x, t in (
+        ("full_row_ptr", np.int32), ("full_col_idx", np.int32), ("part_row_ptr", np.int32),
+        ("part_col_idx", np.int32), ("bitmaps", np.uint64))]
+    arrs = [a if a.size else np.zeros(1, a.dtype) for a in arrs]
+    rc = lib.stof_oracle_decode(n_masks, lq, lk, bm, bn, *[_ptr(a) for a in arrs], _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle decode: bad shape")
+    return out
+
+
+def attention_bhld(q, k, v, mask_of, scale: float, heads=None, rows=None,
+                   n_threads: int | None = None) -> dict:
+    """Multi-head helper.  q, k, v: float64 [B, H, L, d]; mask_of(b, h, rows)
+    returns the uint8 mask rows [len(rows), L] of head (b, h).  Returns
+    {(b, h): o [len(rows), d]} over `heads` (default: all) and `rows`
+    (default: all)."""
+    B, H, L, d = q.shape
+    heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    rows = np.arange(L) if rows is None else np.asarray(rows)
+    out = {}
+    for (b, h) in heads:
+        m = mask_of(b, h, rows)
+        out[(b, h)] = attention(q[b, h, rows], k[b, h], v[b, h], m, scale, n_threads)
+    return out

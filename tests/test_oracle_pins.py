@@ -1,0 +1,252 @@
+"""Pins for the CPU oracle: each check ties an oracle function to something
+other than itself (a library routine, a closed form, a hand-derived fixture,
+a tiny brute force, or a round trip), chosen so that a dropped term, a wrong
+sign or index, or a transposed operand fails at least one of them.
+
+Method: "Accelerating Sparse Transformer Inference on GPU" (gist.science
+technical summary), Methodology 1, Unified MHA module: exact masking over a
+two-level format (outer tiles empty / full / partial, one uint64 per 8x8
+inner tile of a partial outer tile).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from sparse_mask_transformer_gb300 import synth
+from tests.conftest import read_golden
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def _sdpa(q, k, v, mask, scale):
+    """torch's own fp64 attention (library routine) for one head."""
+    tq, tk, tv = (torch.from_numpy(x)[None, None] for x in (q, k, v))
+    am = torch.from_numpy(mask.astype(bool))[None, None]
+    return F.scaled_dot_product_attention(tq, tk, tv, attn_mask=am, scale=scale)[0, 0].numpy()
+
+
+# ---------------------------------------------------------------- attention
+
+@pytest.mark.parametrize("n_q,lk,d", [(1, 1, 64), (37, 53, 64), (64, 200, 128), (5, 300, 16)])
+def test_all_ones_mask_is_dense_attention(n_q, lk, d):
+    q, k, v = _rand((n_q, d), 1), _rand((lk, d), 2), _rand((lk, d), 3)
+    scale = 1 / math.sqrt(d)
+    o = oracle.attention(q, k, v, np.ones((n_q, lk), np.uint8), scale)
+    tq, tk, tv = (torch.from_numpy(x)[None, None] for x in (q, k, v))
+    ref = F.scaled_dot_product_attention(tq, tk, tv, scale=scale)[0, 0].numpy()
+    np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-12)
+    # and against the textbook two-pass softmax written with numpy ops
+    s = scale * q @ k.T
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    np.testing.assert_allclose(o, (p @ v) / p.sum(axis=1, keepdims=True), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("density", [0.05, 0.3, 0.9])
+def test_random_mask_matches_library_masked_attention(density):
+    n_q, lk, d = 96, 160, 64
+    q, k, v = _rand((n_q, d), 4), _rand((lk, d), 5), _rand((lk, d), 6)
+    mask = (np.random.default_rng(7).random((n_q, lk)) < density).astype(np.uint8)
+    mask[3] = 0  # one fully masked row
+    scale = 0.125
+    o = oracle.attention(q, k, v, mask, scale)
+    rows = mask.any(axis=1)
+    ref = _sdpa(q, k, v, mask, scale)
+    np.testing.assert_allclose(o[rows], ref[rows], rtol=1e-11, atol=1e-12)
+    assert np.all(o[~rows] == 0.0)
+
+
+def test_causal_matches_library_is_causal():
+    L, d = 130, 32
+    q, k, v = _rand((L, d), 8), _rand((L, d), 9), _rand((L, d), 10)
+    o = oracle.attention(q, k, v, np.tril(np.ones((L, L), np.uint8)), 0.3)
+    tq, tk, tv = (torch.from_numpy(x)[None, None] for x in (q, k, v))
+    ref = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True, scale=0.3)[0, 0].numpy()
+    np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_mask_orientation_is_query_by_key():
+    # a non-symmetric mask: transposing it must change the answer
+    L, d = 24, 8
+    q, k, v = _rand((L, d), 11), _rand((L, d), 12), _rand((L, d), 13)
+    m = np.triu(np.ones((L, L), np.uint8))
+    o = oracle.attention(q, k, v, m, 1.0)
+    np.testing.assert_allclose(o, _sdpa(q, k, v, m, 1.0), rtol=1e-12, atol=1e-12)
+    assert not np.allclose(o, oracle.attention(q, k, v, m.T.copy(), 1.0))
+
+
+def test_single_valid_key_returns_that_value_row_exactly():
+    n_q, lk, d = 50, 70, 64
+    q, k, v = _rand((n_q, d), 14) * 30, _rand((lk, d), 15), _rand((lk, d), 16)
+    mask = np.zeros((n_q, lk), np.uint8)
+    js = np.random.default_rng(17).integers(0, lk, n_q)
+    mask[np.arange(n_q), js] = 1
+    o = oracle.attention(q, k, v, mask, 0.125)
+    assert np.array_equal(o, v[js])  # softmax of one element is exactly 1
+
+
+def test_fully_masked_rows_are_zero():
+    q, k, v = _rand((4, 8), 18), _rand((9, 8), 19), _rand((9, 8), 20)
+    o = oracle.attention(q, k, v, np.zeros((4, 9), np.uint8), 1.0)
+    assert np.array_equal(o, np.zeros((4, 8)))
+
+
+@pytest.mark.parametrize("L", [8, 16, 24])
+def test_tiny_brute_force_unstabilised_formula(L):
+    # o_i = sum_j m_ij e^{s_ij} v_j / sum_j m_ij e^{s_ij}, pure Python loops
+    d = 4
+    q, k, v = _rand((L, d), 21 + L), _rand((L, d), 22 + L), _rand((L, d), 23 + L)
+    mask = (np.random.default_rng(24 + L).random((L, L)) < 0.4).astype(np.uint8)
+    mask[0] = 0
+    scale = 0.7
+    o = oracle.attention(q, k, v, mask, scale)
+    for i in range(L):
+        num = [0.0] * d
+        den = 0.0
+        for j in range(L):
+            if mask[i, j]:
+                w = math.exp(scale * sum(q[i, t] * k[j, t] for t in range(d)))
+                den += w
+                for t in range(d):
+                    num[t] += w * v[j, t]
+        want = [x / den for x in num] if den > 0 else [0.0] * d
+        np.testing.assert_allclose(o[i], want, rtol=1e-12, atol=1e-13)
+
+
+def test_large_scores_stay_finite():
+    # the max-shift keeps exp() in range where the unstabilised form overflows
+    q = np.full((2, 4), 40.0)
+    k = np.array([[40.0] * 4, [39.0] * 4, [-5.0] * 4])
+    v = np.array([[1.0, 0, 0, 0], [0, 1.0, 0, 0], [0, 0, 1.0, 0]])
+    o = oracle.attention(q, k, v, np.ones((2, 3), np.uint8), 1.0)
+    w1 = math.exp(-160.0)  # s = 6400, 6240, -800
+    np.testing.assert_allclose(o[0], [1 / (1 + w1), w1 / (1 + w1), 0, 0], rtol=1e-15, atol=1e-300)
+
+
+def test_golden_tiny_attention():
+    g = read_golden("attention_tiny.txt")
+    q = np.array([[float(x) for x in g["q"].split()]])
+    k = np.array([[float(x) for x in r.split()] for r in g["k"].split(";")])
+    v = np.array([[float(x) for x in r.split()] for r in g["v"].split(";")])
+    for case in g["case"]:
+        m, want = case.split("->")
+        mask = np.array([[int(x) for x in m.split()]], np.uint8)
+        o = oracle.attention(q, k, v, mask, float(g["scale"]))
+        np.testing.assert_allclose(o[0], [float(x) for x in want.split()], rtol=1e-14, atol=1e-14)
+
+
+def test_threads_do_not_change_results():
+    q, k, v = _rand((301, 64), 25), _rand((77, 64), 26), _rand((77, 64), 27)
+    mask = (np.random.default_rng(28).random((301, 77)) < 0.5).astype(np.uint8)
+    a = oracle.attention(q, k, v, mask, 0.125, n_threads=1)
+    b = oracle.attention(q, k, v, mask, 0.125, n_threads=7)
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- encoder
+
+def _golden_format(name):
+    g = read_golden(name)
+    ints = lambda s: np.array([int(x, 0) for x in s.split()], dtype=np.int64)
+    return g, dict(
+        full_row_ptr=ints(g["full_row_ptr"]), full_col_idx=ints(g["full_col_idx"]),
+        part_row_ptr=ints(g["part_row_ptr"]), part_col_idx=ints(g["part_col_idx"]),
+        bitmaps=np.array([int(x, 16) for x in g["bitmaps"].split()], dtype=np.uint64))
+
+
+@pytest.mark.parametrize("name", ["encode_causal16_ot8.txt", "encode_upper16x32_ot8x16.txt"])
+def test_golden_encodings(name):
+    g, want = _golden_format(name)
+    lq, lk, bm, bn = (int(g[x]) for x in ("lq", "lk", "bm", "bn"))
+    i = np.arange(lq)[:, None]
+    j = np.arange(lk)[None, :]
+    mask = ((j <= i) if g["pattern"] == "causal" else (j >= i)).astype(np.uint8)[None]
+    fmt = oracle.encode(mask, bm, bn)
+    for key in ("full_row_ptr", "full_col_idx", "part_row_ptr", "part_col_idx"):
+        assert fmt[key].tolist() == want[key].tolist(), key
+    assert fmt["bitmaps"].reshape(-1).tolist() == want["bitmaps"].tolist()
+    assert fmt["nnz"] == int(g["nnz"])
+    assert np.array_equal(oracle.decode(fmt), mask)
+
+
+def test_every_single_bit_position():
+    # 64 masks of one 8x8 tile, one valid element each: the tile is partial
+    # and its word has exactly the bit of that element (row-major, bit 0 =
+    # top-left).  Read back through the hand-derived rule r = b // 8, c = b % 8.
+    for b in range(64):
+        mask = np.zeros((1, 8, 16), np.uint8)
+        mask[0, b // 8, 8 + b % 8] = 1  # second IT column: pins the IT order too
+        fmt = oracle.encode(mask, 8, 16)
+        assert fmt["n_full"] == 0 and fmt["n_part"] == 1 and fmt["nnz"] == 1
+        words = fmt["bitmaps"].reshape(-1)
+        assert int(words[0]) == 0
+        assert int(words[1]) == 1 << b
+        assert np.array_equal(oracle.decode(fmt), mask)
+
+
+def test_tile_classes_from_hand_built_masks():
+    mask = np.zeros((2, 32, 32), np.uint8)
+    mask[0, 0:16, 16:32] = 1          # mask 0: OT(0,1) full at 16x16
+    mask[0, 20, 3] = 1                # mask 0: OT(1,0) partial, one element
+    mask[1] = 1                       # mask 1: all four OTs full
+    fmt = oracle.encode(mask, 16, 16)
+    assert fmt["full_row_ptr"].tolist() == [0, 1, 1, 3, 5]
+    assert fmt["full_col_idx"].tolist() == [1, 0, 1, 0, 1]
+    assert fmt["part_row_ptr"].tolist() == [0, 0, 1, 1, 1]
+    assert fmt["part_col_idx"].tolist() == [0]
+    words = fmt["bitmaps"][0]         # [2][2] ITs; element (20,3) -> IT(0,0), r=4, c=3
+    assert int(words[0, 0]) == 1 << (8 * 4 + 3)
+    assert int(words.sum()) == 1 << 35
+    assert fmt["nnz"] == 256 + 1 + 32 * 32
+    assert oracle.encode_count(np.zeros((1, 64, 64), np.uint8), 32, 32) == (0, 0, 0)
+
+
+@pytest.mark.parametrize("bm,bn", [(8, 8), (16, 16), (8, 16), (24, 8), (32, 64)])
+@pytest.mark.parametrize("density", [0.0, 0.02, 0.5, 0.98, 1.0])
+def test_encode_decode_round_trip_random(bm, bn, density):
+    mask = synth.random_mask(3, 96, 128, density, seed=int(density * 100) + bm + bn)
+    fmt = oracle.encode(mask, bm, bn)
+    assert np.array_equal(oracle.decode(fmt), mask)
+    assert fmt["nnz"] == int(mask.sum())
+    n_tiles = 3 * (96 // bm) * (128 // bn)
+    assert fmt["n_full"] + fmt["n_part"] <= n_tiles
+    assert np.all(np.diff(fmt["full_row_ptr"]) >= 0) and np.all(np.diff(fmt["part_row_ptr"]) >= 0)
+
+
+def test_window48_tile_counts_closed_form():
+    # valid iff 0 <= i - j < 48.  At 16x16 an OT(I,J) spans i - j in
+    # [16(I-J) - 15, 16(I-J) + 15]: full iff I-J in {1, 2} (15 + 14 = 29),
+    # partial iff I-J in {0, 3} (16 + 13 = 29), empty otherwise (198).
+    # At 128x128: OT(0,0), OT(1,1) partial (diagonal), OT(1,0) partial
+    # (i - j spans [1, 255]), OT(0,1) empty.
+    w = synth.WORKLOADS["window48_L256"]
+    mask = synth.make_mask(w)
+    assert oracle.encode_count(mask, 16, 16) == (29, 29, 11160)
+    assert oracle.encode_count(mask, 128, 128) == (0, 3, 11160)
+    assert 11160 == sum(min(i + 1, 48) for i in range(256))
+
+
+def test_causal_tile_counts_closed_form():
+    # causal L = 2048 at 128x128, n = 16 OT rows: n(n-1)/2 = 120 full tiles
+    # strictly below the diagonal, n = 16 partial diagonal tiles; nnz = L(L+1)/2
+    w = synth.WORKLOADS["causal_L2048"]
+    mask = synth.make_mask(w)
+    assert oracle.encode_count(mask, 128, 128) == (120, 16, 2048 * 2049 // 2)
+    fmt = oracle.encode(mask, 128, 128)
+    assert np.array_equal(oracle.decode(fmt), mask)
+    assert fmt["full_row_ptr"].tolist() == [I * (I - 1) // 2 for I in range(17)]
+    assert fmt["part_col_idx"].tolist() == list(range(16))
+
+
+@pytest.mark.parametrize("name", ["window48_L256", "bigbird_L512", "causal_L2048", "longformer_L4096"])
+def test_workload_masks_round_trip(name):
+    w = synth.WORKLOADS[name]
+    mask = synth.make_mask(w)
+    fmt = oracle.encode(mask, 128, 128)
+    assert np.array_equal(oracle.decode(fmt), mask)
+    assert fmt["nnz"] == int(mask.sum())
