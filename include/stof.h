@@ -1,0 +1,173 @@
+/*
+ * stof.h -- C ABI of libstof.so: masked multi-head attention (MHA) forward
+ * over an arbitrary sparse mask held in STOF's two-level format, on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Source of the method: "Accelerating Sparse Transformer Inference on GPU"
+ * (Dai et al., arXiv 2506.06095).  Passages cited below:
+ *   [ABS]  arXiv abstract: STOF maps MHA to row-wise or block-wise kernels,
+ *          each with its own storage format, chosen by analytical modelling.
+ *   [FMT]  gist.science technical summary, Methodology 1 "Unified MHA
+ *          module", two-level storage format: BSR over outer tiles (OT);
+ *          empty OTs skipped globally; "full" OTs (all elements valid) and
+ *          "partial" OTs (mixed) tracked by pointer arrays; every 8x8 inner
+ *          tile (IT) of a partial OT is one uint64 bitmap (exact masking
+ *          without materialising the sparse matrix).
+ *   [ROW]  same section, dual-kernel strategy, row-wise kernel: for high
+ *          sparsity and short sequences; Q sliced into rows; warp-level
+ *          shuffles; no inter-warp synchronisation.
+ *   [BLK]  same section, block-wise kernel: general case; Q, K, V split
+ *          into sub-blocks staged in shared memory with asynchronous copies
+ *          that overlap memory transfer and compute.
+ *   [SEL]  same section, kernel selection: an analytical model picks the
+ *          row-wise or the block-wise kernel from mask sparsity and
+ *          sequence length.
+ *   [PROB] same page, Problem statement: arbitrary masks (causal, sliding
+ *          window, random, BigBird); work on masked entries is skipped, not
+ *          computed and reset afterwards.
+ *
+ * Conventions of this library (the pages leave them open):
+ *   - Q, K, V, O are [B][H][L][d] row-major, contiguous, fp16 or bf16,
+ *     16-byte aligned device memory.  d is 64 or 128.
+ *   - A mask is uint8 [n_masks][L][L] (query row i, key column j); an
+ *     element is valid iff its byte is non-zero.  Head (b, h) uses mask
+ *     number b * mask_stride_b + h * mask_stride_h.
+ *   - Scores accumulate in fp32; the softmax runs in fp32; P is rounded to
+ *     the input type before P*V; O is rounded to nearest even.  A query row
+ *     with no valid key gets O = 0.
+ *   - All device pointers are owned by the caller.  The library allocates
+ *     no device memory; the format's arrays live in a caller-provided
+ *     workspace.
+ *   - Every call that takes a stream is asynchronous on that stream (a
+ *     cudaStream_t passed as void*; NULL is the legacy default stream).
+ *     Host-side validation happens before any launch and returns an error
+ *     without touching device memory.  Errors detected on the device set a
+ *     device error word, reported by stof_format_sync().  The library never
+ *     traps.
+ */
+#ifndef STOF_H_
+#define STOF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define STOF_VERSION 1
+
+typedef enum {
+  STOF_OK = 0,
+  STOF_ERR_INVALID_ARG = 1,  /* null pointer, negative size, unknown enum value */
+  STOF_ERR_SHAPE = 2,        /* sizes inconsistent, not tile-divisible, or too large */
+  STOF_ERR_DTYPE = 3,        /* unknown element type */
+  STOF_ERR_ALIGNMENT = 4,    /* a pointer is not aligned as required */
+  STOF_ERR_WORKSPACE = 5,    /* workspace smaller than stof_encode_workspace_bytes() */
+  STOF_ERR_UNSUPPORTED = 6,  /* well-formed but not implemented (head dim, tile size) */
+  STOF_ERR_DEVICE = 7,       /* a kernel reported an error through the device error word */
+  STOF_ERR_CUDA = 8,         /* CUDA runtime error (no device, launch failure, ...) */
+  STOF_ERR_NOT_SYNCED = 9    /* host tile counts needed but stof_format_sync() not called */
+} stof_status;
+
+typedef enum { STOF_F16 = 0, STOF_BF16 = 1 } stof_dtype;
+
+typedef enum {
+  STOF_KERNEL_AUTO = -1,      /* use stof_select_kernel() on the format's density */
+  STOF_KERNEL_ROWWISE = 0,    /* [ROW] */
+  STOF_KERNEL_BLOCKWISE = 1   /* [BLK] */
+} stof_kernel;
+
+/* Device error word bits (stof_format.device_error after a sync). */
+#define STOF_DEVERR_LOOKBACK_TIMEOUT 0x1 /* encoder: a predecessor never published */
+#define STOF_DEVERR_PIPE_TIMEOUT 0x2     /* block-wise kernel: a pipeline wait ran out */
+#define STOF_DEVERR_BAD_FORMAT 0x4       /* an out-of-range column index was skipped */
+
+/*
+ * Two-level sparse mask format [FMT], filled by stof_encode_mask().
+ *
+ * Outer tiles are bm x bn; OT row r = m * n_tr + I numbers the OT rows of
+ * all masks (mask-major).  Full and partial OTs each form a CSR over OT
+ * rows: the tiles of row r are col_idx[row_ptr[r] .. row_ptr[r+1]), column
+ * indices ascending, offsets global across masks.  Empty OTs are not
+ * listed.  bitmaps[e] holds the (bm/8) x (bn/8) IT words of partial tile e
+ * (row-major over ITs); bit (8*r + c) of an IT word is element (r, c) of
+ * that 8x8 tile.
+ *
+ * All pointers are DEVICE memory inside the caller's workspace.  The host
+ * counts are valid only after stof_format_sync().
+ */
+typedef struct {
+  int32_t n_masks, lq, lk, bm, bn, n_tr, n_tc;
+  int32_t synced;           /* 1 after a successful stof_format_sync() */
+  int32_t* full_row_ptr;    /* [n_masks*n_tr + 1] */
+  int32_t* full_col_idx;    /* [n_full] (capacity n_masks*n_tr*n_tc) */
+  int32_t* part_row_ptr;    /* [n_masks*n_tr + 1] */
+  int32_t* part_col_idx;    /* [n_part] */
+  uint64_t* bitmaps;        /* [n_part][bm/8][bn/8] */
+  int64_t* counts_dev;      /* [0] n_full [1] n_part [2] nnz [3] device error word */
+  void* scratch;            /* encoder scratch: tile ticket and look-back state */
+  int64_t n_full, n_part, nnz; /* host copies (valid when synced) */
+  int64_t device_error;        /* host copy of the device error word (valid when synced) */
+} stof_format;
+
+/* Bytes of workspace stof_encode_mask() needs for these sizes, enough for
+ * the worst case (every OT partial).  Returns 0 for invalid sizes. */
+size_t stof_encode_workspace_bytes(int n_masks, int lq, int lk, int bm, int bn);
+
+/*
+ * Encodes a dense mask into the two-level format [FMT]: classifies every OT
+ * as empty / full / partial, builds the two CSR pointer arrays by a prefix
+ * sum, and packs the IT bitmaps of partial OTs, in one pass over the mask.
+ *   mask       device, uint8 [n_masks][lq][lk]; 8-byte aligned.
+ *   bm, bn     OT size: multiples of 8 in [8, 256]; lq % bm == 0, lk % bn == 0.
+ *   workspace  device, >= stof_encode_workspace_bytes(...) bytes, 256-byte
+ *              aligned; owned by the caller and must outlive every use of fmt.
+ *   fmt        host struct, overwritten; its pointers alias the workspace.
+ *   stream     cudaStream_t.
+ * Asynchronous.  fmt->synced is reset to 0.
+ */
+stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, int bm, int bn,
+                             void* workspace, size_t ws_bytes, stof_format* fmt, void* stream);
+
+/* Blocks until the work queued on stream is done, copies the tile counts
+ * and the device error word into fmt, and sets fmt->synced.  Returns
+ * STOF_ERR_DEVICE if the device error word is non-zero. */
+stof_status stof_format_sync(stof_format* fmt, void* stream);
+
+/* Analytic kernel choice [SEL]: row-wise or block-wise from the mask
+ * density (valid elements / all elements, in [0, 1]), the sequence length
+ * and the head dimension.  Pure host arithmetic and deterministic; invalid
+ * arguments give STOF_KERNEL_BLOCKWISE. */
+stof_kernel stof_select_kernel(double density, int seq_len, int head_dim);
+
+/*
+ * Masked MHA forward [ABS][PROB]:
+ *   O[b,h,i,:] = sum_{j valid} softmax_j(scale * Q[b,h,i,:].K[b,h,j,:]) V[b,h,j,:]
+ * over the valid keys of query row i in mask b*mask_stride_b + h*mask_stride_h;
+ * rows without valid keys give 0.  Only listed OTs are touched; full OTs
+ * need no mask test, partial OTs are masked through their IT bitmaps.
+ *   q, k, v, o  device [B][H][L][d], dt, 16-byte aligned; o is written.
+ *   L           == fmt->lq == fmt->lk.   d: 64 or 128.
+ *   fmt         an encoded format (stof_encode_mask) for masks of size L.
+ *   which       STOF_KERNEL_ROWWISE [ROW], STOF_KERNEL_BLOCKWISE [BLK]
+ *               (needs bm == bn == 128) or STOF_KERNEL_AUTO ([SEL], needs a
+ *               synced fmt).
+ * Asynchronous on stream.
+ */
+stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H,
+                         int L, int d, float scale, const stof_format* fmt,
+                         int64_t mask_stride_b, int64_t mask_stride_h, stof_kernel which, void* o,
+                         void* stream);
+
+/* Static description of a status code. */
+const char* stof_status_string(stof_status s);
+
+/* STOF_VERSION of the built library. */
+int stof_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STOF_H_ */

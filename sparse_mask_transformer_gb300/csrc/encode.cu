@@ -1,0 +1,296 @@
+// Mask encoder: dense uint8 mask -> STOF two-level format.
+//
+// "Accelerating Sparse Transformer Inference on GPU" (gist.science technical
+// summary), Methodology 1, Unified MHA module, two-level storage format:
+// outer tiles (OT) are empty (skipped), full (every element valid) or
+// partial (mixed); full and partial OTs are tracked by pointer arrays; each
+// 8x8 inner tile (IT) of a partial OT is one uint64 bitmap.
+//
+// GB300 design: one pass over the mask, which is the only large stream
+// (HBM-bound).  A CTA owns a chunk = one OT row band x `ct` consecutive OTs
+// (about 1024 mask columns).  It
+//   1. reads the chunk with coalesced 8-byte loads and packs each 8x8 IT
+//      into a uint64 in shared memory (bit 8r+c = byte (r, c) non-zero);
+//   2. classifies each OT by AND / OR over its IT words;
+//   3. gets the global offsets of its full and partial OTs from a
+//      single-pass chained prefix sum with decoupled look-back (Merrill and
+//      Garland, "Single-pass Parallel Prefix Scan with Decoupled
+//      Look-back", 2016); chunks are numbered by an atomic ticket in start
+//      order, so every chunk it waits on is already running;
+//   4. writes column indices, row pointers and the bitmaps of its partial
+//      OTs straight into their final slots.
+// Every wait on another CTA is bounded; on timeout the CTA raises
+// STOF_DEVERR_LOOKBACK_TIMEOUT in the device error word and finishes.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace stof {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;              // IT words in flight per thread
+constexpr int kMaxTilesPerChunk = 128;
+constexpr unsigned long long kFlagAgg = 1ull << 62;
+constexpr unsigned long long kFlagInc = 2ull << 62;
+constexpr unsigned long long kValMask = (1ull << 62) - 1;
+constexpr uint64_t kLookbackTimeoutNs = 2000000000ull;
+
+// bit c of the result = (byte c of x != 0)
+__device__ __forceinline__ uint32_t pack_row8(uint64_t x) {
+  x |= x >> 4;
+  x |= x >> 2;
+  x |= x >> 1;
+  x &= 0x0101010101010101ull;
+  return static_cast<uint32_t>((x * 0x0102040810204080ull) >> 56);
+}
+
+__device__ __forceinline__ unsigned long long ld_volatile(const unsigned long long* p) {
+  return *reinterpret_cast<const volatile unsigned long long*>(p);
+}
+__device__ __forceinline__ void st_volatile(unsigned long long* p, unsigned long long v) {
+  *reinterpret_cast<volatile unsigned long long*>(p) = v;
+}
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__global__ void __launch_bounds__(kThreads) encode_kernel(const EncodeParams p) {
+  extern __shared__ uint64_t s_words[];  // [bm/8][nt * bn/8]
+  __shared__ long long s_chunk;
+  __shared__ unsigned long long s_nnz;
+  __shared__ unsigned long long s_excl;
+  __shared__ uint8_t s_class[kMaxTilesPerChunk];
+  __shared__ int s_rank[kMaxTilesPerChunk];
+  __shared__ int s_plist[kMaxTilesPerChunk];
+  __shared__ int s_nf, s_np;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_chunk = static_cast<long long>(atomicAdd(p.ticket, 1ull));
+    s_nnz = 0;
+  }
+  __syncthreads();
+  const long long chunk = s_chunk;
+  if (chunk >= p.n_chunks) return;
+
+  const long long row = chunk / p.cpr;
+  const int cc = static_cast<int>(chunk % p.cpr);
+  const int m = static_cast<int>(row / p.n_tr);
+  const int I = static_cast<int>(row % p.n_tr);
+  const int J0 = cc * p.ct;
+  const int nt = min(p.ct, p.n_tc - J0);
+  const int itc = p.bn >> 3;                 // IT columns per OT
+  const int itcols = nt * itc;               // IT columns in this chunk
+  const int bands = p.bm >> 3;
+  const int nwords = bands * itcols;
+  const uint8_t* base = p.mask + (static_cast<long long>(m) * p.lq + static_cast<long long>(I) * p.bm) * p.lk +
+                        static_cast<long long>(J0) * p.bn;
+
+  // 1. read and pack
+  unsigned long long local_nnz = 0;
+  for (int w0 = tid; w0 < nwords; w0 += kThreads * kUnroll) {
+    uint2 v[kUnroll][8];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int w = w0 + u * kThreads;
+      if (w < nwords) {
+        const int pb = w / itcols, q = w - pb * itcols;
+        const uint8_t* src = base + static_cast<long long>(8 * pb) * p.lk + 8 * q;
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          v[u][r] = __ldcs(reinterpret_cast<const uint2*>(src + static_cast<long long>(r) * p.lk));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int w = w0 + u * kThreads;
+      if (w < nwords) {
+        uint64_t word = 0;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const uint64_t x = (static_cast<uint64_t>(v[u][r].y) << 32) | v[u][r].x;
+          word |= static_cast<uint64_t>(pack_row8(x)) << (8 * r);
+        }
+        s_words[w] = word;
+        local_nnz += __popcll(word);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) local_nnz += __shfl_xor_sync(0xffffffffu, local_nnz, off);
+  if (lane == 0 && local_nnz) atomicAdd(&s_nnz, local_nnz);
+  __syncthreads();
+
+  // 2. classify: 0 empty, 1 full, 2 partial
+  const int wpt = bands * itc;
+  for (int t = warp; t < nt; t += kThreads / 32) {
+    uint64_t any = 0, all = ~0ull;
+    for (int e = lane; e < wpt; e += 32) {
+      const int pb = e / itc, qq = e - pb * itc;
+      const uint64_t w = s_words[pb * itcols + t * itc + qq];
+      any |= w;
+      all &= w;
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      any |= __shfl_xor_sync(0xffffffffu, any, off);
+      all &= __shfl_xor_sync(0xffffffffu, all, off);
+    }
+    if (lane == 0) s_class[t] = any == 0 ? 0 : (all == ~0ull ? 1 : 2);
+  }
+  __syncthreads();
+
+  // 3. local ranks and chained prefix sum (warp 0)
+  if (warp == 0) {
+    int nf = 0, np = 0;
+    for (int t0 = 0; t0 < nt; t0 += 32) {
+      const int t = t0 + lane;
+      const int cls = t < nt ? s_class[t] : 0;
+      const unsigned bf = __ballot_sync(0xffffffffu, cls == 1);
+      const unsigned bp = __ballot_sync(0xffffffffu, cls == 2);
+      const unsigned lt = (1u << lane) - 1u;
+      if (cls == 1) s_rank[t] = nf + __popc(bf & lt);
+      if (cls == 2) {
+        const int r = np + __popc(bp & lt);
+        s_rank[t] = r;
+        s_plist[r] = t;
+      }
+      nf += __popc(bf);
+      np += __popc(bp);
+    }
+    const unsigned long long agg =
+        (static_cast<unsigned long long>(nf) << 31) | static_cast<unsigned long long>(np);
+    unsigned long long excl = 0;
+    if (chunk == 0) {
+      if (lane == 0) st_volatile(&p.status[0], kFlagInc | agg);
+    } else {
+      if (lane == 0) st_volatile(&p.status[chunk], kFlagAgg | agg);
+      long long top = chunk - 1;
+      const uint64_t t_start = now_ns();
+      bool timed_out = false;
+      while (true) {
+        const long long idx = top - lane;
+        const unsigned long long v = idx >= 0 ? ld_volatile(&p.status[idx]) : kFlagInc;
+        const unsigned long long flag = v >> 62;
+        const unsigned inc = __ballot_sync(0xffffffffu, flag == 2);
+        const unsigned notready = __ballot_sync(0xffffffffu, flag == 0);
+        const int first_inc = inc ? __ffs(inc) - 1 : 32;
+        const unsigned needed = first_inc >= 31 ? 0xffffffffu : ((2u << first_inc) - 1u);
+        if ((notready & needed) && !timed_out) {
+          if (now_ns() - t_start > kLookbackTimeoutNs) {
+            timed_out = true;  // treat missing predecessors as empty, report
+            if (lane == 0) atomicOr(reinterpret_cast<unsigned long long*>(&p.counts[3]),
+                                    static_cast<unsigned long long>(STOF_DEVERR_LOOKBACK_TIMEOUT));
+          } else {
+            __nanosleep(64);
+          }
+          continue;
+        }
+        unsigned long long val = (lane <= first_inc && flag != 0) ? (v & kValMask) : 0ull;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) val += __shfl_xor_sync(0xffffffffu, val, off);
+        excl += val;
+        if (first_inc < 32 || timed_out) break;
+        top -= 32;
+      }
+      if (lane == 0) st_volatile(&p.status[chunk], kFlagInc | (excl + agg));
+    }
+    if (lane == 0) {
+      s_excl = excl;
+      s_nf = nf;
+      s_np = np;
+      if (s_nnz) atomicAdd(reinterpret_cast<unsigned long long*>(&p.counts[2]), s_nnz);
+    }
+  }
+  __syncthreads();
+
+  // 4. outputs
+  const long long ef = static_cast<long long>((s_excl >> 31) & 0x7FFFFFFFull);
+  const long long ep = static_cast<long long>(s_excl & 0x7FFFFFFFull);
+  const int nf = s_nf, np = s_np;
+  if (cc == 0 && tid == 0) {
+    p.full_row_ptr[row] = static_cast<int32_t>(ef);
+    p.part_row_ptr[row] = static_cast<int32_t>(ep);
+  }
+  for (int t = tid; t < nt; t += kThreads) {
+    const int cls = s_class[t];
+    if (cls == 1) p.full_col_idx[ef + s_rank[t]] = J0 + t;
+    if (cls == 2) p.part_col_idx[ep + s_rank[t]] = J0 + t;
+  }
+  const int total = np * wpt;
+  for (int e = tid; e < total; e += kThreads) {
+    const int r = e / wpt, x = e - r * wpt;
+    const int t = s_plist[r];
+    const int pb = x / itc, qq = x - pb * itc;
+    p.bitmaps[(ep + r) * wpt + x] = s_words[pb * itcols + t * itc + qq];
+  }
+  if (chunk == p.n_chunks - 1 && tid == 0) {
+    p.full_row_ptr[p.n_rows] = static_cast<int32_t>(ef + nf);
+    p.part_row_ptr[p.n_rows] = static_cast<int32_t>(ep + np);
+    p.counts[0] = ef + nf;
+    p.counts[1] = ep + np;
+  }
+}
+
+}  // namespace
+
+bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g) {
+  if (n_masks < 1 || lq < 1 || lk < 1) return false;
+  if (bm < 8 || bn < 8 || bm > 256 || bn > 256 || bm % 8 || bn % 8) return false;
+  if (lq % bm || lk % bn) return false;
+  g->n_tr = lq / bm;
+  g->n_tc = lk / bn;
+  g->n_rows = static_cast<int64_t>(n_masks) * g->n_tr;
+  g->n_tiles = g->n_rows * g->n_tc;
+  if (g->n_tiles >= (int64_t(1) << 31) - 1) return false;
+  int ct = 1024 / bn;
+  if (ct < 1) ct = 1;
+  if (ct > kMaxTilesPerChunk) ct = kMaxTilesPerChunk;
+  if (ct > g->n_tc) ct = g->n_tc;
+  g->ct = ct;
+  g->cpr = (g->n_tc + ct - 1) / ct;
+  g->n_chunks = g->n_rows * g->cpr;
+  g->words_per_tile = (bm / 8) * (bn / 8);
+  g->smem_bytes = static_cast<size_t>(bm / 8) * (ct * bn / 8) * sizeof(uint64_t);
+  return true;
+}
+
+WorkspaceLayout workspace_layout(const EncodeGeom& g) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  WorkspaceLayout w{};
+  size_t off = 0;
+  w.counts = off;                       // 4 x int64
+  w.ticket = off + 32;                  // 1 x u64
+  w.status = off + 64;                  // n_chunks x u64
+  w.status_bytes = static_cast<size_t>(g.n_chunks) * 8;
+  w.zero_bytes = 64 + w.status_bytes;
+  off = up(w.status + w.status_bytes);
+  w.full_row_ptr = off;
+  off = up(off + (static_cast<size_t>(g.n_rows) + 1) * 4);
+  w.part_row_ptr = off;
+  off = up(off + (static_cast<size_t>(g.n_rows) + 1) * 4);
+  w.full_col_idx = off;
+  off = up(off + static_cast<size_t>(g.n_tiles) * 4);
+  w.part_col_idx = off;
+  off = up(off + static_cast<size_t>(g.n_tiles) * 4);
+  w.bitmaps = off;
+  off = up(off + static_cast<size_t>(g.n_tiles) * g.words_per_tile * 8);
+  w.total = off;
+  return w;
+}
+
+cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s) {
+  if (g.smem_bytes > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(g.smem_bytes));
+    if (e != cudaSuccess) return e;
+  }
+  encode_kernel<<<static_cast<unsigned>(g.n_chunks), kThreads, g.smem_bytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace stof

@@ -1,0 +1,63 @@
+// Internal declarations shared by the translation units of libstof.so.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "stof.h"
+
+namespace stof {
+
+// ---------------------------------------------------------------- encoder
+// A chunk is one OT row band (bm mask rows) times `ct` consecutive OTs.
+struct EncodeGeom {
+  int n_tr, n_tc, ct, cpr;      // cpr = chunks per OT row
+  int64_t n_rows, n_chunks, n_tiles;
+  int words_per_tile;           // (bm/8) * (bn/8)
+  size_t smem_bytes;            // dynamic shared memory of one encoder CTA
+};
+bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g);
+
+// Workspace carve-up (byte offsets, 256-byte aligned sections).
+struct WorkspaceLayout {
+  size_t counts, ticket, status, status_bytes, zero_bytes;  // zero_bytes from `counts`
+  size_t full_row_ptr, part_row_ptr, full_col_idx, part_col_idx, bitmaps, total;
+};
+WorkspaceLayout workspace_layout(const EncodeGeom& g);
+
+struct EncodeParams {
+  const uint8_t* mask;
+  int lq, lk, bm, bn, n_tr, n_tc, ct, cpr;
+  int64_t n_rows, n_chunks;
+  int32_t* full_row_ptr;
+  int32_t* full_col_idx;
+  int32_t* part_row_ptr;
+  int32_t* part_col_idx;
+  uint64_t* bitmaps;
+  int64_t* counts;                 // [0] n_full [1] n_part [2] nnz [3] error word
+  unsigned long long* ticket;      // scratch, zero at launch
+  unsigned long long* status;      // scratch [n_chunks], zero at launch
+};
+cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention
+struct AttnParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  int B, H, L, d;
+  float scale_log2;                // scale * log2(e)
+  int bm, bn, n_tr, n_tc;
+  int64_t stride_b, stride_h;
+  const int32_t* full_row_ptr;
+  const int32_t* full_col_idx;
+  const int32_t* part_row_ptr;
+  const int32_t* part_col_idx;
+  const uint64_t* bitmaps;
+  int64_t* err;                    // device error word (counts[3])
+};
+cudaError_t launch_rowwise(const AttnParams& p, bool bf16, cudaStream_t s);
+// Returns STOF_OK or an error status (tensor-map encoding / launch).
+stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s);
+
+}  // namespace stof

@@ -1,0 +1,220 @@
+// C ABI of libstof.so: argument validation, workspace carve-up, kernel
+// selection and dispatch.  The arithmetic of the method runs in the
+// kernels (encode.cu, rowwise.cu, blockwise.cu); this file only checks
+// arguments and launches.
+//
+// Method: "Accelerating Sparse Transformer Inference on GPU" (gist.science
+// technical summary), Methodology 1, Unified MHA module (two-level storage
+// format; row-wise and block-wise kernels; analytic kernel selection).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+
+using namespace stof;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+int stof_version(void) { return STOF_VERSION; }
+
+const char* stof_status_string(stof_status s) {
+  switch (s) {
+    case STOF_OK: return "ok";
+    case STOF_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or bad enum)";
+    case STOF_ERR_SHAPE: return "bad shape (inconsistent sizes, not tile-divisible, or too large)";
+    case STOF_ERR_DTYPE: return "unknown element type";
+    case STOF_ERR_ALIGNMENT: return "pointer not aligned as required";
+    case STOF_ERR_WORKSPACE: return "workspace too small";
+    case STOF_ERR_UNSUPPORTED: return "unsupported configuration (head dim or tile size)";
+    case STOF_ERR_DEVICE: return "device-side error reported by a kernel";
+    case STOF_ERR_CUDA: return "CUDA runtime error";
+    case STOF_ERR_NOT_SYNCED: return "format counts not synced to the host";
+  }
+  return "unknown status";
+}
+
+size_t stof_encode_workspace_bytes(int n_masks, int lq, int lk, int bm, int bn) {
+  EncodeGeom g;
+  if (!encode_geometry(n_masks, lq, lk, bm, bn, &g)) return 0;
+  return workspace_layout(g).total;
+}
+
+stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, int bm, int bn,
+                             void* workspace, size_t ws_bytes, stof_format* fmt, void* stream) {
+  if (!mask || !workspace || !fmt) return STOF_ERR_INVALID_ARG;
+  if (n_masks < 1 || lq < 1 || lk < 1 || bm < 1 || bn < 1) return STOF_ERR_INVALID_ARG;
+  EncodeGeom g;
+  if (!encode_geometry(n_masks, lq, lk, bm, bn, &g)) return STOF_ERR_SHAPE;
+  if (!aligned(mask, 8) || !aligned(workspace, 256)) return STOF_ERR_ALIGNMENT;
+  const WorkspaceLayout w = workspace_layout(g);
+  if (ws_bytes < w.total) return STOF_ERR_WORKSPACE;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  stof_format f;
+  std::memset(&f, 0, sizeof(f));
+  f.n_masks = n_masks;
+  f.lq = lq;
+  f.lk = lk;
+  f.bm = bm;
+  f.bn = bn;
+  f.n_tr = g.n_tr;
+  f.n_tc = g.n_tc;
+  f.synced = 0;
+  f.counts_dev = reinterpret_cast<int64_t*>(ws + w.counts);
+  f.scratch = ws + w.ticket;
+  f.full_row_ptr = reinterpret_cast<int32_t*>(ws + w.full_row_ptr);
+  f.part_row_ptr = reinterpret_cast<int32_t*>(ws + w.part_row_ptr);
+  f.full_col_idx = reinterpret_cast<int32_t*>(ws + w.full_col_idx);
+  f.part_col_idx = reinterpret_cast<int32_t*>(ws + w.part_col_idx);
+  f.bitmaps = reinterpret_cast<uint64_t*>(ws + w.bitmaps);
+  *fmt = f;
+
+  cudaStream_t s = as_stream(stream);
+  // counts, ticket and look-back state start at zero
+  if (cudaMemsetAsync(ws + w.counts, 0, w.zero_bytes, s) != cudaSuccess) return STOF_ERR_CUDA;
+  EncodeParams p;
+  p.mask = mask;
+  p.lq = lq;
+  p.lk = lk;
+  p.bm = bm;
+  p.bn = bn;
+  p.n_tr = g.n_tr;
+  p.n_tc = g.n_tc;
+  p.ct = g.ct;
+  p.cpr = g.cpr;
+  p.n_rows = g.n_rows;
+  p.n_chunks = g.n_chunks;
+  p.full_row_ptr = f.full_row_ptr;
+  p.full_col_idx = f.full_col_idx;
+  p.part_row_ptr = f.part_row_ptr;
+  p.part_col_idx = f.part_col_idx;
+  p.bitmaps = f.bitmaps;
+  p.counts = f.counts_dev;
+  p.ticket = reinterpret_cast<unsigned long long*>(ws + w.ticket);
+  p.status = reinterpret_cast<unsigned long long*>(ws + w.status);
+  if (launch_encode(p, g, s) != cudaSuccess) return STOF_ERR_CUDA;
+  return STOF_OK;
+}
+
+stof_status stof_format_sync(stof_format* fmt, void* stream) {
+  if (!fmt || !fmt->counts_dev) return STOF_ERR_INVALID_ARG;
+  int64_t c[4] = {0, 0, 0, 0};
+  cudaStream_t s = as_stream(stream);
+  if (cudaMemcpyAsync(c, fmt->counts_dev, sizeof(c), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return STOF_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return STOF_ERR_CUDA;
+  fmt->n_full = c[0];
+  fmt->n_part = c[1];
+  fmt->nnz = c[2];
+  fmt->device_error = c[3];
+  fmt->synced = 1;
+  return c[3] ? STOF_ERR_DEVICE : STOF_OK;
+}
+
+// Analytic kernel choice ("Accelerating Sparse Transformer Inference on
+// GPU", gist.science technical summary, Methodology 1: an analytical model
+// chooses the row-wise or block-wise kernel from mask sparsity and
+// sequence length).
+//
+// Cost per query row, in ns, of each kernel:
+//   row-wise   T_row = A_ROW + rho * L * d * C_ROW
+//              (visits exactly the rho*L valid keys with CUDA-core dot
+//              products and K/V gathers);
+//   block-wise T_blk = A_BLK + L * d * C_BLK
+//              (dense tensor-core work on the tiles it lists; with no tile
+//              statistics at hand the model takes the worst case for an
+//              arbitrary mask, every tile listed, i.e. L keys per row).
+// The row-wise kernel wins for small rho (high sparsity) and short L, the
+// regime the pages give it.  The constants are per-query-row costs fitted
+// once on a GB300 from both kernels' times on the five workloads and are
+// frozen here, so the choice is a deterministic function of (rho, L, d).
+stof_kernel stof_select_kernel(double density, int seq_len, int head_dim) {
+  if (!(density >= 0.0 && density <= 1.0) || seq_len <= 0 || head_dim <= 0)
+    return STOF_KERNEL_BLOCKWISE;
+  const double A_ROW = 0.0, C_ROW = 2.0e-4;  // ns per (key * dim)
+  const double A_BLK = 4.0, C_BLK = 1.0e-5;
+  const double L = seq_len, d = head_dim;
+  const double t_row = A_ROW + density * L * d * C_ROW;
+  const double t_blk = A_BLK + L * d * C_BLK;
+  return t_row <= t_blk ? STOF_KERNEL_ROWWISE : STOF_KERNEL_BLOCKWISE;
+}
+
+stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H,
+                         int L, int d, float scale, const stof_format* fmt,
+                         int64_t mask_stride_b, int64_t mask_stride_h, stof_kernel which, void* o,
+                         void* stream) {
+  if (!q || !k || !v || !o || !fmt) return STOF_ERR_INVALID_ARG;
+  if (!fmt->full_row_ptr || !fmt->full_col_idx || !fmt->part_row_ptr || !fmt->part_col_idx ||
+      !fmt->bitmaps || !fmt->counts_dev)
+    return STOF_ERR_INVALID_ARG;
+  if (dt != STOF_F16 && dt != STOF_BF16) return STOF_ERR_DTYPE;
+  if (which != STOF_KERNEL_AUTO && which != STOF_KERNEL_ROWWISE && which != STOF_KERNEL_BLOCKWISE)
+    return STOF_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || L < 1 || d < 1) return STOF_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return STOF_ERR_INVALID_ARG;
+  if (mask_stride_b < 0 || mask_stride_h < 0) return STOF_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return STOF_ERR_UNSUPPORTED;
+  if (fmt->lq != L || fmt->lk != L) return STOF_ERR_SHAPE;
+  if (fmt->bm < 8 || fmt->bn < 8 || fmt->bm % 8 || fmt->bn % 8 || fmt->bm > 256 || fmt->bn > 256 ||
+      L % fmt->bm || L % fmt->bn || fmt->n_tr != L / fmt->bm || fmt->n_tc != L / fmt->bn)
+    return STOF_ERR_SHAPE;
+  const long double max_mask = static_cast<long double>(B - 1) * mask_stride_b +
+                               static_cast<long double>(H - 1) * mask_stride_h;
+  if (max_mask >= fmt->n_masks) return STOF_ERR_SHAPE;
+  if (static_cast<long double>(B) * H * L >= 2147483647.0L * 8) return STOF_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return STOF_ERR_ALIGNMENT;
+
+  stof_kernel kern = which;
+  if (kern == STOF_KERNEL_AUTO) {
+    if (!fmt->synced) return STOF_ERR_NOT_SYNCED;
+    const double density =
+        static_cast<double>(fmt->nnz) / (static_cast<double>(fmt->n_masks) * fmt->lq * fmt->lk);
+    kern = stof_select_kernel(density, L, d);
+    if (kern == STOF_KERNEL_BLOCKWISE && (fmt->bm != 128 || fmt->bn != 128))
+      kern = STOF_KERNEL_ROWWISE;  // the block-wise kernel needs 128 x 128 OTs
+  }
+  if (kern == STOF_KERNEL_BLOCKWISE && (fmt->bm != 128 || fmt->bn != 128))
+    return STOF_ERR_UNSUPPORTED;
+
+  AttnParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.B = B;
+  p.H = H;
+  p.L = L;
+  p.d = d;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.bm = fmt->bm;
+  p.bn = fmt->bn;
+  p.n_tr = fmt->n_tr;
+  p.n_tc = fmt->n_tc;
+  p.stride_b = mask_stride_b;
+  p.stride_h = mask_stride_h;
+  p.full_row_ptr = fmt->full_row_ptr;
+  p.full_col_idx = fmt->full_col_idx;
+  p.part_row_ptr = fmt->part_row_ptr;
+  p.part_col_idx = fmt->part_col_idx;
+  p.bitmaps = fmt->bitmaps;
+  p.err = fmt->counts_dev + 3;
+  const bool bf16 = dt == STOF_BF16;
+  cudaStream_t s = as_stream(stream);
+  if (kern == STOF_KERNEL_ROWWISE)
+    return launch_rowwise(p, bf16, s) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
+  return launch_blockwise(p, bf16, s);
+}
+
+}  // extern "C"

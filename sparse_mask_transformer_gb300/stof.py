@@ -1,0 +1,205 @@
+"""Python binding of libstof.so (include/stof.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of the method: it takes torch tensors (used only as device
+memory) and the current CUDA stream, passes raw pointers through ctypes,
+and raises StofError on a non-OK status.  The library must have been built
+(``python -m sparse_mask_transformer_gb300.build``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libstof.so")
+SYNTH_LIB_PATH = os.path.join(_PKG, "libstof_synth.so")
+
+STOF_OK = 0
+STOF_ERR_INVALID_ARG = 1
+STOF_ERR_SHAPE = 2
+STOF_ERR_DTYPE = 3
+STOF_ERR_ALIGNMENT = 4
+STOF_ERR_WORKSPACE = 5
+STOF_ERR_UNSUPPORTED = 6
+STOF_ERR_DEVICE = 7
+STOF_ERR_CUDA = 8
+STOF_ERR_NOT_SYNCED = 9
+
+STOF_F16 = 0
+STOF_BF16 = 1
+
+STOF_KERNEL_AUTO = -1
+STOF_KERNEL_ROWWISE = 0
+STOF_KERNEL_BLOCKWISE = 1
+
+STOF_DEVERR_LOOKBACK_TIMEOUT = 0x1
+STOF_DEVERR_PIPE_TIMEOUT = 0x2
+STOF_DEVERR_BAD_FORMAT = 0x4
+
+EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync",
+            "stof_select_kernel", "stof_mha_fwd", "stof_status_string", "stof_version"]
+
+
+class StofError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({stof_status_string(status)})")
+
+
+class stof_format(ctypes.Structure):
+    _fields_ = [
+        ("n_masks", ctypes.c_int32), ("lq", ctypes.c_int32), ("lk", ctypes.c_int32),
+        ("bm", ctypes.c_int32), ("bn", ctypes.c_int32), ("n_tr", ctypes.c_int32),
+        ("n_tc", ctypes.c_int32), ("synced", ctypes.c_int32),
+        ("full_row_ptr", ctypes.c_void_p), ("full_col_idx", ctypes.c_void_p),
+        ("part_row_ptr", ctypes.c_void_p), ("part_col_idx", ctypes.c_void_p),
+        ("bitmaps", ctypes.c_void_p), ("counts_dev", ctypes.c_void_p), ("scratch", ctypes.c_void_p),
+        ("n_full", ctypes.c_int64), ("n_part", ctypes.c_int64), ("nnz", ctypes.c_int64),
+        ("device_error", ctypes.c_int64),
+    ]
+
+
+_lib = None
+_synth = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libstof.so once; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with python -m sparse_mask_transformer_gb300.build")
+        lib = ctypes.CDLL(path)
+        P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        lib.stof_encode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        lib.stof_encode_workspace_bytes.restype = sz
+        lib.stof_encode_mask.argtypes = [P, i32, i32, i32, i32, i32, P, sz, ctypes.POINTER(stof_format), P]
+        lib.stof_encode_mask.restype = i32
+        lib.stof_format_sync.argtypes = [ctypes.POINTER(stof_format), P]
+        lib.stof_format_sync.restype = i32
+        lib.stof_select_kernel.argtypes = [ctypes.c_double, i32, i32]
+        lib.stof_select_kernel.restype = i32
+        lib.stof_mha_fwd.argtypes = [P, P, P, i32, i32, i32, i32, i32, ctypes.c_float,
+                                     ctypes.POINTER(stof_format), i64, i64, i32, P, P]
+        lib.stof_mha_fwd.restype = i32
+        lib.stof_status_string.argtypes = [i32]
+        lib.stof_status_string.restype = ctypes.c_char_p
+        lib.stof_version.argtypes = []
+        lib.stof_version.restype = i32
+        _lib = lib
+    return _lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, where: str):
+    if status != STOF_OK:
+        raise StofError(status, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return STOF_F16
+    if t.dtype == torch.bfloat16:
+        return STOF_BF16
+    raise StofError(STOF_ERR_DTYPE, f"tensor dtype {t.dtype}")
+
+
+def stof_version() -> int:
+    return load_library().stof_version()
+
+
+def stof_status_string(status: int) -> str:
+    return load_library().stof_status_string(int(status)).decode()
+
+
+def stof_encode_workspace_bytes(n_masks: int, lq: int, lk: int, bm: int, bn: int) -> int:
+    return int(load_library().stof_encode_workspace_bytes(n_masks, lq, lk, bm, bn))
+
+
+def stof_encode_mask(mask: torch.Tensor, bm: int, bn: int, workspace: torch.Tensor,
+                     fmt: stof_format | None = None, stream=None) -> stof_format:
+    """mask: device uint8/bool [n_masks, lq, lk]; workspace: device uint8 tensor."""
+    if mask.dim() != 3 or not mask.is_contiguous() or mask.element_size() != 1:
+        raise StofError(STOF_ERR_SHAPE, "stof_encode_mask: mask must be contiguous 1-byte [n_masks, lq, lk]")
+    fmt = fmt if fmt is not None else stof_format()
+    n_masks, lq, lk = mask.shape
+    _check(load_library().stof_encode_mask(
+        mask.data_ptr(), n_masks, lq, lk, bm, bn, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), ctypes.byref(fmt), _stream(stream)),
+        "stof_encode_mask")
+    return fmt
+
+
+def stof_format_sync(fmt: stof_format, stream=None) -> stof_format:
+    _check(load_library().stof_format_sync(ctypes.byref(fmt), _stream(stream)), "stof_format_sync")
+    return fmt
+
+
+def stof_select_kernel(density: float, seq_len: int, head_dim: int) -> int:
+    return int(load_library().stof_select_kernel(float(density), int(seq_len), int(head_dim)))
+
+
+def stof_mha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: stof_format, scale: float,
+                 mask_stride_b: int, mask_stride_h: int, which: int, o: torch.Tensor,
+                 stream=None) -> torch.Tensor:
+    """q, k, v, o: device [B, H, L, d] fp16/bf16, contiguous."""
+    if q.dim() != 4:
+        raise StofError(STOF_ERR_SHAPE, "stof_mha_fwd: q must be [B, H, L, d]")
+    for t in (q, k, v, o):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise StofError(STOF_ERR_SHAPE, "stof_mha_fwd: q, k, v, o must match and be contiguous")
+    B, H, L, d = q.shape
+    _check(load_library().stof_mha_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), _dtype_code(q), B, H, L, d, float(scale),
+        ctypes.byref(fmt), int(mask_stride_b), int(mask_stride_h), int(which), o.data_ptr(),
+        _stream(stream)), "stof_mha_fwd")
+    return o
+
+
+def format_arrays(fmt: stof_format, workspace: torch.Tensor, n_full: int | None = None,
+                  n_part: int | None = None) -> dict:
+    """Device views of the format's arrays (slices of the workspace tensor);
+    counts default to the synced host copies."""
+    base = workspace.data_ptr()
+    n_rows = fmt.n_masks * fmt.n_tr
+    n_full = fmt.n_full if n_full is None else n_full
+    n_part = fmt.n_part if n_part is None else n_part
+    wpt = (fmt.bm // 8) * (fmt.bn // 8)
+
+    def view(ptr, count, dtype, esize):
+        off = ptr - base
+        return workspace[off:off + count * esize].view(dtype)
+
+    return dict(
+        full_row_ptr=view(fmt.full_row_ptr, n_rows + 1, torch.int32, 4),
+        part_row_ptr=view(fmt.part_row_ptr, n_rows + 1, torch.int32, 4),
+        full_col_idx=view(fmt.full_col_idx, n_full, torch.int32, 4),
+        part_col_idx=view(fmt.part_col_idx, n_part, torch.int32, 4),
+        bitmaps=view(fmt.bitmaps, n_part * wpt, torch.int64, 8).view(n_part, fmt.bm // 8, fmt.bn // 8),
+    )
+
+
+def stof_synth_causal_bernoulli_mask(out: torch.Tensor, n_masks: int, L: int, seed: int,
+                                     threshold: int, stream=None) -> torch.Tensor:
+    """Device generator of seeded causal-Bernoulli masks (libstof_synth.so)."""
+    global _synth
+    if _synth is None:
+        if not os.path.exists(SYNTH_LIB_PATH):
+            raise RuntimeError(f"{SYNTH_LIB_PATH} is missing: build it first")
+        _synth = ctypes.CDLL(SYNTH_LIB_PATH)
+        _synth.stof_synth_causal_bernoulli_mask.argtypes = [
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p]
+        _synth.stof_synth_causal_bernoulli_mask.restype = ctypes.c_int
+    assert out.numel() == n_masks * L * L and out.element_size() == 1 and out.is_contiguous()
+    rc = _synth.stof_synth_causal_bernoulli_mask(out.data_ptr(), n_masks, L, seed, threshold, _stream(stream))
+    if rc != 0:
+        raise RuntimeError(f"stof_synth_causal_bernoulli_mask failed: {rc}")
+    return out

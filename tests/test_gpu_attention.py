@@ -1,0 +1,145 @@
+"""Masked MHA forward on the GPU (both kernels, forced and automatic)
+against the fp64 CPU oracle ("Accelerating Sparse Transformer Inference on
+GPU", gist.science technical summary, Methodology 1: exact masking;
+row-wise and block-wise kernels).  Tolerance: max |O - O_oracle| <= 2e-3
+for fp16 inputs and <= 1.5e-2 for bf16 inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_mask_transformer_gb300 import stof, synth
+from tests.conftest import TOL, gpu_encode
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = {"row": stof.STOF_KERNEL_ROWWISE, "block": stof.STOF_KERNEL_BLOCKWISE}
+
+
+def _run(q, k, v, mask_dev, bm, bn, sb, sh, which, scale=None):
+    B, H, L, d = q.shape
+    fmt, ws, _ = gpu_encode(mask_dev, bm, bn)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full_like(qd, float("nan"))
+    scale = 1 / math.sqrt(d) if scale is None else scale
+    stof.stof_mha_fwd(qd, kd, vd, fmt, scale, sb, sh, which, o)
+    torch.cuda.synchronize()
+    return o.cpu(), fmt
+
+
+def _check(o_gpu, q, k, v, mask_of, dtype, heads=None, rows=None, scale=None):
+    B, H, L, d = q.shape
+    scale = 1 / math.sqrt(d) if scale is None else scale
+    q64, k64, v64 = (synth.to_float64(t) for t in (q, k, v))
+    ref = oracle.attention_bhld(q64, k64, v64, mask_of, scale, heads=heads, rows=rows)
+    og = o_gpu.double().numpy()
+    worst = 0.0
+    for (b, h), o_ref in ref.items():
+        got = og[b, h] if rows is None else og[b, h, rows]
+        assert np.all(np.isfinite(got))
+        worst = max(worst, float(np.abs(got - o_ref).max()))
+    assert worst <= TOL[dtype], f"max abs error {worst} > {TOL[dtype]}"
+    return worst
+
+
+def _mask_of_np(mask, sb, sh):
+    return lambda b, h, rows: mask[b * sb + h * sh][rows]
+
+
+@pytest.mark.parametrize("kern", ["row", "block"])
+@pytest.mark.parametrize("name", ["window48_L256", "bigbird_L512", "causal_L2048", "longformer_L4096"])
+def test_workloads_full_size(gpu_lib, name, kern):
+    w = synth.WORKLOADS[name]
+    mask = synth.make_mask(w)
+    q, k, v = synth.make_qkv(w.B, w.H, w.L, w.d, w.dtype, seed=w.seed)
+    o, fmt = _run(q, k, v, torch.from_numpy(mask).cuda(), 128, 128, w.stride_b, w.stride_h, KERNELS[kern])
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    if len(heads) > 6:  # oracle on a seeded sample of heads; the GPU ran them all
+        idx = np.random.default_rng(1).choice(len(heads), 6, replace=False)
+        heads = [heads[i] for i in sorted(idx)]
+    _check(o, q, k, v, _mask_of_np(mask, w.stride_b, w.stride_h), w.dtype, heads=heads)
+    assert fmt.device_error == 0
+
+
+@pytest.mark.parametrize("kern", ["row", "block"])
+def test_bernoulli_L16384_full_size_sampled(gpu_lib, kern):
+    w = synth.WORKLOADS["bernoulli_L16384"]
+    L = w.L
+    mask = torch.empty(w.n_masks, L, L, dtype=torch.uint8, device="cuda")
+    stof.stof_synth_causal_bernoulli_mask(mask, w.n_masks, L, w.seed,
+                                          synth.bernoulli_threshold(synth.BERNOULLI_P))
+    q, k, v = synth.make_qkv(w.B, w.H, w.L, w.d, w.dtype, seed=w.seed)
+    o, fmt = _run(q, k, v, mask, 128, 128, w.stride_b, w.stride_h, KERNELS[kern])
+    del mask
+    torch.cuda.empty_cache()
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([np.arange(64), rng.integers(0, L, 192), [L - 1]]))
+    heads = [(0, 0), (0, 17), (0, 31)]
+    _check(o, q, k, v, lambda b, h, r: synth.mask_rows(w, b * w.stride_b + h * w.stride_h, r),
+           w.dtype, heads=heads, rows=rows)
+
+
+@pytest.mark.parametrize("kern", ["row", "block"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("density", [0.02, 0.3, 0.9])
+def test_random_masks_small(gpu_lib, kern, d, dtype, density):
+    # several OTs per row and column, per-head masks, a fully masked row
+    B, H, L = 2, 3, 384
+    mask = synth.random_mask(B * H, L, L, density, seed=d + int(density * 100))
+    mask[1, 5] = 0
+    mask[2, :, :200] = 0          # empty and partly-empty tile columns
+    q, k, v = synth.make_qkv(B, H, L, d, dtype, seed=3)
+    o, _ = _run(q, k, v, torch.from_numpy(mask).cuda(), 128, 128, H, 1, KERNELS[kern])
+    _check(o, q, k, v, _mask_of_np(mask, H, 1), dtype)
+    assert torch.all(o[0, 1, 5] == 0)
+
+
+@pytest.mark.parametrize("bm,bn", [(16, 16), (64, 32), (8, 8)])
+def test_rowwise_other_tile_sizes(gpu_lib, bm, bn):
+    B, H, L, d = 1, 2, 256, 64
+    mask = synth.random_mask(1, L, L, 0.2, seed=bm + bn)
+    q, k, v = synth.make_qkv(B, H, L, d, "fp16", seed=4)
+    o, _ = _run(q, k, v, torch.from_numpy(mask).cuda(), bm, bn, 0, 0, stof.STOF_KERNEL_ROWWISE)
+    _check(o, q, k, v, _mask_of_np(mask, 0, 0), "fp16")
+
+
+@pytest.mark.parametrize("kern", ["row", "block"])
+def test_edge_cases(gpu_lib, kern):
+    B, H, L, d = 1, 4, 256, 128
+    q, k, v = synth.make_qkv(B, H, L, d, "bf16", seed=6)
+    q = (q.float() * 8).to(torch.bfloat16)  # sharp softmax
+    masks = np.zeros((4, L, L), np.uint8)
+    masks[0] = 1                                       # all valid: dense attention
+    js = np.random.default_rng(7).integers(0, L, L)
+    masks[1, np.arange(L), js] = 1                     # one valid key per row
+    masks[2, :128] = 0                                 # first OT row empty
+    masks[2, 128:, 5] = 1
+    # mask 3 all zero: every row fully masked
+    o, _ = _run(q, k, v, torch.from_numpy(masks).cuda(), 128, 128, 0, 1, KERNELS[kern])
+    assert torch.equal(o[0, 1], v[0, 1, js])           # exactly that V row
+    assert torch.all(o[0, 2, :128] == 0)
+    assert torch.equal(o[0, 2, 128:], v[0, 2, 5].expand(128, d))
+    assert torch.all(o[0, 3] == 0)
+    _check(o, q, k, v, _mask_of_np(masks, 0, 1), "bf16", heads=[(0, 0)])
+
+
+def test_auto_selection_runs_the_selected_kernel(gpu_lib):
+    w = synth.WORKLOADS["window48_L256"]
+    mask = torch.from_numpy(synth.make_mask(w)).cuda()
+    q, k, v = synth.make_qkv(w.B, w.H, w.L, w.d, w.dtype)
+    o, fmt = _run(q, k, v, mask, 128, 128, 0, 0, stof.STOF_KERNEL_AUTO)
+    _check(o, q, k, v, lambda b, h, r: mask.cpu().numpy()[0][r], w.dtype)
+    assert fmt.synced == 1
+
+
+def test_unsynced_auto_is_refused(gpu_lib):
+    mask = torch.ones(1, 128, 128, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(stof.stof_encode_workspace_bytes(1, 128, 128, 128, 128), dtype=torch.uint8, device="cuda")
+    fmt = stof.stof_encode_mask(mask, 128, 128, ws)
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(stof.StofError) as e:
+        stof.stof_mha_fwd(q, q, q, fmt, 0.125, 0, 0, stof.STOF_KERNEL_AUTO, q.clone())
+    assert e.value.status == stof.STOF_ERR_NOT_SYNCED

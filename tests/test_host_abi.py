@@ -1,0 +1,157 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched): the
+library loads, exports every function its headers declare, sizes the
+workspace, selects kernels deterministically, and rejects bad arguments
+with a status before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_mask_transformer_gb300 import build as stof_build
+from sparse_mask_transformer_gb300 import stof
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    stof_build.build()
+    return stof.load_library()
+
+
+def _declared(header):
+    text = open(os.path.join(ROOT, "include", header)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(stof_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared("stof.h")
+    assert set(stof.EXPORTED) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    synth = ctypes.CDLL(stof.SYNTH_LIB_PATH)
+    for n in _declared("stof_synth.h"):
+        assert hasattr(synth, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert stof.stof_version() == 1
+    for s in range(10):
+        assert stof.stof_status_string(s)
+    assert "unknown" in stof.stof_status_string(99)
+
+
+def test_struct_layout_matches_header(lib):
+    # int32 x 8, 7 pointers, int64 x 4
+    assert ctypes.sizeof(stof.stof_format) == 8 * 4 + 7 * 8 + 4 * 8
+
+
+def test_workspace_bytes(lib):
+    ws = stof.stof_encode_workspace_bytes
+    # 16384^2 x 32 masks at 128x128: 524288 tiles x (2 KB bitmap + 8 B indices) + row pointers
+    n = ws(32, 16384, 16384, 128, 128)
+    tiles = 32 * 128 * 128
+    assert tiles * (2048 + 8) <= n <= tiles * (2048 + 8) + (1 << 20)
+    assert ws(1, 256, 256, 16, 16) > 0
+    assert ws(1, 250, 256, 16, 16) == 0      # lq not a multiple of bm
+    assert ws(1, 256, 256, 12, 16) == 0      # bm not a multiple of 8
+    assert ws(1, 512, 512, 512, 128) == 0    # bm above 256
+    assert ws(0, 256, 256, 16, 16) == 0
+
+
+def test_select_kernel_is_deterministic_and_monotone(lib):
+    sel = stof.stof_select_kernel
+    assert sel(0.17, 256, 64) == sel(0.17, 256, 64)
+    # invalid input -> block-wise
+    assert sel(-0.1, 256, 64) == stof.STOF_KERNEL_BLOCKWISE
+    assert sel(float("nan"), 256, 64) == stof.STOF_KERNEL_BLOCKWISE
+    assert sel(0.5, 0, 64) == stof.STOF_KERNEL_BLOCKWISE
+    # denser masks never flip the choice back to row-wise
+    for L in (256, 1024, 4096, 16384):
+        seen_block = False
+        for i in range(101):
+            k = sel(i / 100, L, 64)
+            if k == stof.STOF_KERNEL_BLOCKWISE:
+                seen_block = True
+            else:
+                assert not seen_block
+    assert sel(1.0, 4096, 128) == stof.STOF_KERNEL_BLOCKWISE
+
+
+FAKE = 1 << 20  # never dereferenced: every call below fails validation first
+
+
+def _encode(lib, **kw):
+    a = dict(mask=FAKE, n_masks=1, lq=256, lk=256, bm=128, bn=128, ws=FAKE, ws_bytes=1 << 30)
+    a.update(kw)
+    fmt = stof.stof_format()
+    return lib.stof_encode_mask(a["mask"], a["n_masks"], a["lq"], a["lk"], a["bm"], a["bn"],
+                                a["ws"], a["ws_bytes"], ctypes.byref(fmt), None)
+
+
+def test_encode_rejects_bad_arguments(lib):
+    assert _encode(lib, mask=None) == stof.STOF_ERR_INVALID_ARG
+    assert _encode(lib, ws=None) == stof.STOF_ERR_INVALID_ARG
+    assert _encode(lib, n_masks=0) == stof.STOF_ERR_INVALID_ARG
+    assert _encode(lib, lq=200) == stof.STOF_ERR_SHAPE
+    assert _encode(lib, bm=12) == stof.STOF_ERR_SHAPE
+    assert _encode(lib, bn=512) == stof.STOF_ERR_SHAPE
+    assert _encode(lib, mask=FAKE + 4) == stof.STOF_ERR_ALIGNMENT
+    assert _encode(lib, ws=FAKE + 128) == stof.STOF_ERR_ALIGNMENT
+    assert _encode(lib, ws_bytes=1000) == stof.STOF_ERR_WORKSPACE
+    assert lib.stof_encode_mask(FAKE, 1, 256, 256, 128, 128, FAKE, 1 << 30, None, None) == \
+        stof.STOF_ERR_INVALID_ARG
+
+
+def _fake_format(L=256, bm=128, bn=128, n_masks=1, synced=0):
+    f = stof.stof_format()
+    f.n_masks, f.lq, f.lk, f.bm, f.bn = n_masks, L, L, bm, bn
+    f.n_tr, f.n_tc = L // bm, L // bn
+    for name in ("full_row_ptr", "full_col_idx", "part_row_ptr", "part_col_idx", "bitmaps",
+                 "counts_dev", "scratch"):
+        setattr(f, name, FAKE)
+    f.synced = synced
+    return f
+
+
+def _mha(lib, fmt=None, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dt=stof.STOF_BF16, B=1, H=2, L=256, d=64, scale=0.125,
+             sb=0, sh=0, which=stof.STOF_KERNEL_ROWWISE, o=FAKE)
+    a.update(kw)
+    fmt = fmt if fmt is not None else _fake_format()
+    return lib.stof_mha_fwd(a["q"], a["k"], a["v"], a["dt"], a["B"], a["H"], a["L"], a["d"],
+                            a["scale"], ctypes.byref(fmt), a["sb"], a["sh"], a["which"], a["o"], None)
+
+
+def test_mha_rejects_bad_arguments(lib):
+    assert _mha(lib, q=None) == stof.STOF_ERR_INVALID_ARG
+    assert _mha(lib, o=None) == stof.STOF_ERR_INVALID_ARG
+    assert _mha(lib, dt=7) == stof.STOF_ERR_DTYPE
+    assert _mha(lib, which=5) == stof.STOF_ERR_INVALID_ARG
+    assert _mha(lib, B=0) == stof.STOF_ERR_INVALID_ARG
+    assert _mha(lib, scale=float("inf")) == stof.STOF_ERR_INVALID_ARG
+    assert _mha(lib, sb=-1) == stof.STOF_ERR_INVALID_ARG
+    assert _mha(lib, d=96) == stof.STOF_ERR_UNSUPPORTED
+    assert _mha(lib, L=512) == stof.STOF_ERR_SHAPE                 # format is for L = 256
+    assert _mha(lib, sh=1) == stof.STOF_ERR_SHAPE                  # head 1 -> mask 1 of 1
+    assert _mha(lib, q=FAKE + 8) == stof.STOF_ERR_ALIGNMENT
+    assert _mha(lib, which=stof.STOF_KERNEL_AUTO) == stof.STOF_ERR_NOT_SYNCED
+    assert _mha(lib, fmt=_fake_format(bm=64, bn=64), which=stof.STOF_KERNEL_BLOCKWISE) == \
+        stof.STOF_ERR_UNSUPPORTED
+    f = _fake_format()
+    f.bitmaps = None
+    assert _mha(lib, fmt=f) == stof.STOF_ERR_INVALID_ARG
+    assert lib.stof_format_sync(None, None) == stof.STOF_ERR_INVALID_ARG
+
+
+def test_binding_checks_shapes_before_calling(lib):
+    import torch
+    q = torch.zeros(1, 2, 256, 64, dtype=torch.bfloat16)
+    o = torch.zeros(1, 2, 256, 32, dtype=torch.bfloat16)
+    with pytest.raises(stof.StofError):
+        stof.stof_mha_fwd(q, q, q, _fake_format(), 0.1, 0, 0, 0, o, stream=0)
+    with pytest.raises(stof.StofError):
+        stof.stof_mha_fwd(q.float(), q.float(), q.float(), _fake_format(), 0.1, 0, 0, 0, q.float(),
+                          stream=0)
