@@ -1,7 +1,429 @@
-// Block-wise masked attention kernel (tcgen05 / TMEM / TMA).  Placeholder
-// until the kernel lands: reports the configuration as unsupported.
+// Block-wise masked attention kernel for sm_103a (TMA + tcgen05 + TMEM).
+//
+// "Accelerating Sparse Transformer Inference on GPU" (gist.science technical
+// summary), Methodology 1, dual-kernel strategy, block-wise kernel: Q, K and
+// V are split into sub-blocks staged in shared memory by asynchronous
+// copies that overlap data movement with compute; only outer tiles (OT)
+// listed in the two-level format are opened, full OTs without a mask test
+// and partial OTs through their 8x8 inner-tile bitmaps (same section,
+// two-level storage format: exact masking).
+//
+// One CTA computes one 128-row query tile (b, h, OT row I):
+//   warp 0      TMA producer: the Q tile once, then for each listed OT its
+//               K and V tiles (and, for a partial OT, its 2 KB of IT
+//               bitmaps) into an NS-stage shared-memory ring;
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma:
+//               S[t%2] = Q K_t^T (fp32 in TMEM), and O += P[t%2] V_t with
+//               P read from TMEM;
+//   warps 2..5  softmax warpgroup, one thread per query row: reads its S
+//               row from TMEM, applies the bitmap on partial OTs, runs the
+//               online softmax in fp32 (base 2), writes P (fp16/bf16) to
+//               TMEM, rescales O in TMEM when the running max moved by more
+//               than 2^8 (lazy rescaling, exact at the end because l uses
+//               the same reference max), and finally writes O / l (0 for a
+//               row without valid keys).
+// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512).
+// Every pipeline wait is bounded; on timeout the CTA raises
+// STOF_DEVERR_PIPE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace stof {
-stof_status launch_blockwise(const AttnParams&, bool, cudaStream_t) { return STOF_ERR_UNSUPPORTED; }
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.0f;     // log2 units
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
+
+template <int D>
+struct Cfg {
+  static constexpr int NS = D == 128 ? 2 : 4;       // K/V ring stages
+  static constexpr int REGIONS = D / 64;            // 128-byte swizzle atoms along d
+  static constexpr int TILE_BYTES = kBM * D * 2;    // one Q, K or V tile
+  static constexpr int BITMAP_WORDS = (kBM / 8) * (kBN / 8);
+};
+
+template <int D>
+struct alignas(1024) Smem {
+  uint8_t q[Cfg<D>::TILE_BYTES];
+  uint8_t k[Cfg<D>::NS][Cfg<D>::TILE_BYTES];
+  uint8_t v[Cfg<D>::NS][Cfg<D>::TILE_BYTES];
+  uint64_t bits[Cfg<D>::NS][Cfg<D>::BITMAP_WORDS];
+  uint64_t q_full;
+  uint64_t kv_full[Cfg<D>::NS];
+  uint64_t kv_free[Cfg<D>::NS];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+__device__ __forceinline__ void raise_error(int64_t* err, unsigned long long bit) {
+  atomicOr(reinterpret_cast<unsigned long long*>(err), bit);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    blockwise_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem<D>& s = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // work item: heaviest OT rows first for causal-like masks
+  const int BH = p.B * p.H;
+  const int I = p.n_tr - 1 - static_cast<int>(blockIdx.x / BH);
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int b = bh / p.H, h = bh % p.H;
+  const long long mrow = (b * p.stride_b + h * p.stride_h) * p.n_tr + I;
+  const int f0 = p.full_row_ptr[mrow];
+  const int nf = p.full_row_ptr[mrow + 1] - f0;
+  const int p0 = p.part_row_ptr[mrow];
+  const int np = p.part_row_ptr[mrow + 1] - p0;
+  const int n = nf + np;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&s.q_full, 1);
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(&s.kv_full[i], 1);
+      mbar_init(&s.kv_free[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.s_free[i], 128);
+      mbar_init(&s.p_full[i], 128);
+      mbar_init(&s.pv_done[i], 1);
+    }
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tbase = s.tmem_base;
+  const uint32_t tS0 = tbase, tO = tbase + 256, tP0 = tbase + 384;
+  volatile int* abort_flag = &s.abort_flag;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    raise_error(p.err, STOF_DEVERR_PIPE_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      const int qrow = bh * p.L + I * kBM;
+      mbar_arrive_expect_tx(&s.q_full, C::TILE_BYTES);
+#pragma unroll
+      for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow);
+      int issued = 0;
+      for (int t = 0; t < n; ++t) {
+        const int st = t % C::NS;
+        if (t >= C::NS && !mbar_wait(&s.kv_free[st], ((t / C::NS) - 1) & 1, abort_flag, kWaitNs)) {
+          fail();
+          break;
+        }
+        const bool partial = t >= nf;
+        const long long e = partial ? static_cast<long long>(p0) + (t - nf) : static_cast<long long>(f0) + t;
+        int J = partial ? p.part_col_idx[e] : p.full_col_idx[e];
+        if (J < 0 || J >= p.n_tc) {
+          raise_error(p.err, STOF_DEVERR_BAD_FORMAT);
+          J = 0;
+        }
+        const int krow = bh * p.L + J * kBN;
+        mbar_arrive_expect_tx(&s.kv_full[st], 2 * C::TILE_BYTES + (partial ? C::BITMAP_WORDS * 8 : 0));
+#pragma unroll
+        for (int r = 0; r < C::REGIONS; ++r) {
+          tma_load_2d(s.k[st] + r * 16384, &tmK, &s.kv_full[st], 64 * r, krow);
+          tma_load_2d(s.v[st] + r * 16384, &tmV, &s.kv_full[st], 64 * r, krow);
+        }
+        if (partial) bulk_load(s.bits[st], p.bitmaps + e * C::BITMAP_WORDS, C::BITMAP_WORDS * 8, &s.kv_full[st]);
+        issued = t + 1;
+      }
+      if (*abort_flag) {
+        // let every copy this thread started land before the CTA exits
+        mbar_wait_timeout(&s.q_full, 0, kWaitNs);
+        for (int t = issued - C::NS < 0 ? 0 : issued - C::NS; t < issued; ++t)
+          mbar_wait_timeout(&s.kv_full[t % C::NS], (t / C::NS) & 1, kWaitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(BF16 ? 1 : 0, 0, kBM, kBN);
+      constexpr uint32_t idesc_pv = idesc_f16(BF16 ? 1 : 0, 1, kBM, D);
+      const uint32_t q_addr = smem_u32(s.q);
+      auto issue_pv = [&](int u) -> bool {
+        if (!mbar_wait(&s.p_full[u & 1], (u >> 1) & 1, abort_flag, kWaitNs)) return false;
+        tc_fence_after();
+        const int st = u % C::NS;
+        const uint32_t v_addr = smem_u32(s.v[st]);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t bdesc = smem_desc_sw128(v_addr + kk * 2048, 16384, 1024);
+          mma_f16_ts(tO, tP0 + (u & 1) * 64 + kk * 8, bdesc, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&s.pv_done[u & 1]);
+        mma_commit(&s.kv_free[st]);
+        return true;
+      };
+      bool ok = true;
+      if (n > 0) ok = mbar_wait(&s.q_full, 0, abort_flag, kWaitNs);
+      for (int t = 0; ok && t < n; ++t) {
+        const int st = t % C::NS, sb = t & 1;
+        if (!mbar_wait(&s.kv_full[st], (t / C::NS) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+        if (t >= 2 && !mbar_wait(&s.s_free[sb], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(s.k[st]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_f16_ss(tS0 + sb * 128, smem_desc_sw128(q_addr + off, 16, 1024),
+                     smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s.s_full[sb]);
+        if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
+      }
+      if (ok && n > 0) ok = issue_pv(n - 1);
+      if (!ok) fail();
+      // all MMAs of this CTA complete before TMEM is released
+      mma_commit(&s.drain);
+      mbar_wait_timeout(&s.drain, 0, kWaitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c = p.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    // tcgen05.ld/st are warp-collective: every decision here is warp-uniform
+    auto wwait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitNs));
+    };
+    for (int t = 0; t < n; ++t) {
+      const int sb = t & 1;
+      if (!wwait(&s.s_full[sb], (t >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS0 + sb * 128 + lane_off + cc * 32, sr[cc]);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(sr[cc]);
+      tc_fence_before();
+      mbar_arrive(&s.s_free[sb]);
+
+      float mx = -INFINITY;
+      if (t >= nf) {  // partial OT: keep only the keys whose bit is set
+        // the bitmap bytes came by bulk copy: observe their arrival here too
+        if (!wwait(&s.kv_full[t % C::NS], (t / C::NS) & 1)) { ok = false; break; }
+        const uint64_t* bw = s.bits[t % C::NS] + (r >> 3) * (kBN / 8);
+        const int shift = (r & 7) * 8;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t bits32 = 0;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            bits32 |= (static_cast<uint32_t>(bw[4 * cc + u] >> shift) & 0xFFu) << (8 * u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x = (bits32 >> i) & 1u ? __uint_as_float(sr[cc][i]) : -INFINITY;
+            sr[cc][i] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[cc][i]));
+      }
+      const float mt = mx * c;
+      float alpha = 1.f;
+      if (mt > m_ref + kRescaleThreshold) {  // also the first finite max
+        alpha = ex2(m_ref - mt);             // 0 when m_ref = -inf
+        m_ref = mt;
+      }
+      l *= alpha;
+      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+      uint32_t plo[32], phi[32];  // P columns 0..63 and 64..127, two values per word
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float e0 = ex2(fmaf(__uint_as_float(sr[cc][i]), c, -mu));
+          const float e1 = ex2(fmaf(__uint_as_float(sr[cc][i + 1]), c, -mu));
+          ls0 += e0;
+          ls1 += e1;
+          if (cc < 2) plo[cc * 16 + i / 2] = pack2<BF16>(e0, e1);
+          else phi[(cc - 2) * 16 + i / 2] = pack2<BF16>(e0, e1);
+        }
+      l += ls0 + ls1;
+
+      // P buffer sb is free once PV of tile t-2 is done
+      if (t >= 2 && !wwait(&s.pv_done[sb], ((t - 2) >> 1) & 1)) { ok = false; break; }
+      if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O holds the sum up to tile t-1: wait for it, then rescale
+        if (!wwait(&s.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t orr[32];
+          tmem_ld32(tO + lane_off + cc * 32, orr);
+          tmem_ld_wait(orr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          tmem_st32(tO + lane_off + cc * 32, orr);
+        }
+      }
+      tc_fence_after();
+      tmem_st32(tP0 + sb * 64 + lane_off, plo);
+      tmem_st32(tP0 + sb * 64 + lane_off + 32, phi);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&s.p_full[sb]);
+    }
+    if (!ok) {
+      fail();
+    } else {
+      // epilogue: O / l, rounded to the input type; 0 for rows without keys
+      if (n > 0 && !wwait(&s.pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) {
+        fail();
+      } else {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint8_t* orow = static_cast<uint8_t*>(p.o) +
+                        (static_cast<size_t>(bh) * p.L + static_cast<size_t>(I) * kBM + r) * (D * 2);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t orr[32];
+          if (n > 0) {
+            tmem_ld32(tO + lane_off + cc * 32, orr);
+            tmem_ld_wait(orr);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = 0u;
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack2<BF16>(__uint_as_float(orr[2 * i]) * inv, __uint_as_float(orr[2 * i + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [rows][D] row-major 16-bit matrix, box = 64 columns x 128 rows, 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int D, bool bf16) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool BF16>
+stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
+  const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.L;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, p.q, rows, D, BF16) || !make_map(&mk, p.k, rows, D, BF16) ||
+      !make_map(&mv, p.v, rows, D, BF16))
+    return STOF_ERR_CUDA;
+  const size_t smem = sizeof(Smem<D>) + 1024;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(blockwise_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return STOF_ERR_CUDA;
+    attr_done = true;
+  }
+  const long long grid = static_cast<long long>(p.B) * p.H * p.n_tr;
+  blockwise_kernel<D, BF16><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
+}
+
+}  // namespace
+
+stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s) {
+  if (p.bm != kBM || p.bn != kBN) return STOF_ERR_UNSUPPORTED;
+  if (static_cast<long long>(p.B) * p.H * p.L >= (1ll << 31)) return STOF_ERR_SHAPE;
+  if (p.d == 64) return bf16 ? launch_bw<64, true>(p, s) : launch_bw<64, false>(p, s);
+  return bf16 ? launch_bw<128, true>(p, s) : launch_bw<128, false>(p, s);
+}
+
 }  // namespace stof
