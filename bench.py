@@ -1,0 +1,435 @@
+"""Benchmark of the STOF masked-attention hot path on GB300.
+
+One step = the whole hot path over one batch of synthetic input already
+resident in HBM: encode the dense mask into the two-level format, sync the
+tile counts, select the kernel analytically, run the masked MHA forward.
+Metric: effective TFLOP/s = 4 * d * (valid mask elements over all heads) /
+step time.  The default workload is the 16k one (B=1, H=32, L=16384,
+d=128, bf16, per-head causal AND Bernoulli(0.1) masks with the diagonal
+forced), the configuration the throughput target is quoted on.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, same metric
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs an
+independent replica of the workload on its own GPU (the path needs no
+exchange step); value = units of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_mask_transformer_gb300 import synth  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "masked-MHA fwd effective TFLOP/s (valid elems) and % of GB300 tensor peak"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("blockwise.cu", "sm100_ptx.cuh"):
+        with open(os.path.join(ROOT, "sparse_mask_transformer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the block-wise kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"blockwise_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not src or not tr or src.group(1) != kernel_source_hash():
+        return None
+    return float(tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if _cuda_ok() else "gloo"
+        dist.init_process_group(backend)
+        return rank, world, local, dist
+    return rank, world, local, None
+
+
+def _cuda_ok() -> bool:
+    import torch
+    return torch.cuda.is_available()
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, dist, device) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- inputs
+
+def device_inputs(w: synth.Workload, device):
+    import torch
+    from sparse_mask_transformer_gb300 import stof
+    if w.pattern == "causal_bernoulli":
+        mask = torch.empty(w.n_masks, w.L, w.L, dtype=torch.uint8, device=device)
+        stof.stof_synth_causal_bernoulli_mask(mask, w.n_masks, w.L, w.seed,
+                                              synth.bernoulli_threshold(synth.BERNOULLI_P))
+    else:
+        mask = torch.from_numpy(synth.make_mask(w)).to(device)
+    q, k, v = (t.to(device) for t in synth.make_qkv(w.B, w.H, w.L, w.d, w.dtype, seed=w.seed))
+    return mask, q, k, v
+
+
+def heads_per_mask(w: synth.Workload) -> float:
+    return w.B * w.H / w.n_masks
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args, w: synth.Workload):
+    import torch
+    from sparse_mask_transformer_gb300 import build, stof
+
+    rank, world, local, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    build.build()
+    stof.load_library()
+    peaks, peak_src = load_peaks()
+
+    mask, q, k, v = device_inputs(w, device)
+    o = torch.empty_like(q)
+    bm = bn = 128
+    ws = torch.empty(stof.stof_encode_workspace_bytes(w.n_masks, w.L, w.L, bm, bn), dtype=torch.uint8,
+                     device=device)
+    scale = 1.0 / math.sqrt(w.d)
+    stream = torch.cuda.current_stream(device)
+    fmt = stof.stof_format()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+
+    def step(i=None):
+        stof.stof_encode_mask(mask, bm, bn, ws, fmt)
+        stof.stof_format_sync(fmt)                   # counts to host: feeds the selector
+        if i is not None:
+            ev[i][0].record(stream)
+        stof.stof_mha_fwd(q, k, v, fmt, scale, w.stride_b, w.stride_h, stof.STOF_KERNEL_AUTO, o)
+        if i is not None:
+            ev[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    density = fmt.nnz / (w.n_masks * w.L * w.L)
+    chosen = stof.stof_select_kernel(density, w.L, w.d)
+    valid = fmt.nnz * heads_per_mask(w)
+    tiles = (fmt.n_full + fmt.n_part) * heads_per_mask(w)
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(i)
+        end.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    step_ms_local = start.elapsed_time(end) / args.steps
+    step_ms = max_over_ranks(step_ms_local, dist, device)
+    mha_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    mha_ms = max_over_ranks(mha_ms, dist, device)
+    clocks = clk.summary()
+
+    flops_eff = 4.0 * w.d * valid
+    flops_tile = 4.0 * w.d * 128 * 128 * tiles
+    total_units = sum_over_ranks(flops_eff, dist, device)
+    value = total_units / (step_ms * 1e-3) / 1e12
+
+    # end to end through the same public API with host buffers
+    e2e = run_e2e(args, w, mask, q, k, v, ws, fmt, scale, stream, device, dist)
+
+    kern_name = "blockwise" if chosen == stof.STOF_KERNEL_BLOCKWISE else "rowwise"
+    if chosen == stof.STOF_KERNEL_BLOCKWISE:
+        achieved = flops_tile / (mha_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roofline = {"bound": "tensor", "kernel": "blockwise_kernel", "achieved": round(achieved, 2),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "traffic": profiled_traffic(w.name), "peak_source": f"{peak_src} bf16 burst",
+                    "algorithmic": "4*d*128*128 FLOPs per listed outer tile per head"}
+    else:
+        bytes_alg = 4 * w.B * w.H * w.L * w.d * 2
+        achieved = bytes_alg / (mha_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roofline = {"bound": "hbm", "kernel": "rowwise_kernel", "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                    "peak_source": f"{peak_src} copy", "algorithmic": "Q+K+V+O bytes per launch"}
+
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded masks and N(0,1) Q/K/V)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "mask": w.describe,
+                   "outer_tile": "128x128", "kernel": kern_name, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (mask %.2f GB, Q/K/V %.2f GB)" % (
+                       w.mask_bytes / 1e9, 3 * q.numel() * 2 / 1e9)},
+        "breakdown": {"mha_ms": round(mha_ms, 4), "encode_and_sync_ms": round(step_ms - mha_ms, 4),
+                      "effective_tflops_mha_only": round(flops_eff / (mha_ms * 1e-3) / 1e12, 3),
+                      "tile_tflops": round(flops_tile / (mha_ms * 1e-3) / 1e12, 2),
+                      "pct_of_tensor_peak_tile": round(100 * flops_tile / (mha_ms * 1e-3) / 1e12 /
+                                                       peaks["bf16_tflops"], 2),
+                      "pct_of_tensor_peak_effective": round(100 * value / peaks["bf16_tflops"], 3),
+                      "density": round(density, 6), "nnz_per_mask_set": fmt.nnz,
+                      "tiles_full": fmt.n_full, "tiles_partial": fmt.n_part},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, args)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, mask, q, k, v, ws, fmt, scale, stream, device, dist):
+    """Same metric through the public API from pinned host buffers: each
+    step copies mask, Q, K, V host->device, runs the hot path and reads O
+    back to the host."""
+    import torch
+    from sparse_mask_transformer_gb300 import stof
+    hm = torch.empty(mask.shape, dtype=mask.dtype, pin_memory=True)
+    hm.copy_(mask)
+    hq, hk, hv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in (q, k, v))
+    ho = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    o = torch.empty_like(q)
+    steps = max(1, min(args.steps, args.e2e_steps))
+
+    def step():
+        mask.copy_(hm, non_blocking=True)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        stof.stof_encode_mask(mask, 128, 128, ws, fmt)
+        stof.stof_format_sync(fmt)
+        stof.stof_mha_fwd(q, k, v, fmt, scale, w.stride_b, w.stride_h, stof.STOF_KERNEL_AUTO, o)
+        ho.copy_(o, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1) / steps, dist, device)
+    valid = fmt.nnz * heads_per_mask(w)
+    total = sum_over_ranks(4.0 * w.d * valid, dist, device)
+    h2d = hm.numel() + 3 * hq.numel() * hq.element_size()
+    d2h = ho.numel() * ho.element_size()
+    return {"value": round(total / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w: synth.Workload, budget_rows: int, seed: int = 0):
+    """A bounded, seeded sample of the workload for the fp64 oracle: a few
+    heads and query rows, plus the OT rows those queries fall in for the
+    brute-force encoder."""
+    rng = np.random.default_rng(seed)
+    n_heads = min(w.B * w.H, 2)
+    heads = [(int(x) // w.H, int(x) % w.H) for x in rng.choice(w.B * w.H, n_heads, replace=False)]
+    rows = np.sort(rng.choice(w.L, min(w.L, budget_rows), replace=False))
+    return heads, rows
+
+
+def run_oracle_sample(w: synth.Workload, heads, rows, qkv64=None):
+    """Times the oracle on the sample; returns (seconds, valid elements, threads)."""
+    import oracle
+    q, k, v = qkv64 if qkv64 is not None else (synth.to_float64(t) for t in synth.make_qkv(
+        w.B, w.H, w.L, w.d, w.dtype, seed=w.seed))
+    threads = oracle.default_threads()
+    masks = {}
+    for (b, h) in heads:
+        m = synth.mask_index(w, b, h)
+        masks[(b, h)] = synth.mask_rows(w, m, rows)
+    bands = sorted({int(r) // 128 for r in rows[:4]})
+    band_masks = [(synth.mask_index(w, *heads[0]), I) for I in bands]
+    band_data = [synth.mask_rows(w, m, np.arange(I * 128, I * 128 + 128))[None] for m, I in band_masks]
+    t0 = time.perf_counter()
+    valid = 0
+    for (b, h) in heads:
+        oracle.attention(q[b, h, rows], k[b, h], v[b, h], masks[(b, h)], 1 / math.sqrt(w.d), threads)
+        valid += int(masks[(b, h)].sum())
+    for bd in band_data:
+        oracle.encode(bd, 128, 128)
+    return time.perf_counter() - t0, valid, threads
+
+
+def cpu_baseline(w: synth.Workload, args):
+    heads, rows = oracle_sample(w, args.cpu_rows)
+    secs, valid, threads = run_oracle_sample(w, heads, rows)
+    return {"value": round(4.0 * w.d * valid / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "seconds": round(secs, 3),
+            "sample": f"{len(heads)} heads x {len(rows)} query rows of {w.name} (fp64 C oracle, "
+                      f"masked attention over valid keys) + brute-force encode of 4 OT rows"}
+
+
+def run_reference(args, w: synth.Workload):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    heads, rows = oracle_sample(w, args.cpu_rows)
+    qkv64 = tuple(synth.to_float64(t) for t in synth.make_qkv(w.B, w.H, w.L, w.d, w.dtype, seed=w.seed))
+    for _ in range(args.warmup):
+        run_oracle_sample(w, heads, rows[:64], qkv64)
+    secs, valid = 0.0, 0
+    threads = 1
+    for _ in range(args.steps):
+        s, vld, threads = run_oracle_sample(w, heads, rows, qkv64)
+        secs += s
+        valid += vld
+    value = 4.0 * w.d * valid / secs / 1e12
+    ms = secs / args.steps * 1e3
+    sample = f"{len(heads)} heads x {len(rows)} query rows of {w.name} per step + brute-force encode of 4 OT rows"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded masks and N(0,1) Q/K/V)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "mask": w.describe},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="bernoulli_L16384", choices=list(synth.WORKLOADS))
+    ap.add_argument("--impl", default="stof", choices=["stof", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows per head in the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

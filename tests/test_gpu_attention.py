@@ -29,7 +29,10 @@ def _run(q, k, v, mask_dev, bm, bn, sb, sh, which, scale=None):
     return o.cpu(), fmt
 
 
-def _check(o_gpu, q, k, v, mask_of, dtype, heads=None, rows=None, scale=None):
+def _check(o_gpu, q, k, v, mask_of, dtype, heads=None, rows=None, scale=None, rel=False):
+    """Max |O - O_oracle| <= TOL[dtype].  With rel=True (stress inputs
+    outside the N(0,1) workloads, where |O| can exceed 1 and bf16 output
+    rounding alone reaches 2^-6 |O|) the bound is TOL[dtype] * max(1, |O|)."""
     B, H, L, d = q.shape
     scale = 1 / math.sqrt(d) if scale is None else scale
     q64, k64, v64 = (synth.to_float64(t) for t in (q, k, v))
@@ -39,7 +42,10 @@ def _check(o_gpu, q, k, v, mask_of, dtype, heads=None, rows=None, scale=None):
     for (b, h), o_ref in ref.items():
         got = og[b, h] if rows is None else og[b, h, rows]
         assert np.all(np.isfinite(got))
-        worst = max(worst, float(np.abs(got - o_ref).max()))
+        err = np.abs(got - o_ref)
+        if rel:
+            err = err / np.maximum(1.0, np.abs(o_ref))
+        worst = max(worst, float(err.max()))
     assert worst <= TOL[dtype], f"max abs error {worst} > {TOL[dtype]}"
     return worst
 
@@ -123,7 +129,7 @@ def test_edge_cases(gpu_lib, kern):
     assert torch.all(o[0, 2, :128] == 0)
     assert torch.equal(o[0, 2, 128:], v[0, 2, 5].expand(128, d))
     assert torch.all(o[0, 3] == 0)
-    _check(o, q, k, v, _mask_of_np(masks, 0, 1), "bf16", heads=[(0, 0)])
+    _check(o, q, k, v, _mask_of_np(masks, 0, 1), "bf16", heads=[(0, 0)], rel=True)
 
 
 def test_auto_selection_runs_the_selected_kernel(gpu_lib):
