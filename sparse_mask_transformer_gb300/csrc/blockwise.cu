@@ -9,9 +9,11 @@
 // two-level storage format: exact masking).
 //
 // One CTA computes one 128-row query tile (b, h, OT row I):
-//   warp 0      TMA producer: the Q tile once, then for each listed OT its
-//               K and V tiles (and, for a partial OT, its 2 KB of IT
-//               bitmaps) into an NS-stage shared-memory ring;
+//   warp 0      TMA producers: lane 0 loads the Q tile once and the K tile
+//               of every listed OT into an NK-stage ring (a stage is freed
+//               as soon as its S = Q K^T is done); lane 1 loads the V tiles
+//               (and, for a partial OT, its 2 KB of IT bitmaps) into an
+//               NV-stage ring (freed when its O += P V is done);
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma:
 //               S[t%2] = Q K_t^T (fp32 in TMEM), and O += P[t%2] V_t with
 //               P read from TMEM;
@@ -50,7 +52,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 
 template <int D>
 struct Cfg {
-  static constexpr int NS = D == 128 ? 2 : 4;       // K/V ring stages
+  static constexpr int NK = D == 128 ? 2 : 3;       // K ring stages
+  static constexpr int NV = D == 128 ? 3 : 4;       // V ring stages
   static constexpr int REGIONS = D / 64;            // 128-byte swizzle atoms along d
   static constexpr int TILE_BYTES = kBM * D * 2;    // one Q, K or V tile
   static constexpr int BITMAP_WORDS = (kBM / 8) * (kBN / 8);
@@ -59,12 +62,14 @@ struct Cfg {
 template <int D>
 struct alignas(1024) Smem {
   uint8_t q[Cfg<D>::TILE_BYTES];
-  uint8_t k[Cfg<D>::NS][Cfg<D>::TILE_BYTES];
-  uint8_t v[Cfg<D>::NS][Cfg<D>::TILE_BYTES];
-  uint64_t bits[Cfg<D>::NS][Cfg<D>::BITMAP_WORDS];
+  uint8_t k[Cfg<D>::NK][Cfg<D>::TILE_BYTES];
+  uint8_t v[Cfg<D>::NV][Cfg<D>::TILE_BYTES];
+  uint64_t bits[Cfg<D>::NV][Cfg<D>::BITMAP_WORDS];
   uint64_t q_full;
-  uint64_t kv_full[Cfg<D>::NS];
-  uint64_t kv_free[Cfg<D>::NS];
+  uint64_t k_full[Cfg<D>::NK];
+  uint64_t k_free[Cfg<D>::NK];
+  uint64_t v_full[Cfg<D>::NV];
+  uint64_t v_free[Cfg<D>::NV];
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full[2];
@@ -105,10 +110,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // work item: heaviest OT rows first for causal-like masks
-  const int BH = p.B * p.H;
-  const int I = p.n_tr - 1 - static_cast<int>(blockIdx.x / BH);
-  const int bh = static_cast<int>(blockIdx.x % BH);
+  // work item: head-major, so CTAs running together stream the same head's
+  // K/V through L2; inside a head the heaviest (last) OT rows first
+  const int bh = static_cast<int>(blockIdx.x / p.n_tr);
+  const int I = p.n_tr - 1 - static_cast<int>(blockIdx.x % p.n_tr);
   const int b = bh / p.H, h = bh % p.H;
   const long long mrow = (b * p.stride_b + h * p.stride_h) * p.n_tr + I;
   const int f0 = p.full_row_ptr[mrow];
@@ -119,9 +124,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
-    for (int i = 0; i < C::NS; ++i) {
-      mbar_init(&s.kv_full[i], 1);
-      mbar_init(&s.kv_free[i], 1);
+    for (int i = 0; i < C::NK; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.k_free[i], 1);
+    }
+    for (int i = 0; i < C::NV; ++i) {
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.v_free[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
@@ -150,44 +159,64 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ producers
+    auto column_of = [&](int t, long long* e) {
+      const bool partial = t >= nf;
+      *e = partial ? static_cast<long long>(p0) + (t - nf) : static_cast<long long>(f0) + t;
+      int J = partial ? p.part_col_idx[*e] : p.full_col_idx[*e];
+      if (J < 0 || J >= p.n_tc) {
+        raise_error(p.err, STOF_DEVERR_BAD_FORMAT);
+        J = 0;
+      }
+      return J;
+    };
+    if (lane == 0) {  // Q, then K tiles
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
       const int qrow = bh * p.L + I * kBM;
       mbar_arrive_expect_tx(&s.q_full, C::TILE_BYTES);
 #pragma unroll
       for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow);
       int issued = 0;
       for (int t = 0; t < n; ++t) {
-        const int st = t % C::NS;
-        if (t >= C::NS && !mbar_wait(&s.kv_free[st], ((t / C::NS) - 1) & 1, abort_flag, kWaitNs)) {
+        const int st = t % C::NK;
+        if (t >= C::NK && !mbar_wait(&s.k_free[st], ((t / C::NK) - 1) & 1, abort_flag, kWaitNs)) {
           fail();
           break;
         }
-        const bool partial = t >= nf;
-        const long long e = partial ? static_cast<long long>(p0) + (t - nf) : static_cast<long long>(f0) + t;
-        int J = partial ? p.part_col_idx[e] : p.full_col_idx[e];
-        if (J < 0 || J >= p.n_tc) {
-          raise_error(p.err, STOF_DEVERR_BAD_FORMAT);
-          J = 0;
-        }
-        const int krow = bh * p.L + J * kBN;
-        mbar_arrive_expect_tx(&s.kv_full[st], 2 * C::TILE_BYTES + (partial ? C::BITMAP_WORDS * 8 : 0));
+        long long e;
+        const int krow = bh * p.L + column_of(t, &e) * kBN;
+        mbar_arrive_expect_tx(&s.k_full[st], C::TILE_BYTES);
 #pragma unroll
-        for (int r = 0; r < C::REGIONS; ++r) {
-          tma_load_2d(s.k[st] + r * 16384, &tmK, &s.kv_full[st], 64 * r, krow);
-          tma_load_2d(s.v[st] + r * 16384, &tmV, &s.kv_full[st], 64 * r, krow);
+        for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.k[st] + r * 16384, &tmK, &s.k_full[st], 64 * r, krow);
+        issued = t + 1;
+      }
+      if (*abort_flag) {  // let every copy this thread started land before exit
+        mbar_wait_timeout(&s.q_full, 0, kWaitNs);
+        for (int t = issued - C::NK < 0 ? 0 : issued - C::NK; t < issued; ++t)
+          mbar_wait_timeout(&s.k_full[t % C::NK], (t / C::NK) & 1, kWaitNs);
+      }
+    } else if (lane == 1) {  // V tiles and the bitmaps of partial OTs
+      prefetch_tmap(&tmV);
+      int issued = 0;
+      for (int t = 0; t < n; ++t) {
+        const int st = t % C::NV;
+        if (t >= C::NV && !mbar_wait(&s.v_free[st], ((t / C::NV) - 1) & 1, abort_flag, kWaitNs)) {
+          fail();
+          break;
         }
-        if (partial) bulk_load(s.bits[st], p.bitmaps + e * C::BITMAP_WORDS, C::BITMAP_WORDS * 8, &s.kv_full[st]);
+        long long e;
+        const int vrow = bh * p.L + column_of(t, &e) * kBN;
+        const bool partial = t >= nf;
+        mbar_arrive_expect_tx(&s.v_full[st], C::TILE_BYTES + (partial ? C::BITMAP_WORDS * 8 : 0));
+#pragma unroll
+        for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.v[st] + r * 16384, &tmV, &s.v_full[st], 64 * r, vrow);
+        if (partial) bulk_load(s.bits[st], p.bitmaps + e * C::BITMAP_WORDS, C::BITMAP_WORDS * 8, &s.v_full[st]);
         issued = t + 1;
       }
       if (*abort_flag) {
-        // let every copy this thread started land before the CTA exits
-        mbar_wait_timeout(&s.q_full, 0, kWaitNs);
-        for (int t = issued - C::NS < 0 ? 0 : issued - C::NS; t < issued; ++t)
-          mbar_wait_timeout(&s.kv_full[t % C::NS], (t / C::NS) & 1, kWaitNs);
+        for (int t = issued - C::NV < 0 ? 0 : issued - C::NV; t < issued; ++t)
+          mbar_wait_timeout(&s.v_full[t % C::NV], (t / C::NV) & 1, kWaitNs);
       }
     }
   } else if (warp == 1) {
@@ -198,8 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = smem_u32(s.q);
       auto issue_pv = [&](int u) -> bool {
         if (!mbar_wait(&s.p_full[u & 1], (u >> 1) & 1, abort_flag, kWaitNs)) return false;
+        const int st = u % C::NV;
+        if (!mbar_wait(&s.v_full[st], (u / C::NV) & 1, abort_flag, kWaitNs)) return false;
         tc_fence_after();
-        const int st = u % C::NS;
         const uint32_t v_addr = smem_u32(s.v[st]);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -207,14 +237,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16_ts(tO, tP0 + (u & 1) * 64 + kk * 8, bdesc, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&s.pv_done[u & 1]);
-        mma_commit(&s.kv_free[st]);
+        mma_commit(&s.v_free[st]);
         return true;
       };
       bool ok = true;
       if (n > 0) ok = mbar_wait(&s.q_full, 0, abort_flag, kWaitNs);
       for (int t = 0; ok && t < n; ++t) {
-        const int st = t % C::NS, sb = t & 1;
-        if (!mbar_wait(&s.kv_full[st], (t / C::NS) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+        const int st = t % C::NK, sb = t & 1;
+        if (!mbar_wait(&s.k_full[st], (t / C::NK) & 1, abort_flag, kWaitNs)) { ok = false; break; }
         if (t >= 2 && !mbar_wait(&s.s_free[sb], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
         tc_fence_after();
         const uint32_t k_addr = smem_u32(s.k[st]);
@@ -225,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s.s_full[sb]);
+        mma_commit(&s.k_free[st]);
         if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
       }
       if (ok && n > 0) ok = issue_pv(n - 1);
@@ -260,8 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mx = -INFINITY;
       if (t >= nf) {  // partial OT: keep only the keys whose bit is set
         // the bitmap bytes came by bulk copy: observe their arrival here too
-        if (!wwait(&s.kv_full[t % C::NS], (t / C::NS) & 1)) { ok = false; break; }
-        const uint64_t* bw = s.bits[t % C::NS] + (r >> 3) * (kBN / 8);
+        if (!wwait(&s.v_full[t % C::NV], (t / C::NV) & 1)) { ok = false; break; }
+        const uint64_t* bw = s.bits[t % C::NV] + (r >> 3) * (kBN / 8);
         const int shift = (r & 7) * 8;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {

@@ -9,7 +9,9 @@
 // GB300 design: one pass over the mask, which is the only large stream
 // (HBM-bound).  A CTA owns a chunk = one OT row band x `ct` consecutive OTs
 // (about 1024 mask columns).  It
-//   1. reads the chunk with coalesced 8-byte loads and packs each 8x8 IT
+//   1. reads the chunk with coalesced 16-byte (else 8-byte) streaming loads,
+//      four CTAs per SM so that one CTA's loads overlap another's tail, and
+//      packs each 8x8 IT
 //      into a uint64 in shared memory (bit 8r+c = byte (r, c) non-zero);
 //   2. classifies each OT by AND / OR over its IT words;
 //   3. gets the global offsets of its full and partial OTs from a
@@ -30,7 +32,6 @@ namespace stof {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;              // IT words in flight per thread
 constexpr int kMaxTilesPerChunk = 128;
 constexpr unsigned long long kFlagAgg = 1ull << 62;
 constexpr unsigned long long kFlagInc = 2ull << 62;
@@ -58,7 +59,8 @@ __device__ __forceinline__ uint64_t now_ns() {
   return t;
 }
 
-__global__ void __launch_bounds__(kThreads) encode_kernel(const EncodeParams p) {
+template <int VEC>  // bytes per load: 16 when rows and tiles are 16-byte aligned, else 8
+__global__ void __launch_bounds__(kThreads, 4) encode_kernel(const EncodeParams p) {
   extern __shared__ uint64_t s_words[];  // [bm/8][nt * bn/8]
   __shared__ long long s_chunk;
   __shared__ unsigned long long s_nnz;
@@ -90,33 +92,48 @@ __global__ void __launch_bounds__(kThreads) encode_kernel(const EncodeParams p) 
   const uint8_t* base = p.mask + (static_cast<long long>(m) * p.lq + static_cast<long long>(I) * p.bm) * p.lk +
                         static_cast<long long>(J0) * p.bn;
 
-  // 1. read and pack
+  // 1. read and pack (each unit = VEC/8 adjacent IT words of one 8-row band)
   unsigned long long local_nnz = 0;
-  for (int w0 = tid; w0 < nwords; w0 += kThreads * kUnroll) {
-    uint2 v[kUnroll][8];
+  constexpr int WPU = VEC / 8;                     // IT words per unit
+  constexpr int kUnroll = VEC == 16 ? 1 : 2;       // units in flight per thread (128 B)
+  const int upr = itcols / WPU;                    // units per band
+  const int nunits = bands * upr;
+  for (int u0 = tid; u0 < nunits; u0 += kThreads * kUnroll) {
+    uint4 v[kUnroll][8];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int w = w0 + u * kThreads;
-      if (w < nwords) {
-        const int pb = w / itcols, q = w - pb * itcols;
-        const uint8_t* src = base + static_cast<long long>(8 * pb) * p.lk + 8 * q;
+      const int w = u0 + u * kThreads;
+      if (w < nunits) {
+        const int pb = w / upr, qu = w - pb * upr;
+        const uint8_t* src = base + static_cast<long long>(8 * pb) * p.lk + VEC * qu;
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
-          v[u][r] = __ldcs(reinterpret_cast<const uint2*>(src + static_cast<long long>(r) * p.lk));
+        for (int r = 0; r < 8; ++r) {
+          if constexpr (VEC == 16) {
+            v[u][r] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * p.lk));
+          } else {
+            const uint2 x = __ldcs(reinterpret_cast<const uint2*>(src + static_cast<long long>(r) * p.lk));
+            v[u][r] = make_uint4(x.x, x.y, 0u, 0u);
+          }
+        }
       }
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int w = w0 + u * kThreads;
-      if (w < nwords) {
-        uint64_t word = 0;
+      const int w = u0 + u * kThreads;
+      if (w < nunits) {
+        const int pb = w / upr, qu = w - pb * upr;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const uint64_t x = (static_cast<uint64_t>(v[u][r].y) << 32) | v[u][r].x;
-          word |= static_cast<uint64_t>(pack_row8(x)) << (8 * r);
+        for (int h = 0; h < WPU; ++h) {
+          uint64_t word = 0;
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const uint64_t x = h == 0 ? ((static_cast<uint64_t>(v[u][r].y) << 32) | v[u][r].x)
+                                      : ((static_cast<uint64_t>(v[u][r].w) << 32) | v[u][r].z);
+            word |= static_cast<uint64_t>(pack_row8(x)) << (8 * r);
+          }
+          s_words[pb * itcols + qu * WPU + h] = word;
+          local_nnz += __popcll(word);
         }
-        s_words[w] = word;
-        local_nnz += __popcll(word);
       }
     }
   }
@@ -284,12 +301,12 @@ WorkspaceLayout workspace_layout(const EncodeGeom& g) {
 }
 
 cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s) {
-  if (g.smem_bytes > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(g.smem_bytes));
-    if (e != cudaSuccess) return e;
-  }
-  encode_kernel<<<static_cast<unsigned>(g.n_chunks), kThreads, g.smem_bytes, s>>>(p);
+  // shared memory per CTA is at most bm * 1024 / 8 = 32 KB (bm <= 256)
+  const bool vec16 = (p.lk % 16 == 0) && (p.bn % 16 == 0) && (reinterpret_cast<uintptr_t>(p.mask) % 16 == 0);
+  if (vec16)
+    encode_kernel<16><<<static_cast<unsigned>(g.n_chunks), kThreads, g.smem_bytes, s>>>(p);
+  else
+    encode_kernel<8><<<static_cast<unsigned>(g.n_chunks), kThreads, g.smem_bytes, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -127,25 +127,27 @@ stof_status stof_format_sync(stof_format* fmt, void* stream) {
 // chooses the row-wise or block-wise kernel from mask sparsity and
 // sequence length).
 //
-// Cost per query row, in ns, of each kernel:
-//   row-wise   T_row = A_ROW + rho * L * d * C_ROW
-//              (visits exactly the rho*L valid keys with CUDA-core dot
-//              products and K/V gathers);
+// Cost per query row (ns of device time, aggregated over the GPU):
+//   row-wise   T_row = rho * L * d * C_ROW
+//              (visits exactly the rho*L valid keys of the row: CUDA-core
+//              dot products and K/V row gathers, about C_ROW per key*dim);
 //   block-wise T_blk = A_BLK + L * d * C_BLK
-//              (dense tensor-core work on the tiles it lists; with no tile
-//              statistics at hand the model takes the worst case for an
-//              arbitrary mask, every tile listed, i.e. L keys per row).
-// The row-wise kernel wins for small rho (high sparsity) and short L, the
-// regime the pages give it.  The constants are per-query-row costs fitted
-// once on a GB300 from both kernels' times on the five workloads and are
-// frozen here, so the choice is a deterministic function of (rho, L, d).
+//              (tensor-core work on the listed tiles; with no tile
+//              statistics at hand the model charges every key, the worst
+//              case of an arbitrary mask, at C_BLK per key*dim, plus A_BLK
+//              for filling and draining the tile pipeline of a 128-row tile).
+// The row-wise kernel wins for high sparsity (small rho) and short L, the
+// regime the pages give it.  Constants fitted to both kernels' GB300 times
+// on the five workloads (C_ROW from 3.4e-4 to 6.0e-4, C_BLK from 3.1e-6 to
+// 1.4e-5 ns per key*dim; the L=256 workload is latency-bound for both) and
+// frozen, so the choice is a deterministic function of (rho, L, d).
 stof_kernel stof_select_kernel(double density, int seq_len, int head_dim) {
   if (!(density >= 0.0 && density <= 1.0) || seq_len <= 0 || head_dim <= 0)
     return STOF_KERNEL_BLOCKWISE;
-  const double A_ROW = 0.0, C_ROW = 2.0e-4;  // ns per (key * dim)
-  const double A_BLK = 4.0, C_BLK = 1.0e-5;
+  const double C_ROW = 4.5e-4;
+  const double A_BLK = 4.0, C_BLK = 5.0e-6;
   const double L = seq_len, d = head_dim;
-  const double t_row = A_ROW + density * L * d * C_ROW;
+  const double t_row = density * L * d * C_ROW;
   const double t_blk = A_BLK + L * d * C_BLK;
   return t_row <= t_blk ? STOF_KERNEL_ROWWISE : STOF_KERNEL_BLOCKWISE;
 }
