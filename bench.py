@@ -245,7 +245,7 @@ def run_gpu(args, w: synth.Workload):
     value = total_units / (step_ms * 1e-3) / 1e12
 
     # end to end through the same public API with host buffers
-    e2e = run_e2e(args, w, mask, q, k, v, ws, fmt, scale, stream, device, dist)
+    e2e = None if args.no_e2e else run_e2e(args, w, mask, q, k, v, ws, fmt, scale, stream, device, dist)
 
     kern_name = "blockwise" if chosen == stof.STOF_KERNEL_BLOCKWISE else "rowwise"
     if chosen == stof.STOF_KERNEL_BLOCKWISE:
@@ -268,7 +268,8 @@ def run_gpu(args, w: synth.Workload):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded masks and N(0,1) Q/K/V)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "mask": w.describe,
+        "config": {"workload": w.name + (f"(H={w.H})" if args.heads else ""), "B": w.B, "H": w.H, "L": w.L,
+                   "d": w.d, "mask": w.describe,
                    "outer_tile": "128x128", "kernel": kern_name, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (mask %.2f GB, Q/K/V %.2f GB)" % (
                        w.mask_bytes / 1e9, 3 * q.numel() * 2 / 1e9)},
@@ -421,10 +422,19 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows per head in the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="profiling only: run the workload with this many heads (one mask per head "
+                         "for per-head masks)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = synth.WORKLOADS[args.workload]
+    if args.heads:
+        import dataclasses
+        per_head = w.n_masks == w.B * w.H
+        w = dataclasses.replace(w, H=args.heads, n_masks=w.B * args.heads if per_head else w.n_masks,
+                                stride_b=args.heads if per_head else w.stride_b)
     if args.impl == "reference":
         run_reference(args, w)
     else:
