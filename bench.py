@@ -287,7 +287,7 @@ def run_gpu(args, w: synth.Workload):
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, args)
+        out["cpu_baseline"] = cpu_baseline(w, args, mask, q, k, v)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist is not None:
@@ -374,20 +374,49 @@ def run_oracle_sample(w: synth.Workload, heads, rows, qkv64=None):
     return time.perf_counter() - t0, valid, threads
 
 
-def cpu_baseline(w: synth.Workload, args):
-    heads, rows = oracle_sample(w, args.cpu_rows)
-    secs, valid, threads = run_oracle_sample(w, heads, rows)
-    return {"value": round(4.0 * w.d * valid / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle", "seconds": round(secs, 3),
-            "sample": f"{len(heads)} heads x {len(rows)} query rows of {w.name} (fp64 C oracle, "
-                      f"masked attention over valid keys) + brute-force encode of 4 OT rows"}
+def cpu_baseline(w: synth.Workload, args, mask_dev, q, k, v):
+    """The fp64 oracle, as it stands, on a bounded seeded sample of the
+    same workload: all query rows of a seeded row sample, head after head
+    until about --cpu-seconds of oracle time, plus the brute-force encoder
+    on 4 OT rows scaled to the same fraction of the workload.  Mask rows and
+    Q/K/V are copied from the device inputs (untimed)."""
+    import oracle
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(w.L, min(w.L, args.cpu_rows), replace=False))
+    order = rng.permutation(w.B * w.H)
+    threads = oracle.default_threads()
+    attn_s, valid, done = 0.0, 0, 0
+    for x in order:
+        b, h = int(x) // w.H, int(x) % w.H
+        m = synth.mask_index(w, b, h)
+        mrows = mask_dev[m, rows].cpu().numpy()
+        qh = q[b, h, rows].double().cpu().numpy()
+        kh, vh = k[b, h].double().cpu().numpy(), v[b, h].double().cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.attention(qh, kh, vh, mrows, 1 / math.sqrt(w.d), threads)
+        attn_s += time.perf_counter() - t0
+        valid += int(mrows.sum())
+        done += 1
+        if attn_s >= args.cpu_seconds:
+            break
+    bands = [mask_dev[0, I * 128:(I + 1) * 128].cpu().numpy()[None] for I in rng.choice(w.L // 128, 4)]
+    t0 = time.perf_counter()
+    for bd in bands:
+        oracle.encode(bd, 128, 128)
+    enc_per_row = (time.perf_counter() - t0) / len(bands)
+    frac = done * len(rows) / (w.B * w.H * w.L)
+    enc_s = enc_per_row * w.n_masks * (w.L // 128) * frac
+    return {"value": round(4.0 * w.d * valid / (attn_s + enc_s) / 1e12, 6), "unit": "TFLOP/s",
+            "cores": threads, "kind": "oracle", "seconds": round(attn_s + enc_s, 3),
+            "sample": f"{done} heads x {len(rows)} seeded query rows of {w.name} (fp64 C oracle over valid keys) "
+                      f"+ brute-force encode of 4 OT rows scaled to the same {frac:.3f} of the workload"}
 
 
 def run_reference(args, w: synth.Workload):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    heads, rows = oracle_sample(w, args.cpu_rows)
+    heads, rows = oracle_sample(w, min(args.cpu_rows, 2048))
     qkv64 = tuple(synth.to_float64(t) for t in synth.make_qkv(w.B, w.H, w.L, w.d, w.dtype, seed=w.seed))
     for _ in range(args.warmup):
         run_oracle_sample(w, heads, rows[:64], qkv64)
@@ -420,7 +449,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="bernoulli_L16384", choices=list(synth.WORKLOADS))
     ap.add_argument("--impl", default="stof", choices=["stof", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows per head in the oracle sample")
+    ap.add_argument("--cpu-rows", type=int, default=8192, help="query rows per head in the oracle sample")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle time budget of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--heads", type=int, default=0,

@@ -17,13 +17,15 @@
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma:
 //               S[t%2] = Q K_t^T (fp32 in TMEM), and O += P[t%2] V_t with
 //               P read from TMEM;
-//   warps 2..5  softmax warpgroup, one thread per query row: reads its S
-//               row from TMEM, applies the bitmap on partial OTs, runs the
-//               online softmax in fp32 (base 2), writes P (fp16/bf16) to
-//               TMEM, rescales O in TMEM when the running max moved by more
-//               than 2^8 (lazy rescaling, exact at the end because l uses
-//               the same reference max), and finally writes O / l (0 for a
-//               row without valid keys).
+//   warps 2..9  two softmax warpgroups; thread (warpgroup g, row r) owns
+//               columns 64g..64g+63 of S row r: it reads them from TMEM,
+//               applies the bitmap on partial OTs, meets the other half's
+//               row max in shared memory, runs the online softmax in fp32
+//               (base 2), writes its half of P (fp16/bf16) to TMEM,
+//               rescales its half of the O columns in TMEM when the running
+//               max moved by more than 2^8 (lazy rescaling, exact at the end
+//               because l uses the same reference max), and finally writes
+//               its half of O / l (0 for a row without valid keys).
 // TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512).
 // Every pipeline wait is bounded; on timeout the CTA raises
 // STOF_DEVERR_PIPE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
@@ -46,7 +48,7 @@ using namespace ptx;
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;          // producer warp, MMA warp, 8 softmax warps
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 
@@ -75,14 +77,28 @@ struct alignas(1024) Smem {
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t drain;
+  float rowmax[2][2][kBM];   // [tile parity][column half][row]
+  float rowl[2][kBM];
   uint32_t tmem_base;
   int abort_flag;
+  int fail_tile;             // first tile at which a softmax thread failed
 };
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// Barrier over `count` threads (a multiple of 32) under hardware barrier id.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 template <bool BF16>
@@ -101,7 +117,7 @@ __device__ __forceinline__ void raise_error(int64_t* err, unsigned long long bit
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
     blockwise_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using C = Cfg<D>;
@@ -134,12 +150,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.s_free[i], 128);
-      mbar_init(&s.p_full[i], 128);
+      mbar_init(&s.s_free[i], 256);
+      mbar_init(&s.p_full[i], 256);
       mbar_init(&s.pv_done[i], 1);
     }
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
+    s.fail_tile = 0x7FFFFFFF;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -266,53 +283,78 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
+    // Two warpgroups split every S row: warps 2..5 take columns 0..63 and
+    // warps 6..9 columns 64..127 of the same 128 rows (TMEM lane quarter =
+    // warp % 4).  Partial row maxima meet in shared memory once per tile.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    // tcgen05.ld/st are warp-collective: every decision here is warp-uniform
+    // tcgen05.ld/st are warp-collective: every wait result is warp-uniform
     auto wwait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitNs));
     };
+    // failures are voted before each named barrier so both warpgroups leave
+    // the loop at the same tile (bar.sync has no timeout)
+    auto vote_fail = [&](int t) { atomicMin(&s.fail_tile, t); };
     for (int t = 0; t < n; ++t) {
       const int sb = t & 1;
-      if (!wwait(&s.s_full[sb], (t >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS0 + sb * 128 + lane_off + cc * 32, sr[cc]);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(sr[cc]);
-      tc_fence_before();
-      mbar_arrive(&s.s_free[sb]);
-
+      bool good = ok && wwait(&s.s_full[sb], (t >> 1) & 1);
+      uint32_t sr[2][32];
       float mx = -INFINITY;
-      if (t >= nf) {  // partial OT: keep only the keys whose bit is set
-        // the bitmap bytes came by bulk copy: observe their arrival here too
-        if (!wwait(&s.v_full[t % C::NV], (t / C::NV) & 1)) { ok = false; break; }
-        const uint64_t* bw = s.bits[t % C::NV] + (r >> 3) * (kBN / 8);
-        const int shift = (r & 7) * 8;
+      if (good) {
+        tc_fence_after();
+        tmem_ld32(tS0 + sb * 128 + lane_off + half * 64, sr[0]);
+        tmem_ld32(tS0 + sb * 128 + lane_off + half * 64 + 32, sr[1]);
+        tmem_ld_wait(sr[0]);
+        tmem_ld_wait(sr[1]);
+        tc_fence_before();
+        mbar_arrive(&s.s_free[sb]);
+        if (t >= nf) {  // partial OT: keep only the keys whose bit is set
+          // the bitmap bytes came by bulk copy: observe their arrival here too
+          good = wwait(&s.v_full[t % C::NV], (t / C::NV) & 1);
+          if (good) {
+            const uint64_t* bw = s.bits[t % C::NV] + (r >> 3) * (kBN / 8) + half * 8;
+            const int shift = (r & 7) * 8;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t bits32 = 0;
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t bits32 = 0;
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            bits32 |= (static_cast<uint32_t>(bw[4 * cc + u] >> shift) & 0xFFu) << (8 * u);
+              for (int u = 0; u < 4; ++u)
+                bits32 |= (static_cast<uint32_t>(bw[4 * cc + u] >> shift) & 0xFFu) << (8 * u);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x = (bits32 >> i) & 1u ? __uint_as_float(sr[cc][i]) : -INFINITY;
-            sr[cc][i] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
+              for (int i = 0; i < 32; ++i)
+                sr[cc][i] = (bits32 >> i) & 1u ? sr[cc][i] : 0xFF800000u;  // -inf
+            }
           }
         }
-      } else {
+        if (good) {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+          for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[cc][i]));
+            for (int i = 0; i < 32; i += 8) {
+              const int k4 = (cc * 4 + i / 8) & 3;
+              m4[k4] = max3(m4[k4], __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]));
+              m4[k4] = max3(m4[k4], __uint_as_float(sr[cc][i + 2]), __uint_as_float(sr[cc][i + 3]));
+              m4[k4] = max3(m4[k4], __uint_as_float(sr[cc][i + 4]), __uint_as_float(sr[cc][i + 5]));
+              m4[k4] = max3(m4[k4], __uint_as_float(sr[cc][i + 6]), __uint_as_float(sr[cc][i + 7]));
+            }
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        }
       }
+      if (!good) vote_fail(t);
+      s.rowmax[sb][half][r] = mx;
+      named_bar_sync(1, 256);
+      if (s.fail_tile <= t) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, s.rowmax[sb][half ^ 1][r]);
+
       const float mt = mx * c;
       float alpha = 1.f;
       if (mt > m_ref + kRescaleThreshold) {  // also the first finite max
@@ -321,73 +363,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l *= alpha;
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      uint32_t plo[32], phi[32];  // P columns 0..63 and 64..127, two values per word
-      float ls0 = 0.f, ls1 = 0.f;
+      uint32_t pk[32];  // P columns half*64 .. half*64+63, two values per word
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
+      for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const float e0 = ex2(fmaf(__uint_as_float(sr[cc][i]), c, -mu));
           const float e1 = ex2(fmaf(__uint_as_float(sr[cc][i + 1]), c, -mu));
-          ls0 += e0;
-          ls1 += e1;
-          if (cc < 2) plo[cc * 16 + i / 2] = pack2<BF16>(e0, e1);
-          else phi[(cc - 2) * 16 + i / 2] = pack2<BF16>(e0, e1);
+          ls[(i >> 1) & 3] += e0 + e1;
+          pk[cc * 16 + i / 2] = pack2<BF16>(e0, e1);
         }
-      l += ls0 + ls1;
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 
       // P buffer sb is free once PV of tile t-2 is done
-      if (t >= 2 && !wwait(&s.pv_done[sb], ((t - 2) >> 1) & 1)) { ok = false; break; }
-      if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O holds the sum up to tile t-1: wait for it, then rescale
-        if (!wwait(&s.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
-        tc_fence_after();
+      bool gb = t < 2 || wwait(&s.pv_done[sb], ((t - 2) >> 1) & 1);
+      if (gb && t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O holds the sum up to tile t-1: wait for it, then rescale this
+        // warpgroup's half of the O columns
+        gb = wwait(&s.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1);
+        if (gb) {
+          tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t orr[32];
-          tmem_ld32(tO + lane_off + cc * 32, orr);
-          tmem_ld_wait(orr);
+          for (int cc = 0; cc < D / 64; ++cc) {
+            uint32_t orr[32];
+            const uint32_t col = tO + lane_off + half * (D / 2) + cc * 32;
+            tmem_ld32(col, orr);
+            tmem_ld_wait(orr);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-          tmem_st32(tO + lane_off + cc * 32, orr);
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tmem_st32(col, orr);
+          }
         }
       }
+      if (!gb) {
+        ok = false;  // reported at the next vote
+        continue;
+      }
       tc_fence_after();
-      tmem_st32(tP0 + sb * 64 + lane_off, plo);
-      tmem_st32(tP0 + sb * 64 + lane_off + 32, phi);
+      tmem_st32(tP0 + sb * 64 + lane_off + half * 32, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.p_full[sb]);
     }
-    if (!ok) {
-      fail();
+    // epilogue: O / l (l summed over both halves), rounded to the input type;
+    // 0 for rows without valid keys
+    bool good = ok && (n == 0 || wwait(&s.pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1));
+    if (!good) vote_fail(n);
+    s.rowl[half][r] = l;
+    named_bar_sync(1, 256);
+    if (s.fail_tile <= n) {
+      if (half == 0 && quarter == 0 && lane == 0) fail();
     } else {
-      // epilogue: O / l, rounded to the input type; 0 for rows without keys
-      if (n > 0 && !wwait(&s.pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) {
-        fail();
-      } else {
-        tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint8_t* orow = static_cast<uint8_t*>(p.o) +
-                        (static_cast<size_t>(bh) * p.L + static_cast<size_t>(I) * kBM + r) * (D * 2);
+      tc_fence_after();
+      const float lt = l + s.rowl[half ^ 1][r];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      uint8_t* orow = static_cast<uint8_t*>(p.o) +
+                      (static_cast<size_t>(bh) * p.L + static_cast<size_t>(I) * kBM + r) * (D * 2) + half * D;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t orr[32];
-          if (n > 0) {
-            tmem_ld32(tO + lane_off + cc * 32, orr);
-            tmem_ld_wait(orr);
-          } else {
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t orr[32];
+        if (n > 0) {
+          tmem_ld32(tO + lane_off + half * (D / 2) + cc * 32, orr);
+          tmem_ld_wait(orr);
+        } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = 0u;
-          }
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack2<BF16>(__uint_as_float(orr[2 * i]) * inv, __uint_as_float(orr[2 * i + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 32; ++i) orr[i] = 0u;
         }
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack2<BF16>(__uint_as_float(orr[2 * i]) * inv, __uint_as_float(orr[2 * i + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       }
     }
   }
