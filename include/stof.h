@@ -166,6 +166,10 @@ const char* stof_status_string(stof_status s);
 /* STOF_VERSION of the built library. */
 int stof_version(void);
 
+/* Text of the last CUDA runtime error this library saw on the calling
+ * thread ("no error" if none), to explain a STOF_ERR_CUDA status. */
+const char* stof_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -487,14 +487,15 @@ stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
   const size_t smem = sizeof(Smem<D>) + 1024;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(blockwise_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+    if (record_cuda(cudaFuncSetAttribute(blockwise_kernel<D, BF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem))) != cudaSuccess)
       return STOF_ERR_CUDA;
     attr_done = true;
   }
   const long long grid = static_cast<long long>(p.B) * p.H * p.n_tr;
   blockwise_kernel<D, BF16><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
+  return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
 }
 
 }  // namespace

@@ -7,6 +7,9 @@
 
 namespace stof {
 
+// Remembers e (if it is an error) for stof_last_cuda_error(); returns e.
+cudaError_t record_cuda(cudaError_t e);
+
 // ---------------------------------------------------------------- encoder
 // A chunk is one OT row band (bm mask rows) times `ct` consecutive OTs.
 struct EncodeGeom {

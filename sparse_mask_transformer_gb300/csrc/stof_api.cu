@@ -18,13 +18,24 @@ using namespace stof;
 
 namespace {
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 }  // namespace
 
+namespace stof {
+cudaError_t record_cuda(cudaError_t e) {
+  if (e != cudaSuccess) g_last_cuda_error = e;
+  return e;
+}
+}  // namespace stof
+
 extern "C" {
+
+const char* stof_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 
 int stof_version(void) { return STOF_VERSION; }
 
@@ -82,7 +93,7 @@ stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, i
 
   cudaStream_t s = as_stream(stream);
   // counts, ticket and look-back state start at zero
-  if (cudaMemsetAsync(ws + w.counts, 0, w.zero_bytes, s) != cudaSuccess) return STOF_ERR_CUDA;
+  if (record_cuda(cudaMemsetAsync(ws + w.counts, 0, w.zero_bytes, s)) != cudaSuccess) return STOF_ERR_CUDA;
   EncodeParams p;
   p.mask = mask;
   p.lq = lq;
@@ -103,7 +114,7 @@ stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, i
   p.counts = f.counts_dev;
   p.ticket = reinterpret_cast<unsigned long long*>(ws + w.ticket);
   p.status = reinterpret_cast<unsigned long long*>(ws + w.status);
-  if (launch_encode(p, g, s) != cudaSuccess) return STOF_ERR_CUDA;
+  if (record_cuda(launch_encode(p, g, s)) != cudaSuccess) return STOF_ERR_CUDA;
   return STOF_OK;
 }
 
@@ -111,9 +122,9 @@ stof_status stof_format_sync(stof_format* fmt, void* stream) {
   if (!fmt || !fmt->counts_dev) return STOF_ERR_INVALID_ARG;
   int64_t c[4] = {0, 0, 0, 0};
   cudaStream_t s = as_stream(stream);
-  if (cudaMemcpyAsync(c, fmt->counts_dev, sizeof(c), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  if (record_cuda(cudaMemcpyAsync(c, fmt->counts_dev, sizeof(c), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
     return STOF_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return STOF_ERR_CUDA;
+  if (record_cuda(cudaStreamSynchronize(s)) != cudaSuccess) return STOF_ERR_CUDA;
   fmt->n_full = c[0];
   fmt->n_part = c[1];
   fmt->nnz = c[2];
@@ -215,7 +226,7 @@ stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype
   const bool bf16 = dt == STOF_BF16;
   cudaStream_t s = as_stream(stream);
   if (kern == STOF_KERNEL_ROWWISE)
-    return launch_rowwise(p, bf16, s) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
+    return record_cuda(launch_rowwise(p, bf16, s)) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
   return launch_blockwise(p, bf16, s);
 }
 

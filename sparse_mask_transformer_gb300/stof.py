@@ -40,13 +40,17 @@ STOF_DEVERR_PIPE_TIMEOUT = 0x2
 STOF_DEVERR_BAD_FORMAT = 0x4
 
 EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync",
-            "stof_select_kernel", "stof_mha_fwd", "stof_status_string", "stof_version"]
+            "stof_select_kernel", "stof_mha_fwd", "stof_status_string", "stof_version",
+            "stof_last_cuda_error"]
 
 
 class StofError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: status {status} ({stof_status_string(status)})")
+        msg = f"{where}: status {status} ({stof_status_string(status)})"
+        if status == STOF_ERR_CUDA:
+            msg += f": {stof_last_cuda_error()}"
+        super().__init__(msg)
 
 
 class stof_format(ctypes.Structure):
@@ -89,6 +93,8 @@ def load_library(path: str = LIB_PATH):
         lib.stof_status_string.restype = ctypes.c_char_p
         lib.stof_version.argtypes = []
         lib.stof_version.restype = i32
+        lib.stof_last_cuda_error.argtypes = []
+        lib.stof_last_cuda_error.restype = ctypes.c_char_p
         _lib = lib
     return _lib
 
@@ -114,6 +120,10 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 def stof_version() -> int:
     return load_library().stof_version()
+
+
+def stof_last_cuda_error() -> str:
+    return load_library().stof_last_cuda_error().decode()
 
 
 def stof_status_string(status: int) -> str:
