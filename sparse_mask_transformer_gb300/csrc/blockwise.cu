@@ -48,7 +48,9 @@ using namespace ptx;
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 320;          // producer warp, MMA warp, 8 softmax warps
+// producer warp, MMA warp, 8 softmax warps.  With 10 warps two SM
+// sub-partitions hold 3 warps, which caps a thread at 168 registers.
+constexpr int kThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 
@@ -117,7 +119,7 @@ __device__ __forceinline__ void raise_error(int64_t* err, unsigned long long bit
 }
 
 template <int D, bool BF16>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     blockwise_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using C = Cfg<D>;
@@ -363,21 +365,25 @@ __global__ void __maxnreg__(200)
       }
       l *= alpha;
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      uint32_t pk[32];  // P columns half*64 .. half*64+63, two values per word
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float e0 = ex2(fmaf(__uint_as_float(sr[cc][i]), c, -mu));
-          const float e1 = ex2(fmaf(__uint_as_float(sr[cc][i + 1]), c, -mu));
-          ls[(i >> 1) & 3] += e0 + e1;
-          pk[cc * 16 + i / 2] = pack2<BF16>(e0, e1);
-        }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-
       // P buffer sb is free once PV of tile t-2 is done
       bool gb = t < 2 || wwait(&s.pv_done[sb], ((t - 2) >> 1) & 1);
+      if (gb) {
+        tc_fence_after();
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t pk[16];  // 32 P values, two per TMEM column
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float e0 = ex2(fmaf(__uint_as_float(sr[cc][i]), c, -mu));
+            const float e1 = ex2(fmaf(__uint_as_float(sr[cc][i + 1]), c, -mu));
+            ls[(i >> 1) & 3] += e0 + e1;
+            pk[i / 2] = pack2<BF16>(e0, e1);
+          }
+          tmem_st16(tP0 + sb * 64 + lane_off + half * 32 + cc * 16, pk);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      }
       if (gb && t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // O holds the sum up to tile t-1: wait for it, then rescale this
         // warpgroup's half of the O columns
@@ -397,11 +403,10 @@ __global__ void __maxnreg__(200)
         }
       }
       if (!gb) {
+        tmem_st_wait();
         ok = false;  // reported at the next vote
         continue;
       }
-      tc_fence_after();
-      tmem_st32(tP0 + sb * 64 + lane_off + half * 32, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.p_full[sb]);
