@@ -14,9 +14,10 @@
 //               as soon as its S = Q K^T is done); lane 1 loads the V tiles
 //               (and, for a partial OT, its 2 KB of IT bitmaps) into an
 //               NV-stage ring (freed when its O += P V is done);
-//   warp 1      allocates TMEM; one thread issues tcgen05.mma:
-//               S[t%2] = Q K_t^T (fp32 in TMEM), and O += P[t%2] V_t with
-//               P read from TMEM;
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma, event-driven:
+//               S[t%2] = Q K_t^T (fp32 in TMEM) as soon as K_t and the S
+//               buffer are ready, and O += P[t%2] V_t with P read from TMEM
+//               as soon as P_t and V_t are ready;
 //   warps 2..9  two softmax warpgroups; thread (warpgroup g, row r) owns
 //               columns 64g..64g+63 of S row r: it reads them from TMEM,
 //               applies the bitmap on partial OTs, meets the other half's
@@ -240,44 +241,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Event-driven: S = Q K_t^T is issued as soon as K_t has landed and S
+    // buffer t%2 has been read, O += P_t V_t as soon as P_t and V_t are
+    // ready, whichever comes first, so the score tile of t+2 never waits
+    // behind the softmax of t.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(BF16 ? 1 : 0, 0, kBM, kBN);
       constexpr uint32_t idesc_pv = idesc_f16(BF16 ? 1 : 0, 1, kBM, D);
       const uint32_t q_addr = smem_u32(s.q);
-      auto issue_pv = [&](int u) -> bool {
-        if (!mbar_wait(&s.p_full[u & 1], (u >> 1) & 1, abort_flag, kWaitNs)) return false;
-        const int st = u % C::NV;
-        if (!mbar_wait(&s.v_full[st], (u / C::NV) & 1, abort_flag, kWaitNs)) return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(s.v[st]);
+      bool ok = n == 0 || mbar_wait(&s.q_full, 0, abort_flag, kWaitNs);
+      int qk = 0, pv = 0;
+      uint64_t idle_since = globaltimer_ns();
+      uint32_t spins = 0;
+      while (ok && pv < n) {
+        bool progressed = false;
+        if (qk < n) {
+          const int st = qk % C::NK, sb = qk & 1;
+          if (mbar_test(&s.k_full[st], (qk / C::NK) & 1) &&
+              (qk < 2 || mbar_test(&s.s_free[sb], ((qk - 2) >> 1) & 1))) {
+            tc_fence_after();
+            const uint32_t k_addr = smem_u32(s.k[st]);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t bdesc = smem_desc_sw128(v_addr + kk * 2048, 16384, 1024);
-          mma_f16_ts(tO, tP0 + (u & 1) * 64 + kk * 8, bdesc, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              mma_f16_ss(tS0 + sb * 128, smem_desc_sw128(q_addr + off, 16, 1024),
+                         smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&s.s_full[sb]);
+            mma_commit(&s.k_free[st]);
+            ++qk;
+            progressed = true;
+          }
         }
-        mma_commit(&s.pv_done[u & 1]);
-        mma_commit(&s.v_free[st]);
-        return true;
-      };
-      bool ok = true;
-      if (n > 0) ok = mbar_wait(&s.q_full, 0, abort_flag, kWaitNs);
-      for (int t = 0; ok && t < n; ++t) {
-        const int st = t % C::NK, sb = t & 1;
-        if (!mbar_wait(&s.k_full[st], (t / C::NK) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-        if (t >= 2 && !mbar_wait(&s.s_free[sb], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(s.k[st]);
+        if (pv < qk) {
+          const int st = pv % C::NV;
+          if (mbar_test(&s.p_full[pv & 1], (pv >> 1) & 1) && mbar_test(&s.v_full[st], (pv / C::NV) & 1)) {
+            tc_fence_after();
+            const uint32_t v_addr = smem_u32(s.v[st]);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tS0 + sb * 128, smem_desc_sw128(q_addr + off, 16, 1024),
-                     smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kBN / 16; ++kk) {
+              const uint64_t bdesc = smem_desc_sw128(v_addr + kk * 2048, 16384, 1024);
+              mma_f16_ts(tO, tP0 + (pv & 1) * 64 + kk * 8, bdesc, idesc_pv, (pv > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&s.pv_done[pv & 1]);
+            mma_commit(&s.v_free[st]);
+            ++pv;
+            progressed = true;
+          }
         }
-        mma_commit(&s.s_full[sb]);
-        mma_commit(&s.k_free[st]);
-        if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
+        if (progressed) {
+          idle_since = globaltimer_ns();
+        } else if ((++spins & 63u) == 0) {
+          if (*abort_flag || globaltimer_ns() - idle_since > kWaitNs) ok = false;
+        }
       }
-      if (ok && n > 0) ok = issue_pv(n - 1);
       if (!ok) fail();
       // all MMAs of this CTA complete before TMEM is released
       mma_commit(&s.drain);
