@@ -14,20 +14,20 @@
 //               as soon as its S = Q K^T is done); lane 1 loads the V tiles
 //               (and, for a partial OT, its 2 KB of IT bitmaps) into an
 //               NV-stage ring (freed when its O += P V is done);
-//   warp 1      allocates TMEM; one thread issues tcgen05.mma, event-driven:
-//               S[t%2] = Q K_t^T (fp32 in TMEM) as soon as K_t and the S
-//               buffer are ready, and O += P[t%2] V_t with P read from TMEM
-//               as soon as P_t and V_t are ready;
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma in the order
+//               S_{t+1} = Q K_{t+1}^T, then O += P_t V_t and l += P_t 1
+//               (the row sums come out of the tensor core, from the same
+//               rounded P that multiplies V);
 //   warps 2..9  two softmax warpgroups; thread (warpgroup g, row r) owns
 //               columns 64g..64g+63 of S row r: it reads them from TMEM,
 //               applies the bitmap on partial OTs, meets the other half's
-//               row max in shared memory, runs the online softmax in fp32
-//               (base 2), writes its half of P (fp16/bf16) to TMEM,
-//               rescales its half of the O columns in TMEM when the running
-//               max moved by more than 2^8 (lazy rescaling, exact at the end
-//               because l uses the same reference max), and finally writes
-//               its half of O / l (0 for a row without valid keys).
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512).
+//               row max in shared memory, evaluates exp2 in fp32, writes its
+//               half of P (fp16/bf16) to TMEM, rescales its half of O (and
+//               g = 0 the row sums) in TMEM when the running max moved by
+//               more than 2^8 (lazy rescaling: exact, because O and l share
+//               the reference max), and finally writes its half of O / l
+//               (0 for a row without valid keys).
+// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P [384,448) l [448,464).
 // Every pipeline wait is bounded; on timeout the CTA raises
 // STOF_DEVERR_PIPE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -70,6 +70,7 @@ struct alignas(1024) Smem {
   uint8_t k[Cfg<D>::NK][Cfg<D>::TILE_BYTES];
   uint8_t v[Cfg<D>::NV][Cfg<D>::TILE_BYTES];
   uint64_t bits[Cfg<D>::NV][Cfg<D>::BITMAP_WORDS];
+  uint8_t ones[2][2048];     // B operand of the row-sum MMA: 16 x 128 keys of 1.0
   uint64_t q_full;
   uint64_t k_full[Cfg<D>::NK];
   uint64_t k_free[Cfg<D>::NK];
@@ -77,11 +78,10 @@ struct alignas(1024) Smem {
   uint64_t v_free[Cfg<D>::NV];
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[2];
+  uint64_t p_full;
+  uint64_t pv_done;
   uint64_t drain;
   float rowmax[2][2][kBM];   // [tile parity][column half][row]
-  float rowl[2][kBM];
   uint32_t tmem_base;
   int abort_flag;
   int fail_tile;             // first tile at which a softmax thread failed
@@ -97,6 +97,16 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   float y;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
   return y;
+}
+
+// d0 = a0 * b0 + c0, d1 = a1 * b1 + c1 in one packed fp32x2 FMA
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.ftz.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
 // Barrier over `count` threads (a multiple of 32) under hardware barrier id.
@@ -154,9 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.s_free[i], 256);
-      mbar_init(&s.p_full[i], 256);
-      mbar_init(&s.pv_done[i], 1);
     }
+    mbar_init(&s.p_full, 256);
+    mbar_init(&s.pv_done, 1);
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
     s.fail_tile = 0x7FFFFFFF;
@@ -166,12 +176,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&s.tmem_base, 512);
     tmem_relinquish();
   }
+  {  // 1.0 in the input type; every element equal, so the layout is immaterial
+    const uint32_t one2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
+    uint32_t* o32 = reinterpret_cast<uint32_t*>(&s.ones[0][0]);
+    for (int i = threadIdx.x; i < 1024; i += kThreads) o32[i] = one2;
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
   const uint32_t tbase = s.tmem_base;
-  const uint32_t tS0 = tbase, tO = tbase + 256, tP0 = tbase + 384;
+  const uint32_t tS0 = tbase, tO = tbase + 256, tP = tbase + 384, tL = tbase + 448;
   volatile int* abort_flag = &s.abort_flag;
   auto fail = [&]() {
     *abort_flag = 1;
@@ -241,59 +257,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Event-driven: S = Q K_t^T is issued as soon as K_t has landed and S
-    // buffer t%2 has been read, O += P_t V_t as soon as P_t and V_t are
-    // ready, whichever comes first, so the score tile of t+2 never waits
-    // behind the softmax of t.
+    // Fixed order QK_{t+1}, PV_t with blocking (suspending) waits: issuing
+    // tcgen05.mma stalls while the tensor core is busy anyway, and a thread
+    // that polls without suspending would take issue slots from the softmax
+    // warps of its SM sub-partition.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(BF16 ? 1 : 0, 0, kBM, kBN);
       constexpr uint32_t idesc_pv = idesc_f16(BF16 ? 1 : 0, 1, kBM, D);
+      constexpr uint32_t idesc_l = idesc_f16(BF16 ? 1 : 0, 0, kBM, 16);
       const uint32_t q_addr = smem_u32(s.q);
-      bool ok = n == 0 || mbar_wait(&s.q_full, 0, abort_flag, kWaitNs);
-      int qk = 0, pv = 0;
-      uint64_t idle_since = globaltimer_ns();
-      uint32_t spins = 0;
-      while (ok && pv < n) {
-        bool progressed = false;
-        if (qk < n) {
-          const int st = qk % C::NK, sb = qk & 1;
-          if (mbar_test(&s.k_full[st], (qk / C::NK) & 1) &&
-              (qk < 2 || mbar_test(&s.s_free[sb], ((qk - 2) >> 1) & 1))) {
-            tc_fence_after();
-            const uint32_t k_addr = smem_u32(s.k[st]);
+      const uint32_t ones_addr = smem_u32(&s.ones[0][0]);
+      auto issue_qk = [&](int t) -> bool {
+        const int st = t % C::NK, sb = t & 1;
+        if (!mbar_wait(&s.k_full[st], (t / C::NK) & 1, abort_flag, kWaitNs)) return false;
+        if (t >= 2 && !mbar_wait(&s.s_free[sb], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(s.k[st]);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              mma_f16_ss(tS0 + sb * 128, smem_desc_sw128(q_addr + off, 16, 1024),
-                         smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&s.s_full[sb]);
-            mma_commit(&s.k_free[st]);
-            ++qk;
-            progressed = true;
-          }
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_f16_ss(tS0 + sb * 128, smem_desc_sw128(q_addr + off, 16, 1024),
+                     smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        if (pv < qk) {
-          const int st = pv % C::NV;
-          if (mbar_test(&s.p_full[pv & 1], (pv >> 1) & 1) && mbar_test(&s.v_full[st], (pv / C::NV) & 1)) {
-            tc_fence_after();
-            const uint32_t v_addr = smem_u32(s.v[st]);
+        mma_commit(&s.s_full[sb]);
+        mma_commit(&s.k_free[st]);
+        return true;
+      };
+      auto issue_pv = [&](int t) -> bool {
+        const int st = t % C::NV;
+        if (!mbar_wait(&s.p_full, t & 1, abort_flag, kWaitNs)) return false;
+        if (!mbar_wait(&s.v_full[st], (t / C::NV) & 1, abort_flag, kWaitNs)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(s.v[st]);
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-              const uint64_t bdesc = smem_desc_sw128(v_addr + kk * 2048, 16384, 1024);
-              mma_f16_ts(tO, tP0 + (pv & 1) * 64 + kk * 8, bdesc, idesc_pv, (pv > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&s.pv_done[pv & 1]);
-            mma_commit(&s.v_free[st]);
-            ++pv;
-            progressed = true;
-          }
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+          mma_f16_ts(tO, tP + kk * 8, smem_desc_sw128(v_addr + kk * 2048, 16384, 1024), idesc_pv, acc);
+          mma_f16_ts(tL, tP + kk * 8,
+                     smem_desc_sw128(ones_addr + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024), idesc_l, acc);
         }
-        if (progressed) {
-          idle_since = globaltimer_ns();
-        } else if ((++spins & 63u) == 0) {
-          if (*abort_flag || globaltimer_ns() - idle_since > kWaitNs) ok = false;
-        }
+        mma_commit(&s.pv_done);
+        mma_commit(&s.v_free[st]);
+        return true;
+      };
+      bool ok = n == 0 || (mbar_wait(&s.q_full, 0, abort_flag, kWaitNs) && issue_qk(0));
+      for (int t = 0; ok && t < n; ++t) {
+        if (t + 1 < n && !issue_qk(t + 1)) ok = false;
+        else if (!issue_pv(t)) ok = false;
       }
       if (!ok) fail();
       // all MMAs of this CTA complete before TMEM is released
@@ -310,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = p.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY;
     bool ok = true;
     // tcgen05.ld/st are warp-collective: every wait result is warp-uniform
     auto wwait = [&](uint64_t* bar, uint32_t parity) {
@@ -380,33 +390,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = ex2(m_ref - mt);             // 0 when m_ref = -inf
         m_ref = mt;
       }
-      l *= alpha;
-      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      // P buffer sb is free once PV of tile t-2 is done
-      bool gb = t < 2 || wwait(&s.pv_done[sb], ((t - 2) >> 1) & 1);
+      const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
+      // the P buffer is free, and O, l hold tiles 0..t-1, once PV of t-1 is done
+      bool gb = t == 0 || wwait(&s.pv_done, (t - 1) & 1);
       if (gb) {
         tc_fence_after();
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t pk[16];  // 32 P values, two per TMEM column
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float e0 = ex2(fmaf(__uint_as_float(sr[cc][i]), c, -mu));
-            const float e1 = ex2(fmaf(__uint_as_float(sr[cc][i + 1]), c, -mu));
-            ls[(i >> 1) & 3] += e0 + e1;
-            pk[i / 2] = pack2<BF16>(e0, e1);
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]), c, c, nmu, nmu);
+            pk[i / 2] = pack2<BF16>(ex2(x0), ex2(x1));
           }
-          tmem_st16(tP0 + sb * 64 + lane_off + half * 32 + cc * 16, pk);
+          tmem_st16(tP + lane_off + half * 32 + cc * 16, pk);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      }
-      if (gb && t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O holds the sum up to tile t-1: wait for it, then rescale this
-        // warpgroup's half of the O columns
-        gb = wwait(&s.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1);
-        if (gb) {
-          tc_fence_after();
+        if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // rescale this warpgroup's half of O (and, warpgroup 0, the row sums)
 #pragma unroll
           for (int cc = 0; cc < D / 64; ++cc) {
             uint32_t orr[32];
@@ -417,28 +418,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
             tmem_st32(col, orr);
           }
+          if (half == 0) {
+            uint32_t lr[16];
+            tmem_ld16(tL + lane_off, lr);
+            tmem_ld_wait(lr);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) lr[i] = __float_as_uint(__uint_as_float(lr[i]) * alpha);
+            tmem_st16(tL + lane_off, lr);
+          }
         }
       }
+      tmem_st_wait();
       if (!gb) {
-        tmem_st_wait();
         ok = false;  // reported at the next vote
         continue;
       }
-      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&s.p_full[sb]);
+      mbar_arrive(&s.p_full);
     }
-    // epilogue: O / l (l summed over both halves), rounded to the input type;
-    // 0 for rows without valid keys
-    bool good = ok && (n == 0 || wwait(&s.pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1));
+    // epilogue: O / l, rounded to the input type; 0 for rows without keys
+    bool good = ok && (n == 0 || wwait(&s.pv_done, (n - 1) & 1));
     if (!good) vote_fail(n);
-    s.rowl[half][r] = l;
     named_bar_sync(1, 256);
     if (s.fail_tile <= n) {
       if (half == 0 && quarter == 0 && lane == 0) fail();
     } else {
       tc_fence_after();
-      const float lt = l + s.rowl[half ^ 1][r];
+      float lt = 0.f;
+      if (n > 0) {
+        uint32_t lr[16];
+        tmem_ld16(tL + lane_off, lr);
+        tmem_ld_wait(lr);
+        lt = __uint_as_float(lr[0]);
+      }
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
                       (static_cast<size_t>(bh) * p.L + static_cast<size_t>(I) * kBM + r) * (D * 2) + half * D;
