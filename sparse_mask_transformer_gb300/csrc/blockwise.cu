@@ -265,19 +265,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = idesc_f16(BF16 ? 1 : 0, 0, kBM, kBN);
       constexpr uint32_t idesc_pv = idesc_f16(BF16 ? 1 : 0, 1, kBM, D);
       constexpr uint32_t idesc_l = idesc_f16(BF16 ? 1 : 0, 0, kBM, 16);
-      const uint32_t q_addr = smem_u32(s.q);
-      const uint32_t ones_addr = smem_u32(&s.ones[0][0]);
+      // Descriptors are built once; a K step only adds a compile-time
+      // offset (in 16-byte units) to the start-address field.  A single
+      // issuing thread is latency-bound, so per-MMA descriptor arithmetic
+      // would otherwise throttle the tensor core.
+      constexpr uint64_t kStage = C::TILE_BYTES / 16;
+      const uint64_t qdesc = smem_desc_sw128(smem_u32(s.q), 16, 1024);
+      const uint64_t kdesc0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
+      const uint64_t vdesc0 = smem_desc_sw128(smem_u32(s.v[0]), 16384, 1024);
+      const uint64_t odesc = smem_desc_sw128(smem_u32(&s.ones[0][0]), 16, 1024);
       auto issue_qk = [&](int t) -> bool {
         const int st = t % C::NK, sb = t & 1;
         if (!mbar_wait(&s.k_full[st], (t / C::NK) & 1, abort_flag, kWaitNs)) return false;
         if (t >= 2 && !mbar_wait(&s.s_free[sb], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) return false;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(s.k[st]);
+        const uint64_t kd = kdesc0 + static_cast<uint64_t>(st) * kStage;
+        const uint32_t d_tmem = tS0 + sb * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16_ss(tS0 + sb * 128, smem_desc_sw128(q_addr + off, 16, 1024),
-                     smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          const uint64_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KB per atom, 32 B per K step
+          mma_f16_ss(d_tmem, qdesc + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s.s_full[sb]);
         mma_commit(&s.k_free[st]);
@@ -288,13 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&s.p_full, t & 1, abort_flag, kWaitNs)) return false;
         if (!mbar_wait(&s.v_full[st], (t / C::NV) & 1, abort_flag, kWaitNs)) return false;
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(s.v[st]);
+        const uint64_t vd = vdesc0 + static_cast<uint64_t>(st) * kStage;
+        const uint32_t first = t > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-          mma_f16_ts(tO, tP + kk * 8, smem_desc_sw128(v_addr + kk * 2048, 16384, 1024), idesc_pv, acc);
-          mma_f16_ts(tL, tP + kk * 8,
-                     smem_desc_sw128(ones_addr + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024), idesc_l, acc);
+          const uint32_t acc = kk > 0 ? 1u : first;
+          mma_f16_ts(tO, tP + kk * 8, vd + kk * 128, idesc_pv, acc);  // 16 keys x 128 B per step
+          mma_f16_ts(tL, tP + kk * 8, odesc + (kk >> 2) * 128 + (kk & 3) * 2, idesc_l, acc);
         }
         mma_commit(&s.pv_done);
         mma_commit(&s.v_free[st]);
