@@ -14,20 +14,20 @@
 //               as soon as its S = Q K^T is done); lane 1 loads the V tiles
 //               (and, for a partial OT, its 2 KB of IT bitmaps) into an
 //               NV-stage ring (freed when its O += P V is done);
-//   warp 1      allocates TMEM; one thread issues tcgen05.mma in the order
-//               S_{t+1} = Q K_{t+1}^T, then O += P_t V_t and l += P_t 1
-//               (the row sums come out of the tensor core, from the same
-//               rounded P that multiplies V);
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma: score tiles
+//               run two tiles ahead, S_{t+2} = Q K_{t+2}^T as soon as the
+//               softmax has read S_t out of the same buffer, then
+//               O += P_t V_t once P_t is written;
 //   warps 2..9  two softmax warpgroups; thread (warpgroup g, row r) owns
 //               columns 64g..64g+63 of S row r: it reads them from TMEM,
 //               applies the bitmap on partial OTs, meets the other half's
 //               row max in shared memory, evaluates exp2 in fp32, writes its
-//               half of P (fp16/bf16) to TMEM, rescales its half of O (and
-//               g = 0 the row sums) in TMEM when the running max moved by
-//               more than 2^8 (lazy rescaling: exact, because O and l share
-//               the reference max), and finally writes its half of O / l
-//               (0 for a row without valid keys).
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P [384,448) l [448,464).
+//               half of P (fp16/bf16) to TMEM, keeps its half of the row
+//               sum, rescales its half of O in TMEM when the running max
+//               moved by more than 2^8 (lazy rescaling: exact, because O
+//               and l share the reference max), and finally writes its half
+//               of O / l (0 for a row without valid keys).
+// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512).
 // Every pipeline wait is bounded; on timeout the CTA raises
 // STOF_DEVERR_PIPE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -70,7 +70,6 @@ struct alignas(1024) Smem {
   uint8_t k[Cfg<D>::NK][Cfg<D>::TILE_BYTES];
   uint8_t v[Cfg<D>::NV][Cfg<D>::TILE_BYTES];
   uint64_t bits[Cfg<D>::NV][Cfg<D>::BITMAP_WORDS];
-  uint8_t ones[2][2048];     // B operand of the row-sum MMA: 16 x 128 keys of 1.0
   uint64_t q_full;
   uint64_t k_full[Cfg<D>::NK];
   uint64_t k_free[Cfg<D>::NK];
@@ -78,10 +77,11 @@ struct alignas(1024) Smem {
   uint64_t v_free[Cfg<D>::NV];
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t p_full;
-  uint64_t pv_done;
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
   uint64_t drain;
   float rowmax[2][2][kBM];   // [tile parity][column half][row]
+  float rowl[2][kBM];
   uint32_t tmem_base;
   int abort_flag;
   int fail_tile;             // first tile at which a softmax thread failed
@@ -165,8 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.s_free[i], 256);
     }
-    mbar_init(&s.p_full, 256);
-    mbar_init(&s.pv_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.p_full[i], 256);
+      mbar_init(&s.pv_done[i], 1);
+    }
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
     s.fail_tile = 0x7FFFFFFF;
@@ -176,18 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&s.tmem_base, 512);
     tmem_relinquish();
   }
-  {  // 1.0 in the input type; every element equal, so the layout is immaterial
-    const uint32_t one2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
-    uint32_t* o32 = reinterpret_cast<uint32_t*>(&s.ones[0][0]);
-    for (int i = threadIdx.x; i < 1024; i += kThreads) o32[i] = one2;
-    fence_proxy_async_smem();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
   const uint32_t tbase = s.tmem_base;
-  const uint32_t tS0 = tbase, tO = tbase + 256, tP = tbase + 384, tL = tbase + 448;
+  const uint32_t tS0 = tbase, tO = tbase + 256, tP0 = tbase + 384;
   volatile int* abort_flag = &s.abort_flag;
   auto fail = [&]() {
     *abort_flag = 1;
@@ -257,14 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Fixed order QK_{t+1}, PV_t with blocking (suspending) waits: issuing
-    // tcgen05.mma stalls while the tensor core is busy anyway, and a thread
-    // that polls without suspending would take issue slots from the softmax
-    // warps of its SM sub-partition.
+    // Static order QK_0, QK_1, then per tile t: QK_{t+2} (once the softmax
+    // has read S_t out of buffer t%2), PV_t (once P_t is written).  Waits
+    // suspend the thread, so it takes no issue slots from the softmax warps
+    // sharing its SM sub-partition; MMA groups are straight-line code.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(BF16 ? 1 : 0, 0, kBM, kBN);
       constexpr uint32_t idesc_pv = idesc_f16(BF16 ? 1 : 0, 1, kBM, D);
-      constexpr uint32_t idesc_l = idesc_f16(BF16 ? 1 : 0, 0, kBM, 16);
       // Descriptors are built once; a K step only adds a compile-time
       // offset (in 16-byte units) to the start-address field.  A single
       // issuing thread is latency-bound, so per-MMA descriptor arithmetic
@@ -273,11 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qdesc = smem_desc_sw128(smem_u32(s.q), 16, 1024);
       const uint64_t kdesc0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
       const uint64_t vdesc0 = smem_desc_sw128(smem_u32(s.v[0]), 16384, 1024);
-      const uint64_t odesc = smem_desc_sw128(smem_u32(&s.ones[0][0]), 16, 1024);
       auto issue_qk = [&](int t) -> bool {
         const int st = t % C::NK, sb = t & 1;
-        if (!mbar_wait(&s.k_full[st], (t / C::NK) & 1, abort_flag, kWaitNs)) return false;
         if (t >= 2 && !mbar_wait(&s.s_free[sb], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) return false;
+        if (!mbar_wait(&s.k_full[st], (t / C::NK) & 1, abort_flag, kWaitNs)) return false;
         tc_fence_after();
         const uint64_t kd = kdesc0 + static_cast<uint64_t>(st) * kStage;
         const uint32_t d_tmem = tS0 + sb * 128;
@@ -291,25 +285,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto issue_pv = [&](int t) -> bool {
-        const int st = t % C::NV;
-        if (!mbar_wait(&s.p_full, t & 1, abort_flag, kWaitNs)) return false;
+        const int st = t % C::NV, pb = t & 1;
+        if (!mbar_wait(&s.p_full[pb], (t >> 1) & 1, abort_flag, kWaitNs)) return false;
         if (!mbar_wait(&s.v_full[st], (t / C::NV) & 1, abort_flag, kWaitNs)) return false;
         tc_fence_after();
         const uint64_t vd = vdesc0 + static_cast<uint64_t>(st) * kStage;
-        const uint32_t first = t > 0 ? 1u : 0u;
+        const uint32_t a_tmem = tP0 + pb * 64;
+        mma_f16_ts(tO, a_tmem, vd, idesc_pv, t > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t acc = kk > 0 ? 1u : first;
-          mma_f16_ts(tO, tP + kk * 8, vd + kk * 128, idesc_pv, acc);  // 16 keys x 128 B per step
-          mma_f16_ts(tL, tP + kk * 8, odesc + (kk >> 2) * 128 + (kk & 3) * 2, idesc_l, acc);
-        }
-        mma_commit(&s.pv_done);
+        for (int kk = 1; kk < kBN / 16; ++kk)  // 16 keys x 128 B per K step
+          mma_f16_ts(tO, a_tmem + kk * 8, vd + kk * 128, idesc_pv, 1u);
+        mma_commit(&s.pv_done[pb]);
         mma_commit(&s.v_free[st]);
         return true;
       };
-      bool ok = n == 0 || (mbar_wait(&s.q_full, 0, abort_flag, kWaitNs) && issue_qk(0));
+      bool ok = n == 0 || mbar_wait(&s.q_full, 0, abort_flag, kWaitNs);
+      if (ok && n > 0) ok = issue_qk(0);
+      if (ok && n > 1) ok = issue_qk(1);
       for (int t = 0; ok && t < n; ++t) {
-        if (t + 1 < n && !issue_qk(t + 1)) ok = false;
+        if (t + 2 < n && !issue_qk(t + 2)) ok = false;
         else if (!issue_pv(t)) ok = false;
       }
       if (!ok) fail();
@@ -327,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = p.scale_log2;
-    float m_ref = -INFINITY;
+    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     // tcgen05.ld/st are warp-collective: every wait result is warp-uniform
     auto wwait = [&](uint64_t* bar, uint32_t parity) {
@@ -397,11 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = ex2(m_ref - mt);             // 0 when m_ref = -inf
         m_ref = mt;
       }
+      l *= alpha;
       const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
-      // the P buffer is free, and O, l hold tiles 0..t-1, once PV of t-1 is done
-      bool gb = t == 0 || wwait(&s.pv_done, (t - 1) & 1);
+      // P buffer sb is free once PV of tile t-2 is done
+      bool gb = t < 2 || wwait(&s.pv_done[sb], ((t - 2) >> 1) & 1);
       if (gb) {
         tc_fence_after();
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t pk[16];  // 32 P values, two per TMEM column
@@ -409,29 +405,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; i += 2) {
             float x0, x1;
             ffma2(x0, x1, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]), c, c, nmu, nmu);
-            pk[i / 2] = pack2<BF16>(ex2(x0), ex2(x1));
+            const float e0 = ex2(x0), e1 = ex2(x1);
+            ls[(i >> 1) & 3] += e0 + e1;
+            pk[i / 2] = pack2<BF16>(e0, e1);
           }
-          tmem_st16(tP + lane_off + half * 32 + cc * 16, pk);
+          tmem_st16(tP0 + sb * 64 + lane_off + half * 32 + cc * 16, pk);
         }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // rescale this warpgroup's half of O (and, warpgroup 0, the row sums)
+          // O holds tiles 0..t-1 once PV of t-1 is done: then rescale this
+          // warpgroup's half of the O columns
+          gb = wwait(&s.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1);
+          if (gb) {
+            tc_fence_after();
 #pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc) {
-            uint32_t orr[32];
-            const uint32_t col = tO + lane_off + half * (D / 2) + cc * 32;
-            tmem_ld32(col, orr);
-            tmem_ld_wait(orr);
+            for (int cc = 0; cc < D / 64; ++cc) {
+              uint32_t orr[32];
+              const uint32_t col = tO + lane_off + half * (D / 2) + cc * 32;
+              tmem_ld32(col, orr);
+              tmem_ld_wait(orr);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tmem_st32(col, orr);
-          }
-          if (half == 0) {
-            uint32_t lr[16];
-            tmem_ld16(tL + lane_off, lr);
-            tmem_ld_wait(lr);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) lr[i] = __float_as_uint(__uint_as_float(lr[i]) * alpha);
-            tmem_st16(tL + lane_off, lr);
+              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+              tmem_st32(col, orr);
+            }
           }
         }
       }
@@ -441,23 +437,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       tc_fence_before();
-      mbar_arrive(&s.p_full);
+      mbar_arrive(&s.p_full[sb]);
     }
-    // epilogue: O / l, rounded to the input type; 0 for rows without keys
-    bool good = ok && (n == 0 || wwait(&s.pv_done, (n - 1) & 1));
+    // epilogue: O / l (l summed over both halves), rounded to the input type;
+    // 0 for rows without valid keys
+    bool good = ok && (n == 0 || wwait(&s.pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1));
     if (!good) vote_fail(n);
+    s.rowl[half][r] = l;
     named_bar_sync(1, 256);
     if (s.fail_tile <= n) {
       if (half == 0 && quarter == 0 && lane == 0) fail();
     } else {
       tc_fence_after();
-      float lt = 0.f;
-      if (n > 0) {
-        uint32_t lr[16];
-        tmem_ld16(tL + lane_off, lr);
-        tmem_ld_wait(lr);
-        lt = __uint_as_float(lr[0]);
-      }
+      const float lt = l + s.rowl[half ^ 1][r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
                       (static_cast<size_t>(bh) * p.L + static_cast<size_t>(I) * kBM + r) * (D * 2) + half * D;
