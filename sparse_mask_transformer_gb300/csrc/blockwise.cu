@@ -14,10 +14,11 @@
 //               as soon as its S = Q K^T is done); lane 1 loads the V tiles
 //               (and, for a partial OT, its 2 KB of IT bitmaps) into an
 //               NV-stage ring (freed when its O += P V is done);
-//   warp 1      allocates TMEM; one thread issues tcgen05.mma: score tiles
-//               run two tiles ahead, S_{t+2} = Q K_{t+2}^T as soon as the
-//               softmax has read S_t out of the same buffer, then
-//               O += P_t V_t once P_t is written;
+//   warp 1      allocates TMEM; lane 0 issues the score MMAs, running two
+//               tiles ahead: S_{t+2} = Q K_{t+2}^T as soon as K_{t+2} has
+//               landed and the softmax has read S_t out of the same buffer;
+//               lane 1 issues O += P_t V_t as soon as P_t and V_t are ready
+//               (two issuers, so a late K tile never holds back a ready PV);
 //   warps 2..9  two softmax warpgroups; thread (warpgroup g, row r) owns
 //               columns 64g..64g+63 of S row r: it reads them from TMEM,
 //               applies the bitmap on partial OTs, meets the other half's
@@ -57,8 +58,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 
 template <int D>
 struct Cfg {
-  static constexpr int NK = D == 128 ? 2 : 3;       // K ring stages
-  static constexpr int NV = D == 128 ? 3 : 4;       // V ring stages
+  static constexpr int NK = D == 128 ? 3 : 4;       // K ring stages
+  static constexpr int NV = D == 128 ? 2 : 4;       // V ring stages
   static constexpr int REGIONS = D / 64;            // 128-byte swizzle atoms along d
   static constexpr int TILE_BYTES = kBM * D * 2;    // one Q, K or V tile
   static constexpr int BITMAP_WORDS = (kBM / 8) * (kBN / 8);
@@ -80,6 +81,7 @@ struct alignas(1024) Smem {
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t drain;
+  uint64_t drain_qk;
   float rowmax[2][2][kBM];   // [tile parity][column half][row]
   float rowl[2][kBM];
   uint32_t tmem_base;
@@ -170,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.pv_done[i], 1);
     }
     mbar_init(&s.drain, 1);
+    mbar_init(&s.drain_qk, 1);
     s.abort_flag = 0;
     s.fail_tile = 0x7FFFFFFF;
     fence_mbar_init();
@@ -252,26 +255,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Static order QK_0, QK_1, then per tile t: QK_{t+2} (once the softmax
-    // has read S_t out of buffer t%2), PV_t (once P_t is written).  Waits
-    // suspend the thread, so it takes no issue slots from the softmax warps
-    // sharing its SM sub-partition; MMA groups are straight-line code.
+    // ------------------------------------------------------------ MMA issuers
+    // Lane 0 issues the score MMAs, lane 1 the PV MMAs; each commits to its
+    // own barriers (a commit tracks the issuing thread's MMAs only), and the
+    // TMEM regions they write are disjoint.  Waits suspend the thread, so
+    // it takes no issue slots from the softmax warps sharing its SM
+    // sub-partition; each MMA group is straight-line code.
+    constexpr uint32_t idesc_qk = idesc_f16(BF16 ? 1 : 0, 0, kBM, kBN);
+    constexpr uint32_t idesc_pv = idesc_f16(BF16 ? 1 : 0, 1, kBM, D);
+    // Descriptors are built once; a K step only adds a compile-time offset
+    // (in 16-byte units) to the start-address field.  An issuing thread is
+    // latency-bound, so per-MMA descriptor arithmetic would otherwise
+    // throttle the tensor core.
+    constexpr uint64_t kStage = C::TILE_BYTES / 16;
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_f16(BF16 ? 1 : 0, 0, kBM, kBN);
-      constexpr uint32_t idesc_pv = idesc_f16(BF16 ? 1 : 0, 1, kBM, D);
-      // Descriptors are built once; a K step only adds a compile-time
-      // offset (in 16-byte units) to the start-address field.  A single
-      // issuing thread is latency-bound, so per-MMA descriptor arithmetic
-      // would otherwise throttle the tensor core.
-      constexpr uint64_t kStage = C::TILE_BYTES / 16;
       const uint64_t qdesc = smem_desc_sw128(smem_u32(s.q), 16, 1024);
       const uint64_t kdesc0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
-      const uint64_t vdesc0 = smem_desc_sw128(smem_u32(s.v[0]), 16384, 1024);
-      auto issue_qk = [&](int t) -> bool {
+      bool ok = n == 0 || mbar_wait(&s.q_full, 0, abort_flag, kWaitNs);
+      for (int t = 0; ok && t < n; ++t) {
         const int st = t % C::NK, sb = t & 1;
-        if (t >= 2 && !mbar_wait(&s.s_free[sb], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) return false;
-        if (!mbar_wait(&s.k_full[st], (t / C::NK) & 1, abort_flag, kWaitNs)) return false;
+        if (t >= 2 && !mbar_wait(&s.s_free[sb], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+        if (!mbar_wait(&s.k_full[st], (t / C::NK) & 1, abort_flag, kWaitNs)) { ok = false; break; }
         tc_fence_after();
         const uint64_t kd = kdesc0 + static_cast<uint64_t>(st) * kStage;
         const uint32_t d_tmem = tS0 + sb * 128;
@@ -282,12 +286,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&s.s_full[sb]);
         mma_commit(&s.k_free[st]);
-        return true;
-      };
-      auto issue_pv = [&](int t) -> bool {
+      }
+      if (!ok) fail();
+      mma_commit(&s.drain_qk);  // all of this thread's MMAs done before TMEM is freed
+      mbar_wait_timeout(&s.drain_qk, 0, kWaitNs);
+    } else if (lane == 1) {
+      const uint64_t vdesc0 = smem_desc_sw128(smem_u32(s.v[0]), 16384, 1024);
+      bool ok = true;
+      for (int t = 0; ok && t < n; ++t) {
         const int st = t % C::NV, pb = t & 1;
-        if (!mbar_wait(&s.p_full[pb], (t >> 1) & 1, abort_flag, kWaitNs)) return false;
-        if (!mbar_wait(&s.v_full[st], (t / C::NV) & 1, abort_flag, kWaitNs)) return false;
+        if (!mbar_wait(&s.p_full[pb], (t >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+        if (!mbar_wait(&s.v_full[st], (t / C::NV) & 1, abort_flag, kWaitNs)) { ok = false; break; }
         tc_fence_after();
         const uint64_t vd = vdesc0 + static_cast<uint64_t>(st) * kStage;
         const uint32_t a_tmem = tP0 + pb * 64;
@@ -297,17 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16_ts(tO, a_tmem + kk * 8, vd + kk * 128, idesc_pv, 1u);
         mma_commit(&s.pv_done[pb]);
         mma_commit(&s.v_free[st]);
-        return true;
-      };
-      bool ok = n == 0 || mbar_wait(&s.q_full, 0, abort_flag, kWaitNs);
-      if (ok && n > 0) ok = issue_qk(0);
-      if (ok && n > 1) ok = issue_qk(1);
-      for (int t = 0; ok && t < n; ++t) {
-        if (t + 2 < n && !issue_qk(t + 2)) ok = false;
-        else if (!issue_pv(t)) ok = false;
       }
       if (!ok) fail();
-      // all MMAs of this CTA complete before TMEM is released
       mma_commit(&s.drain);
       mbar_wait_timeout(&s.drain, 0, kWaitNs);
     }
