@@ -9,17 +9,19 @@
 // two-level storage format: exact masking).
 //
 // One CTA computes one 128-row query tile (b, h, OT row I):
-//   warp 0      TMA producers: lane 0 loads the Q tile once and the K tile
-//               of every listed OT into an NK-stage ring (a stage is freed
-//               as soon as its S = Q K^T is done); lane 1 loads the V tiles
-//               (and, for a partial OT, its 2 KB of IT bitmaps) into an
-//               NV-stage ring (freed when its O += P V is done);
-//   warp 1      allocates TMEM; lane 0 issues the score MMAs, running two
-//               tiles ahead: S_{t+2} = Q K_{t+2}^T as soon as K_{t+2} has
-//               landed and the softmax has read S_t out of the same buffer;
-//               lane 1 issues O += P_t V_t as soon as P_t and V_t are ready
-//               (two issuers, so a late K tile never holds back a ready PV);
-//   warps 2..9  two softmax warpgroups; thread (warpgroup g, row r) owns
+//   warp 0      TMA producer: the Q tile once, then the K tile of every
+//               listed OT into an NK-stage ring (a stage is freed as soon
+//               as its S = Q K^T is done);
+//   warp 1      TMA producer: the V tiles (and, for a partial OT, its 2 KB
+//               of IT bitmaps) into an NV-stage ring (freed when its
+//               O += P V is done);
+//   warp 2      allocates TMEM and issues the score MMAs, two tiles ahead:
+//               S_{t+2} = Q K_{t+2}^T as soon as K_{t+2} has landed and the
+//               softmax has read S_t out of the same buffer;
+//   warp 3      issues O += P_t V_t as soon as P_t and V_t are ready.
+//               Each role has a warp of its own: divergent lanes of one warp
+//               are not scheduled promptly while another lane waits;
+//   warps 4..11 two softmax warpgroups; thread (warpgroup g, row r) owns
 //               columns 64g..64g+63 of S row r: it reads them from TMEM,
 //               applies the bitmap on partial OTs, meets the other half's
 //               row max in shared memory, evaluates exp2 in fp32, writes its
@@ -50,9 +52,9 @@ using namespace ptx;
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-// producer warp, MMA warp, 8 softmax warps.  With 10 warps two SM
-// sub-partitions hold 3 warps, which caps a thread at 168 registers.
-constexpr int kThreads = 320;
+// 2 producer warps, 2 MMA-issuer warps, 8 softmax warps.  Three warps per
+// SM sub-partition cap a thread at 168 registers.
+constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.fail_tile = 0x7FFFFFFF;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 2) {
     tmem_alloc(&s.tmem_base, 512);
     tmem_relinquish();
   }
@@ -193,18 +195,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     raise_error(p.err, STOF_DEVERR_PIPE_TIMEOUT);
   };
 
+  // column index of the t-th listed OT of this row (full OTs first)
+  auto column_of = [&](int t, long long* e) {
+    const bool partial = t >= nf;
+    *e = partial ? static_cast<long long>(p0) + (t - nf) : static_cast<long long>(f0) + t;
+    int J = partial ? p.part_col_idx[*e] : p.full_col_idx[*e];
+    if (J < 0 || J >= p.n_tc) {
+      raise_error(p.err, STOF_DEVERR_BAD_FORMAT);
+      J = 0;
+    }
+    return J;
+  };
+
   if (warp == 0) {
-    // ------------------------------------------------------------ producers
-    auto column_of = [&](int t, long long* e) {
-      const bool partial = t >= nf;
-      *e = partial ? static_cast<long long>(p0) + (t - nf) : static_cast<long long>(f0) + t;
-      int J = partial ? p.part_col_idx[*e] : p.full_col_idx[*e];
-      if (J < 0 || J >= p.n_tc) {
-        raise_error(p.err, STOF_DEVERR_BAD_FORMAT);
-        J = 0;
-      }
-      return J;
-    };
+    // ------------------------------------------------------------ K producer
     if (lane == 0) {  // Q, then K tiles
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
@@ -231,7 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = issued - C::NK < 0 ? 0 : issued - C::NK; t < issued; ++t)
           mbar_wait_timeout(&s.k_full[t % C::NK], (t / C::NK) & 1, kWaitNs);
       }
-    } else if (lane == 1) {  // V tiles and the bitmaps of partial OTs
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ V producer
+    if (lane == 0) {  // V tiles and the bitmaps of partial OTs
       prefetch_tmap(&tmV);
       int issued = 0;
       for (int t = 0; t < n; ++t) {
@@ -254,9 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_timeout(&s.v_full[t % C::NV], (t / C::NV) & 1, kWaitNs);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ MMA issuers
-    // Lane 0 issues the score MMAs, lane 1 the PV MMAs; each commits to its
+    // Warp 2 issues the score MMAs, warp 3 the PV MMAs; each commits to its
     // own barriers (a commit tracks the issuing thread's MMAs only), and the
     // TMEM regions they write are disjoint.  Waits suspend the thread, so
     // it takes no issue slots from the softmax warps sharing its SM
@@ -268,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // latency-bound, so per-MMA descriptor arithmetic would otherwise
     // throttle the tensor core.
     constexpr uint64_t kStage = C::TILE_BYTES / 16;
-    if (lane == 0) {
+    if (warp == 2 && lane == 0) {
       const uint64_t qdesc = smem_desc_sw128(smem_u32(s.q), 16, 1024);
       const uint64_t kdesc0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
       bool ok = n == 0 || mbar_wait(&s.q_full, 0, abort_flag, kWaitNs);
@@ -290,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) fail();
       mma_commit(&s.drain_qk);  // all of this thread's MMAs done before TMEM is freed
       mbar_wait_timeout(&s.drain_qk, 0, kWaitNs);
-    } else if (lane == 1) {
+    } else if (warp == 3 && lane == 0) {
       const uint64_t vdesc0 = smem_desc_sw128(smem_u32(s.v[0]), 16384, 1024);
       bool ok = true;
       for (int t = 0; ok && t < n; ++t) {
@@ -313,11 +320,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // Two warpgroups split every S row: warps 2..5 take columns 0..63 and
-    // warps 6..9 columns 64..127 of the same 128 rows (TMEM lane quarter =
+    // Two warpgroups split every S row: warps 4..7 take columns 0..63 and
+    // warps 8..11 columns 64..127 of the same 128 rows (TMEM lane quarter =
     // warp % 4).  Partial row maxima meet in shared memory once per tile.
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - 4) >> 2;
     const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = p.scale_log2;
@@ -476,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
