@@ -130,6 +130,34 @@ size_t stof_encode_workspace_bytes(int n_masks, int lq, int lk, int bm, int bn);
 stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, int bm, int bn,
                              void* workspace, size_t ws_bytes, stof_format* fmt, void* stream);
 
+/*
+ * Same as stof_encode_mask(), for callers that cannot allocate device
+ * memory at this point -- for instance code running inside a framework's
+ * memory pool or allocator callback, or a pre-planned inference runtime
+ * where every buffer is laid out ahead of time -- and so cannot provide
+ * scratch space beyond the workspace they already own.  The paper has no
+ * counterpart; this is a convenience of this library.
+ *   - Allocates nothing: the encoder's scratch (its tile ticket and one
+ *     look-back word per chunk) is a static device array inside
+ *     libstof.so, 1 MiB + 8 bytes, held by every GPU that loads the
+ *     library until the process exits.
+ *   - Size limit: at most 131072 chunks, a chunk being one OT row band of
+ *     W mask columns: chunks = n_masks * (lq / bm) * ceil(lk / W) with
+ *     W = bn * min(lk / bn, max(1, 1024 / bn)) (W = 1024 for bn = 128).
+ *     Larger masks return STOF_ERR_SHAPE before any launch.  The
+ *     16384 x 16384, 32-mask workload needs 65536 chunks.
+ *   - The workspace (same size as for stof_encode_mask) receives the
+ *     format; its scratch section is not used.
+ *   - The first call on a device looks up the static array's device
+ *     address (with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (the call clears what must start at zero): calls that may overlap on
+ *     the GPU, from several streams or threads, race and must not be made.
+ */
+stof_status stof_encode_mask_noalloc(const uint8_t* mask, int n_masks, int lq, int lk, int bm, int bn,
+                                     void* workspace, size_t ws_bytes, stof_format* fmt, void* stream);
+
 /* Blocks until the work queued on stream is done, copies the tile counts
  * and the device error word into fmt, and sets fmt->synced.  Returns
  * STOF_ERR_DEVICE if the device error word is non-zero. */

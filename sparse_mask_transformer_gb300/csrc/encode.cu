@@ -25,6 +25,8 @@
 // STOF_DEVERR_LOOKBACK_TIMEOUT in the device error word and finishes.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "internal.h"
 
 namespace stof {
@@ -308,6 +310,34 @@ cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream
   else
     encode_kernel<8><<<static_cast<unsigned>(g.n_chunks), kThreads, g.smem_bytes, s>>>(p);
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------
+// Scratch for stof_encode_mask_noalloc(): the tile ticket (word 0) and one
+// look-back status word per chunk, in a file-scope device array, so that
+// callers who cannot allocate device memory can still encode.  Each GPU
+// that loads the library holds these 1 MiB + 8 bytes until the process
+// exits.  Host code must not use the array's name as a device address (on
+// the host it names a shadow variable): the address is looked up below.
+static __device__ __align__(256) unsigned long long g_noalloc_scratch[1 + kNoAllocMaxChunks];
+
+cudaError_t noalloc_scratch_address(unsigned long long** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static unsigned long long* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {  // once per device, with that device current
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<unsigned long long*>(ptr);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace stof

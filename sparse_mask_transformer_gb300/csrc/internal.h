@@ -42,6 +42,12 @@ struct EncodeParams {
 };
 cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s);
 
+// Scratch of stof_encode_mask_noalloc(): a static device array with room
+// for the ticket and kNoAllocMaxChunks look-back words.  The address is
+// looked up once per device (the current one) and cached.
+constexpr long long kNoAllocMaxChunks = 131072;
+cudaError_t noalloc_scratch_address(unsigned long long** out);
+
 // ---------------------------------------------------------------- attention
 struct AttnParams {
   const void* q;

@@ -118,6 +118,73 @@ stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, i
   return STOF_OK;
 }
 
+// Variant of stof_encode_mask() that allocates nothing and needs no device
+// scratch from the caller: the tile ticket and look-back words live in a
+// static device array of this library (see encode.cu).  Same arguments;
+// the workspace receives the format, its scratch section is left unused.
+stof_status stof_encode_mask_noalloc(const uint8_t* mask, int n_masks, int lq, int lk, int bm, int bn,
+                                     void* workspace, size_t ws_bytes, stof_format* fmt, void* stream) {
+  if (!mask || !workspace || !fmt) return STOF_ERR_INVALID_ARG;
+  if (n_masks < 1 || lq < 1 || lk < 1 || bm < 1 || bn < 1) return STOF_ERR_INVALID_ARG;
+  EncodeGeom g;
+  if (!encode_geometry(n_masks, lq, lk, bm, bn, &g)) return STOF_ERR_SHAPE;
+  if (g.n_chunks > kNoAllocMaxChunks) return STOF_ERR_SHAPE;  // beyond the static scratch
+  if (!aligned(mask, 8) || !aligned(workspace, 256)) return STOF_ERR_ALIGNMENT;
+  const WorkspaceLayout w = workspace_layout(g);
+  if (ws_bytes < w.total) return STOF_ERR_WORKSPACE;
+  unsigned long long* scratch = nullptr;
+  if (record_cuda(noalloc_scratch_address(&scratch)) != cudaSuccess) return STOF_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  stof_format f;
+  std::memset(&f, 0, sizeof(f));
+  f.n_masks = n_masks;
+  f.lq = lq;
+  f.lk = lk;
+  f.bm = bm;
+  f.bn = bn;
+  f.n_tr = g.n_tr;
+  f.n_tc = g.n_tc;
+  f.synced = 0;
+  f.counts_dev = reinterpret_cast<int64_t*>(ws + w.counts);
+  f.scratch = scratch;
+  f.full_row_ptr = reinterpret_cast<int32_t*>(ws + w.full_row_ptr);
+  f.part_row_ptr = reinterpret_cast<int32_t*>(ws + w.part_row_ptr);
+  f.full_col_idx = reinterpret_cast<int32_t*>(ws + w.full_col_idx);
+  f.part_col_idx = reinterpret_cast<int32_t*>(ws + w.part_col_idx);
+  f.bitmaps = reinterpret_cast<uint64_t*>(ws + w.bitmaps);
+  *fmt = f;
+
+  cudaStream_t s = as_stream(stream);
+  // the static scratch keeps the previous call's words: the counts, the
+  // ticket and this call's look-back words start at zero
+  if (record_cuda(cudaMemsetAsync(ws + w.counts, 0, 32, s)) != cudaSuccess) return STOF_ERR_CUDA;
+  if (record_cuda(cudaMemsetAsync(scratch, 0, (static_cast<size_t>(g.n_chunks) + 1) * 8, s)) != cudaSuccess)
+    return STOF_ERR_CUDA;
+  EncodeParams p;
+  p.mask = mask;
+  p.lq = lq;
+  p.lk = lk;
+  p.bm = bm;
+  p.bn = bn;
+  p.n_tr = g.n_tr;
+  p.n_tc = g.n_tc;
+  p.ct = g.ct;
+  p.cpr = g.cpr;
+  p.n_rows = g.n_rows;
+  p.n_chunks = g.n_chunks;
+  p.full_row_ptr = f.full_row_ptr;
+  p.full_col_idx = f.full_col_idx;
+  p.part_row_ptr = f.part_row_ptr;
+  p.part_col_idx = f.part_col_idx;
+  p.bitmaps = f.bitmaps;
+  p.counts = f.counts_dev;
+  p.ticket = scratch;
+  p.status = scratch + 1;
+  if (record_cuda(launch_encode(p, g, s)) != cudaSuccess) return STOF_ERR_CUDA;
+  return STOF_OK;
+}
+
 stof_status stof_format_sync(stof_format* fmt, void* stream) {
   if (!fmt || !fmt->counts_dev) return STOF_ERR_INVALID_ARG;
   int64_t c[4] = {0, 0, 0, 0};
