@@ -11,10 +11,12 @@
 // One CTA computes one 128-row query tile (b, h, OT row I):
 //   warp 0      TMA producer: the Q tile once, then the K tile of every
 //               listed OT into an NK-stage ring (a stage is freed as soon
-//               as its S = Q K^T is done);
-//   warp 1      TMA producer: the V tiles (and, for a partial OT, its 2 KB
-//               of IT bitmaps) into an NV-stage ring (freed when its
-//               O += P V is done);
+//               as its S = Q K^T is done) and, for a partial OT, its 2 KB of
+//               IT bitmaps into an NB-stage ring (freed as soon as the
+//               softmax has read them: the softmax needs the bitmap right
+//               after S, long before the tile's V);
+//   warp 1      TMA producer: the V tiles into an NV-stage ring (freed when
+//               its O += P V is done);
 //   warp 2      allocates TMEM and issues the score MMAs, two tiles ahead:
 //               S_{t+2} = Q K_{t+2}^T as soon as K_{t+2} has landed and the
 //               softmax has read S_t out of the same buffer;
@@ -60,8 +62,9 @@ constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 
 template <int D>
 struct Cfg {
-  static constexpr int NK = D == 128 ? 3 : 4;       // K ring stages
-  static constexpr int NV = D == 128 ? 2 : 4;       // V ring stages
+  static constexpr int NK = D == 128 ? 2 : 4;       // K ring stages
+  static constexpr int NV = D == 128 ? 3 : 4;       // V ring stages
+  static constexpr int NB = 4;                      // IT-bitmap ring stages
   static constexpr int REGIONS = D / 64;            // 128-byte swizzle atoms along d
   static constexpr int TILE_BYTES = kBM * D * 2;    // one Q, K or V tile
   static constexpr int BITMAP_WORDS = (kBM / 8) * (kBN / 8);
@@ -72,12 +75,14 @@ struct alignas(1024) Smem {
   uint8_t q[Cfg<D>::TILE_BYTES];
   uint8_t k[Cfg<D>::NK][Cfg<D>::TILE_BYTES];
   uint8_t v[Cfg<D>::NV][Cfg<D>::TILE_BYTES];
-  uint64_t bits[Cfg<D>::NV][Cfg<D>::BITMAP_WORDS];
+  uint64_t bits[Cfg<D>::NB][Cfg<D>::BITMAP_WORDS];
   uint64_t q_full;
   uint64_t k_full[Cfg<D>::NK];
   uint64_t k_free[Cfg<D>::NK];
   uint64_t v_full[Cfg<D>::NV];
   uint64_t v_free[Cfg<D>::NV];
+  uint64_t b_full[Cfg<D>::NB];
+  uint64_t b_free[Cfg<D>::NB];
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full[2];
@@ -165,6 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.v_free[i], 1);
     }
+    for (int i = 0; i < C::NB; ++i) {
+      mbar_init(&s.b_full[i], 1);
+      mbar_init(&s.b_free[i], 256);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.s_free[i], 256);
@@ -216,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&s.q_full, C::TILE_BYTES);
 #pragma unroll
       for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow);
-      int issued = 0;
+      int issued = 0, bits_issued = 0;
       for (int t = 0; t < n; ++t) {
         const int st = t % C::NK;
         if (t >= C::NK && !mbar_wait(&s.k_free[st], ((t / C::NK) - 1) & 1, abort_flag, kWaitNs)) {
@@ -225,6 +234,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         long long e;
         const int krow = bh * p.L + column_of(t, &e) * kBN;
+        if (t >= nf) {  // the IT bitmaps of a partial OT, into their own ring
+          const int u = t - nf, bst = u % C::NB;
+          if (u >= C::NB && !mbar_wait(&s.b_free[bst], ((u / C::NB) - 1) & 1, abort_flag, kWaitNs)) {
+            fail();
+            break;
+          }
+          mbar_arrive_expect_tx(&s.b_full[bst], C::BITMAP_WORDS * 8);
+          bulk_load(s.bits[bst], p.bitmaps + e * C::BITMAP_WORDS, C::BITMAP_WORDS * 8, &s.b_full[bst]);
+          bits_issued = u + 1;
+        }
         mbar_arrive_expect_tx(&s.k_full[st], C::TILE_BYTES);
 #pragma unroll
         for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.k[st] + r * 16384, &tmK, &s.k_full[st], 64 * r, krow);
@@ -234,11 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_timeout(&s.q_full, 0, kWaitNs);
         for (int t = issued - C::NK < 0 ? 0 : issued - C::NK; t < issued; ++t)
           mbar_wait_timeout(&s.k_full[t % C::NK], (t / C::NK) & 1, kWaitNs);
+        for (int u = bits_issued - C::NB < 0 ? 0 : bits_issued - C::NB; u < bits_issued; ++u)
+          mbar_wait_timeout(&s.b_full[u % C::NB], (u / C::NB) & 1, kWaitNs);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ V producer
-    if (lane == 0) {  // V tiles and the bitmaps of partial OTs
+    if (lane == 0) {  // V tiles
       prefetch_tmap(&tmV);
       int issued = 0;
       for (int t = 0; t < n; ++t) {
@@ -249,11 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         long long e;
         const int vrow = bh * p.L + column_of(t, &e) * kBN;
-        const bool partial = t >= nf;
-        mbar_arrive_expect_tx(&s.v_full[st], C::TILE_BYTES + (partial ? C::BITMAP_WORDS * 8 : 0));
+        mbar_arrive_expect_tx(&s.v_full[st], C::TILE_BYTES);
 #pragma unroll
         for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.v[st] + r * 16384, &tmV, &s.v_full[st], 64 * r, vrow);
-        if (partial) bulk_load(s.bits[st], p.bitmaps + e * C::BITMAP_WORDS, C::BITMAP_WORDS * 8, &s.v_full[st]);
         issued = t + 1;
       }
       if (*abort_flag) {
@@ -351,10 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&s.s_free[sb]);
         if (t >= nf) {  // partial OT: keep only the keys whose bit is set
-          // the bitmap bytes came by bulk copy: observe their arrival here too
-          good = wwait(&s.v_full[t % C::NV], (t / C::NV) & 1);
+          const int u = t - nf, bst = u % C::NB;
+          good = wwait(&s.b_full[bst], (u / C::NB) & 1);
           if (good) {
-            const uint64_t* bw = s.bits[t % C::NV] + (r >> 3) * (kBN / 8) + half * 8;
+            const uint64_t* bw = s.bits[bst] + (r >> 3) * (kBN / 8) + half * 8;
             const int shift = (r & 7) * 8;
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -366,6 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < 32; ++i)
                 sr[cc][i] = (bits32 >> i) & 1u ? sr[cc][i] : 0xFF800000u;  // -inf
             }
+            mbar_arrive(&s.b_free[bst]);  // this thread is done with the bitmap
           }
         }
         if (good) {
