@@ -7,27 +7,36 @@
 // 8x8 inner tile (IT) of a partial OT is one uint64 bitmap.
 //
 // GB300 design: one pass over the mask, which is the only large stream
-// (HBM-bound).  A CTA owns a chunk = one OT row band x `ct` consecutive OTs
-// (about 1024 mask columns).  It
-//   1. reads the chunk with coalesced 16-byte (else 8-byte) streaming loads,
-//      four CTAs per SM so that one CTA's loads overlap another's tail, and
-//      packs each 8x8 IT
-//      into a uint64 in shared memory (bit 8r+c = byte (r, c) non-zero);
+// (HBM-bound).  The work unit is a chunk = one OT row band x `ct`
+// consecutive OTs (about 1024 mask columns).  For a chunk the encoder
+//   1. packs each 8x8 IT of the chunk into a uint64 in shared memory
+//      (bit 8r+c = byte (r, c) non-zero);
 //   2. classifies each OT by AND / OR over its IT words;
 //   3. gets the global offsets of its full and partial OTs from a
 //      single-pass chained prefix sum with decoupled look-back (Merrill and
 //      Garland, "Single-pass Parallel Prefix Scan with Decoupled
-//      Look-back", 2016); chunks are numbered by an atomic ticket in start
-//      order, so every chunk it waits on is already running;
+//      Look-back", 2016); chunks are numbered by an atomic ticket in the
+//      order they are started, so every chunk it waits on is already being
+//      worked on;
 //   4. writes column indices, row pointers and the bitmaps of its partial
 //      OTs straight into their final slots.
-// Every wait on another CTA is bounded; on timeout the CTA raises
+// Two kernels share phases 2-4:
+//   encode_tma_kernel  (rows and tiles 16-byte aligned, bm <= 128): one
+//      persistent CTA per SM; a producer warp streams 256-column x bm-row
+//      boxes of the mask with TMA through a 4-stage shared-memory ring, a
+//      chunk ahead, while eight consumer warps pack, classify and write, so
+//      the mask stream does not stop during a chunk's look-back and writes;
+//   encode_kernel      (any other shape): one chunk per CTA, coalesced
+//      streaming loads, four CTAs per SM.
+// Every wait on another CTA or warp is bounded; on timeout the CTA raises
 // STOF_DEVERR_LOOKBACK_TIMEOUT in the device error word and finishes.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace stof {
 
@@ -40,13 +49,21 @@ constexpr unsigned long long kFlagInc = 2ull << 62;
 constexpr unsigned long long kValMask = (1ull << 62) - 1;
 constexpr uint64_t kLookbackTimeoutNs = 2000000000ull;
 
-// bit c of the result = (byte c of x != 0)
+// bit c of the result = (byte c of x != 0), 8 bytes
 __device__ __forceinline__ uint32_t pack_row8(uint64_t x) {
   x |= x >> 4;
   x |= x >> 2;
   x |= x >> 1;
   x &= 0x0101010101010101ull;
   return static_cast<uint32_t>((x * 0x0102040810204080ull) >> 56);
+}
+
+// bit c of the result = (byte c of w != 0), 4 bytes.  The msb of
+// ((w & 0x7F..) + 0x7F..) | w is set iff the byte is non-zero (no carry
+// crosses a byte); the multiply gathers bits 7, 15, 23, 31 into 28..31.
+__device__ __forceinline__ uint32_t pack_word4(uint32_t w) {
+  const uint32_t h = (((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w) & 0x80808080u;
+  return (h * 0x00204081u) >> 28;
 }
 
 __device__ __forceinline__ unsigned long long ld_volatile(const unsigned long long* p) {
@@ -61,45 +78,175 @@ __device__ __forceinline__ uint64_t now_ns() {
   return t;
 }
 
+// Per-chunk state shared by a CTA's threads.
+struct ChunkState {
+  unsigned long long nnz;
+  unsigned long long excl;
+  int nf, np;
+  uint8_t cls[kMaxTilesPerChunk];
+  int rank[kMaxTilesPerChunk];
+  int plist[kMaxTilesPerChunk];
+};
+
+struct ChunkGeom {
+  long long row;
+  int cc, m, I, J0, nt, itc, itcols, bands, wpt;
+};
+
+__device__ __forceinline__ ChunkGeom chunk_geom(const EncodeParams& p, long long chunk) {
+  ChunkGeom g;
+  g.row = chunk / p.cpr;
+  g.cc = static_cast<int>(chunk % p.cpr);
+  g.m = static_cast<int>(g.row / p.n_tr);
+  g.I = static_cast<int>(g.row % p.n_tr);
+  g.J0 = g.cc * p.ct;
+  g.nt = min(p.ct, p.n_tc - g.J0);
+  g.itc = p.bn >> 3;
+  g.itcols = g.nt * g.itc;
+  g.bands = p.bm >> 3;
+  g.wpt = g.bands * g.itc;
+  return g;
+}
+
+// Phase 2: class of every OT of the chunk (0 empty, 1 full, 2 partial), one
+// warp per OT.
+__device__ __forceinline__ void classify(const uint64_t* words, const ChunkGeom& g, ChunkState& cs, int warp,
+                                         int lane, int nwarps) {
+  for (int t = warp; t < g.nt; t += nwarps) {
+    uint64_t any = 0, all = ~0ull;
+    for (int e = lane; e < g.wpt; e += 32) {
+      const int pb = e / g.itc, qq = e - pb * g.itc;
+      const uint64_t w = words[pb * g.itcols + t * g.itc + qq];
+      any |= w;
+      all &= w;
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      any |= __shfl_xor_sync(0xffffffffu, any, off);
+      all &= __shfl_xor_sync(0xffffffffu, all, off);
+    }
+    if (lane == 0) cs.cls[t] = any == 0 ? 0 : (all == ~0ull ? 1 : 2);
+  }
+}
+
+// Phase 3 (one warp): ranks inside the chunk and the chained prefix sum.
+__device__ __forceinline__ void rank_and_lookback(const EncodeParams& p, long long chunk, const ChunkGeom& g,
+                                                  ChunkState& cs, int lane) {
+  int nf = 0, np = 0;
+  for (int t0 = 0; t0 < g.nt; t0 += 32) {
+    const int t = t0 + lane;
+    const int cls = t < g.nt ? cs.cls[t] : 0;
+    const unsigned bf = __ballot_sync(0xffffffffu, cls == 1);
+    const unsigned bp = __ballot_sync(0xffffffffu, cls == 2);
+    const unsigned lt = (1u << lane) - 1u;
+    if (cls == 1) cs.rank[t] = nf + __popc(bf & lt);
+    if (cls == 2) {
+      const int r = np + __popc(bp & lt);
+      cs.rank[t] = r;
+      cs.plist[r] = t;
+    }
+    nf += __popc(bf);
+    np += __popc(bp);
+  }
+  const unsigned long long agg = (static_cast<unsigned long long>(nf) << 31) | static_cast<unsigned long long>(np);
+  unsigned long long excl = 0;
+  if (chunk == 0) {
+    if (lane == 0) st_volatile(&p.status[0], kFlagInc | agg);
+  } else {
+    if (lane == 0) st_volatile(&p.status[chunk], kFlagAgg | agg);
+    long long top = chunk - 1;
+    const uint64_t t_start = now_ns();
+    bool timed_out = false;
+    while (true) {
+      const long long idx = top - lane;
+      const unsigned long long v = idx >= 0 ? ld_volatile(&p.status[idx]) : kFlagInc;
+      const unsigned long long flag = v >> 62;
+      const unsigned inc = __ballot_sync(0xffffffffu, flag == 2);
+      const unsigned notready = __ballot_sync(0xffffffffu, flag == 0);
+      const int first_inc = inc ? __ffs(inc) - 1 : 32;
+      const unsigned needed = first_inc >= 31 ? 0xffffffffu : ((2u << first_inc) - 1u);
+      if ((notready & needed) && !timed_out) {
+        if (now_ns() - t_start > kLookbackTimeoutNs) {
+          timed_out = true;  // treat missing predecessors as empty, report
+          if (lane == 0)
+            atomicOr(reinterpret_cast<unsigned long long*>(&p.counts[3]),
+                     static_cast<unsigned long long>(STOF_DEVERR_LOOKBACK_TIMEOUT));
+        } else {
+          __nanosleep(64);
+        }
+        continue;
+      }
+      unsigned long long val = (lane <= first_inc && flag != 0) ? (v & kValMask) : 0ull;
+#pragma unroll
+      for (int off = 16; off; off >>= 1) val += __shfl_xor_sync(0xffffffffu, val, off);
+      excl += val;
+      if (first_inc < 32 || timed_out) break;
+      top -= 32;
+    }
+    if (lane == 0) st_volatile(&p.status[chunk], kFlagInc | (excl + agg));
+  }
+  if (lane == 0) {
+    cs.excl = excl;
+    cs.nf = nf;
+    cs.np = np;
+    if (cs.nnz) atomicAdd(reinterpret_cast<unsigned long long*>(&p.counts[2]), cs.nnz);
+  }
+}
+
+// Phase 4: column indices, row pointers and bitmaps into their final slots.
+__device__ __forceinline__ void write_outputs(const EncodeParams& p, long long chunk, const uint64_t* words,
+                                              const ChunkGeom& g, const ChunkState& cs, int tid, int nthreads) {
+  const long long ef = static_cast<long long>((cs.excl >> 31) & 0x7FFFFFFFull);
+  const long long ep = static_cast<long long>(cs.excl & 0x7FFFFFFFull);
+  const int nf = cs.nf, np = cs.np;
+  if (g.cc == 0 && tid == 0) {
+    p.full_row_ptr[g.row] = static_cast<int32_t>(ef);
+    p.part_row_ptr[g.row] = static_cast<int32_t>(ep);
+  }
+  for (int t = tid; t < g.nt; t += nthreads) {
+    const int cls = cs.cls[t];
+    if (cls == 1) p.full_col_idx[ef + cs.rank[t]] = g.J0 + t;
+    if (cls == 2) p.part_col_idx[ep + cs.rank[t]] = g.J0 + t;
+  }
+  const int total = np * g.wpt;
+  for (int e = tid; e < total; e += nthreads) {
+    const int r = e / g.wpt, x = e - r * g.wpt;
+    const int t = cs.plist[r];
+    const int pb = x / g.itc, qq = x - pb * g.itc;
+    p.bitmaps[(ep + r) * g.wpt + x] = words[pb * g.itcols + t * g.itc + qq];
+  }
+  if (chunk == p.n_chunks - 1 && tid == 0) {
+    p.full_row_ptr[p.n_rows] = static_cast<int32_t>(ef + nf);
+    p.part_row_ptr[p.n_rows] = static_cast<int32_t>(ep + np);
+    p.counts[0] = ef + nf;
+    p.counts[1] = ep + np;
+  }
+}
+
+// ---------------------------------------------------------------- kernel 1
 template <int VEC>  // bytes per load: 16 when rows and tiles are 16-byte aligned, else 8
 __global__ void __launch_bounds__(kThreads, 4) encode_kernel(const EncodeParams p) {
   extern __shared__ uint64_t s_words[];  // [bm/8][nt * bn/8]
   __shared__ long long s_chunk;
-  __shared__ unsigned long long s_nnz;
-  __shared__ unsigned long long s_excl;
-  __shared__ uint8_t s_class[kMaxTilesPerChunk];
-  __shared__ int s_rank[kMaxTilesPerChunk];
-  __shared__ int s_plist[kMaxTilesPerChunk];
-  __shared__ int s_nf, s_np;
-
+  __shared__ ChunkState cs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_chunk = static_cast<long long>(atomicAdd(p.ticket, 1ull));
-    s_nnz = 0;
+    cs.nnz = 0;
   }
   __syncthreads();
   const long long chunk = s_chunk;
   if (chunk >= p.n_chunks) return;
-
-  const long long row = chunk / p.cpr;
-  const int cc = static_cast<int>(chunk % p.cpr);
-  const int m = static_cast<int>(row / p.n_tr);
-  const int I = static_cast<int>(row % p.n_tr);
-  const int J0 = cc * p.ct;
-  const int nt = min(p.ct, p.n_tc - J0);
-  const int itc = p.bn >> 3;                 // IT columns per OT
-  const int itcols = nt * itc;               // IT columns in this chunk
-  const int bands = p.bm >> 3;
-  const int nwords = bands * itcols;
-  const uint8_t* base = p.mask + (static_cast<long long>(m) * p.lq + static_cast<long long>(I) * p.bm) * p.lk +
-                        static_cast<long long>(J0) * p.bn;
+  const ChunkGeom g = chunk_geom(p, chunk);
+  const uint8_t* base = p.mask + (static_cast<long long>(g.m) * p.lq + static_cast<long long>(g.I) * p.bm) * p.lk +
+                        static_cast<long long>(g.J0) * p.bn;
 
   // 1. read and pack (each unit = VEC/8 adjacent IT words of one 8-row band)
   unsigned long long local_nnz = 0;
-  constexpr int WPU = VEC / 8;                     // IT words per unit
-  constexpr int kUnroll = VEC == 16 ? 1 : 2;       // units in flight per thread (128 B)
-  const int upr = itcols / WPU;                    // units per band
-  const int nunits = bands * upr;
+  constexpr int WPU = VEC / 8;                 // IT words per unit
+  constexpr int kUnroll = VEC == 16 ? 1 : 2;   // units in flight per thread (128 B)
+  const int upr = g.itcols / WPU;              // units per band
+  const int nunits = g.bands * upr;
   for (int u0 = tid; u0 < nunits; u0 += kThreads * kUnroll) {
     uint4 v[kUnroll][8];
 #pragma unroll
@@ -133,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 4) encode_kernel(const EncodeParams 
                                       : ((static_cast<uint64_t>(v[u][r].w) << 32) | v[u][r].z);
             word |= static_cast<uint64_t>(pack_row8(x)) << (8 * r);
           }
-          s_words[pb * itcols + qu * WPU + h] = word;
+          s_words[pb * g.itcols + qu * WPU + h] = word;
           local_nnz += __popcll(word);
         }
       }
@@ -141,118 +288,161 @@ __global__ void __launch_bounds__(kThreads, 4) encode_kernel(const EncodeParams 
   }
 #pragma unroll
   for (int off = 16; off; off >>= 1) local_nnz += __shfl_xor_sync(0xffffffffu, local_nnz, off);
-  if (lane == 0 && local_nnz) atomicAdd(&s_nnz, local_nnz);
+  if (lane == 0 && local_nnz) atomicAdd(&cs.nnz, local_nnz);
   __syncthreads();
+  classify(s_words, g, cs, warp, lane, kThreads / 32);
+  __syncthreads();
+  if (warp == 0) rank_and_lookback(p, chunk, g, cs, lane);
+  __syncthreads();
+  write_outputs(p, chunk, s_words, g, cs, tid, kThreads);
+}
 
-  // 2. classify: 0 empty, 1 full, 2 partial
-  const int wpt = bands * itc;
-  for (int t = warp; t < nt; t += kThreads / 32) {
-    uint64_t any = 0, all = ~0ull;
-    for (int e = lane; e < wpt; e += 32) {
-      const int pb = e / itc, qq = e - pb * itc;
-      const uint64_t w = s_words[pb * itcols + t * itc + qq];
-      any |= w;
-      all &= w;
+// ---------------------------------------------------------------- kernel 2
+constexpr int kTmaStages = 4;
+constexpr int kSubW = 256;                 // mask columns per TMA box
+constexpr int kConsumers = 256;            // eight consumer warps
+constexpr uint64_t kPipeTimeoutNs = 2000000000ull;
+
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+__global__ void __launch_bounds__(kConsumers + 32, 1)
+    encode_tma_kernel(const __grid_constant__ CUtensorMap tm_mask, const EncodeParams p) {
+  using namespace ptx;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ uint64_t full[kTmaStages], empty[kTmaStages];
+  __shared__ long long stage_chunk[kTmaStages];
+  __shared__ long long s_cur;
+  __shared__ int s_fail_iter;
+  __shared__ int abort_flag;
+  __shared__ ChunkState cs;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int stage_bytes = p.bm * kSubW;
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
+  uint64_t* words = reinterpret_cast<uint64_t*>(smem + kTmaStages * stage_bytes);
+  if (tid == 0) {
+    for (int i = 0; i < kTmaStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumers);
     }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      any |= __shfl_xor_sync(0xffffffffu, any, off);
-      all &= __shfl_xor_sync(0xffffffffu, all, off);
-    }
-    if (lane == 0) s_class[t] = any == 0 ? 0 : (all == ~0ull ? 1 : 2);
+    s_fail_iter = 0x7FFFFFFF;
+    abort_flag = 0;
+    cs.nnz = 0;
+    fence_mbar_init();
   }
   __syncthreads();
+  volatile int* abort_v = &abort_flag;
 
-  // 3. local ranks and chained prefix sum (warp 0)
-  if (warp == 0) {
-    int nf = 0, np = 0;
-    for (int t0 = 0; t0 < nt; t0 += 32) {
-      const int t = t0 + lane;
-      const int cls = t < nt ? s_class[t] : 0;
-      const unsigned bf = __ballot_sync(0xffffffffu, cls == 1);
-      const unsigned bp = __ballot_sync(0xffffffffu, cls == 2);
-      const unsigned lt = (1u << lane) - 1u;
-      if (cls == 1) s_rank[t] = nf + __popc(bf & lt);
-      if (cls == 2) {
-        const int r = np + __popc(bp & lt);
-        s_rank[t] = r;
-        s_plist[r] = t;
-      }
-      nf += __popc(bf);
-      np += __popc(bp);
-    }
-    const unsigned long long agg =
-        (static_cast<unsigned long long>(nf) << 31) | static_cast<unsigned long long>(np);
-    unsigned long long excl = 0;
-    if (chunk == 0) {
-      if (lane == 0) st_volatile(&p.status[0], kFlagInc | agg);
-    } else {
-      if (lane == 0) st_volatile(&p.status[chunk], kFlagAgg | agg);
-      long long top = chunk - 1;
-      const uint64_t t_start = now_ns();
-      bool timed_out = false;
-      while (true) {
-        const long long idx = top - lane;
-        const unsigned long long v = idx >= 0 ? ld_volatile(&p.status[idx]) : kFlagInc;
-        const unsigned long long flag = v >> 62;
-        const unsigned inc = __ballot_sync(0xffffffffu, flag == 2);
-        const unsigned notready = __ballot_sync(0xffffffffu, flag == 0);
-        const int first_inc = inc ? __ffs(inc) - 1 : 32;
-        const unsigned needed = first_inc >= 31 ? 0xffffffffu : ((2u << first_inc) - 1u);
-        if ((notready & needed) && !timed_out) {
-          if (now_ns() - t_start > kLookbackTimeoutNs) {
-            timed_out = true;  // treat missing predecessors as empty, report
-            if (lane == 0) atomicOr(reinterpret_cast<unsigned long long*>(&p.counts[3]),
-                                    static_cast<unsigned long long>(STOF_DEVERR_LOOKBACK_TIMEOUT));
-          } else {
-            __nanosleep(64);
-          }
-          continue;
-        }
-        unsigned long long val = (lane <= first_inc && flag != 0) ? (v & kValMask) : 0ull;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) val += __shfl_xor_sync(0xffffffffu, val, off);
-        excl += val;
-        if (first_inc < 32 || timed_out) break;
-        top -= 32;
-      }
-      if (lane == 0) st_volatile(&p.status[chunk], kFlagInc | (excl + agg));
-    }
+  if (warp == kConsumers / 32) {
+    // ---------------------------------------------------------- producer
     if (lane == 0) {
-      s_excl = excl;
-      s_nf = nf;
-      s_np = np;
-      if (s_nnz) atomicAdd(reinterpret_cast<unsigned long long*>(&p.counts[2]), s_nnz);
+      prefetch_tmap(&tm_mask);
+      uint32_t gq = 0;
+      bool ok = true;
+      while (ok) {
+        const long long chunk = static_cast<long long>(atomicAdd(p.ticket, 1ull));
+        const bool last = chunk >= p.n_chunks;
+        int nsub = 1, x0 = 0, y = 0;
+        if (!last) {
+          const ChunkGeom g = chunk_geom(p, chunk);
+          x0 = g.J0 * p.bn;
+          y = g.m * p.lq + g.I * p.bm;
+          nsub = (g.nt * p.bn + kSubW - 1) / kSubW;
+        }
+        for (int sub = 0; sub < nsub; ++sub, ++gq) {
+          const int st = gq % kTmaStages;
+          if (!mbar_wait(&empty[st], ((gq / kTmaStages) & 1) ^ 1, abort_v, kPipeTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          stage_chunk[st] = last ? -1 : chunk;
+          if (last) {
+            mbar_arrive(&full[st]);  // no data: tells the consumers to stop
+          } else {
+            mbar_arrive_expect_tx(&full[st], stage_bytes);
+            tma_load_2d(stages + st * stage_bytes, &tm_mask, &full[st], x0 + sub * kSubW, y);
+          }
+        }
+        if (last) break;
+      }
+      if (!ok) {
+        *abort_v = 1;
+        atomicOr(reinterpret_cast<unsigned long long*>(&p.counts[3]),
+                 static_cast<unsigned long long>(STOF_DEVERR_LOOKBACK_TIMEOUT));
+        // let the copies this thread started land before the CTA exits
+        for (uint32_t k = gq > kTmaStages ? gq - kTmaStages : 0; k < gq; ++k)
+          mbar_wait_timeout(&full[k % kTmaStages], (k / kTmaStages) & 1, kPipeTimeoutNs);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- consumers
+    uint32_t gq = 0;
+    for (int iter = 0;; ++iter) {
+      if (tid == 0) {
+        const int st = gq % kTmaStages;
+        const bool ok = mbar_wait(&full[st], (gq / kTmaStages) & 1, abort_v, kPipeTimeoutNs);
+        s_cur = ok ? stage_chunk[st] : -2;
+      }
+      consumer_bar();
+      const long long chunk = s_cur;
+      if (chunk < 0) {
+        if (chunk == -2 && tid == 0)
+          atomicOr(reinterpret_cast<unsigned long long*>(&p.counts[3]),
+                   static_cast<unsigned long long>(STOF_DEVERR_LOOKBACK_TIMEOUT));
+        break;
+      }
+      const ChunkGeom g = chunk_geom(p, chunk);
+      const int nsub = (g.nt * p.bn + kSubW - 1) / kSubW;
+      // 1. pack: unit (band pb, 16-byte column group cg) of a 256-column box
+      unsigned long long local_nnz = 0;
+      bool bad = false;
+      const int nunits = g.bands * (kSubW / 16);
+      for (int sub = 0; sub < nsub; ++sub, ++gq) {
+        const int st = gq % kTmaStages;
+        if (!mbar_wait(&full[st], (gq / kTmaStages) & 1, abort_v, kPipeTimeoutNs)) bad = true;
+        const uint8_t* box = stages + st * stage_bytes;
+        for (int u = tid; u < nunits && !bad; u += kConsumers) {
+          const int pb = u >> 4, cgp = u & 15;
+          const int q0 = sub * (kSubW / 8) + 2 * cgp;  // IT column of the unit's first word
+          if (q0 >= g.itcols) continue;
+          uint64_t w0 = 0, w1 = 0;
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const uint4 x = *reinterpret_cast<const uint4*>(box + (8 * pb + r) * kSubW + 16 * cgp);
+            w0 |= static_cast<uint64_t>(pack_word4(x.x) | (pack_word4(x.y) << 4)) << (8 * r);
+            w1 |= static_cast<uint64_t>(pack_word4(x.z) | (pack_word4(x.w) << 4)) << (8 * r);
+          }
+          words[pb * g.itcols + q0] = w0;
+          local_nnz += __popcll(w0);
+          if (q0 + 1 < g.itcols) {
+            words[pb * g.itcols + q0 + 1] = w1;
+            local_nnz += __popcll(w1);
+          }
+        }
+        mbar_arrive(&empty[st]);
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) local_nnz += __shfl_xor_sync(0xffffffffu, local_nnz, off);
+      if (lane == 0 && local_nnz) atomicAdd(&cs.nnz, local_nnz);
+      if (bad) atomicMin(&s_fail_iter, iter);
+      consumer_bar();
+      if (s_fail_iter <= iter) {  // same decision in every consumer thread
+        if (tid == 0)
+          atomicOr(reinterpret_cast<unsigned long long*>(&p.counts[3]),
+                   static_cast<unsigned long long>(STOF_DEVERR_LOOKBACK_TIMEOUT));
+        *abort_v = 1;
+        break;
+      }
+      classify(words, g, cs, warp, lane, kConsumers / 32);
+      consumer_bar();
+      if (warp == 0) rank_and_lookback(p, chunk, g, cs, lane);
+      consumer_bar();
+      write_outputs(p, chunk, words, g, cs, tid, kConsumers);
+      if (tid == 0) cs.nnz = 0;  // read by rank_and_lookback before the barrier above
     }
   }
   __syncthreads();
-
-  // 4. outputs
-  const long long ef = static_cast<long long>((s_excl >> 31) & 0x7FFFFFFFull);
-  const long long ep = static_cast<long long>(s_excl & 0x7FFFFFFFull);
-  const int nf = s_nf, np = s_np;
-  if (cc == 0 && tid == 0) {
-    p.full_row_ptr[row] = static_cast<int32_t>(ef);
-    p.part_row_ptr[row] = static_cast<int32_t>(ep);
-  }
-  for (int t = tid; t < nt; t += kThreads) {
-    const int cls = s_class[t];
-    if (cls == 1) p.full_col_idx[ef + s_rank[t]] = J0 + t;
-    if (cls == 2) p.part_col_idx[ep + s_rank[t]] = J0 + t;
-  }
-  const int total = np * wpt;
-  for (int e = tid; e < total; e += kThreads) {
-    const int r = e / wpt, x = e - r * wpt;
-    const int t = s_plist[r];
-    const int pb = x / itc, qq = x - pb * itc;
-    p.bitmaps[(ep + r) * wpt + x] = s_words[pb * itcols + t * itc + qq];
-  }
-  if (chunk == p.n_chunks - 1 && tid == 0) {
-    p.full_row_ptr[p.n_rows] = static_cast<int32_t>(ef + nf);
-    p.part_row_ptr[p.n_rows] = static_cast<int32_t>(ep + np);
-    p.counts[0] = ef + nf;
-    p.counts[1] = ep + np;
-  }
 }
 
 }  // namespace
@@ -303,8 +493,29 @@ WorkspaceLayout workspace_layout(const EncodeGeom& g) {
 }
 
 cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s) {
-  // shared memory per CTA is at most bm * 1024 / 8 = 32 KB (bm <= 256)
   const bool vec16 = (p.lk % 16 == 0) && (p.bn % 16 == 0) && (reinterpret_cast<uintptr_t>(p.mask) % 16 == 0);
+  const bool tma = vec16 && p.bm <= 128 && static_cast<long long>(p.lq) * (p.n_rows / p.n_tr) < (1ll << 31);
+  if (tma) {
+    CUtensorMap map;
+    const uint64_t rows = static_cast<uint64_t>(p.n_rows / p.n_tr) * p.lq;
+    if (encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.mask, static_cast<uint64_t>(p.lk), rows,
+                             static_cast<uint64_t>(p.lk), kSubW, static_cast<uint32_t>(p.bm),
+                             CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      // stages + packed words + alignment slack: at most 128 KB + 16 KB + 1 KB (bm <= 128)
+      const size_t smem = static_cast<size_t>(kTmaStages) * p.bm * kSubW + g.smem_bytes + 1024;
+      static bool attr_done = false;
+      if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(encode_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kTmaStages * 128 * kSubW + 16 * 1024 + 1024));
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+      }
+      const long long grid = g.n_chunks < device_sm_count() ? g.n_chunks : device_sm_count();
+      encode_tma_kernel<<<static_cast<unsigned>(grid), kConsumers + 32, smem, s>>>(map, p);
+      return cudaGetLastError();
+    }
+  }
+  // shared memory per CTA is at most bm * 1024 / 8 = 32 KB (bm <= 256)
   if (vec16)
     encode_kernel<16><<<static_cast<unsigned>(g.n_chunks), kThreads, g.smem_bytes, s>>>(p);
   else

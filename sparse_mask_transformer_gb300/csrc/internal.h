@@ -1,5 +1,6 @@
 // Internal declarations shared by the translation units of libstof.so.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -9,6 +10,15 @@ namespace stof {
 
 // Remembers e (if it is an error) for stof_last_cuda_error(); returns e.
 cudaError_t record_cuda(cudaError_t e);
+
+// 2-D row-major tensor map (inner dimension contiguous, rows row_bytes
+// apart) through the driver entry point; false on failure.
+bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                          CUtensorMapSwizzle swizzle);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
 
 // ---------------------------------------------------------------- encoder
 // A chunk is one OT row band (bm mask rows) times `ct` consecutive OTs.
