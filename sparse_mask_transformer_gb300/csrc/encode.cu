@@ -20,23 +20,18 @@
 //      worked on;
 //   4. writes column indices, row pointers and the bitmaps of its partial
 //      OTs straight into their final slots.
-// Two kernels share phases 2-4:
-//   encode_tma_kernel  (rows and tiles 16-byte aligned, bm <= 128): one
-//      persistent CTA per SM; a producer warp streams 256-column x bm-row
-//      boxes of the mask with TMA through a 4-stage shared-memory ring, a
-//      chunk ahead, while eight consumer warps pack, classify and write, so
-//      the mask stream does not stop during a chunk's look-back and writes;
-//   encode_kernel      (any other shape): one chunk per CTA, coalesced
-//      streaming loads, four CTAs per SM.
+// One CTA per chunk, 256 threads, seven CTAs per SM so that the loads of
+// some CTAs overlap the look-back and writes of others; 16-byte (else
+// 8-byte) coalesced streaming loads.  (A persistent variant that streamed
+// the mask through a TMA ring with a producer warp was measured 3x slower
+// on the 16k workload: one CTA per SM cannot hide each chunk's look-back.)
 // Every wait on another CTA or warp is bounded; on timeout the CTA raises
 // STOF_DEVERR_LOOKBACK_TIMEOUT in the device error word and finishes.
-#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "internal.h"
-#include "sm100_ptx.cuh"
 
 namespace stof {
 
@@ -48,15 +43,6 @@ constexpr unsigned long long kFlagAgg = 1ull << 62;
 constexpr unsigned long long kFlagInc = 2ull << 62;
 constexpr unsigned long long kValMask = (1ull << 62) - 1;
 constexpr uint64_t kLookbackTimeoutNs = 2000000000ull;
-
-// bit c of the result = (byte c of x != 0), 8 bytes
-__device__ __forceinline__ uint32_t pack_row8(uint64_t x) {
-  x |= x >> 4;
-  x |= x >> 2;
-  x |= x >> 1;
-  x &= 0x0101010101010101ull;
-  return static_cast<uint32_t>((x * 0x0102040810204080ull) >> 56);
-}
 
 // bit c of the result = (byte c of w != 0), 4 bytes.  The msb of
 // ((w & 0x7F..) + 0x7F..) | w is set iff the byte is non-zero (no carry
@@ -225,7 +211,7 @@ __device__ __forceinline__ void write_outputs(const EncodeParams& p, long long c
 
 // ---------------------------------------------------------------- kernel 1
 template <int VEC>  // bytes per load: 16 when rows and tiles are 16-byte aligned, else 8
-__global__ void __launch_bounds__(kThreads, 4) encode_kernel(const EncodeParams p) {
+__global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams p) {
   extern __shared__ uint64_t s_words[];  // [bm/8][nt * bn/8]
   __shared__ long long s_chunk;
   __shared__ ChunkState cs;
@@ -276,9 +262,9 @@ __global__ void __launch_bounds__(kThreads, 4) encode_kernel(const EncodeParams 
           uint64_t word = 0;
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
-            const uint64_t x = h == 0 ? ((static_cast<uint64_t>(v[u][r].y) << 32) | v[u][r].x)
-                                      : ((static_cast<uint64_t>(v[u][r].w) << 32) | v[u][r].z);
-            word |= static_cast<uint64_t>(pack_row8(x)) << (8 * r);
+            const uint32_t lo = h == 0 ? v[u][r].x : v[u][r].z;
+            const uint32_t hi = h == 0 ? v[u][r].y : v[u][r].w;
+            word |= static_cast<uint64_t>(pack_word4(lo) | (pack_word4(hi) << 4)) << (8 * r);
           }
           s_words[pb * g.itcols + qu * WPU + h] = word;
           local_nnz += __popcll(word);
@@ -295,154 +281,6 @@ __global__ void __launch_bounds__(kThreads, 4) encode_kernel(const EncodeParams 
   if (warp == 0) rank_and_lookback(p, chunk, g, cs, lane);
   __syncthreads();
   write_outputs(p, chunk, s_words, g, cs, tid, kThreads);
-}
-
-// ---------------------------------------------------------------- kernel 2
-constexpr int kTmaStages = 4;
-constexpr int kSubW = 256;                 // mask columns per TMA box
-constexpr int kConsumers = 256;            // eight consumer warps
-constexpr uint64_t kPipeTimeoutNs = 2000000000ull;
-
-__device__ __forceinline__ void consumer_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-}
-
-__global__ void __launch_bounds__(kConsumers + 32, 1)
-    encode_tma_kernel(const __grid_constant__ CUtensorMap tm_mask, const EncodeParams p) {
-  using namespace ptx;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ uint64_t full[kTmaStages], empty[kTmaStages];
-  __shared__ long long stage_chunk[kTmaStages];
-  __shared__ long long s_cur;
-  __shared__ int s_fail_iter;
-  __shared__ int abort_flag;
-  __shared__ ChunkState cs;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int stage_bytes = p.bm * kSubW;
-  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
-  uint64_t* words = reinterpret_cast<uint64_t*>(smem + kTmaStages * stage_bytes);
-  if (tid == 0) {
-    for (int i = 0; i < kTmaStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kConsumers);
-    }
-    s_fail_iter = 0x7FFFFFFF;
-    abort_flag = 0;
-    cs.nnz = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  volatile int* abort_v = &abort_flag;
-
-  if (warp == kConsumers / 32) {
-    // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_mask);
-      uint32_t gq = 0;
-      bool ok = true;
-      while (ok) {
-        const long long chunk = static_cast<long long>(atomicAdd(p.ticket, 1ull));
-        const bool last = chunk >= p.n_chunks;
-        int nsub = 1, x0 = 0, y = 0;
-        if (!last) {
-          const ChunkGeom g = chunk_geom(p, chunk);
-          x0 = g.J0 * p.bn;
-          y = g.m * p.lq + g.I * p.bm;
-          nsub = (g.nt * p.bn + kSubW - 1) / kSubW;
-        }
-        for (int sub = 0; sub < nsub; ++sub, ++gq) {
-          const int st = gq % kTmaStages;
-          if (!mbar_wait(&empty[st], ((gq / kTmaStages) & 1) ^ 1, abort_v, kPipeTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          stage_chunk[st] = last ? -1 : chunk;
-          if (last) {
-            mbar_arrive(&full[st]);  // no data: tells the consumers to stop
-          } else {
-            mbar_arrive_expect_tx(&full[st], stage_bytes);
-            tma_load_2d(stages + st * stage_bytes, &tm_mask, &full[st], x0 + sub * kSubW, y);
-          }
-        }
-        if (last) break;
-      }
-      if (!ok) {
-        *abort_v = 1;
-        atomicOr(reinterpret_cast<unsigned long long*>(&p.counts[3]),
-                 static_cast<unsigned long long>(STOF_DEVERR_LOOKBACK_TIMEOUT));
-        // let the copies this thread started land before the CTA exits
-        for (uint32_t k = gq > kTmaStages ? gq - kTmaStages : 0; k < gq; ++k)
-          mbar_wait_timeout(&full[k % kTmaStages], (k / kTmaStages) & 1, kPipeTimeoutNs);
-      }
-    }
-  } else {
-    // ---------------------------------------------------------- consumers
-    uint32_t gq = 0;
-    for (int iter = 0;; ++iter) {
-      if (tid == 0) {
-        const int st = gq % kTmaStages;
-        const bool ok = mbar_wait(&full[st], (gq / kTmaStages) & 1, abort_v, kPipeTimeoutNs);
-        s_cur = ok ? stage_chunk[st] : -2;
-      }
-      consumer_bar();
-      const long long chunk = s_cur;
-      if (chunk < 0) {
-        if (chunk == -2 && tid == 0)
-          atomicOr(reinterpret_cast<unsigned long long*>(&p.counts[3]),
-                   static_cast<unsigned long long>(STOF_DEVERR_LOOKBACK_TIMEOUT));
-        break;
-      }
-      const ChunkGeom g = chunk_geom(p, chunk);
-      const int nsub = (g.nt * p.bn + kSubW - 1) / kSubW;
-      // 1. pack: unit (band pb, 16-byte column group cg) of a 256-column box
-      unsigned long long local_nnz = 0;
-      bool bad = false;
-      const int nunits = g.bands * (kSubW / 16);
-      for (int sub = 0; sub < nsub; ++sub, ++gq) {
-        const int st = gq % kTmaStages;
-        if (!mbar_wait(&full[st], (gq / kTmaStages) & 1, abort_v, kPipeTimeoutNs)) bad = true;
-        const uint8_t* box = stages + st * stage_bytes;
-        for (int u = tid; u < nunits && !bad; u += kConsumers) {
-          const int pb = u >> 4, cgp = u & 15;
-          const int q0 = sub * (kSubW / 8) + 2 * cgp;  // IT column of the unit's first word
-          if (q0 >= g.itcols) continue;
-          uint64_t w0 = 0, w1 = 0;
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const uint4 x = *reinterpret_cast<const uint4*>(box + (8 * pb + r) * kSubW + 16 * cgp);
-            w0 |= static_cast<uint64_t>(pack_word4(x.x) | (pack_word4(x.y) << 4)) << (8 * r);
-            w1 |= static_cast<uint64_t>(pack_word4(x.z) | (pack_word4(x.w) << 4)) << (8 * r);
-          }
-          words[pb * g.itcols + q0] = w0;
-          local_nnz += __popcll(w0);
-          if (q0 + 1 < g.itcols) {
-            words[pb * g.itcols + q0 + 1] = w1;
-            local_nnz += __popcll(w1);
-          }
-        }
-        mbar_arrive(&empty[st]);
-      }
-#pragma unroll
-      for (int off = 16; off; off >>= 1) local_nnz += __shfl_xor_sync(0xffffffffu, local_nnz, off);
-      if (lane == 0 && local_nnz) atomicAdd(&cs.nnz, local_nnz);
-      if (bad) atomicMin(&s_fail_iter, iter);
-      consumer_bar();
-      if (s_fail_iter <= iter) {  // same decision in every consumer thread
-        if (tid == 0)
-          atomicOr(reinterpret_cast<unsigned long long*>(&p.counts[3]),
-                   static_cast<unsigned long long>(STOF_DEVERR_LOOKBACK_TIMEOUT));
-        *abort_v = 1;
-        break;
-      }
-      classify(words, g, cs, warp, lane, kConsumers / 32);
-      consumer_bar();
-      if (warp == 0) rank_and_lookback(p, chunk, g, cs, lane);
-      consumer_bar();
-      write_outputs(p, chunk, words, g, cs, tid, kConsumers);
-      if (tid == 0) cs.nnz = 0;  // read by rank_and_lookback before the barrier above
-    }
-  }
-  __syncthreads();
 }
 
 }  // namespace
@@ -494,27 +332,6 @@ WorkspaceLayout workspace_layout(const EncodeGeom& g) {
 
 cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s) {
   const bool vec16 = (p.lk % 16 == 0) && (p.bn % 16 == 0) && (reinterpret_cast<uintptr_t>(p.mask) % 16 == 0);
-  const bool tma = vec16 && p.bm <= 128 && static_cast<long long>(p.lq) * (p.n_rows / p.n_tr) < (1ll << 31);
-  if (tma) {
-    CUtensorMap map;
-    const uint64_t rows = static_cast<uint64_t>(p.n_rows / p.n_tr) * p.lq;
-    if (encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.mask, static_cast<uint64_t>(p.lk), rows,
-                             static_cast<uint64_t>(p.lk), kSubW, static_cast<uint32_t>(p.bm),
-                             CU_TENSOR_MAP_SWIZZLE_NONE)) {
-      // stages + packed words + alignment slack: at most 128 KB + 16 KB + 1 KB (bm <= 128)
-      const size_t smem = static_cast<size_t>(kTmaStages) * p.bm * kSubW + g.smem_bytes + 1024;
-      static bool attr_done = false;
-      if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(encode_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kTmaStages * 128 * kSubW + 16 * 1024 + 1024));
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-      }
-      const long long grid = g.n_chunks < device_sm_count() ? g.n_chunks : device_sm_count();
-      encode_tma_kernel<<<static_cast<unsigned>(grid), kConsumers + 32, smem, s>>>(map, p);
-      return cudaGetLastError();
-    }
-  }
   // shared memory per CTA is at most bm * 1024 / 8 = 32 KB (bm <= 256)
   if (vec16)
     encode_kernel<16><<<static_cast<unsigned>(g.n_chunks), kThreads, g.smem_bytes, s>>>(p);
