@@ -118,6 +118,15 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+// d0 += a0, d1 += a1 in one packed fp32x2 add
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rd;\n\t"
+      "mov.b64 rd, {%0, %1};\n\tmov.b64 ra, {%2, %3};\n\t"
+      "add.rn.ftz.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+
 // Barrier over `count` threads (a multiple of 32) under hardware barrier id.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float x0, x1;
             ffma2(x0, x1, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]), c, c, nmu, nmu);
             const float e0 = ex2(x0), e1 = ex2(x1);
-            ls[(i >> 1) & 3] += e0 + e1;
+            fadd2(ls[((i >> 1) & 1) * 2], ls[((i >> 1) & 1) * 2 + 1], e0, e1);
             pk[i / 2] = pack2<BF16>(e0, e1);
           }
           tmem_st16(tP0 + sb * 64 + lane_off + half * 32 + cc * 16, pk);
