@@ -8,31 +8,33 @@
 // and partial OTs through their 8x8 inner-tile bitmaps (same section,
 // two-level storage format: exact masking).
 //
-// One CTA computes one 128-row query tile (b, h, OT row I):
+// One CTA computes one 128-row query tile (b, h, OT row I) over the n OTs
+// listed for its row (full OTs first):
 //   warp 0      TMA producer: the Q tile once, then the K tile of every
 //               listed OT into an NK-stage ring (a stage is freed as soon
 //               as its S = Q K^T is done) and, for a partial OT, its 2 KB of
 //               IT bitmaps into an NB-stage ring (freed as soon as the
-//               softmax has read them: the softmax needs the bitmap right
-//               after S, long before the tile's V);
+//               softmax has read them);
 //   warp 1      TMA producer: the V tiles into an NV-stage ring (freed when
 //               its O += P V is done);
-//   warp 2      allocates TMEM and issues the score MMAs, two tiles ahead:
-//               S_{t+2} = Q K_{t+2}^T as soon as K_{t+2} has landed and the
-//               softmax has read S_t out of the same buffer;
-//   warp 3      issues O += P_t V_t as soon as P_t and V_t are ready.
-//               Each role has a warp of its own: divergent lanes of one warp
-//               are not scheduled promptly while another lane waits;
-//   warps 4..11 two softmax warpgroups; thread (warpgroup g, row r) owns
-//               columns 64g..64g+63 of S row r: it reads them from TMEM,
-//               applies the bitmap on partial OTs, meets the other half's
-//               row max in shared memory, evaluates exp2 in fp32, writes its
-//               half of P (fp16/bf16) to TMEM, keeps its half of the row
-//               sum, rescales its half of O in TMEM when the running max
-//               moved by more than 2^8 (lazy rescaling: exact, because O
-//               and l share the reference max), and finally writes its half
-//               of O / l (0 for a row without valid keys).
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512).
+//   warp 2      allocates TMEM and issues the score MMAs S_g = Q K_t^T;
+//   warp 3      issues the PV MMAs O_g += P_t V_t.
+//               (Every role has a warp of its own: divergent lanes of one
+//               warp are not scheduled promptly while another lane waits.)
+//   warps 4..7  softmax warpgroup 0, tiles t = 0, 2, 4, ...;
+//   warps 8..11 softmax warpgroup 1, tiles t = 1, 3, 5, ...
+// Warpgroup g owns its score buffer S_g, its accumulator O_g, and its own
+// running max and sum: the two warpgroups never wait for each other inside
+// the tile loop, so one computes while the other waits for its next S.  A
+// thread owns one query row (= TMEM lane): it reads its 128 scores, masks
+// partial OTs by their IT bitmaps, updates its running max lazily (O_g is
+// rescaled in TMEM only when the max grows by more than 2^8; exact, because
+// O_g and l_g share the reference), evaluates exp2 in fp32, and writes P as
+// fp16/bf16 over the first 64 columns of S_g, where the PV MMA reads it.  The
+// next score MMA into S_g waits for that PV to complete.  At the end the two
+// partial results are merged: O = (a0 O_0 + a1 O_1) / (a0 l_0 + a1 l_1),
+// a_g = 2^(m_g - max(m_0, m_1)); 0 for a row without valid keys.
+// TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,256+d) O_1 [256+d,256+2d).
 // Every pipeline wait is bounded; on timeout the CTA raises
 // STOF_DEVERR_PIPE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -84,13 +86,12 @@ struct alignas(1024) Smem {
   uint64_t b_full[Cfg<D>::NB];
   uint64_t b_free[Cfg<D>::NB];
   uint64_t s_full[2];
-  uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t drain;
   uint64_t drain_qk;
-  float rowmax[2][2][kBM];   // [tile parity][column half][row]
-  float rowl[2][kBM];
+  float rowm[2][kBM];        // final running max of each warpgroup, per row
+  float rowl[2][kBM];        // final running sum of each warpgroup, per row
   uint32_t tmem_base;
   int abort_flag;
   int fail_tile;             // first tile at which a softmax thread failed
@@ -147,6 +148,15 @@ __device__ __forceinline__ void raise_error(int64_t* err, unsigned long long bit
   atomicOr(reinterpret_cast<unsigned long long*>(err), bit);
 }
 
+// Register split: the kernel is launched with kLaunchRegs per thread (the
+// most 384 threads can have); warpgroup 0 (producers, MMA issuers) drops to
+// kProducerRegs, the two softmax warpgroups rise to kSoftmaxRegs.  The host
+// refuses to launch a build whose register count is not kLaunchRegs, since
+// the raise would then wait for registers that are never released.
+constexpr int kLaunchRegs = 168, kProducerRegs = 56, kSoftmaxRegs = 224;
+static_assert(kProducerRegs * 128 + kSoftmaxRegs * 256 <= kLaunchRegs * kThreads, "register split");
+static_assert(kLaunchRegs * kThreads <= 65536, "register file");
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     blockwise_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -181,14 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < C::NB; ++i) {
       mbar_init(&s.b_full[i], 1);
-      mbar_init(&s.b_free[i], 256);
+      mbar_init(&s.b_free[i], 128);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.s_free[i], 256);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.p_full[i], 256);
+      mbar_init(&s.p_full[i], 128);
       mbar_init(&s.pv_done[i], 1);
     }
     mbar_init(&s.drain, 1);
@@ -204,13 +213,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-
   const uint32_t tbase = s.tmem_base;
-  const uint32_t tS0 = tbase, tO = tbase + 256, tP0 = tbase + 384;
+  const uint32_t tS0 = tbase, tO0 = tbase + 256;  // S_g at tS0 + 128 g, O_g at tO0 + D g
   volatile int* abort_flag = &s.abort_flag;
   auto fail = [&]() {
     *abort_flag = 1;
     raise_error(p.err, STOF_DEVERR_PIPE_TIMEOUT);
+  };
+
+  // a wait whose result is the same in every lane of the warp (tcgen05.ld/st
+  // and the issuers' loops are warp-collective)
+  auto wwait = [&](uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitNs));
   };
 
   // column index of the t-th listed OT of this row (full OTs first)
@@ -225,284 +239,279 @@ __global__ void __launch_bounds__(kThreads, 1)
     return J;
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ K producer
-    if (lane == 0) {  // Q, then K tiles
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      const int qrow = bh * p.L + I * kBM;
-      mbar_arrive_expect_tx(&s.q_full, C::TILE_BYTES);
+  // the softmax rows (128 fp32 scores each) get the registers that the
+  // producer and issuer warpgroup does not need
+  if (warp < 4) {
+    regs_dec<kProducerRegs>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ K producer
+      if (lane == 0) {  // Q, then K tiles
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        const int qrow = bh * p.L + I * kBM;
+        mbar_arrive_expect_tx(&s.q_full, C::TILE_BYTES);
 #pragma unroll
-      for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow);
-      int issued = 0, bits_issued = 0;
-      for (int t = 0; t < n; ++t) {
-        const int st = t % C::NK;
-        if (t >= C::NK && !mbar_wait(&s.k_free[st], ((t / C::NK) - 1) & 1, abort_flag, kWaitNs)) {
-          fail();
-          break;
-        }
-        long long e;
-        const int krow = bh * p.L + column_of(t, &e) * kBN;
-        if (t >= nf) {  // the IT bitmaps of a partial OT, into their own ring
-          const int u = t - nf, bst = u % C::NB;
-          if (u >= C::NB && !mbar_wait(&s.b_free[bst], ((u / C::NB) - 1) & 1, abort_flag, kWaitNs)) {
+        for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow);
+        int issued = 0, bits_issued = 0;
+        for (int t = 0; t < n; ++t) {
+          const int st = t % C::NK;
+          if (t >= C::NK && !mbar_wait(&s.k_free[st], ((t / C::NK) - 1) & 1, abort_flag, kWaitNs)) {
             fail();
             break;
           }
-          mbar_arrive_expect_tx(&s.b_full[bst], C::BITMAP_WORDS * 8);
-          bulk_load(s.bits[bst], p.bitmaps + e * C::BITMAP_WORDS, C::BITMAP_WORDS * 8, &s.b_full[bst]);
-          bits_issued = u + 1;
+          long long e;
+          const int krow = bh * p.L + column_of(t, &e) * kBN;
+          if (t >= nf) {  // the IT bitmaps of a partial OT, into their own ring
+            const int u = t - nf, bst = u % C::NB;
+            if (u >= C::NB && !mbar_wait(&s.b_free[bst], ((u / C::NB) - 1) & 1, abort_flag, kWaitNs)) {
+              fail();
+              break;
+            }
+            mbar_arrive_expect_tx(&s.b_full[bst], C::BITMAP_WORDS * 8);
+            bulk_load(s.bits[bst], p.bitmaps + e * C::BITMAP_WORDS, C::BITMAP_WORDS * 8, &s.b_full[bst]);
+            bits_issued = u + 1;
+          }
+          mbar_arrive_expect_tx(&s.k_full[st], C::TILE_BYTES);
+#pragma unroll
+          for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.k[st] + r * 16384, &tmK, &s.k_full[st], 64 * r, krow);
+          issued = t + 1;
         }
-        mbar_arrive_expect_tx(&s.k_full[st], C::TILE_BYTES);
-#pragma unroll
-        for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.k[st] + r * 16384, &tmK, &s.k_full[st], 64 * r, krow);
-        issued = t + 1;
-      }
-      if (*abort_flag) {  // let every copy this thread started land before exit
-        mbar_wait_timeout(&s.q_full, 0, kWaitNs);
-        for (int t = issued - C::NK < 0 ? 0 : issued - C::NK; t < issued; ++t)
-          mbar_wait_timeout(&s.k_full[t % C::NK], (t / C::NK) & 1, kWaitNs);
-        for (int u = bits_issued - C::NB < 0 ? 0 : bits_issued - C::NB; u < bits_issued; ++u)
-          mbar_wait_timeout(&s.b_full[u % C::NB], (u / C::NB) & 1, kWaitNs);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ V producer
-    if (lane == 0) {  // V tiles
-      prefetch_tmap(&tmV);
-      int issued = 0;
-      for (int t = 0; t < n; ++t) {
-        const int st = t % C::NV;
-        if (t >= C::NV && !mbar_wait(&s.v_free[st], ((t / C::NV) - 1) & 1, abort_flag, kWaitNs)) {
-          fail();
-          break;
+        if (*abort_flag) {  // let every copy this thread started land before exit
+          mbar_wait_timeout(&s.q_full, 0, kWaitNs);
+          for (int t = issued - C::NK < 0 ? 0 : issued - C::NK; t < issued; ++t)
+            mbar_wait_timeout(&s.k_full[t % C::NK], (t / C::NK) & 1, kWaitNs);
+          for (int u = bits_issued - C::NB < 0 ? 0 : bits_issued - C::NB; u < bits_issued; ++u)
+            mbar_wait_timeout(&s.b_full[u % C::NB], (u / C::NB) & 1, kWaitNs);
         }
-        long long e;
-        const int vrow = bh * p.L + column_of(t, &e) * kBN;
-        mbar_arrive_expect_tx(&s.v_full[st], C::TILE_BYTES);
-#pragma unroll
-        for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.v[st] + r * 16384, &tmV, &s.v_full[st], 64 * r, vrow);
-        issued = t + 1;
       }
-      if (*abort_flag) {
-        for (int t = issued - C::NV < 0 ? 0 : issued - C::NV; t < issued; ++t)
-          mbar_wait_timeout(&s.v_full[t % C::NV], (t / C::NV) & 1, kWaitNs);
-      }
-    }
-  } else if (warp == 2 || warp == 3) {
-    // ------------------------------------------------------------ MMA issuers
-    // Warp 2 issues the score MMAs, warp 3 the PV MMAs; each commits to its
-    // own barriers (a commit tracks the issuing thread's MMAs only), and the
-    // TMEM regions they write are disjoint.  Waits suspend the thread, so
-    // it takes no issue slots from the softmax warps sharing its SM
-    // sub-partition; each MMA group is straight-line code.
-    constexpr uint32_t idesc_qk = idesc_f16(BF16 ? 1 : 0, 0, kBM, kBN);
-    constexpr uint32_t idesc_pv = idesc_f16(BF16 ? 1 : 0, 1, kBM, D);
-    // Descriptors are built once; a K step only adds a compile-time offset
-    // (in 16-byte units) to the start-address field.  An issuing thread is
-    // latency-bound, so per-MMA descriptor arithmetic would otherwise
-    // throttle the tensor core.
-    constexpr uint64_t kStage = C::TILE_BYTES / 16;
-    if (warp == 2 && lane == 0) {
-      const uint64_t qdesc = smem_desc_sw128(smem_u32(s.q), 16, 1024);
-      const uint64_t kdesc0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
-      bool ok = n == 0 || mbar_wait(&s.q_full, 0, abort_flag, kWaitNs);
-      for (int t = 0; ok && t < n; ++t) {
-        const int st = t % C::NK, sb = t & 1;
-        if (t >= 2 && !mbar_wait(&s.s_free[sb], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-        if (!mbar_wait(&s.k_full[st], (t / C::NK) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t kd = kdesc0 + static_cast<uint64_t>(st) * kStage;
-        const uint32_t d_tmem = tS0 + sb * 128;
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ V producer
+      if (lane == 0) {  // V tiles
+        prefetch_tmap(&tmV);
+        int issued = 0;
+        for (int t = 0; t < n; ++t) {
+          const int st = t % C::NV;
+          if (t >= C::NV && !mbar_wait(&s.v_free[st], ((t / C::NV) - 1) & 1, abort_flag, kWaitNs)) {
+            fail();
+            break;
+          }
+          long long e;
+          const int vrow = bh * p.L + column_of(t, &e) * kBN;
+          mbar_arrive_expect_tx(&s.v_full[st], C::TILE_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KB per atom, 32 B per K step
-          mma_f16_ss(d_tmem, qdesc + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+          for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.v[st] + r * 16384, &tmV, &s.v_full[st], 64 * r, vrow);
+          issued = t + 1;
         }
-        mma_commit(&s.s_full[sb]);
-        mma_commit(&s.k_free[st]);
+        if (*abort_flag) {
+          for (int t = issued - C::NV < 0 ? 0 : issued - C::NV; t < issued; ++t)
+            mbar_wait_timeout(&s.v_full[t % C::NV], (t / C::NV) & 1, kWaitNs);
+        }
       }
-      if (!ok) fail();
-      mma_commit(&s.drain_qk);  // all of this thread's MMAs done before TMEM is freed
-      mbar_wait_timeout(&s.drain_qk, 0, kWaitNs);
-    } else if (warp == 3 && lane == 0) {
-      const uint64_t vdesc0 = smem_desc_sw128(smem_u32(s.v[0]), 16384, 1024);
-      bool ok = true;
-      for (int t = 0; ok && t < n; ++t) {
-        const int st = t % C::NV, pb = t & 1;
-        if (!mbar_wait(&s.p_full[pb], (t >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-        if (!mbar_wait(&s.v_full[st], (t / C::NV) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t vd = vdesc0 + static_cast<uint64_t>(st) * kStage;
-        const uint32_t a_tmem = tP0 + pb * 64;
-        mma_f16_ts(tO, a_tmem, vd, idesc_pv, t > 0 ? 1u : 0u);
+    } else {  // warps 2 and 3
+      // ------------------------------------------------------------ MMA issuers
+      // Warp 2 issues the score MMAs, warp 3 the PV MMAs; each commits to its
+      // own barriers (a commit tracks the issuing thread's MMAs only).  Each
+      // MMA group is straight-line code.
+      constexpr uint32_t idesc_qk = idesc_f16(BF16 ? 1 : 0, 0, kBM, kBN);
+      constexpr uint32_t idesc_pv = idesc_f16(BF16 ? 1 : 0, 1, kBM, D);
+      // Descriptors are built once; a K step only adds a compile-time offset
+      // (in 16-byte units) to the start-address field.  An issuing thread is
+      // latency-bound, so per-MMA descriptor arithmetic would otherwise
+      // throttle the tensor core.
+      constexpr uint64_t kStage = C::TILE_BYTES / 16;
+      // The whole warp runs the loop (warp-uniform waits and descriptor
+      // arithmetic, which keeps the descriptors in uniform registers); one
+      // elected lane issues the MMAs and commits.
+      if (warp == 2) {
+        const uint64_t qdesc = smem_desc_sw128(smem_u32(s.q), 16, 1024);
+        const uint64_t kdesc0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
+        bool ok = n == 0 || wwait(&s.q_full, 0);
+        for (int t = 0; ok && t < n; ++t) {
+          const int st = t % C::NK, g = t & 1;
+          // S_g still holds P of tile t-2 until that tile's PV is done
+          if (t >= 2 && !wwait(&s.pv_done[g], ((t - 2) >> 1) & 1)) { ok = false; break; }
+          if (!wwait(&s.k_full[st], (t / C::NK) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t kd = kdesc0 + static_cast<uint64_t>(st) * kStage;
+          const uint32_t d_tmem = tS0 + g * 128;
+          if (elect_one()) {
 #pragma unroll
-        for (int kk = 1; kk < kBN / 16; ++kk)  // 16 keys x 128 B per K step
-          mma_f16_ts(tO, a_tmem + kk * 8, vd + kk * 128, idesc_pv, 1u);
-        mma_commit(&s.pv_done[pb]);
-        mma_commit(&s.v_free[st]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KB per atom, 32 B per K step
+              mma_f16_ss(d_tmem, qdesc + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&s.s_full[g]);
+            mma_commit(&s.k_free[st]);
+          }
+          __syncwarp();
+        }
+        if (elect_one()) {  // the lane that issued the MMAs
+          if (!ok) fail();
+          mma_commit(&s.drain_qk);  // all of this thread's MMAs done before TMEM is freed
+          mbar_wait_timeout(&s.drain_qk, 0, kWaitNs);
+        }
+      } else {
+        const uint64_t vdesc0 = smem_desc_sw128(smem_u32(s.v[0]), 16384, 1024);
+        bool ok = true;
+        for (int t = 0; ok && t < n; ++t) {
+          const int st = t % C::NV, g = t & 1;
+          if (!wwait(&s.p_full[g], (t >> 1) & 1)) { ok = false; break; }
+          if (!wwait(&s.v_full[st], (t / C::NV) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t vd = vdesc0 + static_cast<uint64_t>(st) * kStage;
+          const uint32_t a_tmem = tS0 + g * 128;  // P_t over the first 64 columns of S_g
+          const uint32_t d_tmem = tO0 + g * D;
+          if (elect_one()) {
+            mma_f16_ts(d_tmem, a_tmem, vd, idesc_pv, t >= 2 ? 1u : 0u);  // first tile of O_g overwrites
+#pragma unroll
+            for (int kk = 1; kk < kBN / 16; ++kk)  // 16 keys x 128 B per K step
+              mma_f16_ts(d_tmem, a_tmem + kk * 8, vd + kk * 128, idesc_pv, 1u);
+            mma_commit(&s.pv_done[g]);
+            mma_commit(&s.v_free[st]);
+          }
+          __syncwarp();
+        }
+        if (elect_one()) {  // the lane that issued the MMAs
+          if (!ok) fail();
+          mma_commit(&s.drain);
+          mbar_wait_timeout(&s.drain, 0, kWaitNs);
+        }
       }
-      if (!ok) fail();
-      mma_commit(&s.drain);
-      mbar_wait_timeout(&s.drain, 0, kWaitNs);
     }
   } else {
+    regs_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
-    // Two warpgroups split every S row: warps 4..7 take columns 0..63 and
-    // warps 8..11 columns 64..127 of the same 128 rows (TMEM lane quarter =
-    // warp % 4).  Partial row maxima meet in shared memory once per tile.
     const int quarter = warp & 3;
-    const int half = (warp - 4) >> 2;
+    const int g = (warp - 4) >> 2;      // warpgroup: tiles t with t % 2 == g
     const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tS0 + g * 128 + lane_off;
+    const uint32_t tO = tO0 + g * D + lane_off;
     const float c = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    // tcgen05.ld/st are warp-collective: every wait result is warp-uniform
-    auto wwait = [&](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitNs));
-    };
-    // failures are voted before each named barrier so both warpgroups leave
-    // the loop at the same tile (bar.sync has no timeout)
-    auto vote_fail = [&](int t) { atomicMin(&s.fail_tile, t); };
-    for (int t = 0; t < n; ++t) {
-      const int sb = t & 1;
-      bool good = ok && wwait(&s.s_full[sb], (t >> 1) & 1);
-      uint32_t sr[2][32];
-      float mx = -INFINITY;
-      if (good) {
-        tc_fence_after();
-        tmem_ld32(tS0 + sb * 128 + lane_off + half * 64, sr[0]);
-        tmem_ld32(tS0 + sb * 128 + lane_off + half * 64 + 32, sr[1]);
-        tmem_ld_wait(sr[0]);
-        tmem_ld_wait(sr[1]);
-        tc_fence_before();
-        mbar_arrive(&s.s_free[sb]);
-        if (t >= nf) {  // partial OT: keep only the keys whose bit is set
-          const int u = t - nf, bst = u % C::NB;
-          good = wwait(&s.b_full[bst], (u / C::NB) & 1);
-          if (good) {
-            const uint64_t* bw = s.bits[bst] + (r >> 3) * (kBN / 8) + half * 8;
-            const int shift = (r & 7) * 8;
+    for (int t = g; ok && t < n; t += 2) {
+      const int j = t >> 1;  // this warpgroup's j-th tile
+      if (!wwait(&s.s_full[g], j & 1)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[4][32];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              uint32_t bits32 = 0;
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                bits32 |= (static_cast<uint32_t>(bw[4 * cc + u] >> shift) & 0xFFu) << (8 * u);
+      for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(sr[cc]);
+      if (t >= nf) {  // partial OT: keep only the keys whose bit is set
+        const int u = t - nf, bst = u % C::NB;
+        if (!wwait(&s.b_full[bst], (u / C::NB) & 1)) { ok = false; break; }
+        const uint64_t* bw = s.bits[bst] + (r >> 3) * (kBN / 8);
+        const int shift = (r & 7) * 8;
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                sr[cc][i] = (bits32 >> i) & 1u ? sr[cc][i] : 0xFF800000u;  // -inf
-            }
-            mbar_arrive(&s.b_free[bst]);  // this thread is done with the bitmap
-          }
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t bits32 = 0;
+#pragma unroll
+          for (int uu = 0; uu < 4; ++uu)
+            bits32 |= (static_cast<uint32_t>(bw[4 * cc + uu] >> shift) & 0xFFu) << (8 * uu);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sr[cc][i] = (bits32 >> i) & 1u ? sr[cc][i] : 0xFF800000u;  // -inf
         }
-        if (good) {
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        mbar_arrive(&s.b_free[bst]);  // this thread is done with the bitmap
+      }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc)
+      for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              const int k4 = (cc * 4 + i / 8) & 3;
-              m4[k4] = max3(m4[k4], __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]));
-              m4[k4] = max3(m4[k4], __uint_as_float(sr[cc][i + 2]), __uint_as_float(sr[cc][i + 3]));
-              m4[k4] = max3(m4[k4], __uint_as_float(sr[cc][i + 4]), __uint_as_float(sr[cc][i + 5]));
-              m4[k4] = max3(m4[k4], __uint_as_float(sr[cc][i + 6]), __uint_as_float(sr[cc][i + 7]));
-            }
-          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        for (int i = 0; i < 32; i += 8) {
+          m4[cc] = max3(m4[cc], __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]));
+          m4[cc] = max3(m4[cc], __uint_as_float(sr[cc][i + 2]), __uint_as_float(sr[cc][i + 3]));
+          m4[cc] = max3(m4[cc], __uint_as_float(sr[cc][i + 4]), __uint_as_float(sr[cc][i + 5]));
+          m4[cc] = max3(m4[cc], __uint_as_float(sr[cc][i + 6]), __uint_as_float(sr[cc][i + 7]));
         }
-      }
-      if (!good) vote_fail(t);
-      s.rowmax[sb][half][r] = mx;
-      named_bar_sync(1, 256);
-      if (s.fail_tile <= t) {
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, s.rowmax[sb][half ^ 1][r]);
-
-      const float mt = mx * c;
+      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c;
       float alpha = 1.f;
       if (mt > m_ref + kRescaleThreshold) {  // also the first finite max
         alpha = ex2(m_ref - mt);             // 0 when m_ref = -inf
         m_ref = mt;
       }
       l *= alpha;
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O_g holds tiles g, g+2, ..., t-2; their PVs are complete (the
+        // score MMA of tile t waited for the last of them)
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t orr[32];
+          tmem_ld32(tO + cc * 32, orr);
+          tmem_ld_wait(orr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          tmem_st32(tO + cc * 32, orr);
+        }
+      }
       const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
-      // P buffer sb is free once PV of tile t-2 is done
-      bool gb = t < 2 || wwait(&s.pv_done[sb], ((t - 2) >> 1) & 1);
-      if (gb) {
-        tc_fence_after();
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t pk[16];  // 32 P values, two per TMEM column
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t pk[16];  // 32 P values, two per TMEM column
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float x0, x1;
-            ffma2(x0, x1, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]), c, c, nmu, nmu);
-            const float e0 = ex2(x0), e1 = ex2(x1);
-            fadd2(ls[((i >> 1) & 1) * 2], ls[((i >> 1) & 1) * 2 + 1], e0, e1);
-            pk[i / 2] = pack2<BF16>(e0, e1);
-          }
-          tmem_st16(tP0 + sb * 64 + lane_off + half * 32 + cc * 16, pk);
+        for (int i = 0; i < 32; i += 2) {
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]), c, c, nmu, nmu);
+          const float e0 = ex2(x0), e1 = ex2(x1);
+          fadd2(ls[((i >> 1) & 1) * 2], ls[((i >> 1) & 1) * 2 + 1], e0, e1);
+          pk[i / 2] = pack2<BF16>(e0, e1);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // O holds tiles 0..t-1 once PV of t-1 is done: then rescale this
-          // warpgroup's half of the O columns
-          gb = wwait(&s.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1);
-          if (gb) {
-            tc_fence_after();
-#pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) {
-              uint32_t orr[32];
-              const uint32_t col = tO + lane_off + half * (D / 2) + cc * 32;
-              tmem_ld32(col, orr);
-              tmem_ld_wait(orr);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-              tmem_st32(col, orr);
-            }
-          }
-        }
+        tmem_st16(tS + cc * 16, pk);  // P over S: every score of this row is in registers
       }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tmem_st_wait();
-      if (!gb) {
-        ok = false;  // reported at the next vote
-        continue;
-      }
       tc_fence_before();
-      mbar_arrive(&s.p_full[sb]);
+      mbar_arrive(&s.p_full[g]);
     }
-    // epilogue: O / l (l summed over both halves), rounded to the input type;
-    // 0 for rows without valid keys
-    bool good = ok && (n == 0 || wwait(&s.pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1));
-    if (!good) vote_fail(n);
-    s.rowl[half][r] = l;
+    // epilogue: merge the two warpgroups' partial results; warpgroup g
+    // writes columns g*D/2 .. g*D/2 + D/2 - 1 of each row
+    const int n_mine = n > g ? (n - 1 - g) / 2 + 1 : 0;  // tiles of this warpgroup
+    bool good = ok && (n_mine == 0 || wwait(&s.pv_done[g], (n_mine - 1) & 1));
+    if (!good) atomicMin(&s.fail_tile, 0);
+    s.rowm[g][r] = m_ref;
+    s.rowl[g][r] = l;
     named_bar_sync(1, 256);
-    if (s.fail_tile <= n) {
-      if (half == 0 && quarter == 0 && lane == 0) fail();
+    if (s.fail_tile < 0x7FFFFFFF) {
+      if (g == 0 && quarter == 0 && lane == 0) fail();
     } else {
       tc_fence_after();
-      const float lt = l + s.rowl[half ^ 1][r];
+      const float m0 = s.rowm[0][r], m1 = s.rowm[1][r];
+      const float m = fmaxf(m0, m1);
+      const float a0 = (n > 0 && m0 != -INFINITY) ? ex2(m0 - m) : 0.f;
+      const float a1 = (n > 1 && m1 != -INFINITY) ? ex2(m1 - m) : 0.f;
+      const float lt = a0 * s.rowl[0][r] + a1 * s.rowl[1][r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float w0 = a0 * inv, w1 = a1 * inv;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
-                      (static_cast<size_t>(bh) * p.L + static_cast<size_t>(I) * kBM + r) * (D * 2) + half * D;
+                      (static_cast<size_t>(bh) * p.L + static_cast<size_t>(I) * kBM + r) * (D * 2) + g * D;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
-        uint32_t orr[32];
+        const int col = g * (D / 2) + cc * 32;
+        uint32_t o0[32], o1[32];
         if (n > 0) {
-          tmem_ld32(tO + lane_off + half * (D / 2) + cc * 32, orr);
-          tmem_ld_wait(orr);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) orr[i] = 0u;
+          tmem_ld32(tO0 + lane_off + col, o0);
+          tmem_ld_wait(o0);
+        }
+        if (n > 1) {
+          tmem_ld32(tO0 + D + lane_off + col, o1);
+          tmem_ld_wait(o1);
         }
         uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack2<BF16>(__uint_as_float(orr[2 * i]) * inv, __uint_as_float(orr[2 * i + 1]) * inv);
+        for (int i = 0; i < 16; ++i) {
+          float v0 = 0.f, v1 = 0.f;
+          if (n > 0) {
+            v0 = w0 * __uint_as_float(o0[2 * i]);
+            v1 = w0 * __uint_as_float(o0[2 * i + 1]);
+          }
+          if (n > 1) {
+            v0 = fmaf(w1, __uint_as_float(o1[2 * i]), v0);
+            v1 = fmaf(w1, __uint_as_float(o1[2 * i + 1]), v1);
+          }
+          w[i] = pack2<BF16>(v0, v1);
+        }
         uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
 #pragma unroll
         for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
@@ -539,6 +548,9 @@ stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem))) != cudaSuccess)
       return STOF_ERR_CUDA;
+    cudaFuncAttributes fa;
+    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_kernel<D, BF16>)) != cudaSuccess) return STOF_ERR_CUDA;
+    if (fa.numRegs != kLaunchRegs) return STOF_ERR_UNSUPPORTED;  // the register split needs exactly this
     attr_done = true;
   }
   const long long grid = static_cast<long long>(p.B) * p.H * p.n_tr;
