@@ -11,10 +11,8 @@
 // One CTA computes one 128-row query tile (b, h, OT row I) over the n OTs
 // listed for its row (full OTs first):
 //   warp 0      TMA producer: the Q tile once, then the K tile of every
-//               listed OT into an NK-stage ring (a stage is freed as soon
-//               as its S = Q K^T is done) and, for a partial OT, its 2 KB of
-//               IT bitmaps into an NB-stage ring (freed as soon as the
-//               softmax has read them);
+//               listed OT into an NK-stage ring (a stage is freed as soon as
+//               its S = Q K^T is done);
 //   warp 1      TMA producer: the V tiles into an NV-stage ring (freed when
 //               its O += P V is done);
 //   warp 2      allocates TMEM and issues the score MMAs S_g = Q K_t^T;
@@ -23,17 +21,19 @@
 //               warp are not scheduled promptly while another lane waits.)
 //   warps 4..7  softmax warpgroup 0, tiles t = 0, 2, 4, ...;
 //   warps 8..11 softmax warpgroup 1, tiles t = 1, 3, 5, ...
-// Warpgroup g owns its score buffer S_g, its accumulator O_g, and its own
-// running max and sum: the two warpgroups never wait for each other inside
-// the tile loop, so one computes while the other waits for its next S.  A
-// thread owns one query row (= TMEM lane): it reads its 128 scores, masks
-// partial OTs by their IT bitmaps, updates its running max lazily (O_g is
-// rescaled in TMEM only when the max grows by more than 2^8; exact, because
-// O_g and l_g share the reference), evaluates exp2 in fp32, and writes P as
-// fp16/bf16 over the first 64 columns of S_g, where the PV MMA reads it.  The
-// next score MMA into S_g waits for that PV to complete.  At the end the two
-// partial results are merged: O = (a0 O_0 + a1 O_1) / (a0 l_0 + a1 l_1),
-// a_g = 2^(m_g - max(m_0, m_1)); 0 for a row without valid keys.
+// Warpgroup g owns a score buffer S_g and an accumulator O_g in TMEM, a P
+// buffer in shared memory, and its own running max and sum.  A thread owns
+// one query row (= TMEM lane): it loads its 128 scores into registers and at
+// once hands S_g back, so the score MMA of the warpgroup's next tile runs
+// while this one is processed.  It masks partial OTs by their IT bitmaps
+// (read from global memory one tile ahead), updates its running max lazily
+// (O_g is rescaled in TMEM only when the max grows by more than 2^8; exact,
+// because O_g and l_g share the reference), evaluates exp2 in fp32 and
+// stores P as fp16/bf16 into its P buffer in the swizzled K-major layout of
+// the MMA operand.  The two warpgroups never wait for each other inside the
+// tile loop.  At the end their partial results are merged:
+// O = (a0 O_0 + a1 O_1) / (a0 l_0 + a1 l_1), a_g = 2^(m_g - max(m_0, m_1));
+// 0 for a row without valid keys.
 // TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,256+d) O_1 [256+d,256+2d).
 // Every pipeline wait is bounded; on timeout the CTA raises
 // STOF_DEVERR_PIPE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
@@ -65,37 +65,35 @@ constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 template <int D>
 struct Cfg {
   static constexpr int NK = D == 128 ? 2 : 4;       // K ring stages
-  static constexpr int NV = D == 128 ? 3 : 4;       // V ring stages
-  static constexpr int NB = 4;                      // IT-bitmap ring stages
+  static constexpr int NV = D == 128 ? 2 : 4;       // V ring stages
   static constexpr int REGIONS = D / 64;            // 128-byte swizzle atoms along d
   static constexpr int TILE_BYTES = kBM * D * 2;    // one Q, K or V tile
   static constexpr int BITMAP_WORDS = (kBM / 8) * (kBN / 8);
 };
+constexpr int kPBytes = kBM * kBN * 2;              // one P tile (128 keys: two swizzle atoms)
 
 template <int D>
 struct alignas(1024) Smem {
   uint8_t q[Cfg<D>::TILE_BYTES];
+  uint8_t p[2][kPBytes];     // P of each warpgroup's current tile; then its final max and sum
   uint8_t k[Cfg<D>::NK][Cfg<D>::TILE_BYTES];
   uint8_t v[Cfg<D>::NV][Cfg<D>::TILE_BYTES];
-  uint64_t bits[Cfg<D>::NB][Cfg<D>::BITMAP_WORDS];
   uint64_t q_full;
   uint64_t k_full[Cfg<D>::NK];
   uint64_t k_free[Cfg<D>::NK];
   uint64_t v_full[Cfg<D>::NV];
   uint64_t v_free[Cfg<D>::NV];
-  uint64_t b_full[Cfg<D>::NB];
-  uint64_t b_free[Cfg<D>::NB];
   uint64_t s_full[2];
+  uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t drain;
   uint64_t drain_qk;
-  float rowm[2][kBM];        // final running max of each warpgroup, per row
-  float rowl[2][kBM];        // final running sum of each warpgroup, per row
   uint32_t tmem_base;
   int abort_flag;
-  int fail_tile;             // first tile at which a softmax thread failed
+  int fail_tile;             // 0 once a softmax thread has failed
 };
+static_assert(sizeof(Smem<128>) + 1024 <= 232448, "shared memory");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -189,14 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.v_free[i], 1);
     }
-    for (int i = 0; i < C::NB; ++i) {
-      mbar_init(&s.b_full[i], 1);
-      mbar_init(&s.b_free[i], 128);
-    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_free[i], 128);
       mbar_init(&s.p_full[i], 128);
       mbar_init(&s.pv_done[i], 1);
     }
@@ -228,10 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // column index of the t-th listed OT of this row (full OTs first)
-  auto column_of = [&](int t, long long* e) {
-    const bool partial = t >= nf;
-    *e = partial ? static_cast<long long>(p0) + (t - nf) : static_cast<long long>(f0) + t;
-    int J = partial ? p.part_col_idx[*e] : p.full_col_idx[*e];
+  auto column_of = [&](int t) {
+    int J = t >= nf ? p.part_col_idx[p0 + (t - nf)] : p.full_col_idx[f0 + t];
     if (J < 0 || J >= p.n_tc) {
       raise_error(p.err, STOF_DEVERR_BAD_FORMAT);
       J = 0;
@@ -252,25 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&s.q_full, C::TILE_BYTES);
 #pragma unroll
         for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow);
-        int issued = 0, bits_issued = 0;
+        int issued = 0;
         for (int t = 0; t < n; ++t) {
           const int st = t % C::NK;
           if (t >= C::NK && !mbar_wait(&s.k_free[st], ((t / C::NK) - 1) & 1, abort_flag, kWaitNs)) {
             fail();
             break;
           }
-          long long e;
-          const int krow = bh * p.L + column_of(t, &e) * kBN;
-          if (t >= nf) {  // the IT bitmaps of a partial OT, into their own ring
-            const int u = t - nf, bst = u % C::NB;
-            if (u >= C::NB && !mbar_wait(&s.b_free[bst], ((u / C::NB) - 1) & 1, abort_flag, kWaitNs)) {
-              fail();
-              break;
-            }
-            mbar_arrive_expect_tx(&s.b_full[bst], C::BITMAP_WORDS * 8);
-            bulk_load(s.bits[bst], p.bitmaps + e * C::BITMAP_WORDS, C::BITMAP_WORDS * 8, &s.b_full[bst]);
-            bits_issued = u + 1;
-          }
+          const int krow = bh * p.L + column_of(t) * kBN;
           mbar_arrive_expect_tx(&s.k_full[st], C::TILE_BYTES);
 #pragma unroll
           for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.k[st] + r * 16384, &tmK, &s.k_full[st], 64 * r, krow);
@@ -280,8 +260,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_timeout(&s.q_full, 0, kWaitNs);
           for (int t = issued - C::NK < 0 ? 0 : issued - C::NK; t < issued; ++t)
             mbar_wait_timeout(&s.k_full[t % C::NK], (t / C::NK) & 1, kWaitNs);
-          for (int u = bits_issued - C::NB < 0 ? 0 : bits_issued - C::NB; u < bits_issued; ++u)
-            mbar_wait_timeout(&s.b_full[u % C::NB], (u / C::NB) & 1, kWaitNs);
         }
       }
     } else if (warp == 1) {
@@ -295,8 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fail();
             break;
           }
-          long long e;
-          const int vrow = bh * p.L + column_of(t, &e) * kBN;
+          const int vrow = bh * p.L + column_of(t) * kBN;
           mbar_arrive_expect_tx(&s.v_full[st], C::TILE_BYTES);
 #pragma unroll
           for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.v[st] + r * 16384, &tmV, &s.v_full[st], 64 * r, vrow);
@@ -328,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = n == 0 || wwait(&s.q_full, 0);
         for (int t = 0; ok && t < n; ++t) {
           const int st = t % C::NK, g = t & 1;
-          // S_g still holds P of tile t-2 until that tile's PV is done
-          if (t >= 2 && !wwait(&s.pv_done[g], ((t - 2) >> 1) & 1)) { ok = false; break; }
+          // S_g is free once the softmax has loaded tile t-2's scores
+          if (t >= 2 && !wwait(&s.s_free[g], ((t - 2) >> 1) & 1)) { ok = false; break; }
           if (!wwait(&s.k_full[st], (t / C::NK) & 1)) { ok = false; break; }
           tc_fence_after();
           const uint64_t kd = kdesc0 + static_cast<uint64_t>(st) * kStage;
@@ -352,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const uint64_t vdesc0 = smem_desc_sw128(smem_u32(s.v[0]), 16384, 1024);
+        const uint64_t pdesc0 = smem_desc_sw128(smem_u32(s.p[0]), 16, 1024);
         bool ok = true;
         for (int t = 0; ok && t < n; ++t) {
           const int st = t % C::NV, g = t & 1;
@@ -359,13 +337,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wwait(&s.v_full[st], (t / C::NV) & 1)) { ok = false; break; }
           tc_fence_after();
           const uint64_t vd = vdesc0 + static_cast<uint64_t>(st) * kStage;
-          const uint32_t a_tmem = tS0 + g * 128;  // P_t over the first 64 columns of S_g
+          const uint64_t pd = pdesc0 + static_cast<uint64_t>(g) * (kPBytes / 16);
           const uint32_t d_tmem = tO0 + g * D;
           if (elect_one()) {
-            mma_f16_ts(d_tmem, a_tmem, vd, idesc_pv, t >= 2 ? 1u : 0u);  // first tile of O_g overwrites
 #pragma unroll
-            for (int kk = 1; kk < kBN / 16; ++kk)  // 16 keys x 128 B per K step
-              mma_f16_ts(d_tmem, a_tmem + kk * 8, vd + kk * 128, idesc_pv, 1u);
+            for (int kk = 0; kk < kBN / 16; ++kk) {  // 16 keys per K step
+              const uint64_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
+              // the first tile of O_g overwrites it
+              mma_f16_ss(d_tmem, pd + off, vd + kk * 128, idesc_pv, (t >= 2 || kk > 0) ? 1u : 0u);
+            }
             mma_commit(&s.pv_done[g]);
             mma_commit(&s.v_free[st]);
           }
@@ -388,8 +368,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tS0 + g * 128 + lane_off;
     const uint32_t tO = tO0 + g * D + lane_off;
     const float c = p.scale_log2;
+    // row r of an OT's bitmaps: byte r % 8 of words (r / 8) * 16 + 0..15
+    const uint8_t* bits_row = reinterpret_cast<const uint8_t*>(p.bitmaps) + (r >> 3) * 128 + (r & 7);
+    uint32_t nb[16];  // bitmap bytes of this warpgroup's next partial tile, loaded a tile ahead
+    auto fetch_bits = [&](int t) {
+      if (t < n && t >= nf) {
+        const uint8_t* src = bits_row + static_cast<long long>(p0 + (t - nf)) * (C::BITMAP_WORDS * 8);
+#pragma unroll
+        for (int w = 0; w < 16; ++w) nb[w] = __ldg(src + w * 8);
+      }
+    };
+    // P row r: 16-byte chunk q of swizzle atom a sits at a * 16 KB + r * 128 + (q ^ (r % 8)) * 16
+    uint8_t* prow = s.p[g] + r * 128;
+    const int sw = r & 7;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    fetch_bits(g);
     for (int t = g; ok && t < n; t += 2) {
       const int j = t >> 1;  // this warpgroup's j-th tile
       if (!wwait(&s.s_full[g], j & 1)) { ok = false; break; }
@@ -399,21 +393,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(sr[cc]);
-      if (t >= nf) {  // partial OT: keep only the keys whose bit is set
-        const int u = t - nf, bst = u % C::NB;
-        if (!wwait(&s.b_full[bst], (u / C::NB) & 1)) { ok = false; break; }
-        const uint64_t* bw = s.bits[bst] + (r >> 3) * (kBN / 8);
-        const int shift = (r & 7) * 8;
+      tc_fence_before();
+      mbar_arrive(&s.s_free[g]);  // the scores are in registers: S_g may be overwritten
+      const bool partial = t >= nf;
+      uint32_t bits[4];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t bits32 = 0;
+      for (int cc = 0; cc < 4; ++cc)
+        bits[cc] = partial ? nb[4 * cc] | (nb[4 * cc + 1] << 8) | (nb[4 * cc + 2] << 16) | (nb[4 * cc + 3] << 24) : 0u;
+      fetch_bits(t + 2);
+      if (partial) {  // keep only the keys whose bit is set
 #pragma unroll
-          for (int uu = 0; uu < 4; ++uu)
-            bits32 |= (static_cast<uint32_t>(bw[4 * cc + uu] >> shift) & 0xFFu) << (8 * uu);
+        for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sr[cc][i] = (bits32 >> i) & 1u ? sr[cc][i] : 0xFF800000u;  // -inf
-        }
-        mbar_arrive(&s.b_free[bst]);  // this thread is done with the bitmap
+          for (int i = 0; i < 32; ++i) sr[cc][i] = (bits[cc] >> i) & 1u ? sr[cc][i] : 0xFF800000u;  // -inf
       }
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -432,24 +424,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = mt;
       }
       l *= alpha;
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O_g holds tiles g, g+2, ..., t-2; their PVs are complete (the
-        // score MMA of tile t waited for the last of them)
+      if (j > 0) {
+        // the PV of this warpgroup's previous tile must be done before its P
+        // buffer is rewritten and before O_g is rescaled
+        if (!wwait(&s.pv_done[g], (j - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t orr[32];
-          tmem_ld32(tO + cc * 32, orr);
-          tmem_ld_wait(orr);
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t orr[32];
+            tmem_ld32(tO + cc * 32, orr);
+            tmem_ld_wait(orr);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-          tmem_st32(tO + cc * 32, orr);
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tmem_st32(tO + cc * 32, orr);
+          }
+          tmem_st_wait();
         }
       }
       const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        uint32_t pk[16];  // 32 P values, two per TMEM column
+        uint32_t pk[16];  // keys 32 cc .. 32 cc + 31, two per word
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           float x0, x1;
@@ -458,30 +455,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           fadd2(ls[((i >> 1) & 1) * 2], ls[((i >> 1) & 1) * 2 + 1], e0, e1);
           pk[i / 2] = pack2<BF16>(e0, e1);
         }
-        tmem_st16(tS + cc * 16, pk);  // P over S: every score of this row is in registers
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {  // 8 keys per 16-byte chunk
+          const int q = (cc & 1) * 4 + h;
+          *reinterpret_cast<uint4*>(prow + (cc >> 1) * 16384 + ((q ^ sw) << 4)) =
+              make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
+        }
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      tmem_st_wait();
+      fence_proxy_async_smem();  // P stores visible to the tensor core
       tc_fence_before();
       mbar_arrive(&s.p_full[g]);
     }
     // epilogue: merge the two warpgroups' partial results; warpgroup g
     // writes columns g*D/2 .. g*D/2 + D/2 - 1 of each row
     const int n_mine = n > g ? (n - 1 - g) / 2 + 1 : 0;  // tiles of this warpgroup
-    bool good = ok && (n_mine == 0 || wwait(&s.pv_done[g], (n_mine - 1) & 1));
+    const bool good = ok && (n_mine == 0 || wwait(&s.pv_done[g], (n_mine - 1) & 1));
     if (!good) atomicMin(&s.fail_tile, 0);
-    s.rowm[g][r] = m_ref;
-    s.rowl[g][r] = l;
+    // P_g is no longer read (this warpgroup's last PV is done): it carries
+    // the final max and sum to the other warpgroup
+    float* xg = reinterpret_cast<float*>(s.p[g]);
+    xg[r] = m_ref;
+    xg[kBM + r] = l;
     named_bar_sync(1, 256);
     if (s.fail_tile < 0x7FFFFFFF) {
       if (g == 0 && quarter == 0 && lane == 0) fail();
     } else {
       tc_fence_after();
-      const float m0 = s.rowm[0][r], m1 = s.rowm[1][r];
+      const float* x0 = reinterpret_cast<const float*>(s.p[0]);
+      const float* x1 = reinterpret_cast<const float*>(s.p[1]);
+      const float m0 = x0[r], m1 = x1[r];
       const float m = fmaxf(m0, m1);
       const float a0 = (n > 0 && m0 != -INFINITY) ? ex2(m0 - m) : 0.f;
       const float a1 = (n > 1 && m1 != -INFINITY) ? ex2(m1 - m) : 0.f;
-      const float lt = a0 * s.rowl[0][r] + a1 * s.rowl[1][r];
+      const float lt = a0 * x0[kBM + r] + a1 * x1[kBM + r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float w0 = a0 * inv, w1 = a1 * inv;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
