@@ -11,10 +11,10 @@
 // One CTA computes one 128-row query tile (b, h, OT row I) over the n OTs
 // listed for its row (full OTs first):
 //   warp 0      TMA producer: the Q tile once, then the K tile of every
-//               listed OT into an NK-stage ring (a stage is freed as soon as
-//               its S = Q K^T is done);
-//   warp 1      TMA producer: the V tiles into an NV-stage ring (freed when
-//               its O += P V is done);
+//               listed OT into a two-stage ring (stage t % 2 is refilled
+//               once S = Q K_{t-2}^T is done);
+//   warp 1      TMA producer: the V tiles into a two-stage ring (refilled
+//               once O += P_{t-2} V_{t-2} is done);
 //   warp 2      allocates TMEM and issues the score MMAs S_g = Q K_t^T;
 //   warp 3      issues the PV MMAs O_g += P_t V_t.
 //               (Every role has a warp of its own: divergent lanes of one
@@ -64,8 +64,6 @@ constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 
 template <int D>
 struct Cfg {
-  static constexpr int NK = D == 128 ? 2 : 4;       // K ring stages
-  static constexpr int NV = D == 128 ? 2 : 4;       // V ring stages
   static constexpr int REGIONS = D / 64;            // 128-byte swizzle atoms along d
   static constexpr int TILE_BYTES = kBM * D * 2;    // one Q, K or V tile
   static constexpr int BITMAP_WORDS = (kBM / 8) * (kBN / 8);
@@ -76,13 +74,11 @@ template <int D>
 struct alignas(1024) Smem {
   uint8_t q[Cfg<D>::TILE_BYTES];
   uint8_t p[2][kPBytes];     // P of each warpgroup's current tile; then its final max and sum
-  uint8_t k[Cfg<D>::NK][Cfg<D>::TILE_BYTES];
-  uint8_t v[Cfg<D>::NV][Cfg<D>::TILE_BYTES];
+  uint8_t k[2][Cfg<D>::TILE_BYTES];  // K ring: stage t % 2 = the warpgroup of tile t
+  uint8_t v[2][Cfg<D>::TILE_BYTES];  // V ring, likewise
   uint64_t q_full;
-  uint64_t k_full[Cfg<D>::NK];
-  uint64_t k_free[Cfg<D>::NK];
-  uint64_t v_full[Cfg<D>::NV];
-  uint64_t v_free[Cfg<D>::NV];
+  uint64_t k_full[2];
+  uint64_t v_full[2];
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full[2];
@@ -179,13 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
-    for (int i = 0; i < C::NK; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s.k_full[i], 1);
-      mbar_init(&s.k_free[i], 1);
-    }
-    for (int i = 0; i < C::NV; ++i) {
       mbar_init(&s.v_full[i], 1);
-      mbar_init(&s.v_free[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
@@ -245,8 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow);
         int issued = 0;
         for (int t = 0; t < n; ++t) {
-          const int st = t % C::NK;
-          if (t >= C::NK && !mbar_wait(&s.k_free[st], ((t / C::NK) - 1) & 1, abort_flag, kWaitNs)) {
+          // stage t % 2 held K_{t-2}: free once that tile's scores are done
+          const int st = t & 1;
+          if (t >= 2 && !mbar_wait(&s.s_full[st], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) {
             fail();
             break;
           }
@@ -258,8 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (*abort_flag) {  // let every copy this thread started land before exit
           mbar_wait_timeout(&s.q_full, 0, kWaitNs);
-          for (int t = issued - C::NK < 0 ? 0 : issued - C::NK; t < issued; ++t)
-            mbar_wait_timeout(&s.k_full[t % C::NK], (t / C::NK) & 1, kWaitNs);
+          for (int t = issued - 2 < 0 ? 0 : issued - 2; t < issued; ++t)
+            mbar_wait_timeout(&s.k_full[t & 1], (t >> 1) & 1, kWaitNs);
         }
       }
     } else if (warp == 1) {
@@ -268,8 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmV);
         int issued = 0;
         for (int t = 0; t < n; ++t) {
-          const int st = t % C::NV;
-          if (t >= C::NV && !mbar_wait(&s.v_free[st], ((t / C::NV) - 1) & 1, abort_flag, kWaitNs)) {
+          // stage t % 2 held V_{t-2}: free once that tile's PV is done
+          const int st = t & 1;
+          if (t >= 2 && !mbar_wait(&s.pv_done[st], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) {
             fail();
             break;
           }
@@ -280,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued = t + 1;
         }
         if (*abort_flag) {
-          for (int t = issued - C::NV < 0 ? 0 : issued - C::NV; t < issued; ++t)
-            mbar_wait_timeout(&s.v_full[t % C::NV], (t / C::NV) & 1, kWaitNs);
+          for (int t = issued - 2 < 0 ? 0 : issued - 2; t < issued; ++t)
+            mbar_wait_timeout(&s.v_full[t & 1], (t >> 1) & 1, kWaitNs);
         }
       }
     } else {  // warps 2 and 3
@@ -304,12 +298,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t kdesc0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
         bool ok = n == 0 || wwait(&s.q_full, 0);
         for (int t = 0; ok && t < n; ++t) {
-          const int st = t % C::NK, g = t & 1;
+          const int g = t & 1;  // warpgroup, score buffer and K stage of tile t
           // S_g is free once the softmax has loaded tile t-2's scores
           if (t >= 2 && !wwait(&s.s_free[g], ((t - 2) >> 1) & 1)) { ok = false; break; }
-          if (!wwait(&s.k_full[st], (t / C::NK) & 1)) { ok = false; break; }
+          if (!wwait(&s.k_full[g], (t >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t kd = kdesc0 + static_cast<uint64_t>(st) * kStage;
+          const uint64_t kd = kdesc0 + static_cast<uint64_t>(g) * kStage;
           const uint32_t d_tmem = tS0 + g * 128;
           if (elect_one()) {
 #pragma unroll
@@ -317,10 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KB per atom, 32 B per K step
               mma_f16_ss(d_tmem, qdesc + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
             }
-            mma_commit(&s.s_full[g]);
-            mma_commit(&s.k_free[st]);
+            mma_commit(&s.s_full[g]);  // also frees K stage g
           }
-          __syncwarp();
         }
         if (elect_one()) {  // the lane that issued the MMAs
           if (!ok) fail();
@@ -332,11 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pdesc0 = smem_desc_sw128(smem_u32(s.p[0]), 16, 1024);
         bool ok = true;
         for (int t = 0; ok && t < n; ++t) {
-          const int st = t % C::NV, g = t & 1;
+          const int g = t & 1;  // warpgroup, accumulator and V stage of tile t
           if (!wwait(&s.p_full[g], (t >> 1) & 1)) { ok = false; break; }
-          if (!wwait(&s.v_full[st], (t / C::NV) & 1)) { ok = false; break; }
+          if (!wwait(&s.v_full[g], (t >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t vd = vdesc0 + static_cast<uint64_t>(st) * kStage;
+          const uint64_t vd = vdesc0 + static_cast<uint64_t>(g) * kStage;
           const uint64_t pd = pdesc0 + static_cast<uint64_t>(g) * (kPBytes / 16);
           const uint32_t d_tmem = tO0 + g * D;
           if (elect_one()) {
@@ -346,10 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               // the first tile of O_g overwrites it
               mma_f16_ss(d_tmem, pd + off, vd + kk * 128, idesc_pv, (t >= 2 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(&s.pv_done[g]);
-            mma_commit(&s.v_free[st]);
+            mma_commit(&s.pv_done[g]);  // also frees V stage g and P buffer g
           }
-          __syncwarp();
         }
         if (elect_one()) {  // the lane that issued the MMAs
           if (!ok) fail();
