@@ -179,8 +179,9 @@ stof_kernel stof_select_kernel(double density, int seq_len, int head_dim);
  *   L           == fmt->lq == fmt->lk.   d: 64 or 128.
  *   fmt         an encoded format (stof_encode_mask) for masks of size L.
  *   which       STOF_KERNEL_ROWWISE [ROW], STOF_KERNEL_BLOCKWISE [BLK]
- *               (needs bm == bn == 128) or STOF_KERNEL_AUTO ([SEL], needs a
- *               synced fmt).
+ *               (needs bm == 128 and bn == 64 or 128; else
+ *               STOF_ERR_UNSUPPORTED) or STOF_KERNEL_AUTO ([SEL], needs a
+ *               synced fmt; falls back to row-wise for other tile sizes).
  * Asynchronous on stream.
  */
 stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H,

@@ -54,28 +54,32 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBM = 128;
-constexpr int kBN = 128;
+constexpr int kBM = 128;  // query rows per tile (the MMA's M); key columns per OT: BN = 64 or 128
 // 2 producer warps, 2 MMA-issuer warps, 8 softmax warps.  Three warps per
 // SM sub-partition cap a thread at 168 registers.
 constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 
-template <int D>
+// Tiles in shared memory are 128-byte-swizzled: a matrix of R rows is stored
+// as d/64 (or keys/64) atoms of R rows x 128 bytes, 8-row groups 1 KB apart.
+template <int D, int BN>
 struct Cfg {
-  static constexpr int REGIONS = D / 64;            // 128-byte swizzle atoms along d
-  static constexpr int TILE_BYTES = kBM * D * 2;    // one Q, K or V tile
-  static constexpr int BITMAP_WORDS = (kBM / 8) * (kBN / 8);
+  static constexpr int REGIONS = D / 64;            // swizzle atoms along d
+  static constexpr int Q_BYTES = kBM * D * 2;       // the Q tile
+  static constexpr int KV_BYTES = BN * D * 2;       // one K or V tile
+  static constexpr int KV_ATOM = BN * 128;          // one swizzle atom of a K or V tile
+  static constexpr int P_BYTES = kBM * BN * 2;      // one P tile (BN / 64 atoms of 16 KB)
+  static constexpr int CHUNKS = BN / 32;            // 32-score chunks of a softmax row
+  static constexpr int BITMAP_WORDS = (kBM / 8) * (BN / 8);
 };
-constexpr int kPBytes = kBM * kBN * 2;              // one P tile (128 keys: two swizzle atoms)
 
-template <int D>
+template <int D, int BN>
 struct alignas(1024) Smem {
-  uint8_t q[Cfg<D>::TILE_BYTES];
-  uint8_t p[2][kPBytes];     // P of each warpgroup's current tile; then its final max and sum
-  uint8_t k[2][Cfg<D>::TILE_BYTES];  // K ring: stage t % 2 = the warpgroup of tile t
-  uint8_t v[2][Cfg<D>::TILE_BYTES];  // V ring, likewise
+  uint8_t q[Cfg<D, BN>::Q_BYTES];
+  uint8_t p[2][Cfg<D, BN>::P_BYTES];   // P of each warpgroup's current tile; then its final max and sum
+  uint8_t k[2][Cfg<D, BN>::KV_BYTES];  // K ring: stage t % 2 = the warpgroup of tile t
+  uint8_t v[2][Cfg<D, BN>::KV_BYTES];  // V ring, likewise
   uint64_t q_full;
   uint64_t k_full[2];
   uint64_t v_full[2];
@@ -89,7 +93,7 @@ struct alignas(1024) Smem {
   int abort_flag;
   int fail_tile;             // 0 once a softmax thread has failed
 };
-static_assert(sizeof(Smem<128>) + 1024 <= 232448, "shared memory");
+static_assert(sizeof(Smem<128, 128>) + 1024 <= 232448, "shared memory");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -151,13 +155,13 @@ constexpr int kLaunchRegs = 168, kProducerRegs = 56, kSoftmaxRegs = 224;
 static_assert(kProducerRegs * 128 + kSoftmaxRegs * 256 <= kLaunchRegs * kThreads, "register split");
 static_assert(kLaunchRegs * kThreads <= 65536, "register file");
 
-template <int D, bool BF16>
+template <int D, int BN, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     blockwise_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, BN>;
   extern __shared__ uint8_t smem_raw[];
-  Smem<D>& s = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+  Smem<D, BN>& s = *reinterpret_cast<Smem<D, BN>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -232,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
         const int qrow = bh * p.L + I * kBM;
-        mbar_arrive_expect_tx(&s.q_full, C::TILE_BYTES);
+        mbar_arrive_expect_tx(&s.q_full, C::Q_BYTES);
 #pragma unroll
         for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow);
         int issued = 0;
@@ -243,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             fail();
             break;
           }
-          const int krow = bh * p.L + column_of(t) * kBN;
-          mbar_arrive_expect_tx(&s.k_full[st], C::TILE_BYTES);
+          const int krow = bh * p.L + column_of(t) * BN;
+          mbar_arrive_expect_tx(&s.k_full[st], C::KV_BYTES);
 #pragma unroll
-          for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.k[st] + r * 16384, &tmK, &s.k_full[st], 64 * r, krow);
+          for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.k[st] + r * C::KV_ATOM, &tmK, &s.k_full[st], 64 * r, krow);
           issued = t + 1;
         }
         if (*abort_flag) {  // let every copy this thread started land before exit
@@ -267,10 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             fail();
             break;
           }
-          const int vrow = bh * p.L + column_of(t) * kBN;
-          mbar_arrive_expect_tx(&s.v_full[st], C::TILE_BYTES);
+          const int vrow = bh * p.L + column_of(t) * BN;
+          mbar_arrive_expect_tx(&s.v_full[st], C::KV_BYTES);
 #pragma unroll
-          for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.v[st] + r * 16384, &tmV, &s.v_full[st], 64 * r, vrow);
+          for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.v[st] + r * C::KV_ATOM, &tmV, &s.v_full[st], 64 * r, vrow);
           issued = t + 1;
         }
         if (*abort_flag) {
@@ -283,13 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Warp 2 issues the score MMAs, warp 3 the PV MMAs; each commits to its
       // own barriers (a commit tracks the issuing thread's MMAs only).  Each
       // MMA group is straight-line code.
-      constexpr uint32_t idesc_qk = idesc_f16(BF16 ? 1 : 0, 0, kBM, kBN);
+      constexpr uint32_t idesc_qk = idesc_f16(BF16 ? 1 : 0, 0, kBM, BN);
       constexpr uint32_t idesc_pv = idesc_f16(BF16 ? 1 : 0, 1, kBM, D);
       // Descriptors are built once; a K step only adds a compile-time offset
       // (in 16-byte units) to the start-address field.  An issuing thread is
       // latency-bound, so per-MMA descriptor arithmetic would otherwise
       // throttle the tensor core.
-      constexpr uint64_t kStage = C::TILE_BYTES / 16;
+      constexpr uint64_t kStage = C::KV_BYTES / 16;
       // The whole warp runs the loop (warp-uniform waits and descriptor
       // arithmetic, which keeps the descriptors in uniform registers); one
       // elected lane issues the MMAs and commits.
@@ -308,8 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KB per atom, 32 B per K step
-              mma_f16_ss(d_tmem, qdesc + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+              // 32 B per K step inside an atom; Q atoms are 16 KB apart, K atoms BN * 128 B
+              const uint64_t qoff = (kk >> 2) * (C::Q_BYTES / C::REGIONS / 16) + (kk & 3) * 2;
+              const uint64_t koff = (kk >> 2) * (C::KV_ATOM / 16) + (kk & 3) * 2;
+              mma_f16_ss(d_tmem, qdesc + qoff, kd + koff, idesc_qk, kk > 0 ? 1u : 0u);
             }
             mma_commit(&s.s_full[g]);  // also frees K stage g
           }
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_timeout(&s.drain_qk, 0, kWaitNs);
         }
       } else {
-        const uint64_t vdesc0 = smem_desc_sw128(smem_u32(s.v[0]), 16384, 1024);
+        const uint64_t vdesc0 = smem_desc_sw128(smem_u32(s.v[0]), C::KV_ATOM, 1024);
         const uint64_t pdesc0 = smem_desc_sw128(smem_u32(s.p[0]), 16, 1024);
         bool ok = true;
         for (int t = 0; ok && t < n; ++t) {
@@ -329,11 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wwait(&s.v_full[g], (t >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           const uint64_t vd = vdesc0 + static_cast<uint64_t>(g) * kStage;
-          const uint64_t pd = pdesc0 + static_cast<uint64_t>(g) * (kPBytes / 16);
+          const uint64_t pd = pdesc0 + static_cast<uint64_t>(g) * (C::P_BYTES / 16);
           const uint32_t d_tmem = tO0 + g * D;
           if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {  // 16 keys per K step
+            for (int kk = 0; kk < BN / 16; ++kk) {  // 16 keys per K step
               const uint64_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
               // the first tile of O_g overwrites it
               mma_f16_ss(d_tmem, pd + off, vd + kk * 128, idesc_pv, (t >= 2 || kk > 0) ? 1u : 0u);
@@ -358,14 +364,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tS0 + g * 128 + lane_off;
     const uint32_t tO = tO0 + g * D + lane_off;
     const float c = p.scale_log2;
-    // row r of an OT's bitmaps: byte r % 8 of words (r / 8) * 16 + 0..15
-    const uint8_t* bits_row = reinterpret_cast<const uint8_t*>(p.bitmaps) + (r >> 3) * 128 + (r & 7);
-    uint32_t nb[16];  // bitmap bytes of this warpgroup's next partial tile, loaded a tile ahead
+    // row r of an OT's bitmaps: byte r % 8 of words (r / 8) * BN / 8 + 0 .. BN / 8 - 1
+    const uint8_t* bits_row = reinterpret_cast<const uint8_t*>(p.bitmaps) + (r >> 3) * BN + (r & 7);
+    uint32_t nb[BN / 8];  // bitmap bytes of this warpgroup's next partial tile, loaded a tile ahead
     auto fetch_bits = [&](int t) {
       if (t < n && t >= nf) {
         const uint8_t* src = bits_row + static_cast<long long>(p0 + (t - nf)) * (C::BITMAP_WORDS * 8);
 #pragma unroll
-        for (int w = 0; w < 16; ++w) nb[w] = __ldg(src + w * 8);
+        for (int w = 0; w < BN / 8; ++w) nb[w] = __ldg(src + w * 8);
       }
     };
     // P row r: 16-byte chunk q of swizzle atom a sits at a * 16 KB + r * 128 + (q ^ (r % 8)) * 16
@@ -378,28 +384,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = t >> 1;  // this warpgroup's j-th tile
       if (!wwait(&s.s_full[g], j & 1)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[4][32];
+      uint32_t sr[C::CHUNKS][32];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+      for (int cc = 0; cc < C::CHUNKS; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(sr[cc]);
+      for (int cc = 0; cc < C::CHUNKS; ++cc) tmem_ld_wait(sr[cc]);
       tc_fence_before();
       mbar_arrive(&s.s_free[g]);  // the scores are in registers: S_g may be overwritten
       const bool partial = t >= nf;
-      uint32_t bits[4];
+      uint32_t bits[C::CHUNKS];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
+      for (int cc = 0; cc < C::CHUNKS; ++cc)
         bits[cc] = partial ? nb[4 * cc] | (nb[4 * cc + 1] << 8) | (nb[4 * cc + 2] << 16) | (nb[4 * cc + 3] << 24) : 0u;
       fetch_bits(t + 2);
       if (partial) {  // keep only the keys whose bit is set
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+        for (int cc = 0; cc < C::CHUNKS; ++cc)
 #pragma unroll
           for (int i = 0; i < 32; ++i) sr[cc][i] = (bits[cc] >> i) & 1u ? sr[cc][i] : 0xFF800000u;  // -inf
       }
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // one chain per 32 scores
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
+      for (int cc = 0; cc < C::CHUNKS; ++cc)
 #pragma unroll
         for (int i = 0; i < 32; i += 8) {
           m4[cc] = max3(m4[cc], __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]));
@@ -435,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < C::CHUNKS; ++cc) {
         uint32_t pk[16];  // keys 32 cc .. 32 cc + 31, two per word
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
@@ -524,44 +530,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// [rows][D] row-major 16-bit matrix, box = 64 columns x 128 rows, 128-byte swizzle
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int D, bool bf16) {
+// [rows][D] row-major 16-bit matrix, box = 64 columns x box_rows rows, 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_rows, bool bf16) {
   return encode_tensor_map_2d(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                              base, static_cast<uint64_t>(D), rows, static_cast<uint64_t>(D) * 2, 64, 128,
-                              CU_TENSOR_MAP_SWIZZLE_128B);
+                              base, static_cast<uint64_t>(D), rows, static_cast<uint64_t>(D) * 2, 64,
+                              static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D, bool BF16>
+template <int D, int BN, bool BF16>
 stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.L;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, rows, D, BF16) || !make_map(&mk, p.k, rows, D, BF16) ||
-      !make_map(&mv, p.v, rows, D, BF16))
+  if (!make_map(&mq, p.q, rows, D, kBM, BF16) || !make_map(&mk, p.k, rows, D, BN, BF16) ||
+      !make_map(&mv, p.v, rows, D, BN, BF16))
     return STOF_ERR_CUDA;
-  const size_t smem = sizeof(Smem<D>) + 1024;
+  const size_t smem = sizeof(Smem<D, BN>) + 1024;
   static bool attr_done = false;
   if (!attr_done) {
-    if (record_cuda(cudaFuncSetAttribute(blockwise_kernel<D, BF16>,
+    if (record_cuda(cudaFuncSetAttribute(blockwise_kernel<D, BN, BF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem))) != cudaSuccess)
       return STOF_ERR_CUDA;
     cudaFuncAttributes fa;
-    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_kernel<D, BF16>)) != cudaSuccess) return STOF_ERR_CUDA;
+    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_kernel<D, BN, BF16>)) != cudaSuccess) return STOF_ERR_CUDA;
     if (fa.numRegs != kLaunchRegs) return STOF_ERR_UNSUPPORTED;  // the register split needs exactly this
     attr_done = true;
   }
   const long long grid = static_cast<long long>(p.B) * p.H * p.n_tr;
-  blockwise_kernel<D, BF16><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
+  blockwise_kernel<D, BN, BF16><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
   return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
 }
 
 }  // namespace
 
 stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s) {
-  if (p.bm != kBM || p.bn != kBN) return STOF_ERR_UNSUPPORTED;
+  if (p.bm != kBM || (p.bn != 64 && p.bn != 128)) return STOF_ERR_UNSUPPORTED;
   if (static_cast<long long>(p.B) * p.H * p.L >= (1ll << 31)) return STOF_ERR_SHAPE;
-  if (p.d == 64) return bf16 ? launch_bw<64, true>(p, s) : launch_bw<64, false>(p, s);
-  return bf16 ? launch_bw<128, true>(p, s) : launch_bw<128, false>(p, s);
+  if (p.bn == 64) {
+    if (p.d == 64) return bf16 ? launch_bw<64, 64, true>(p, s) : launch_bw<64, 64, false>(p, s);
+    return bf16 ? launch_bw<128, 64, true>(p, s) : launch_bw<128, 64, false>(p, s);
+  }
+  if (p.d == 64) return bf16 ? launch_bw<64, 128, true>(p, s) : launch_bw<64, 128, false>(p, s);
+  return bf16 ? launch_bw<128, 128, true>(p, s) : launch_bw<128, 128, false>(p, s);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

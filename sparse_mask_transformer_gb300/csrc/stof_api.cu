@@ -230,6 +230,10 @@ stof_kernel stof_select_kernel(double density, int seq_len, int head_dim) {
   return t_row <= t_blk ? STOF_KERNEL_ROWWISE : STOF_KERNEL_BLOCKWISE;
 }
 
+// OT sizes the block-wise kernel runs: 128 query rows (the MMA's M) by 64 or
+// 128 key columns.
+static bool blockwise_tiles(const stof_format& f) { return f.bm == 128 && (f.bn == 64 || f.bn == 128); }
+
 stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H,
                          int L, int d, float scale, const stof_format* fmt,
                          int64_t mask_stride_b, int64_t mask_stride_h, stof_kernel which, void* o,
@@ -262,11 +266,10 @@ stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype
     const double density =
         static_cast<double>(fmt->nnz) / (static_cast<double>(fmt->n_masks) * fmt->lq * fmt->lk);
     kern = stof_select_kernel(density, L, d);
-    if (kern == STOF_KERNEL_BLOCKWISE && (fmt->bm != 128 || fmt->bn != 128))
-      kern = STOF_KERNEL_ROWWISE;  // the block-wise kernel needs 128 x 128 OTs
+    if (kern == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(*fmt))
+      kern = STOF_KERNEL_ROWWISE;  // the block-wise kernel needs 128 x 64 or 128 x 128 OTs
   }
-  if (kern == STOF_KERNEL_BLOCKWISE && (fmt->bm != 128 || fmt->bn != 128))
-    return STOF_ERR_UNSUPPORTED;
+  if (kern == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(*fmt)) return STOF_ERR_UNSUPPORTED;
 
   AttnParams p;
   p.q = q;

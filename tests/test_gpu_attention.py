@@ -87,18 +87,18 @@ def test_bernoulli_L16384_full_size_sampled(gpu_lib, kern):
            w.dtype, heads=heads, rows=rows)
 
 
-@pytest.mark.parametrize("kern", ["row", "block"])
+@pytest.mark.parametrize("kern,bn", [("row", 128), ("block", 128), ("block", 64)])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("density", [0.02, 0.3, 0.9])
-def test_random_masks_small(gpu_lib, kern, d, dtype, density):
+def test_random_masks_small(gpu_lib, kern, bn, d, dtype, density):
     # several OTs per row and column, per-head masks, a fully masked row
     B, H, L = 2, 3, 384
     mask = synth.random_mask(B * H, L, L, density, seed=d + int(density * 100))
     mask[1, 5] = 0
     mask[2, :, :200] = 0          # empty and partly-empty tile columns
     q, k, v = synth.make_qkv(B, H, L, d, dtype, seed=3)
-    o, _ = _run(q, k, v, torch.from_numpy(mask).cuda(), 128, 128, H, 1, KERNELS[kern])
+    o, _ = _run(q, k, v, torch.from_numpy(mask).cuda(), 128, bn, H, 1, KERNELS[kern])
     _check(o, q, k, v, _mask_of_np(mask, H, 1), dtype)
     assert torch.all(o[0, 1, 5] == 0)
 
@@ -112,8 +112,8 @@ def test_rowwise_other_tile_sizes(gpu_lib, bm, bn):
     _check(o, q, k, v, _mask_of_np(mask, 0, 0), "fp16")
 
 
-@pytest.mark.parametrize("kern", ["row", "block"])
-def test_edge_cases(gpu_lib, kern):
+@pytest.mark.parametrize("kern,bn", [("row", 128), ("block", 128), ("block", 64)])
+def test_edge_cases(gpu_lib, kern, bn):
     B, H, L, d = 1, 4, 256, 128
     q, k, v = synth.make_qkv(B, H, L, d, "bf16", seed=6)
     q = (q.float() * 8).to(torch.bfloat16)  # sharp softmax
@@ -124,12 +124,37 @@ def test_edge_cases(gpu_lib, kern):
     masks[2, :128] = 0                                 # first OT row empty
     masks[2, 128:, 5] = 1
     # mask 3 all zero: every row fully masked
-    o, _ = _run(q, k, v, torch.from_numpy(masks).cuda(), 128, 128, 0, 1, KERNELS[kern])
+    o, _ = _run(q, k, v, torch.from_numpy(masks).cuda(), 128, bn, 0, 1, KERNELS[kern])
     assert torch.equal(o[0, 1], v[0, 1, js])           # exactly that V row
     assert torch.all(o[0, 2, :128] == 0)
     assert torch.equal(o[0, 2, 128:], v[0, 2, 5].expand(128, d))
     assert torch.all(o[0, 3] == 0)
     _check(o, q, k, v, _mask_of_np(masks, 0, 1), "bf16", heads=[(0, 0)], rel=True)
+
+
+@pytest.mark.parametrize("name", ["bigbird_L512", "longformer_L4096"])
+def test_blockwise_128x64_tiles_full_size(gpu_lib, name):
+    # 128 x 64 OTs: half-width key tiles, 1 KB bitmaps, N = 64 score MMAs
+    w = synth.WORKLOADS[name]
+    mask = synth.make_mask(w)
+    q, k, v = synth.make_qkv(w.B, w.H, w.L, w.d, w.dtype, seed=w.seed)
+    o, fmt = _run(q, k, v, torch.from_numpy(mask).cuda(), 128, 64, w.stride_b, w.stride_h,
+                  stof.STOF_KERNEL_BLOCKWISE)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    idx = np.random.default_rng(5).choice(len(heads), min(4, len(heads)), replace=False)
+    _check(o, q, k, v, _mask_of_np(mask, w.stride_b, w.stride_h), w.dtype,
+           heads=[heads[i] for i in sorted(idx)])
+    assert fmt.device_error == 0
+
+
+def test_blockwise_other_tiles_refused(gpu_lib):
+    mask = torch.ones(1, 256, 256, dtype=torch.uint8, device="cuda")
+    q = torch.zeros(1, 1, 256, 64, dtype=torch.float16, device="cuda")
+    for bm, bn in ((64, 64), (128, 32), (128, 256)):
+        fmt, ws, _ = gpu_encode(mask, bm, bn)
+        with pytest.raises(stof.StofError) as e:
+            stof.stof_mha_fwd(q, q, q, fmt, 0.125, 0, 0, stof.STOF_KERNEL_BLOCKWISE, q.clone())
+        assert e.value.status == stof.STOF_ERR_UNSUPPORTED
 
 
 def test_auto_selection_runs_the_selected_kernel(gpu_lib):
