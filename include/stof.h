@@ -189,6 +189,56 @@ stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype
                          int64_t mask_stride_b, int64_t mask_stride_h, stof_kernel which, void* o,
                          void* stream);
 
+/*
+ * Measured parameter choice for the MHA step, with a result cache.  The
+ * pages' tuner samples kernel parameters (block size, pipeline stages) by
+ * running them once the operator boundaries are fixed, and caches what it
+ * measured (gist.science technical summary, Methodology 2, two-stage
+ * tuning, stage 2 "parameter sampling").  Here the candidates are the
+ * row-wise kernel on 128x128 OTs and the block-wise kernel on 128x128 and
+ * 128x64 OTs.
+ */
+#define STOF_TUNE_CANDIDATES 3
+typedef struct {
+  stof_kernel kernel;        /* fastest candidate */
+  int bn;                    /* its OT width (bm = 128) */
+  float ms;                  /* its time per stof_mha_fwd call */
+  double density;            /* density of the tuned mask */
+  stof_kernel cand_kernel[STOF_TUNE_CANDIDATES];
+  int cand_bn[STOF_TUNE_CANDIDATES];
+  float cand_ms[STOF_TUNE_CANDIDATES]; /* -1 for a candidate the sizes do not admit */
+} stof_tune_result;
+
+/* Workspace bytes stof_tune() needs (the largest encode workspace over the
+ * candidates' OT sizes); 0 for invalid sizes. */
+size_t stof_tune_workspace_bytes(int n_masks, int L);
+
+/*
+ * Encodes the mask for each candidate OT size, runs every candidate kernel
+ * (one untimed call, then three timed with CUDA events) and returns the
+ * fastest in *out; the result is also cached under (L, d, density bucket).
+ * Arguments as for stof_encode_mask() and stof_mha_fwd(); the workspace must
+ * hold stof_tune_workspace_bytes(n_masks, L) bytes and o is overwritten.
+ * Blocks until the timing is done.  A candidate whose run reports a device
+ * error ends the call with that error.
+ */
+stof_status stof_tune(const uint8_t* mask, int n_masks, const void* q, const void* k, const void* v,
+                      stof_dtype dt, int B, int H, int L, int d, float scale, int64_t mask_stride_b,
+                      int64_t mask_stride_h, void* workspace, size_t ws_bytes, void* o, stof_tune_result* out,
+                      void* stream);
+
+/* Cached result for (L, d, the density's bucket): 1 and *out filled (when
+ * out is not NULL) if present, else 0.  Thread-safe; the cache lives for the
+ * process. */
+int stof_tune_lookup(int L, int d, double density, stof_tune_result* out);
+
+/* Empties the cache. */
+void stof_tune_clear(void);
+
+/* The cache's density bucket: round(2 log2(density)), clamped to >= -60;
+ * -61 for density 0. */
+int stof_tune_density_bucket(double density);
+
 /* Static description of a status code. */
 const char* stof_status_string(stof_status s);
 

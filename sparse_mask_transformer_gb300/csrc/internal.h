@@ -76,6 +76,8 @@ struct AttnParams {
   int64_t* err;                    // device error word (counts[3])
 };
 cudaError_t launch_rowwise(const AttnParams& p, bool bf16, cudaStream_t s);
+// Density bucket of the tuning cache.
+int tune_density_bucket(double density);
 // Returns STOF_OK or an error status (tensor-map encoding / launch).
 stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s);
 

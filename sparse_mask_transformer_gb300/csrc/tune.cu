@@ -1,0 +1,151 @@
+// Measured choice of the MHA step's parameters, with a result cache.
+//
+// "Accelerating Sparse Transformer Inference on GPU" (gist.science technical
+// summary), Methodology 2, operator fusion module, two-stage tuning, stage 2
+// (parameter sampling): once the operator boundaries are fixed, kernel
+// parameters such as block size and pipeline stages are sampled by running
+// them, and (same page, "autopilot" summary) what was measured is cached so
+// that a configuration is not timed again.  For the masked MHA step the
+// sampled parameters are the kernel (row-wise or block-wise) and the OT width
+// (64 or 128 key columns; 128 query rows).  A result is cached under
+// (sequence length, head dim, density bucket), the bucket being the density
+// rounded to half powers of two.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "internal.h"
+
+namespace stof {
+namespace {
+
+struct Candidate {
+  stof_kernel kernel;
+  int bn;
+};
+constexpr Candidate kCandidates[STOF_TUNE_CANDIDATES] = {
+    {STOF_KERNEL_ROWWISE, 128}, {STOF_KERNEL_BLOCKWISE, 128}, {STOF_KERNEL_BLOCKWISE, 64}};
+constexpr int kTimedCalls = 3;
+
+std::mutex g_mu;
+std::map<std::tuple<int, int, int>, stof_tune_result> g_cache;
+
+// Streams the candidates run on: the caller's stream.
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+int tune_density_bucket(double density) {
+  if (!(density > 0.0)) return -61;
+  const double b = std::floor(2.0 * std::log2(std::min(density, 1.0)) + 0.5);
+  return static_cast<int>(std::max(-60.0, b));
+}
+
+}  // namespace stof
+
+using namespace stof;
+
+extern "C" {
+
+size_t stof_tune_workspace_bytes(int n_masks, int L) {
+  size_t best = 0;
+  for (const Candidate& c : kCandidates) best = std::max(best, stof_encode_workspace_bytes(n_masks, L, L, 128, c.bn));
+  return best;
+}
+
+stof_status stof_tune(const uint8_t* mask, int n_masks, const void* q, const void* k, const void* v,
+                      stof_dtype dt, int B, int H, int L, int d, float scale, int64_t mask_stride_b,
+                      int64_t mask_stride_h, void* workspace, size_t ws_bytes, void* o, stof_tune_result* out,
+                      void* stream) {
+  if (!mask || !q || !k || !v || !o || !workspace || !out) return STOF_ERR_INVALID_ARG;
+  const size_t need = stof_tune_workspace_bytes(n_masks, L);
+  if (need == 0) return STOF_ERR_SHAPE;
+  if (ws_bytes < need) return STOF_ERR_WORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  cudaEvent_t ev[2];
+  if (record_cuda(cudaEventCreate(&ev[0])) != cudaSuccess) return STOF_ERR_CUDA;
+  if (record_cuda(cudaEventCreate(&ev[1])) != cudaSuccess) {
+    cudaEventDestroy(ev[0]);
+    return STOF_ERR_CUDA;
+  }
+  stof_tune_result r;
+  r.kernel = STOF_KERNEL_AUTO;
+  r.bn = 0;
+  r.ms = -1.f;
+  r.density = 0.0;
+  for (int i = 0; i < STOF_TUNE_CANDIDATES; ++i) {
+    r.cand_kernel[i] = kCandidates[i].kernel;
+    r.cand_bn[i] = kCandidates[i].bn;
+    r.cand_ms[i] = -1.f;
+  }
+  stof_status st = STOF_OK;
+  for (int bn : {128, 64}) {
+    stof_format fmt;
+    st = stof_encode_mask(mask, n_masks, L, L, 128, bn, workspace, ws_bytes, &fmt, stream);
+    if (st == STOF_OK) st = stof_format_sync(&fmt, stream);
+    if (st != STOF_OK) break;
+    r.density = static_cast<double>(fmt.nnz) / (static_cast<double>(n_masks) * L * L);
+    for (int i = 0; i < STOF_TUNE_CANDIDATES && st == STOF_OK; ++i) {
+      if (kCandidates[i].bn != bn) continue;
+      const stof_kernel kern = kCandidates[i].kernel;
+      st = stof_mha_fwd(q, k, v, dt, B, H, L, d, scale, &fmt, mask_stride_b, mask_stride_h, kern, o, stream);
+      if (st == STOF_ERR_UNSUPPORTED) {  // not a candidate for these sizes
+        st = STOF_OK;
+        continue;
+      }
+      if (st != STOF_OK) break;
+      if (record_cuda(cudaEventRecord(ev[0], s)) != cudaSuccess) { st = STOF_ERR_CUDA; break; }
+      for (int c = 0; c < kTimedCalls && st == STOF_OK; ++c)
+        st = stof_mha_fwd(q, k, v, dt, B, H, L, d, scale, &fmt, mask_stride_b, mask_stride_h, kern, o, stream);
+      if (st != STOF_OK) break;
+      float ms = 0.f;
+      if (record_cuda(cudaEventRecord(ev[1], s)) != cudaSuccess ||
+          record_cuda(cudaEventSynchronize(ev[1])) != cudaSuccess ||
+          record_cuda(cudaEventElapsedTime(&ms, ev[0], ev[1])) != cudaSuccess) {
+        st = STOF_ERR_CUDA;
+        break;
+      }
+      // a device-side failure of a candidate is reported, not chosen
+      st = stof_format_sync(&fmt, stream);
+      if (st != STOF_OK) break;
+      r.cand_ms[i] = ms / kTimedCalls;
+      if (r.ms < 0.f || r.cand_ms[i] < r.ms) {
+        r.ms = r.cand_ms[i];
+        r.kernel = kern;
+        r.bn = bn;
+      }
+    }
+    if (st != STOF_OK) break;
+  }
+  cudaEventDestroy(ev[0]);
+  cudaEventDestroy(ev[1]);
+  if (st != STOF_OK) return st;
+  if (r.ms < 0.f) return STOF_ERR_UNSUPPORTED;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_cache[std::make_tuple(L, d, tune_density_bucket(r.density))] = r;
+  }
+  *out = r;
+  return STOF_OK;
+}
+
+int stof_tune_lookup(int L, int d, double density, stof_tune_result* out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  const auto it = g_cache.find(std::make_tuple(L, d, tune_density_bucket(density)));
+  if (it == g_cache.end()) return 0;
+  if (out) *out = it->second;
+  return 1;
+}
+
+void stof_tune_clear(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_cache.clear();
+}
+
+int stof_tune_density_bucket(double density) { return tune_density_bucket(density); }
+
+}  // extern "C"

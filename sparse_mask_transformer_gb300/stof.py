@@ -41,7 +41,10 @@ STOF_DEVERR_BAD_FORMAT = 0x4
 
 EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync",
             "stof_select_kernel", "stof_mha_fwd", "stof_status_string", "stof_version",
-            "stof_last_cuda_error"]
+            "stof_last_cuda_error", "stof_tune_workspace_bytes", "stof_tune", "stof_tune_lookup",
+            "stof_tune_clear", "stof_tune_density_bucket"]
+
+STOF_TUNE_CANDIDATES = 3
 
 
 class StofError(RuntimeError):
@@ -63,6 +66,14 @@ class stof_format(ctypes.Structure):
         ("bitmaps", ctypes.c_void_p), ("counts_dev", ctypes.c_void_p), ("scratch", ctypes.c_void_p),
         ("n_full", ctypes.c_int64), ("n_part", ctypes.c_int64), ("nnz", ctypes.c_int64),
         ("device_error", ctypes.c_int64),
+    ]
+
+
+class stof_tune_result(ctypes.Structure):
+    _fields_ = [
+        ("kernel", ctypes.c_int), ("bn", ctypes.c_int), ("ms", ctypes.c_float), ("density", ctypes.c_double),
+        ("cand_kernel", ctypes.c_int * STOF_TUNE_CANDIDATES), ("cand_bn", ctypes.c_int * STOF_TUNE_CANDIDATES),
+        ("cand_ms", ctypes.c_float * STOF_TUNE_CANDIDATES),
     ]
 
 
@@ -95,6 +106,17 @@ def load_library(path: str = LIB_PATH):
         lib.stof_version.restype = i32
         lib.stof_last_cuda_error.argtypes = []
         lib.stof_last_cuda_error.restype = ctypes.c_char_p
+        lib.stof_tune_workspace_bytes.argtypes = [i32, i32]
+        lib.stof_tune_workspace_bytes.restype = sz
+        lib.stof_tune.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, i32, ctypes.c_float, i64, i64, P, sz, P,
+                                  ctypes.POINTER(stof_tune_result), P]
+        lib.stof_tune.restype = i32
+        lib.stof_tune_lookup.argtypes = [i32, i32, ctypes.c_double, ctypes.POINTER(stof_tune_result)]
+        lib.stof_tune_lookup.restype = i32
+        lib.stof_tune_clear.argtypes = []
+        lib.stof_tune_clear.restype = None
+        lib.stof_tune_density_bucket.argtypes = [ctypes.c_double]
+        lib.stof_tune_density_bucket.restype = i32
         _lib = lib
     return _lib
 
@@ -172,6 +194,43 @@ def stof_mha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: stof_fo
         ctypes.byref(fmt), int(mask_stride_b), int(mask_stride_h), int(which), o.data_ptr(),
         _stream(stream)), "stof_mha_fwd")
     return o
+
+
+def stof_tune_workspace_bytes(n_masks: int, L: int) -> int:
+    return int(load_library().stof_tune_workspace_bytes(n_masks, L))
+
+
+def stof_tune(mask: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
+              mask_stride_b: int, mask_stride_h: int, workspace: torch.Tensor, o: torch.Tensor,
+              stream=None) -> stof_tune_result:
+    """mask: device uint8 [n_masks, L, L]; q, k, v, o: device [B, H, L, d]."""
+    if mask.dim() != 3 or not mask.is_contiguous() or mask.element_size() != 1:
+        raise StofError(STOF_ERR_SHAPE, "stof_tune: mask must be contiguous 1-byte [n_masks, L, L]")
+    for t in (q, k, v, o):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise StofError(STOF_ERR_SHAPE, "stof_tune: q, k, v, o must match and be contiguous")
+    B, H, L, d = q.shape
+    res = stof_tune_result()
+    _check(load_library().stof_tune(
+        mask.data_ptr(), mask.shape[0], q.data_ptr(), k.data_ptr(), v.data_ptr(), _dtype_code(q), B, H, L, d,
+        float(scale), int(mask_stride_b), int(mask_stride_h), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), o.data_ptr(), ctypes.byref(res), _stream(stream)),
+        "stof_tune")
+    return res
+
+
+def stof_tune_lookup(L: int, d: int, density: float):
+    """The cached stof_tune_result for (L, d, density bucket), or None."""
+    res = stof_tune_result()
+    return res if load_library().stof_tune_lookup(int(L), int(d), float(density), ctypes.byref(res)) else None
+
+
+def stof_tune_clear() -> None:
+    load_library().stof_tune_clear()
+
+
+def stof_tune_density_bucket(density: float) -> int:
+    return int(load_library().stof_tune_density_bucket(float(density)))
 
 
 def format_arrays(fmt: stof_format, workspace: torch.Tensor, n_full: int | None = None,

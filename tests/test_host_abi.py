@@ -155,3 +155,26 @@ def test_binding_checks_shapes_before_calling(lib):
     with pytest.raises(stof.StofError):
         stof.stof_mha_fwd(q.float(), q.float(), q.float(), _fake_format(), 0.1, 0, 0, 0, q.float(),
                           stream=0)
+
+
+def test_tune_cache_host_side(lib):
+    b = stof.stof_tune_density_bucket
+    assert b(1.0) == 0 and b(0.5) == -2 and b(0.25) == -4
+    assert b(0.7) == -1                      # 2 log2(0.7) = -1.03
+    assert b(0.0) == -61 and b(1e-30) == -60
+    stof.stof_tune_clear()
+    assert stof.stof_tune_lookup(16384, 128, 0.05) is None
+    assert stof.stof_tune_workspace_bytes(32, 16384) == max(
+        stof.stof_encode_workspace_bytes(32, 16384, 16384, 128, bn) for bn in (64, 128))
+    assert stof.stof_tune_workspace_bytes(1, 100) == 0
+
+
+def test_tune_rejects_bad_arguments(lib):
+    res = stof.stof_tune_result()
+    st = lib.stof_tune(None, 1, None, None, None, 0, 1, 1, 128, 64, 0.125, 0, 0, None, 0, None,
+                       ctypes.byref(res), None)
+    assert st == stof.STOF_ERR_INVALID_ARG
+    one = ctypes.c_void_p(16)
+    st = lib.stof_tune(one, 1, one, one, one, 0, 1, 1, 128, 64, 0.125, 0, 0, one, 16, one,
+                       ctypes.byref(res), None)
+    assert st == stof.STOF_ERR_WORKSPACE
