@@ -246,6 +246,8 @@ def run_gpu(args, w: synth.Workload):
 
     # end to end through the same public API with host buffers
     e2e = None if args.no_e2e else run_e2e(args, w, mask, q, k, v, ws, fmt, scale, stream, device, dist)
+    # the same step from the bit-packed mask (stof_encode_mask_bits)
+    bitmask = None if args.no_bitmask else run_bitmask(args, w, mask, q, k, v, ws, scale, stream, device, dist)
 
     kern_name = "blockwise" if chosen == stof.STOF_KERNEL_BLOCKWISE else "rowwise"
     if chosen == stof.STOF_KERNEL_BLOCKWISE:
@@ -283,6 +285,7 @@ def run_gpu(args, w: synth.Workload):
                       "tiles_full": fmt.n_full, "tiles_partial": fmt.n_part},
         "roofline": roofline,
         "e2e": e2e,
+        "bitmask": bitmask,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
@@ -293,6 +296,61 @@ def run_gpu(args, w: synth.Workload):
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_bitmask(args, w, mask, q, k, v, ws, scale, stream, device, dist):
+    """The step with the mask given bit-packed (one bit per element, an
+    eighth of the bytes): device-timed, and end to end from pinned host
+    buffers of the packed mask and Q/K/V."""
+    import torch
+    from sparse_mask_transformer_gb300 import stof
+    bits = stof.stof_synth_pack_bits(mask)
+    fmt = stof.stof_format()
+    o = torch.empty_like(q)
+
+    def step():
+        stof.stof_encode_mask_bits(bits, w.L, 128, 128, ws, fmt)
+        stof.stof_format_sync(fmt)
+        stof.stof_mha_fwd(q, k, v, fmt, scale, w.stride_b, w.stride_h, stof.STOF_KERNEL_AUTO, o)
+
+    def timed(fn, n):
+        fn()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(a.elapsed_time(b) / n, dist, device)
+
+    enc_ms = timed(lambda: stof.stof_encode_mask_bits(bits, w.L, 128, 128, ws, fmt), args.steps)
+    step_ms = timed(step, args.steps)
+    valid = sum_over_ranks(4.0 * w.d * fmt.nnz * heads_per_mask(w), dist, device)
+    out = {"mask_bytes": int(bits.numel()), "encode_ms": round(enc_ms, 4), "ms_per_step": round(step_ms, 4),
+           "value": round(valid / (step_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s"}
+    if not args.no_e2e:
+        hb = torch.empty(bits.shape, dtype=torch.uint8, pin_memory=True).copy_(bits)
+        hq, hk, hv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in (q, k, v))
+        ho = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+
+        def e2e_step():
+            bits.copy_(hb, non_blocking=True)
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+
+        ms = timed(e2e_step, max(1, min(args.steps, args.e2e_steps)))
+        out["e2e"] = {"value": round(valid / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
+                      "h2d_bytes_per_step": int(hb.numel() + 3 * hq.numel() * hq.element_size()),
+                      "d2h_bytes_per_step": int(ho.numel() * ho.element_size())}
+    del bits
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, w, mask, q, k, v, ws, fmt, scale, stream, device, dist):
@@ -453,6 +511,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle time budget of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-bitmask", action="store_true", help="skip the bit-packed-mask measurement")
     ap.add_argument("--heads", type=int, default=0,
                     help="profiling only: run the workload with this many heads (one mask per head "
                          "for per-head masks)")

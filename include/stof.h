@@ -131,6 +131,21 @@ stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, i
                              void* workspace, size_t ws_bytes, stof_format* fmt, void* stream);
 
 /*
+ * Same as stof_encode_mask() for a bit-packed mask: mask_bits is device
+ * uint8 [n_masks][lq][lk / 8], bit c (least significant first) of byte jb
+ * of row i being element (i, 8 jb + c) -- numpy's packbits along the key
+ * axis with bitorder="little".  One byte of a row is then one IT row, so
+ * the encoder reads an eighth of the bytes of the dense mask; the format
+ * it produces is identical.  The pages note that STOF keeps working at
+ * sequence lengths where other systems run out of memory (scifaro.com
+ * summary, Results, scalability up to 16k); a 16384-long dense mask per
+ * head is 256 MB, its bit-packed form 32 MB.  Same sizes, workspace,
+ * alignment (8 bytes) and errors as stof_encode_mask().
+ */
+stof_status stof_encode_mask_bits(const uint8_t* mask_bits, int n_masks, int lq, int lk, int bm, int bn,
+                                  void* workspace, size_t ws_bytes, stof_format* fmt, void* stream);
+
+/*
  * Same as stof_encode_mask(), for callers that cannot allocate device
  * memory at this point -- for instance code running inside a framework's
  * memory pool or allocator callback, or a pre-planned inference runtime

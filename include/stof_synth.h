@@ -18,6 +18,16 @@ extern "C" {
 int stof_synth_causal_bernoulli_mask(uint8_t* out, int n_masks, int L, uint64_t seed,
                                      uint64_t threshold, void* stream);
 
+/* The same masks bit-packed: out[n_masks][L][L/8], bit c (least
+ * significant first) of byte jb of row i = element (i, 8 jb + c).  Requires
+ * L % 64 == 0 and the limits above. */
+int stof_synth_causal_bernoulli_mask_bits(uint8_t* out, int n_masks, int L, uint64_t seed,
+                                          uint64_t threshold, void* stream);
+
+/* Packs n_in mask bytes (device, 8-byte aligned, n_in % 8 == 0; non-zero =
+ * valid) into n_in / 8 bytes, least significant bit first. */
+int stof_synth_pack_bits(const uint8_t* in, uint8_t* out, long long n_in, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -209,8 +209,72 @@ __device__ __forceinline__ void write_outputs(const EncodeParams& p, long long c
   }
 }
 
+// Columns c0..c0+3 of rows a, b, c, d (one byte per column in each word) to
+// one word per column holding rows a, b, c, d in bytes 0..3.
+__device__ __forceinline__ void transpose4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t (&out)[4]) {
+  const uint32_t ab01 = __byte_perm(a, b, 0x5140), ab23 = __byte_perm(a, b, 0x7362);
+  const uint32_t cd01 = __byte_perm(c, d, 0x5140), cd23 = __byte_perm(c, d, 0x7362);
+  out[0] = __byte_perm(ab01, cd01, 0x5410);
+  out[1] = __byte_perm(ab01, cd01, 0x7632);
+  out[2] = __byte_perm(ab23, cd23, 0x5410);
+  out[3] = __byte_perm(ab23, cd23, 0x7632);
+}
+
+// Phase 1 for a bit-packed mask (bit c of byte jb of a row = column 8 jb + c):
+// one byte of a row is one IT row, so an IT word is the bytes of its eight
+// rows in order.  A unit is VEC bytes (VEC IT columns) of each of the 8 rows
+// of a band.
+template <int VEC>
+__device__ __forceinline__ unsigned long long pack_bits_phase(const EncodeParams& p, const ChunkGeom& g,
+                                                              const uint8_t* base, long long row_bytes,
+                                                              uint64_t* words, int tid) {
+  unsigned long long nnz = 0;
+  const int upr = g.itcols / VEC;  // units per band
+  const int nunits = g.bands * upr;
+  for (int w = tid; w < nunits; w += kThreads) {
+    const int pb = w / upr, qu = w - pb * upr;
+    const uint8_t* src = base + static_cast<long long>(8 * pb) * row_bytes + VEC * qu;
+    uint64_t* dst = words + pb * g.itcols + qu * VEC;
+    if constexpr (VEC == 1) {
+      uint64_t word = 0;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) word |= static_cast<uint64_t>(__ldcs(src + r * row_bytes)) << (8 * r);
+      dst[0] = word;
+      nnz += __popcll(word);
+    } else {
+      constexpr int G = VEC / 4;  // 4-column groups
+      uint32_t x[8][G];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if constexpr (VEC == 16) {
+          const uint4 t = __ldcs(reinterpret_cast<const uint4*>(src + r * row_bytes));
+          x[r][0] = t.x; x[r][1] = t.y; x[r][2] = t.z; x[r][3] = t.w;
+        } else {
+          const uint2 t = __ldcs(reinterpret_cast<const uint2*>(src + r * row_bytes));
+          x[r][0] = t.x; x[r][1] = t.y;
+        }
+      }
+#pragma unroll
+      for (int cg = 0; cg < G; ++cg) {
+        uint32_t lo[4], hi[4];
+        transpose4(x[0][cg], x[1][cg], x[2][cg], x[3][cg], lo);
+        transpose4(x[4][cg], x[5][cg], x[6][cg], x[7][cg], hi);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint64_t word = static_cast<uint64_t>(lo[i]) | (static_cast<uint64_t>(hi[i]) << 32);
+          dst[4 * cg + i] = word;
+          nnz += __popcll(word);
+        }
+      }
+    }
+  }
+  return nnz;
+}
+
 // ---------------------------------------------------------------- kernel 1
-template <int VEC>  // bytes per load: 16 when rows and tiles are 16-byte aligned, else 8
+// VEC: bytes per load (dense: 16 when rows and tiles are 16-byte aligned,
+// else 8; bit-packed: 16, 8 or 1).  BITS: the mask is bit-packed.
+template <int VEC, bool BITS>
 __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams p) {
   extern __shared__ uint64_t s_words[];  // [bm/8][nt * bn/8]
   __shared__ long long s_chunk;
@@ -224,11 +288,15 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
   const long long chunk = s_chunk;
   if (chunk >= p.n_chunks) return;
   const ChunkGeom g = chunk_geom(p, chunk);
-  const uint8_t* base = p.mask + (static_cast<long long>(g.m) * p.lq + static_cast<long long>(g.I) * p.bm) * p.lk +
-                        static_cast<long long>(g.J0) * p.bn;
+  const long long row_bytes = BITS ? (p.lk >> 3) : p.lk;
+  const uint8_t* base = p.mask + (static_cast<long long>(g.m) * p.lq + static_cast<long long>(g.I) * p.bm) * row_bytes +
+                        static_cast<long long>(g.J0) * (BITS ? (p.bn >> 3) : p.bn);
 
   // 1. read and pack (each unit = VEC/8 adjacent IT words of one 8-row band)
   unsigned long long local_nnz = 0;
+  if constexpr (BITS) {
+    local_nnz = pack_bits_phase<VEC>(p, g, base, row_bytes, s_words, tid);
+  } else {
   constexpr int WPU = VEC / 8;                 // IT words per unit
   constexpr int kUnroll = VEC == 16 ? 1 : 2;   // units in flight per thread (128 B)
   const int upr = g.itcols / WPU;              // units per band
@@ -271,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
         }
       }
     }
+  }
   }
 #pragma unroll
   for (int off = 16; off; off >>= 1) local_nnz += __shfl_xor_sync(0xffffffffu, local_nnz, off);
@@ -331,12 +400,25 @@ WorkspaceLayout workspace_layout(const EncodeGeom& g) {
 }
 
 cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s) {
-  const bool vec16 = (p.lk % 16 == 0) && (p.bn % 16 == 0) && (reinterpret_cast<uintptr_t>(p.mask) % 16 == 0);
   // shared memory per CTA is at most bm * 1024 / 8 = 32 KB (bm <= 256)
+  const unsigned grid = static_cast<unsigned>(g.n_chunks);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p.mask);
+  if (p.bits) {
+    // a unit of VEC bytes per row must tile every chunk and start aligned
+    const int rb = p.lk / 8, tb = p.bn / 8;
+    if (rb % 16 == 0 && tb % 16 == 0 && a % 16 == 0)
+      encode_kernel<16, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
+    else if (rb % 8 == 0 && tb % 8 == 0 && a % 8 == 0)
+      encode_kernel<8, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
+    else
+      encode_kernel<1, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
+    return cudaGetLastError();
+  }
+  const bool vec16 = (p.lk % 16 == 0) && (p.bn % 16 == 0) && (a % 16 == 0);
   if (vec16)
-    encode_kernel<16><<<static_cast<unsigned>(g.n_chunks), kThreads, g.smem_bytes, s>>>(p);
+    encode_kernel<16, false><<<grid, kThreads, g.smem_bytes, s>>>(p);
   else
-    encode_kernel<8><<<static_cast<unsigned>(g.n_chunks), kThreads, g.smem_bytes, s>>>(p);
+    encode_kernel<8, false><<<grid, kThreads, g.smem_bytes, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -38,7 +38,8 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(const EncodeGeom& g);
 
 struct EncodeParams {
-  const uint8_t* mask;
+  const uint8_t* mask;             // byte mask [n][lq][lk], or bit-packed [n][lq][lk / 8] if bits
+  int bits;
   int lq, lk, bm, bn, n_tr, n_tc, ct, cpr;
   int64_t n_rows, n_chunks;
   int32_t* full_row_ptr;

@@ -61,8 +61,8 @@ size_t stof_encode_workspace_bytes(int n_masks, int lq, int lk, int bm, int bn) 
   return workspace_layout(g).total;
 }
 
-stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, int bm, int bn,
-                             void* workspace, size_t ws_bytes, stof_format* fmt, void* stream) {
+static stof_status encode_impl(const uint8_t* mask, int bits, int n_masks, int lq, int lk, int bm, int bn,
+                               void* workspace, size_t ws_bytes, stof_format* fmt, void* stream) {
   if (!mask || !workspace || !fmt) return STOF_ERR_INVALID_ARG;
   if (n_masks < 1 || lq < 1 || lk < 1 || bm < 1 || bn < 1) return STOF_ERR_INVALID_ARG;
   EncodeGeom g;
@@ -96,6 +96,7 @@ stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, i
   if (record_cuda(cudaMemsetAsync(ws + w.counts, 0, w.zero_bytes, s)) != cudaSuccess) return STOF_ERR_CUDA;
   EncodeParams p;
   p.mask = mask;
+  p.bits = bits;
   p.lq = lq;
   p.lk = lk;
   p.bm = bm;
@@ -116,6 +117,16 @@ stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, i
   p.status = reinterpret_cast<unsigned long long*>(ws + w.status);
   if (record_cuda(launch_encode(p, g, s)) != cudaSuccess) return STOF_ERR_CUDA;
   return STOF_OK;
+}
+
+stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, int bm, int bn,
+                             void* workspace, size_t ws_bytes, stof_format* fmt, void* stream) {
+  return encode_impl(mask, 0, n_masks, lq, lk, bm, bn, workspace, ws_bytes, fmt, stream);
+}
+
+stof_status stof_encode_mask_bits(const uint8_t* mask_bits, int n_masks, int lq, int lk, int bm, int bn,
+                                  void* workspace, size_t ws_bytes, stof_format* fmt, void* stream) {
+  return encode_impl(mask_bits, 1, n_masks, lq, lk, bm, bn, workspace, ws_bytes, fmt, stream);
 }
 
 // Variant of stof_encode_mask() that allocates nothing and needs no device
@@ -163,6 +174,7 @@ stof_status stof_encode_mask_noalloc(const uint8_t* mask, int n_masks, int lq, i
     return STOF_ERR_CUDA;
   EncodeParams p;
   p.mask = mask;
+  p.bits = 0;
   p.lq = lq;
   p.lk = lk;
   p.bm = bm;

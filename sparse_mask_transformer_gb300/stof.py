@@ -42,7 +42,7 @@ STOF_DEVERR_BAD_FORMAT = 0x4
 EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync",
             "stof_select_kernel", "stof_mha_fwd", "stof_status_string", "stof_version",
             "stof_last_cuda_error", "stof_tune_workspace_bytes", "stof_tune", "stof_tune_lookup",
-            "stof_tune_clear", "stof_tune_density_bucket"]
+            "stof_tune_clear", "stof_tune_density_bucket", "stof_encode_mask_bits"]
 
 STOF_TUNE_CANDIDATES = 3
 
@@ -93,6 +93,8 @@ def load_library(path: str = LIB_PATH):
         lib.stof_encode_workspace_bytes.restype = sz
         lib.stof_encode_mask.argtypes = [P, i32, i32, i32, i32, i32, P, sz, ctypes.POINTER(stof_format), P]
         lib.stof_encode_mask.restype = i32
+        lib.stof_encode_mask_bits.argtypes = [P, i32, i32, i32, i32, i32, P, sz, ctypes.POINTER(stof_format), P]
+        lib.stof_encode_mask_bits.restype = i32
         lib.stof_format_sync.argtypes = [ctypes.POINTER(stof_format), P]
         lib.stof_format_sync.restype = i32
         lib.stof_select_kernel.argtypes = [ctypes.c_double, i32, i32]
@@ -167,6 +169,21 @@ def stof_encode_mask(mask: torch.Tensor, bm: int, bn: int, workspace: torch.Tens
         mask.data_ptr(), n_masks, lq, lk, bm, bn, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), ctypes.byref(fmt), _stream(stream)),
         "stof_encode_mask")
+    return fmt
+
+
+def stof_encode_mask_bits(mask_bits: torch.Tensor, lk: int, bm: int, bn: int, workspace: torch.Tensor,
+                          fmt: stof_format | None = None, stream=None) -> stof_format:
+    """mask_bits: device uint8 [n_masks, lq, lk / 8], bit c of byte jb = key 8 jb + c."""
+    if (mask_bits.dim() != 3 or not mask_bits.is_contiguous() or mask_bits.element_size() != 1
+            or lk % 8 or mask_bits.shape[2] != lk // 8):
+        raise StofError(STOF_ERR_SHAPE, "stof_encode_mask_bits: mask must be contiguous uint8 [n_masks, lq, lk/8]")
+    fmt = fmt if fmt is not None else stof_format()
+    n_masks, lq, _ = mask_bits.shape
+    _check(load_library().stof_encode_mask_bits(
+        mask_bits.data_ptr(), n_masks, lq, lk, bm, bn, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), ctypes.byref(fmt), _stream(stream)),
+        "stof_encode_mask_bits")
     return fmt
 
 
@@ -256,19 +273,52 @@ def format_arrays(fmt: stof_format, workspace: torch.Tensor, n_full: int | None 
     )
 
 
-def stof_synth_causal_bernoulli_mask(out: torch.Tensor, n_masks: int, L: int, seed: int,
-                                     threshold: int, stream=None) -> torch.Tensor:
-    """Device generator of seeded causal-Bernoulli masks (libstof_synth.so)."""
+def _synth_lib():
     global _synth
     if _synth is None:
         if not os.path.exists(SYNTH_LIB_PATH):
             raise RuntimeError(f"{SYNTH_LIB_PATH} is missing: build it first")
-        _synth = ctypes.CDLL(SYNTH_LIB_PATH)
-        _synth.stof_synth_causal_bernoulli_mask.argtypes = [
+        lib = ctypes.CDLL(SYNTH_LIB_PATH)
+        lib.stof_synth_causal_bernoulli_mask.argtypes = [
             ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p]
-        _synth.stof_synth_causal_bernoulli_mask.restype = ctypes.c_int
+        lib.stof_synth_causal_bernoulli_mask.restype = ctypes.c_int
+        lib.stof_synth_causal_bernoulli_mask_bits.argtypes = [
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p]
+        lib.stof_synth_causal_bernoulli_mask_bits.restype = ctypes.c_int
+        lib.stof_synth_pack_bits.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p]
+        lib.stof_synth_pack_bits.restype = ctypes.c_int
+        _synth = lib
+    return _synth
+
+
+def stof_synth_causal_bernoulli_mask_bits(out: torch.Tensor, n_masks: int, L: int, seed: int,
+                                          threshold: int, stream=None) -> torch.Tensor:
+    """Bit-packed form of stof_synth_causal_bernoulli_mask: out uint8 [n_masks, L, L/8]."""
+    assert out.numel() == n_masks * L * L // 8 and out.element_size() == 1 and out.is_contiguous()
+    rc = _synth_lib().stof_synth_causal_bernoulli_mask_bits(out.data_ptr(), n_masks, L, seed, threshold,
+                                                            _stream(stream))
+    if rc != 0:
+        raise RuntimeError(f"stof_synth_causal_bernoulli_mask_bits failed: {rc}")
+    return out
+
+
+def stof_synth_pack_bits(dense: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Device uint8 [..., n] (n % 8 == 0) -> bit-packed uint8 [..., n / 8]."""
+    assert dense.element_size() == 1 and dense.is_contiguous() and dense.shape[-1] % 8 == 0
+    if out is None:
+        out = torch.empty(*dense.shape[:-1], dense.shape[-1] // 8, dtype=torch.uint8, device=dense.device)
+    rc = _synth_lib().stof_synth_pack_bits(dense.data_ptr(), out.data_ptr(), dense.numel(), _stream(stream))
+    if rc != 0:
+        raise RuntimeError(f"stof_synth_pack_bits failed: {rc}")
+    return out
+
+
+def stof_synth_causal_bernoulli_mask(out: torch.Tensor, n_masks: int, L: int, seed: int,
+                                     threshold: int, stream=None) -> torch.Tensor:
+    """Device generator of seeded causal-Bernoulli masks (libstof_synth.so)."""
     assert out.numel() == n_masks * L * L and out.element_size() == 1 and out.is_contiguous()
-    rc = _synth.stof_synth_causal_bernoulli_mask(out.data_ptr(), n_masks, L, seed, threshold, _stream(stream))
+    rc = _synth_lib().stof_synth_causal_bernoulli_mask(out.data_ptr(), n_masks, L, seed, threshold,
+                                                       _stream(stream))
     if rc != 0:
         raise RuntimeError(f"stof_synth_causal_bernoulli_mask failed: {rc}")
     return out

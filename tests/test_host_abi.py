@@ -178,3 +178,14 @@ def test_tune_rejects_bad_arguments(lib):
     st = lib.stof_tune(one, 1, one, one, one, 0, 1, 1, 128, 64, 0.125, 0, 0, one, 16, one,
                        ctypes.byref(res), None)
     assert st == stof.STOF_ERR_WORKSPACE
+
+
+def test_encode_bits_rejects_bad_arguments(lib):
+    fmt = stof.stof_format()
+    one = ctypes.c_void_p(256)
+    f = lib.stof_encode_mask_bits
+    assert f(None, 1, 256, 256, 128, 128, one, 1 << 30, ctypes.byref(fmt), None) == stof.STOF_ERR_INVALID_ARG
+    assert f(one, 1, 256, 250, 128, 128, one, 1 << 30, ctypes.byref(fmt), None) == stof.STOF_ERR_SHAPE
+    assert f(ctypes.c_void_p(257), 1, 256, 256, 128, 128, one, 1 << 30, ctypes.byref(fmt),
+             None) == stof.STOF_ERR_ALIGNMENT
+    assert f(one, 1, 256, 256, 128, 128, one, 16, ctypes.byref(fmt), None) == stof.STOF_ERR_WORKSPACE
