@@ -254,6 +254,25 @@ void stof_tune_clear(void);
  * -61 for density 0. */
 int stof_tune_density_bucket(double density);
 
+/*
+ * Output projection after the MHA with a fused epilogue (gist.science
+ * technical summary, Methodology 2: fusion carried past the MHA layer into
+ * the operators that follow it):
+ *   y[b, l, n] = sum_{h, c} O[b, h, l, c] * W[n, h*d + c] + bias[n] + residual[b, l, n]
+ *   o         device [B][H][L][d] (the MHA output), dt.
+ *   w         device [N][H*d] row-major (a linear layer's weight), dt.
+ *   bias      device [N] or NULL; residual device [B][L][N] or NULL; dt.
+ *   y         device [B][L][N], written; must not overlap the inputs.
+ *   device_error  device int64 word that a pipeline timeout ORs
+ *             STOF_DEVERR_PIPE_TIMEOUT into, or NULL.
+ * fp32 accumulation; bias and residual are added in fp32 and y is rounded
+ * once to nearest even.  Requires d = 64 or 128, L % 128 == 0,
+ * N % 256 == 0 and 16-byte aligned pointers.  Asynchronous on stream.
+ */
+stof_status stof_oproj_fwd(const void* o, const void* w, const void* bias, const void* residual,
+                           stof_dtype dt, int B, int H, int L, int d, int N, void* y,
+                           int64_t* device_error, void* stream);
+
 /* Static description of a status code. */
 const char* stof_status_string(stof_status s);
 

@@ -15,6 +15,13 @@ GPU", gist.science technical summary):
   - ``encode`` / ``decode``: the two-level format by brute force
     (Methodology 1: OT classes empty / full / partial, pointer arrays for
     full and partial OTs, one uint64 per 8x8 IT of a partial OT).
+  - ``oproj``: the operator after the MHA, the output projection with bias
+    and residual, by its definition in fp64 (Methodology 2, operator fusion
+    module: fusion carried past the MHA layer): heads concatenated along
+    the reduction axis, y = O_cat W^T + bias + residual.  A numpy matmul is
+    its one library step.
+  - ``unpack_bits``: a bit-packed mask (least significant bit first along
+    the key axis) back to bytes, by explicit shifts.
 
 Pins (tests/test_oracle_pins.py) tie every function to something other than
 itself: library dense attention, closed forms, tiny brute force, round trips
@@ -158,4 +165,27 @@ def attention_bhld(q, k, v, mask_of, scale: float, heads=None, rows=None,
     for (b, h) in heads:
         m = mask_of(b, h, rows)
         out[(b, h)] = attention(q[b, h, rows], k[b, h], v[b, h], m, scale, n_threads)
+    return out
+
+
+def oproj(o, w, bias=None, residual=None) -> np.ndarray:
+    """y[b, l, n] = sum_{h, c} o[b, h, l, c] w[n, h d + c] + bias[n] + residual[b, l, n],
+    fp64.  o: [B, H, L, d]; w: [N, H d]; bias: [N] or None; residual: [B, L, N] or None."""
+    o = np.asarray(o, np.float64)
+    B, H, L, d = o.shape
+    o_cat = o.transpose(0, 2, 1, 3).reshape(B, L, H * d)   # token-major, heads side by side
+    y = o_cat @ np.asarray(w, np.float64).T
+    if bias is not None:
+        y = y + np.asarray(bias, np.float64)
+    if residual is not None:
+        y = y + np.asarray(residual, np.float64)
+    return y
+
+
+def unpack_bits(bits, lk: int) -> np.ndarray:
+    """uint8 [..., lk / 8] -> uint8 [..., lk]: element 8 jb + c = bit c of byte jb."""
+    bits = np.asarray(bits, np.uint8)
+    out = np.zeros(bits.shape[:-1] + (lk,), np.uint8)
+    for c in range(8):
+        out[..., c::8] = (bits >> c) & 1
     return out

@@ -1,0 +1,336 @@
+// Attention output projection with a fused epilogue, for sm_103a.
+//
+// "Accelerating Sparse Transformer Inference on GPU" (gist.science technical
+// summary), Methodology 2, operator fusion module: fusion is carried past
+// the MHA layer into the operators that follow it.  The operator right after
+// masked MHA in a transformer layer is the output projection with its bias
+// and the residual connection:
+//   y[b, l, n] = sum_{h, c} O[b, h, l, c] * W[n, h*d + c] + bias[n] + res[b, l, n]
+// with O the MHA output [B][H][L][d] (heads concatenated along the
+// reduction axis, as the projection sees them), W a [N][H*d] row-major
+// weight and res [B][L][N].  Here it is one GEMM whose epilogue adds the
+// bias and the residual and rounds once, so the projection's output is
+// written once and never re-read for the additions.
+//
+// GB300 design: a persistent kernel, one CTA per SM, 192 threads:
+//   warp 0      TMA producer: for every (128-token, 256-feature) output
+//               tile and every 64-wide slice of the reduction, the O slice
+//               (128 tokens of one head, 64 of its d columns: rows of O
+//               viewed as [B*H*L][d]) and the W slice (256 rows x 64) into a
+//               four-stage ring;
+//   warp 1      allocates TMEM and issues the tcgen05 MMAs (M = 128,
+//               N = 256, K = 16; both operands K-major, 128-byte swizzle)
+//               into one of two TMEM accumulators;
+//   warps 2..5  epilogue: a thread owns one token row (= TMEM lane), reads
+//               its 256 fp32 sums, adds bias and residual in fp32, rounds to
+//               fp16/bf16 and stores; the accumulator then goes back to the
+//               issuer, so the epilogue of one tile overlaps the MMAs of the
+//               next.
+// Every wait is bounded; on timeout the CTA raises STOF_DEVERR_PIPE_TIMEOUT
+// in the caller's error word (if given), drains and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace stof {
+namespace {
+
+using namespace ptx;
+
+constexpr int kTM = 128;     // tokens per tile (MMA M)
+constexpr int kTN = 256;     // output features per tile (MMA N)
+constexpr int kTK = 64;      // reduction slice per stage (one 128-byte swizzle atom)
+constexpr int kStages = 4;
+constexpr int kThreadsOP = 192;
+constexpr int kABytes = kTM * kTK * 2;  // 16 KB
+constexpr int kBBytes = kTN * kTK * 2;  // 32 KB
+constexpr uint64_t kWaitNsOP = 2000000000ull;
+
+struct alignas(1024) OpSmem {
+  uint8_t a[kStages][kABytes];
+  uint8_t b[kStages][kBBytes];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct OpParams {
+  const void* bias;      // [N] or null
+  const void* residual;  // [B][L][N] or null
+  void* y;               // [B][L][N]
+  int64_t* err;          // device error word or null
+  int B, H, L, d, N;
+  int m_tiles, n_tiles, k_blocks;
+};
+
+template <bool BF16>
+__device__ __forceinline__ float to_f32(uint16_t x) {
+  if constexpr (BF16)
+    return __bfloat162float(__ushort_as_bfloat16(x));
+  else
+    return __half2float(__ushort_as_half(x));
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2f(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreadsOP, 1)
+    oproj_kernel(const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmW,
+                 const OpParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  OpSmem& s = *reinterpret_cast<OpSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.acc_full[i], 1);
+      mbar_init(&s.acc_empty[i], 128);
+    }
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem_base;  // accumulator a at columns a * 256
+  volatile int* abort_flag = &s.abort_flag;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    if (p.err) atomicOr(reinterpret_cast<unsigned long long*>(p.err), STOF_DEVERR_PIPE_TIMEOUT);
+  };
+  const int n_tiles_total = p.m_tiles * p.n_tiles;
+  const int kb_per_head = p.d / kTK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmO);
+      prefetch_tmap(&tmW);
+      int it = 0, issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x) {
+        const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+        const int tok0 = mt * kTM;                      // token index b * L + l
+        const int b = tok0 / p.L, l0 = tok0 - b * p.L;  // a tile never straddles a batch (L % 128 == 0)
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const int st = it % kStages;
+          if (it >= kStages && !mbar_wait(&s.empty[st], ((it / kStages) - 1) & 1, abort_flag, kWaitNsOP)) {
+            ok = false;
+            break;
+          }
+          const int h = kb / kb_per_head, c0 = (kb - h * kb_per_head) * kTK;
+          mbar_arrive_expect_tx(&s.full[st], kABytes + kBBytes);
+          tma_load_2d(s.a[st], &tmO, &s.full[st], c0, (b * p.H + h) * p.L + l0);
+          tma_load_2d(s.b[st], &tmW, &s.full[st], kb * kTK, nt * kTN);
+          issued = it + 1;
+        }
+      }
+      if (!ok) fail();
+      if (*abort_flag) {  // let the copies in flight land before exit
+        for (int i = issued - kStages < 0 ? 0 : issued - kStages; i < issued; ++i)
+          mbar_wait_timeout(&s.full[i % kStages], (i / kStages) & 1, kWaitNsOP);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_f16(BF16 ? 1 : 0, 0, kTM, kTN);
+    const uint64_t adesc0 = smem_desc_sw128(smem_u32(s.a[0]), 16, 1024);
+    const uint64_t bdesc0 = smem_desc_sw128(smem_u32(s.b[0]), 16, 1024);
+    auto wwait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitNsOP));
+    };
+    int it = 0, j = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x, ++j) {
+      const int a = j & 1;
+      // the epilogue has read this accumulator's previous tile
+      if (j >= 2 && !wwait(&s.acc_empty[a], ((j >> 1) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tbase + a * kTN;
+      for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+        const int st = it % kStages;
+        if (!wwait(&s.full[st], (it / kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = adesc0 + static_cast<uint64_t>(st) * (kABytes / 16);
+        const uint64_t bd = bdesc0 + static_cast<uint64_t>(st) * (kBBytes / 16);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kTK / 16; ++kk)  // 32 B per K step inside the atom
+            mma_f16_ss(d_tmem, ad + kk * 2, bd + kk * 2, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&s.empty[st]);                            // stage free once these MMAs are done
+          if (kb == p.k_blocks - 1) mma_commit(&s.acc_full[a]);  // the tile's sums are complete
+        }
+        __syncwarp();
+      }
+    }
+    if (elect_one()) {
+      if (!ok) fail();
+      mma_commit(&s.drain);
+      mbar_wait_timeout(&s.drain, 0, kWaitNsOP);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // token row of the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint16_t* bias = static_cast<const uint16_t*>(p.bias);
+    const uint16_t* res = static_cast<const uint16_t*>(p.residual);
+    uint16_t* y = static_cast<uint16_t*>(p.y);
+    int j = 0;
+    for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x, ++j) {
+      const int a = j & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&s.acc_full[a], (j >> 1) & 1, abort_flag, kWaitNsOP));
+      if (!ok) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+      const long long row = static_cast<long long>(mt) * kTM + r;
+      const int n0 = nt * kTN;
+#pragma unroll 1
+      for (int cc = 0; cc < kTN / 32; ++cc) {
+        uint32_t acc[32];
+        tmem_ld32(tbase + a * kTN + lane_off + cc * 32, acc);
+        tmem_ld_wait(acc);
+        const int n = n0 + cc * 32;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
+        if (bias) {
+          const uint4* bv = reinterpret_cast<const uint4*>(bias + n);  // same address in every lane
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 t = __ldg(bv + q);
+            const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[8 * q + 2 * e] += to_f32<BF16>(static_cast<uint16_t>(w4[e] & 0xFFFFu));
+              v[8 * q + 2 * e + 1] += to_f32<BF16>(static_cast<uint16_t>(w4[e] >> 16));
+            }
+          }
+        }
+        if (res) {
+          const uint4* rv = reinterpret_cast<const uint4*>(res + row * p.N + n);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 t = __ldcs(rv + q);
+            const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[8 * q + 2 * e] += to_f32<BF16>(static_cast<uint16_t>(w4[e] & 0xFFFFu));
+              v[8 * q + 2 * e + 1] += to_f32<BF16>(static_cast<uint16_t>(w4[e] >> 16));
+            }
+          }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(y + row * p.N + n);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[q] = make_uint4(pack2f<BF16>(v[8 * q], v[8 * q + 1]), pack2f<BF16>(v[8 * q + 2], v[8 * q + 3]),
+                              pack2f<BF16>(v[8 * q + 4], v[8 * q + 5]), pack2f<BF16>(v[8 * q + 6], v[8 * q + 7]));
+      }
+      tc_fence_before();
+      mbar_arrive(&s.acc_empty[a]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <bool BF16>
+stof_status launch_op(const void* o, const void* w, const OpParams& p, cudaStream_t s) {
+  const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t K = static_cast<uint64_t>(p.H) * p.d;
+  CUtensorMap mo, mw;
+  // O viewed as [B*H*L][d]; W as [N][K]; boxes of 64 columns (one swizzle atom)
+  if (!encode_tensor_map_2d(&mo, dt, o, static_cast<uint64_t>(p.d), static_cast<uint64_t>(p.B) * p.H * p.L,
+                            static_cast<uint64_t>(p.d) * 2, kTK, kTM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map_2d(&mw, dt, w, K, static_cast<uint64_t>(p.N), K * 2, kTK, kTN,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+    return STOF_ERR_CUDA;
+  const size_t smem = sizeof(OpSmem) + 1024;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (record_cuda(cudaFuncSetAttribute(oproj_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem))) != cudaSuccess)
+      return STOF_ERR_CUDA;
+    attr_done = true;
+  }
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
+  oproj_kernel<BF16><<<grid, kThreadsOP, smem, s>>>(mo, mw, p);
+  return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace stof
+
+using namespace stof;
+
+extern "C" stof_status stof_oproj_fwd(const void* o, const void* w, const void* bias, const void* residual,
+                                      stof_dtype dt, int B, int H, int L, int d, int N, void* y,
+                                      int64_t* device_error, void* stream) {
+  if (!o || !w || !y) return STOF_ERR_INVALID_ARG;
+  if (dt != STOF_F16 && dt != STOF_BF16) return STOF_ERR_DTYPE;
+  if (B < 1 || H < 1 || L < 1 || d < 1 || N < 1) return STOF_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return STOF_ERR_UNSUPPORTED;
+  if (L % kTM || N % kTN) return STOF_ERR_SHAPE;
+  if (static_cast<long long>(B) * H * L >= (1ll << 31) || static_cast<long long>(B) * L * N >= (1ll << 40) ||
+      static_cast<long long>(H) * d > (1 << 20))
+    return STOF_ERR_SHAPE;
+  auto al16 = [](const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; };
+  if (!al16(o) || !al16(w) || !al16(y) || (bias && !al16(bias)) || (residual && !al16(residual)))
+    return STOF_ERR_ALIGNMENT;
+  OpParams p;
+  p.bias = bias;
+  p.residual = residual;
+  p.y = y;
+  p.err = device_error;
+  p.B = B;
+  p.H = H;
+  p.L = L;
+  p.d = d;
+  p.N = N;
+  p.m_tiles = B * L / kTM;
+  p.n_tiles = N / kTN;
+  p.k_blocks = H * d / kTK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return dt == STOF_BF16 ? launch_op<true>(o, w, p, s) : launch_op<false>(o, w, p, s);
+}

@@ -42,7 +42,7 @@ STOF_DEVERR_BAD_FORMAT = 0x4
 EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync",
             "stof_select_kernel", "stof_mha_fwd", "stof_status_string", "stof_version",
             "stof_last_cuda_error", "stof_tune_workspace_bytes", "stof_tune", "stof_tune_lookup",
-            "stof_tune_clear", "stof_tune_density_bucket", "stof_encode_mask_bits"]
+            "stof_tune_clear", "stof_tune_density_bucket", "stof_encode_mask_bits", "stof_oproj_fwd"]
 
 STOF_TUNE_CANDIDATES = 3
 
@@ -108,6 +108,8 @@ def load_library(path: str = LIB_PATH):
         lib.stof_version.restype = i32
         lib.stof_last_cuda_error.argtypes = []
         lib.stof_last_cuda_error.restype = ctypes.c_char_p
+        lib.stof_oproj_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]
+        lib.stof_oproj_fwd.restype = i32
         lib.stof_tune_workspace_bytes.argtypes = [i32, i32]
         lib.stof_tune_workspace_bytes.restype = sz
         lib.stof_tune.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, i32, ctypes.c_float, i64, i64, P, sz, P,
@@ -211,6 +213,30 @@ def stof_mha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: stof_fo
         ctypes.byref(fmt), int(mask_stride_b), int(mask_stride_h), int(which), o.data_ptr(),
         _stream(stream)), "stof_mha_fwd")
     return o
+
+
+def stof_oproj_fwd(o: torch.Tensor, w: torch.Tensor, bias: torch.Tensor | None, residual: torch.Tensor | None,
+                   y: torch.Tensor, device_error: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """o: device [B, H, L, d]; w: [N, H*d]; bias: [N] or None; residual: [B, L, N] or None;
+    y: [B, L, N] (written).  device_error: optional device int64 tensor of one element."""
+    if o.dim() != 4:
+        raise StofError(STOF_ERR_SHAPE, "stof_oproj_fwd: o must be [B, H, L, d]")
+    B, H, L, d = o.shape
+    N = w.shape[0]
+    if w.shape != (N, H * d) or y.shape != (B, L, N):
+        raise StofError(STOF_ERR_SHAPE, "stof_oproj_fwd: w must be [N, H*d] and y [B, L, N]")
+    for t in (o, w, y, bias, residual):
+        if t is not None and (t.dtype != o.dtype or not t.is_contiguous()):
+            raise StofError(STOF_ERR_SHAPE, "stof_oproj_fwd: tensors must share o's dtype and be contiguous")
+    if bias is not None and bias.shape != (N,):
+        raise StofError(STOF_ERR_SHAPE, "stof_oproj_fwd: bias must be [N]")
+    if residual is not None and residual.shape != (B, L, N):
+        raise StofError(STOF_ERR_SHAPE, "stof_oproj_fwd: residual must be [B, L, N]")
+    ptr = lambda t: None if t is None else t.data_ptr()
+    _check(load_library().stof_oproj_fwd(
+        o.data_ptr(), w.data_ptr(), ptr(bias), ptr(residual), _dtype_code(o), B, H, L, d, N, y.data_ptr(),
+        ptr(device_error), _stream(stream)), "stof_oproj_fwd")
+    return y
 
 
 def stof_tune_workspace_bytes(n_masks: int, L: int) -> int:

@@ -1,0 +1,84 @@
+"""Output projection after the MHA with the fused bias + residual epilogue
+(gist.science technical summary, Methodology 2: fusion carried past the MHA
+layer) against the fp64 oracle.  Tolerance from the arithmetic: inputs are
+exact fp16/bf16 values and sums accumulate in fp32 (relative error of the
+sum far below the output's rounding), so the error is the output's single
+rounding: |y - y_ref| <= 2^-8 (|y_ref| + 1) for bf16 and 2^-11 (|y_ref| + 1)
+for fp16."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_mask_transformer_gb300 import stof, synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11}
+DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+def _case(B, H, L, d, N, dtype, bias=True, residual=True, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    o = torch.randn(B, H, L, d, generator=g).to(DT[dtype])
+    w = (torch.randn(N, H * d, generator=g) / (H * d) ** 0.5).to(DT[dtype])
+    b = (0.1 * torch.randn(N, generator=g)).to(DT[dtype]) if bias else None
+    r = torch.randn(B, L, N, generator=g).to(DT[dtype]) if residual else None
+    err = torch.zeros(1, dtype=torch.int64, device="cuda")
+    y = torch.full((B, L, N), float("nan"), dtype=DT[dtype], device="cuda")
+    cuda = lambda t: None if t is None else t.cuda()
+    stof.stof_oproj_fwd(o.cuda(), w.cuda(), cuda(b), cuda(r), y, err)
+    torch.cuda.synchronize()
+    f64 = lambda t: None if t is None else t.double().numpy()
+    want = oracle.oproj(f64(o), f64(w), f64(b), f64(r))
+    got = y.double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - want) <= TOL_REL[dtype] * (np.abs(want) + 1.0))
+    assert int(err.item()) == 0
+    return got, want
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_small_shapes(gpu_lib, dtype, d):
+    _case(2, 3, 256, d, 512, dtype, seed=d)
+
+
+@pytest.mark.parametrize("bias,residual", [(False, False), (True, False), (False, True)])
+def test_without_bias_or_residual(gpu_lib, bias, residual):
+    _case(1, 2, 128, 64, 256, "bf16", bias=bias, residual=residual, seed=3)
+
+
+def test_bert_base_layer_shape(gpu_lib):
+    # BERT-base attention output: 12 heads x 64 = 768 features, 512 tokens x 16
+    _case(16, 12, 512, 64, 768, "bf16", seed=4)
+
+
+def test_more_tiles_than_sms(gpu_lib):
+    # 8 x 1024 tokens / 128 x 1024 / 256 = 256 output tiles: more than one per SM, so CTAs loop
+    _case(8, 8, 1024, 128, 1024, "fp16", seed=5)
+
+
+def test_identity_weight_concatenates_heads(gpu_lib):
+    B, H, L, d = 1, 4, 128, 64
+    o = torch.randn(B, H, L, d, generator=torch.Generator().manual_seed(6)).to(torch.bfloat16)
+    w = torch.eye(H * d).to(torch.bfloat16)
+    y = torch.empty(B, L, H * d, dtype=torch.bfloat16, device="cuda")
+    stof.stof_oproj_fwd(o.cuda(), w.cuda(), None, None, y)
+    torch.cuda.synchronize()
+    assert torch.equal(y.cpu(), o.transpose(1, 2).reshape(B, L, H * d))
+
+
+def test_shape_errors(gpu_lib):
+    o = torch.zeros(1, 2, 100, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(256, 128, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(1, 100, 256, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(stof.StofError) as e:
+        stof.stof_oproj_fwd(o, w, None, None, y)
+    assert e.value.status == stof.STOF_ERR_SHAPE          # L not a multiple of 128
+    o = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(200, 128, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(1, 128, 200, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(stof.StofError) as e:
+        stof.stof_oproj_fwd(o, w, None, None, y)
+    assert e.value.status == stof.STOF_ERR_SHAPE          # N not a multiple of 256

@@ -250,3 +250,43 @@ def test_workload_masks_round_trip(name):
     fmt = oracle.encode(mask, 128, 128)
     assert np.array_equal(oracle.decode(fmt), mask)
     assert fmt["nnz"] == int(mask.sum())
+
+
+def test_oproj_brute_force_tiny():
+    # the definition written out as loops on a tiny case
+    rng = np.random.default_rng(11)
+    B, H, L, d, N = 2, 3, 4, 2, 5
+    o = rng.standard_normal((B, H, L, d))
+    w = rng.standard_normal((N, H * d))
+    bias = rng.standard_normal(N)
+    res = rng.standard_normal((B, L, N))
+    y = oracle.oproj(o, w, bias, res)
+    for b in range(B):
+        for l in range(L):
+            for n in range(N):
+                acc = bias[n] + res[b, l, n]
+                for h in range(H):
+                    for c in range(d):
+                        acc += o[b, h, l, c] * w[n, h * d + c]
+                assert abs(y[b, l, n] - acc) < 1e-12
+
+
+def test_oproj_identity_weight_concatenates_heads():
+    # W = I: y is the heads' outputs side by side (plus bias and residual)
+    rng = np.random.default_rng(12)
+    B, H, L, d = 1, 4, 3, 8
+    o = rng.standard_normal((B, H, L, d))
+    y = oracle.oproj(o, np.eye(H * d), np.zeros(H * d), None)
+    for h in range(H):
+        assert np.array_equal(y[0, :, h * d:(h + 1) * d], o[0, h])
+    assert np.array_equal(oracle.oproj(o, np.zeros((5, H * d)), np.arange(5.0), None)[0, 2], np.arange(5.0))
+
+
+def test_unpack_bits_inverts_numpy_packbits():
+    rng = np.random.default_rng(13)
+    m = (rng.random((3, 5, 64)) < 0.3).astype(np.uint8)
+    assert np.array_equal(oracle.unpack_bits(np.packbits(m, axis=-1, bitorder="little"), 64), m)
+    one = np.zeros((1, 16), np.uint8)
+    one[0, 9] = 1                                  # key 9 = bit 1 of byte 1
+    assert list(np.packbits(one, axis=-1, bitorder="little")[0]) == [0, 2]
+    assert np.array_equal(oracle.unpack_bits(np.array([[0, 2]], np.uint8), 16), one)
