@@ -354,7 +354,13 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
 
 }  // namespace
 
-bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g) {
+// Mask columns per chunk.  A bit-packed mask carries an eighth of the bytes
+// per column, so its chunks are wider to keep every thread loading and the
+// per-chunk look-back and barriers rarer.
+constexpr int kChunkColsDense = 1024;
+constexpr int kChunkColsBits = 2048;
+
+bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g, bool bits) {
   if (n_masks < 1 || lq < 1 || lk < 1) return false;
   if (bm < 8 || bn < 8 || bm > 256 || bn > 256 || bm % 8 || bn % 8) return false;
   if (lq % bm || lk % bn) return false;
@@ -363,7 +369,7 @@ bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g)
   g->n_rows = static_cast<int64_t>(n_masks) * g->n_tr;
   g->n_tiles = g->n_rows * g->n_tc;
   if (g->n_tiles >= (int64_t(1) << 31) - 1) return false;
-  int ct = 1024 / bn;
+  int ct = (bits ? kChunkColsBits : kChunkColsDense) / bn;
   if (ct < 1) ct = 1;
   if (ct > kMaxTilesPerChunk) ct = kMaxTilesPerChunk;
   if (ct > g->n_tc) ct = g->n_tc;
@@ -400,18 +406,36 @@ WorkspaceLayout workspace_layout(const EncodeGeom& g) {
 }
 
 cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s) {
-  // shared memory per CTA is at most bm * 1024 / 8 = 32 KB (bm <= 256)
+  // shared memory per CTA: (bm / 8) * (chunk columns / 8) words
   const unsigned grid = static_cast<unsigned>(g.n_chunks);
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.mask);
   if (p.bits) {
     // a unit of VEC bytes per row must tile every chunk and start aligned
     const int rb = p.lk / 8, tb = p.bn / 8;
     if (rb % 16 == 0 && tb % 16 == 0 && a % 16 == 0)
-      encode_kernel<16, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
+      {
+        if (g.smem_bytes > 48 * 1024 &&
+            cudaFuncSetAttribute(encode_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(g.smem_bytes)) != cudaSuccess)
+          return cudaGetLastError();
+        encode_kernel<16, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
+      }
     else if (rb % 8 == 0 && tb % 8 == 0 && a % 8 == 0)
-      encode_kernel<8, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
+      {
+        if (g.smem_bytes > 48 * 1024 &&
+            cudaFuncSetAttribute(encode_kernel<8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(g.smem_bytes)) != cudaSuccess)
+          return cudaGetLastError();
+        encode_kernel<8, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
+      }
     else
-      encode_kernel<1, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
+      {
+        if (g.smem_bytes > 48 * 1024 &&
+            cudaFuncSetAttribute(encode_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(g.smem_bytes)) != cudaSuccess)
+          return cudaGetLastError();
+        encode_kernel<1, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
+      }
     return cudaGetLastError();
   }
   const bool vec16 = (p.lk % 16 == 0) && (p.bn % 16 == 0) && (a % 16 == 0);

@@ -28,7 +28,9 @@ struct EncodeGeom {
   int words_per_tile;           // (bm/8) * (bn/8)
   size_t smem_bytes;            // dynamic shared memory of one encoder CTA
 };
-bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g);
+// chunk_cols: mask columns per chunk (rounded to whole OTs); 0 = the width
+// the encoder uses for a dense (bits = false) or bit-packed mask.
+bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g, bool bits = false);
 
 // Workspace carve-up (byte offsets, 256-byte aligned sections).
 struct WorkspaceLayout {
