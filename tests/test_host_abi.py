@@ -157,6 +157,34 @@ def test_binding_checks_shapes_before_calling(lib):
                           stream=0)
 
 
+def test_binding_checks_new_entry_points_before_calling(lib):
+    import torch
+    with pytest.raises(stof.StofError):        # last axis must be lk / 8
+        stof.stof_encode_mask_bits(torch.zeros(1, 64, 7, dtype=torch.uint8), 64, 16, 16,
+                                   torch.zeros(16, dtype=torch.uint8))
+    o = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16)
+    w = torch.zeros(256, 128, dtype=torch.bfloat16)
+    y = torch.zeros(1, 128, 256, dtype=torch.bfloat16)
+    with pytest.raises(stof.StofError):        # w must be [N, H*d]
+        stof.stof_oproj_fwd(o, torch.zeros(256, 64, dtype=torch.bfloat16), None, None, y)
+    with pytest.raises(stof.StofError):        # bias must be [N]
+        stof.stof_oproj_fwd(o, w, torch.zeros(128, dtype=torch.bfloat16), None, y)
+    with pytest.raises(stof.StofError):        # dtypes must agree
+        stof.stof_oproj_fwd(o, w.float(), None, None, y)
+
+
+def test_oproj_rejects_bad_arguments(lib):
+    f = lib.stof_oproj_fwd
+    one = ctypes.c_void_p(256)
+    assert f(None, one, None, None, 0, 1, 2, 128, 64, 256, one, None, None) == stof.STOF_ERR_INVALID_ARG
+    assert f(one, one, None, None, 7, 1, 2, 128, 64, 256, one, None, None) == stof.STOF_ERR_DTYPE
+    assert f(one, one, None, None, 0, 1, 2, 128, 96, 256, one, None, None) == stof.STOF_ERR_UNSUPPORTED
+    assert f(one, one, None, None, 0, 1, 2, 100, 64, 256, one, None, None) == stof.STOF_ERR_SHAPE
+    assert f(one, one, None, None, 0, 1, 2, 128, 64, 200, one, None, None) == stof.STOF_ERR_SHAPE
+    assert f(ctypes.c_void_p(8), one, None, None, 0, 1, 2, 128, 64, 256, one, None,
+             None) == stof.STOF_ERR_ALIGNMENT
+
+
 def test_tune_cache_host_side(lib):
     b = stof.stof_tune_density_bucket
     assert b(1.0) == 0 and b(0.5) == -2 and b(0.25) == -4
