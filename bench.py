@@ -50,11 +50,17 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+HOST_CODE_MARK = b"// [rows][D] row-major 16-bit matrix"
+
+
 def kernel_source_hash() -> str:
+    """Hash of the block-wise kernel's device code: blockwise.cu up to its
+    host-side launch code, and the PTX wrappers it includes."""
     h = hashlib.sha256()
     for f in ("blockwise.cu", "sm100_ptx.cuh"):
         with open(os.path.join(ROOT, "sparse_mask_transformer_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+            text = fh.read()
+        h.update(text.split(HOST_CODE_MARK)[0] if f == "blockwise.cu" else text)
     return h.hexdigest()[:16]
 
 

@@ -545,17 +545,26 @@ stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
       !make_map(&mv, p.v, rows, D, BN, BF16))
     return STOF_ERR_CUDA;
   const size_t smem = sizeof(Smem<D, BN>) + 1024;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (record_cuda(cudaFuncSetAttribute(blockwise_kernel<D, BN, BF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem))) != cudaSuccess)
-      return STOF_ERR_CUDA;
+  stof_status prep = STOF_OK;
+  auto prepare = [](const void* arg) {
+    stof_status* st = static_cast<stof_status*>(const_cast<void*>(arg));
+    if (record_cuda(cudaFuncSetAttribute(blockwise_kernel<D, BN, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sizeof(Smem<D, BN>) + 1024))) != cudaSuccess) {
+      *st = STOF_ERR_CUDA;
+      return false;
+    }
     cudaFuncAttributes fa;
-    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_kernel<D, BN, BF16>)) != cudaSuccess) return STOF_ERR_CUDA;
-    if (fa.numRegs != kLaunchRegs) return STOF_ERR_UNSUPPORTED;  // the register split needs exactly this
-    attr_done = true;
-  }
+    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_kernel<D, BN, BF16>)) != cudaSuccess) {
+      *st = STOF_ERR_CUDA;
+      return false;
+    }
+    if (fa.numRegs != kLaunchRegs) {  // the register split needs exactly this
+      *st = STOF_ERR_UNSUPPORTED;
+      return false;
+    }
+    return true;
+  };
+  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_kernel<D, BN, BF16>), prepare, &prep)) return prep;
   const long long grid = static_cast<long long>(p.B) * p.H * p.n_tr;
   blockwise_kernel<D, BN, BF16><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
   return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;

@@ -19,6 +19,10 @@ bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ba
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+// Runs prepare() (function attributes, checks) once per (current device, key)
+// and remembers success; thread-safe.  Returns prepare()'s result, or true
+// when it already succeeded on this device.
+bool once_per_device(const void* key, bool (*prepare)(const void*), const void* arg);
 
 // ---------------------------------------------------------------- encoder
 // A chunk is one OT row band (bm mask rows) times `ct` consecutive OTs.

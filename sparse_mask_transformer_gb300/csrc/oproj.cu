@@ -286,13 +286,11 @@ stof_status launch_op(const void* o, const void* w, const OpParams& p, cudaStrea
                             CU_TENSOR_MAP_SWIZZLE_128B))
     return STOF_ERR_CUDA;
   const size_t smem = sizeof(OpSmem) + 1024;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (record_cuda(cudaFuncSetAttribute(oproj_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem))) != cudaSuccess)
-      return STOF_ERR_CUDA;
-    attr_done = true;
-  }
+  auto prepare = [](const void*) {
+    return record_cuda(cudaFuncSetAttribute(oproj_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(sizeof(OpSmem) + 1024))) == cudaSuccess;
+  };
+  if (!once_per_device(reinterpret_cast<const void*>(&oproj_kernel<BF16>), prepare, nullptr)) return STOF_ERR_CUDA;
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
   oproj_kernel<BF16><<<grid, kThreadsOP, smem, s>>>(mo, mw, p);

@@ -12,6 +12,10 @@
 #include <cstdint>
 #include <cstring>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "internal.h"
 
 using namespace stof;
@@ -31,6 +35,22 @@ cudaError_t record_cuda(cudaError_t e) {
   if (e != cudaSuccess) g_last_cuda_error = e;
   return e;
 }
+
+// Runs prepare(arg) once per (current device, key); a failed preparation is
+// retried on the next call.  Guards the per-kernel function attributes, which
+// are per-device state in the CUDA runtime.
+bool once_per_device(const void* key, bool (*prepare)(const void*), const void* arg) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return prepare(arg);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({dev, key})) return true;
+  if (!prepare(arg)) return false;
+  done.insert({dev, key});
+  return true;
+}
+
 }  // namespace stof
 
 extern "C" {
