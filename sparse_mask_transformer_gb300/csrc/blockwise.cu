@@ -11,30 +11,33 @@
 // One CTA computes one 128-row query tile (b, h, OT row I) over the n OTs
 // listed for its row (full OTs first):
 //   warp 0      TMA producer: the Q tile once, then the K tile of every
-//               listed OT into a two-stage ring (stage t % 2 is refilled
-//               once S = Q K_{t-2}^T is done);
-//   warp 1      TMA producer: the V tiles into a two-stage ring (refilled
-//               once O += P_{t-2} V_{t-2} is done);
-//   warp 2      allocates TMEM and issues the score MMAs S_g = Q K_t^T;
-//   warp 3      issues the PV MMAs O_g += P_t V_t.
+//               listed OT into a three-stage ring (stage t % 3 is refilled
+//               once S = Q K_{t-3}^T is done);
+//   warp 1      TMA producer: the V tiles into a three-stage ring (refilled
+//               once O += P_{t-3} V_{t-3} is done);
+//   warp 2      allocates TMEM and issues the score MMAs S = Q K_t^T;
+//   warp 3      issues the PV MMAs O_g += P_t V_t, P read from TMEM.
 //               (Every role has a warp of its own: divergent lanes of one
 //               warp are not scheduled promptly while another lane waits.)
 //   warps 4..7  softmax warpgroup 0, tiles t = 0, 2, 4, ...;
 //   warps 8..11 softmax warpgroup 1, tiles t = 1, 3, 5, ...
-// Warpgroup g owns a score buffer S_g and an accumulator O_g in TMEM, a P
-// buffer in shared memory, and its own running max and sum.  A thread owns
-// one query row (= TMEM lane): it loads its 128 scores into registers and at
-// once hands S_g back, so the score MMA of the warpgroup's next tile runs
-// while this one is processed.  It masks partial OTs by their IT bitmaps
-// (read from global memory one tile ahead), updates its running max lazily
-// (O_g is rescaled in TMEM only when the max grows by more than 2^8; exact,
-// because O_g and l_g share the reference), evaluates exp2 in fp32 and
-// stores P as fp16/bf16 into its P buffer in the swizzled K-major layout of
-// the MMA operand.  The two warpgroups never wait for each other inside the
-// tile loop.  At the end their partial results are merged:
+// The score MMA writes one TMEM buffer S.  Warpgroup g owns a P buffer P_g
+// and an accumulator O_g in TMEM and its own running max and sum.  A thread
+// owns one query row (= TMEM lane): it loads its scores into registers and
+// at once hands S back, so the score MMA of the next tile (the other
+// warpgroup's) runs while this one is processed.  It masks partial OTs by
+// their IT bitmaps (read from global memory one tile ahead), updates its
+// running max lazily (O_g is rescaled in TMEM only when the max grows by
+// more than 2^8; exact, because O_g and l_g share the reference), evaluates
+// exp2 in fp32 and writes P as fp16/bf16 pairs into P_g, where the PV MMA
+// reads it as its A operand.  Keeping P out of shared memory leaves the
+// shared-memory bandwidth to the MMA operands and the K/V copies.  The two
+// warpgroups never wait for each other inside the tile loop.  At the end
+// their partial results are merged:
 // O = (a0 O_0 + a1 O_1) / (a0 l_0 + a1 l_1), a_g = 2^(m_g - max(m_0, m_1));
 // 0 for a row without valid keys.
-// TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,256+d) O_1 [256+d,256+2d).
+// TMEM columns: S [0,BN) P_0 [128,128+BN/2) P_1 [192,192+BN/2)
+// O_0 [256,256+d) O_1 [256+d,256+2d).
 // Every pipeline wait is bounded; on timeout the CTA raises
 // STOF_DEVERR_PIPE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -58,6 +61,7 @@ constexpr int kBM = 128;  // query rows per tile (the MMA's M); key columns per 
 // 2 producer warps, 2 MMA-issuer warps, 8 softmax warps.  Three warps per
 // SM sub-partition cap a thread at 168 registers.
 constexpr int kThreads = 384;
+constexpr int kStages = 3;                    // K and V ring depth
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 
@@ -69,7 +73,6 @@ struct Cfg {
   static constexpr int Q_BYTES = kBM * D * 2;       // the Q tile
   static constexpr int KV_BYTES = BN * D * 2;       // one K or V tile
   static constexpr int KV_ATOM = BN * 128;          // one swizzle atom of a K or V tile
-  static constexpr int P_BYTES = kBM * BN * 2;      // one P tile (BN / 64 atoms of 16 KB)
   static constexpr int CHUNKS = BN / 32;            // 32-score chunks of a softmax row
   static constexpr int BITMAP_WORDS = (kBM / 8) * (BN / 8);
 };
@@ -77,16 +80,17 @@ struct Cfg {
 template <int D, int BN>
 struct alignas(1024) Smem {
   uint8_t q[Cfg<D, BN>::Q_BYTES];
-  uint8_t p[2][Cfg<D, BN>::P_BYTES];   // P of each warpgroup's current tile; then its final max and sum
-  uint8_t k[2][Cfg<D, BN>::KV_BYTES];  // K ring: stage t % 2 = the warpgroup of tile t
-  uint8_t v[2][Cfg<D, BN>::KV_BYTES];  // V ring, likewise
+  uint8_t k[kStages][Cfg<D, BN>::KV_BYTES];  // K ring, stage t % 3; at the end the warpgroups' max and sum
+  uint8_t v[kStages][Cfg<D, BN>::KV_BYTES];  // V ring, stage t % 3
   uint64_t q_full;
-  uint64_t k_full[2];
-  uint64_t v_full[2];
-  uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[2];
+  uint64_t k_full[kStages];
+  uint64_t k_free[kStages];
+  uint64_t v_full[kStages];
+  uint64_t v_free[kStages];
+  uint64_t s_full[2];   // per warpgroup: the scores of its next tile are in S
+  uint64_t s_free[2];   // per warpgroup: it has loaded its tile's scores
+  uint64_t p_full[2];   // per warpgroup: P_g written
+  uint64_t pv_done[2];  // per warpgroup: its last PV is done (P_g free, O_g current)
   uint64_t drain;
   uint64_t drain_qk;
   uint32_t tmem_base;
@@ -179,9 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.k_free[i], 1);
       mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.v_free[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
@@ -203,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
-  const uint32_t tS0 = tbase, tO0 = tbase + 256;  // S_g at tS0 + 128 g, O_g at tO0 + D g
+  // S at tbase, P_g at tbase + 128 + 64 g, O_g at tbase + 256 + D g
+  const uint32_t tS = tbase, tP0 = tbase + 128, tO0 = tbase + 256;
   volatile int* abort_flag = &s.abort_flag;
   auto fail = [&]() {
     *abort_flag = 1;
@@ -240,10 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow);
         int issued = 0;
-        for (int t = 0; t < n; ++t) {
-          // stage t % 2 held K_{t-2}: free once that tile's scores are done
-          const int st = t & 1;
-          if (t >= 2 && !mbar_wait(&s.s_full[st], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) {
+        for (int t = 0, st = 0, ph = 0; t < n; ++t) {
+          // stage st = t % 3 held K_{t-3}: free once that tile's scores are done
+          if (t >= kStages && !mbar_wait(&s.k_free[st], ph ^ 1, abort_flag, kWaitNs)) {
             fail();
             break;
           }
@@ -252,11 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.k[st] + r * C::KV_ATOM, &tmK, &s.k_full[st], 64 * r, krow);
           issued = t + 1;
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1;
+          }
         }
         if (*abort_flag) {  // let every copy this thread started land before exit
           mbar_wait_timeout(&s.q_full, 0, kWaitNs);
-          for (int t = issued - 2 < 0 ? 0 : issued - 2; t < issued; ++t)
-            mbar_wait_timeout(&s.k_full[t & 1], (t >> 1) & 1, kWaitNs);
+          for (int t = issued - kStages < 0 ? 0 : issued - kStages; t < issued; ++t)
+            mbar_wait_timeout(&s.k_full[t % kStages], (t / kStages) & 1, kWaitNs);
         }
       }
     } else if (warp == 1) {
@@ -264,10 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {  // V tiles
         prefetch_tmap(&tmV);
         int issued = 0;
-        for (int t = 0; t < n; ++t) {
-          // stage t % 2 held V_{t-2}: free once that tile's PV is done
-          const int st = t & 1;
-          if (t >= 2 && !mbar_wait(&s.pv_done[st], ((t - 2) >> 1) & 1, abort_flag, kWaitNs)) {
+        for (int t = 0, st = 0, ph = 0; t < n; ++t) {
+          // stage st = t % 3 held V_{t-3}: free once that tile's PV is done
+          if (t >= kStages && !mbar_wait(&s.v_free[st], ph ^ 1, abort_flag, kWaitNs)) {
             fail();
             break;
           }
@@ -276,10 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.v[st] + r * C::KV_ATOM, &tmV, &s.v_full[st], 64 * r, vrow);
           issued = t + 1;
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1;
+          }
         }
         if (*abort_flag) {
-          for (int t = issued - 2 < 0 ? 0 : issued - 2; t < issued; ++t)
-            mbar_wait_timeout(&s.v_full[t & 1], (t >> 1) & 1, kWaitNs);
+          for (int t = issued - kStages < 0 ? 0 : issued - kStages; t < issued; ++t)
+            mbar_wait_timeout(&s.v_full[t % kStages], (t / kStages) & 1, kWaitNs);
         }
       }
     } else {  // warps 2 and 3
@@ -301,23 +314,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t qdesc = smem_desc_sw128(smem_u32(s.q), 16, 1024);
         const uint64_t kdesc0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
         bool ok = n == 0 || wwait(&s.q_full, 0);
-        for (int t = 0; ok && t < n; ++t) {
-          const int g = t & 1;  // warpgroup, score buffer and K stage of tile t
-          // S_g is free once the softmax has loaded tile t-2's scores
-          if (t >= 2 && !wwait(&s.s_free[g], ((t - 2) >> 1) & 1)) { ok = false; break; }
-          if (!wwait(&s.k_full[g], (t >> 1) & 1)) { ok = false; break; }
+        for (int t = 0, st = 0, ph = 0; ok && t < n; ++t) {
+          // S is free once the previous tile's scores are loaded (by the
+          // other warpgroup)
+          if (t >= 1 && !wwait(&s.s_free[(t - 1) & 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
+          if (!wwait(&s.k_full[st], ph)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t kd = kdesc0 + static_cast<uint64_t>(g) * kStage;
-          const uint32_t d_tmem = tS0 + g * 128;
+          const uint64_t kd = kdesc0 + static_cast<uint64_t>(st) * kStage;
           if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               // 32 B per K step inside an atom; Q atoms are 16 KB apart, K atoms BN * 128 B
               const uint64_t qoff = (kk >> 2) * (C::Q_BYTES / C::REGIONS / 16) + (kk & 3) * 2;
               const uint64_t koff = (kk >> 2) * (C::KV_ATOM / 16) + (kk & 3) * 2;
-              mma_f16_ss(d_tmem, qdesc + qoff, kd + koff, idesc_qk, kk > 0 ? 1u : 0u);
+              mma_f16_ss(tS, qdesc + qoff, kd + koff, idesc_qk, kk > 0 ? 1u : 0u);
             }
-            mma_commit(&s.s_full[g]);  // also frees K stage g
+            mma_commit(&s.s_full[t & 1]);
+            mma_commit(&s.k_free[st]);
+          }
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1;
           }
         }
         if (elect_one()) {  // the lane that issued the MMAs
@@ -327,24 +344,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const uint64_t vdesc0 = smem_desc_sw128(smem_u32(s.v[0]), C::KV_ATOM, 1024);
-        const uint64_t pdesc0 = smem_desc_sw128(smem_u32(s.p[0]), 16, 1024);
         bool ok = true;
-        for (int t = 0; ok && t < n; ++t) {
-          const int g = t & 1;  // warpgroup, accumulator and V stage of tile t
+        for (int t = 0, st = 0, ph = 0; ok && t < n; ++t) {
+          const int g = t & 1;  // warpgroup, P buffer and accumulator of tile t
           if (!wwait(&s.p_full[g], (t >> 1) & 1)) { ok = false; break; }
-          if (!wwait(&s.v_full[g], (t >> 1) & 1)) { ok = false; break; }
+          if (!wwait(&s.v_full[st], ph)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t vd = vdesc0 + static_cast<uint64_t>(g) * kStage;
-          const uint64_t pd = pdesc0 + static_cast<uint64_t>(g) * (C::P_BYTES / 16);
+          const uint64_t vd = vdesc0 + static_cast<uint64_t>(st) * kStage;
           const uint32_t d_tmem = tO0 + g * D;
+          const uint32_t a_tmem = tP0 + g * 64;
           if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {  // 16 keys per K step
-              const uint64_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
+            for (int kk = 0; kk < BN / 16; ++kk) {  // 16 keys (8 TMEM columns of P) per K step
               // the first tile of O_g overwrites it
-              mma_f16_ss(d_tmem, pd + off, vd + kk * 128, idesc_pv, (t >= 2 || kk > 0) ? 1u : 0u);
+              mma_f16_ts(d_tmem, a_tmem + kk * 8, vd + kk * 128, idesc_pv, (t >= 2 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(&s.pv_done[g]);  // also frees V stage g and P buffer g
+            mma_commit(&s.pv_done[g]);
+            mma_commit(&s.v_free[st]);
+          }
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1;
           }
         }
         if (elect_one()) {  // the lane that issued the MMAs
@@ -361,7 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = (warp - 4) >> 2;      // warpgroup: tiles t with t % 2 == g
     const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tS0 + g * 128 + lane_off;
+    const uint32_t tSr = tS + lane_off;
+    const uint32_t tP = tP0 + g * 64 + lane_off;
     const uint32_t tO = tO0 + g * D + lane_off;
     const float c = p.scale_log2;
     // row r of an OT's bitmaps: byte r % 8 of words (r / 8) * BN / 8 + 0 .. BN / 8 - 1
@@ -374,9 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int w = 0; w < BN / 8; ++w) nb[w] = __ldg(src + w * 8);
       }
     };
-    // P row r: 16-byte chunk q of swizzle atom a sits at a * 16 KB + r * 128 + (q ^ (r % 8)) * 16
-    uint8_t* prow = s.p[g] + r * 128;
-    const int sw = r & 7;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     fetch_bits(g);
@@ -386,11 +404,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t sr[C::CHUNKS][32];
 #pragma unroll
-      for (int cc = 0; cc < C::CHUNKS; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+      for (int cc = 0; cc < C::CHUNKS; ++cc) tmem_ld32(tSr + cc * 32, sr[cc]);
 #pragma unroll
       for (int cc = 0; cc < C::CHUNKS; ++cc) tmem_ld_wait(sr[cc]);
       tc_fence_before();
-      mbar_arrive(&s.s_free[g]);  // the scores are in registers: S_g may be overwritten
+      mbar_arrive(&s.s_free[g]);  // the scores are in registers: S may be overwritten
       const bool partial = t >= nf;
       uint32_t bits[C::CHUNKS];
 #pragma unroll
@@ -420,9 +438,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = mt;
       }
       l *= alpha;
+      // P in registers, two keys per word: keys 32 cc + 2 i, 32 cc + 2 i + 1 in pk[cc][i]
+      const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[C::CHUNKS][16];
+#pragma unroll
+      for (int cc = 0; cc < C::CHUNKS; ++cc)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]), c, c, nmu, nmu);
+          const float e0 = ex2(x0), e1 = ex2(x1);
+          fadd2(ls[((i >> 1) & 1) * 2], ls[((i >> 1) & 1) * 2 + 1], e0, e1);
+          pk[cc][i / 2] = pack2<BF16>(e0, e1);
+        }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (j > 0) {
-        // the PV of this warpgroup's previous tile must be done before its P
-        // buffer is rewritten and before O_g is rescaled
+        // P_g is rewritten and O_g rescaled once the PV of this warpgroup's
+        // previous tile is done
         if (!wwait(&s.pv_done[g], (j - 1) & 1)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -435,31 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
             tmem_st32(tO + cc * 32, orr);
           }
-          tmem_st_wait();
         }
       }
-      const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int cc = 0; cc < C::CHUNKS; ++cc) {
-        uint32_t pk[16];  // keys 32 cc .. 32 cc + 31, two per word
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float x0, x1;
-          ffma2(x0, x1, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]), c, c, nmu, nmu);
-          const float e0 = ex2(x0), e1 = ex2(x1);
-          fadd2(ls[((i >> 1) & 1) * 2], ls[((i >> 1) & 1) * 2 + 1], e0, e1);
-          pk[i / 2] = pack2<BF16>(e0, e1);
-        }
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {  // 8 keys per 16-byte chunk
-          const int q = (cc & 1) * 4 + h;
-          *reinterpret_cast<uint4*>(prow + (cc >> 1) * 16384 + ((q ^ sw) << 4)) =
-              make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
-        }
-      }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      fence_proxy_async_smem();  // P stores visible to the tensor core
+      for (int cc = 0; cc < C::CHUNKS; ++cc) tmem_st16(tP + cc * 16, pk[cc]);
+      tmem_st_wait();  // P (and a rescaled O) in TMEM before the PV MMA reads them
       tc_fence_before();
       mbar_arrive(&s.p_full[g]);
     }
@@ -468,18 +481,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_mine = n > g ? (n - 1 - g) / 2 + 1 : 0;  // tiles of this warpgroup
     const bool good = ok && (n_mine == 0 || wwait(&s.pv_done[g], (n_mine - 1) & 1));
     if (!good) atomicMin(&s.fail_tile, 0);
-    // P_g is no longer read (this warpgroup's last PV is done): it carries
-    // the final max and sum to the other warpgroup
-    float* xg = reinterpret_cast<float*>(s.p[g]);
-    xg[r] = m_ref;
-    xg[kBM + r] = l;
+    // Once both warpgroups' last PVs are done, every MMA and every K copy
+    // has finished: K stage 0 then carries each warpgroup's final max and
+    // sum to the other.
+    named_bar_sync(1, 256);
+    float* xg = reinterpret_cast<float*>(s.k[0]) + g * 2 * kBM;
+    if (s.fail_tile == 0x7FFFFFFF) {
+      xg[r] = m_ref;
+      xg[kBM + r] = l;
+    }
     named_bar_sync(1, 256);
     if (s.fail_tile < 0x7FFFFFFF) {
       if (g == 0 && quarter == 0 && lane == 0) fail();
     } else {
       tc_fence_after();
-      const float* x0 = reinterpret_cast<const float*>(s.p[0]);
-      const float* x1 = reinterpret_cast<const float*>(s.p[1]);
+      const float* x0 = reinterpret_cast<const float*>(s.k[0]);
+      const float* x1 = x0 + 2 * kBM;
       const float m0 = x0[r], m1 = x1[r];
       const float m = fmaxf(m0, m1);
       const float a0 = (n > 0 && m0 != -INFINITY) ? ex2(m0 - m) : 0.f;
