@@ -316,9 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = n == 0 || wwait(&s.q_full, 0);
         for (int t = 0, st = 0, ph = 0; ok && t < n; ++t) {
           // S is free once the previous tile's scores are loaded (by the
-          // other warpgroup)
-          if (t >= 1 && !wwait(&s.s_free[(t - 1) & 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
+          // other warpgroup).  K_t is usually in place first, so that wait
+          // comes first and the issue follows the hand-back of S at once.
           if (!wwait(&s.k_full[st], ph)) { ok = false; break; }
+          if (t >= 1 && !wwait(&s.s_free[(t - 1) & 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           const uint64_t kd = kdesc0 + static_cast<uint64_t>(st) * kStage;
           if (elect_one()) {
@@ -347,8 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int t = 0, st = 0, ph = 0; ok && t < n; ++t) {
           const int g = t & 1;  // warpgroup, P buffer and accumulator of tile t
-          if (!wwait(&s.p_full[g], (t >> 1) & 1)) { ok = false; break; }
+          // V_t is usually in place before P_t
           if (!wwait(&s.v_full[st], ph)) { ok = false; break; }
+          if (!wwait(&s.p_full[g], (t >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           const uint64_t vd = vdesc0 + static_cast<uint64_t>(st) * kStage;
           const uint32_t d_tmem = tO0 + g * D;
