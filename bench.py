@@ -254,6 +254,8 @@ def run_gpu(args, w: synth.Workload):
     e2e = None if args.no_e2e else run_e2e(args, w, mask, q, k, v, ws, fmt, scale, stream, device, dist)
     # the same step from the bit-packed mask (stof_encode_mask_bits)
     bitmask = None if args.no_bitmask else run_bitmask(args, w, mask, q, k, v, ws, scale, stream, device, dist)
+    # the same step from the mask's rule, where the workload has one
+    rules = None if args.no_bitmask else run_rules(args, w, q, k, v, ws, scale, stream, device, dist)
 
     kern_name = "blockwise" if chosen == stof.STOF_KERNEL_BLOCKWISE else "rowwise"
     if chosen == stof.STOF_KERNEL_BLOCKWISE:
@@ -292,6 +294,7 @@ def run_gpu(args, w: synth.Workload):
         "roofline": roofline,
         "e2e": e2e,
         "bitmask": bitmask,
+        "rules": rules,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
@@ -357,6 +360,46 @@ def run_bitmask(args, w, mask, q, k, v, ws, scale, stream, device, dist):
     del bits
     torch.cuda.empty_cache()
     return out
+
+
+def run_rules(args, w, q, k, v, ws, scale, stream, device, dist):
+    """The step with the mask given as a rule (stof_encode_rules: band,
+    global tokens, blocks), for the workloads that have one: no mask is
+    read, only the format is written."""
+    import torch
+    from sparse_mask_transformer_gb300 import stof
+    rule = synth.workload_rule(w)
+    if rule is None:
+        return None
+    bits = lambda a: None if a is None else stof.bitset_words(a, device)  # noqa: E731
+    rules = [stof.MaskRule(rule["band_lo"], rule["band_hi"], bits(rule["global_rows"]), bits(rule["global_cols"]),
+                           bits(rule["blocks"]), rule["block"])] * w.n_masks
+    fmt = stof.stof_format()
+    o = torch.empty_like(q)
+
+    def step():
+        stof.stof_encode_rules(rules, w.L, w.L, 128, 128, ws, fmt)
+        stof.stof_format_sync(fmt)
+        stof.stof_mha_fwd(q, k, v, fmt, scale, w.stride_b, w.stride_h, stof.STOF_KERNEL_AUTO, o)
+
+    def timed(fn, n):
+        fn()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(a.elapsed_time(b) / n, dist, device)
+
+    enc_ms = timed(lambda: stof.stof_encode_rules(rules, w.L, w.L, 128, 128, ws, fmt), args.steps)
+    step_ms = timed(step, args.steps)
+    valid = sum_over_ranks(4.0 * w.d * fmt.nnz * heads_per_mask(w), dist, device)
+    return {"encode_ms": round(enc_ms, 4), "ms_per_step": round(step_ms, 4),
+            "value": round(valid / (step_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s"}
 
 
 def run_e2e(args, w, mask, q, k, v, ws, fmt, scale, stream, device, dist):
@@ -517,7 +560,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle time budget of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-bitmask", action="store_true", help="skip the bit-packed-mask measurement")
+    ap.add_argument("--no-bitmask", action="store_true", help="skip the bit-packed-mask and mask-rule measurements")
     ap.add_argument("--heads", type=int, default=0,
                     help="profiling only: run the workload with this many heads (one mask per head "
                          "for per-head masks)")

@@ -173,6 +173,50 @@ stof_status stof_encode_mask_bits(const uint8_t* mask_bits, int n_masks, int lq,
 stof_status stof_encode_mask_noalloc(const uint8_t* mask, int n_masks, int lq, int lk, int bm, int bn,
                                      void* workspace, size_t ws_bytes, stof_format* fmt, void* stream);
 
+/*
+ * A mask given by a rule instead of stored elements: the union of the
+ * pattern families the pages name -- a diagonal band (causal, sliding
+ * window), global tokens (Longformer) and a block pattern (BigBird)
+ * [PROB]; gist.science technical summary, Experimental results.  Element
+ * (i, j) of a mask is valid iff
+ *     band_lo <= i - j <= band_hi             (empty band if band_lo > band_hi)
+ *  or bit i of global_rows is set              (query row i sees every key)
+ *  or bit j of global_cols is set              (every query row sees key j)
+ *  or bit (i / block) * (lk / block) + j / block of blocks is set.
+ * A bitset is DEVICE memory: uint32 words, bit b at position b % 32 of
+ * word b / 32 (least significant first), 4-byte aligned; NULL is empty.
+ *   global_rows   ceil(lq / 32) words;   global_cols   ceil(lk / 32) words;
+ *   blocks        ceil((lq / block) * (lk / block) / 32) words;
+ *   block         edge of a block: a multiple of 8 dividing lq and lk
+ *                 (read only when blocks is not NULL).
+ * Examples: causal = {0, INT32_MAX}; causal sliding window w = {0, w - 1};
+ * symmetric window |i - j| <= w = {-w, w}.
+ */
+typedef struct {
+  int32_t band_lo, band_hi;
+  const uint32_t* global_rows;
+  const uint32_t* global_cols;
+  const uint32_t* blocks;
+  int32_t block;
+} stof_mask_rule;
+
+#define STOF_MAX_RULES 64
+
+/*
+ * Encodes n_masks parametric masks (rules: HOST array of n_masks rules, at
+ * most STOF_MAX_RULES) into the two-level format [FMT].  The result is the
+ * format that stof_encode_mask() gives for the dense masks the rules define,
+ * but no mask is read: the encoder computes every IT word from the rule, so
+ * long sequences need no L x L mask in memory at all (the pages' long-
+ * sequence results: scifaro.com summary, Results).  The rules are copied at
+ * the call; the bitsets they point to must stay valid until the encoding is
+ * done on the stream.  Sizes, workspace and errors as stof_encode_mask();
+ * STOF_ERR_UNSUPPORTED for more than STOF_MAX_RULES masks, STOF_ERR_SHAPE
+ * for a bad block edge, STOF_ERR_ALIGNMENT for a bitset not 4-byte aligned.
+ */
+stof_status stof_encode_rules(const stof_mask_rule* rules, int n_masks, int lq, int lk, int bm, int bn,
+                              void* workspace, size_t ws_bytes, stof_format* fmt, void* stream);
+
 /* Blocks until the work queued on stream is done, copies the tile counts
  * and the device error word into fmt, and sets fmt->synced.  Returns
  * STOF_ERR_DEVICE if the device error word is non-zero. */

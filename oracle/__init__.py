@@ -22,6 +22,10 @@ GPU", gist.science technical summary):
     its one library step.
   - ``unpack_bits``: a bit-packed mask (least significant bit first along
     the key axis) back to bytes, by explicit shifts.
+  - ``rule_mask``: the dense mask a parametric rule stands for, by its
+    definition: the union of a diagonal band, global rows, global columns
+    and a block pattern (Problem statement and Experimental results: the
+    causal, sliding-window, Longformer and BigBird families).
 
 Pins (tests/test_oracle_pins.py) tie every function to something other than
 itself: library dense attention, closed forms, tiny brute force, round trips
@@ -189,3 +193,21 @@ def unpack_bits(bits, lk: int) -> np.ndarray:
     for c in range(8):
         out[..., c::8] = (bits >> c) & 1
     return out
+
+
+def rule_mask(lq: int, lk: int, band_lo: int, band_hi: int, global_rows=None, global_cols=None,
+              blocks=None, block: int = 0) -> np.ndarray:
+    """uint8 [lq, lk]: element (i, j) is 1 iff band_lo <= i - j <= band_hi,
+    or global_rows[i], or global_cols[j], or blocks[i // block, j // block]
+    (bool arrays; None for an empty set)."""
+    i = np.arange(lq, dtype=np.int64)[:, None]
+    j = np.arange(lk, dtype=np.int64)[None, :]
+    m = (i - j >= band_lo) & (i - j <= band_hi)
+    if global_rows is not None:
+        m = m | np.asarray(global_rows, bool)[:, None]
+    if global_cols is not None:
+        m = m | np.asarray(global_cols, bool)[None, :]
+    if blocks is not None:
+        b = np.asarray(blocks, bool)
+        m = m | b[i // block, j // block]
+    return m.astype(np.uint8)

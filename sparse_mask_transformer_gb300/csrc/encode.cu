@@ -271,6 +271,23 @@ __device__ __forceinline__ unsigned long long pack_bits_phase(const EncodeParams
   return nnz;
 }
 
+// Phases 2-4 of a chunk whose IT words are in shared memory: the chunk's
+// valid-element count, OT classes, global offsets and outputs.
+__device__ __forceinline__ void finish_chunk(const EncodeParams& p, long long chunk, const ChunkGeom& g,
+                                             ChunkState& cs, const uint64_t* s_words,
+                                             unsigned long long local_nnz, int tid) {
+  const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) local_nnz += __shfl_xor_sync(0xffffffffu, local_nnz, off);
+  if (lane == 0 && local_nnz) atomicAdd(&cs.nnz, local_nnz);
+  __syncthreads();
+  classify(s_words, g, cs, warp, lane, kThreads / 32);
+  __syncthreads();
+  if (warp == 0) rank_and_lookback(p, chunk, g, cs, lane);
+  __syncthreads();
+  write_outputs(p, chunk, s_words, g, cs, tid, kThreads);
+}
+
 // ---------------------------------------------------------------- kernel 1
 // VEC: bytes per load (dense: 16 when rows and tiles are 16-byte aligned,
 // else 8; bit-packed: 16, 8 or 1).  BITS: the mask is bit-packed.
@@ -279,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
   extern __shared__ uint64_t s_words[];  // [bm/8][nt * bn/8]
   __shared__ long long s_chunk;
   __shared__ ChunkState cs;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   if (tid == 0) {
     s_chunk = static_cast<long long>(atomicAdd(p.ticket, 1ull));
     cs.nnz = 0;
@@ -341,15 +358,63 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
     }
   }
   }
+  finish_chunk(p, chunk, g, cs, s_words, local_nnz, tid);
+}
+
+// Phase 1 for a parametric mask (one rule per mask): every IT word is
+// computed from the rule, nothing is read but the rule's small bitsets.
+// Element (i, j) is valid iff band_lo <= i - j <= band_hi, or row i is a
+// global row, or column j a global column, or block (i / block, j / block)
+// is set.  An IT (8x8, rows and columns multiples of 8) lies in one block
+// and reads one byte of each bitset.
+__device__ __forceinline__ unsigned long long rule_phase(const EncodeParams& p, const ChunkGeom& g,
+                                                         const RuleDev& ru, uint64_t* words, int tid) {
+  unsigned long long nnz = 0;
+  const long long i_base = static_cast<long long>(g.I) * p.bm;
+  const long long j_base = static_cast<long long>(g.J0) * p.bn;
+  const int nw = g.bands * g.itcols;
+  for (int w = tid; w < nw; w += kThreads) {
+    const int pb = w / g.itcols, qc = w - pb * g.itcols;
+    const long long i0 = i_base + 8 * pb, j0 = j_base + 8 * qc;
+    uint32_t all_rows = 0;  // bits valid in every row of the IT
+    if (ru.global_cols) all_rows |= (__ldg(ru.global_cols + (j0 >> 5)) >> (j0 & 31)) & 0xFFu;
+    if (ru.blocks) {
+      const long long bi = (i0 / ru.block) * ru.nbc + j0 / ru.block;
+      if ((__ldg(ru.blocks + (bi >> 5)) >> (bi & 31)) & 1u) all_rows = 0xFFu;
+    }
+    const uint32_t grow = ru.global_rows ? (__ldg(ru.global_rows + (i0 >> 5)) >> (i0 & 31)) & 0xFFu : 0u;
+    uint64_t word = 0;
 #pragma unroll
-  for (int off = 16; off; off >>= 1) local_nnz += __shfl_xor_sync(0xffffffffu, local_nnz, off);
-  if (lane == 0 && local_nnz) atomicAdd(&cs.nnz, local_nnz);
+    for (int r = 0; r < 8; ++r) {
+      // band: i - band_hi <= j <= i - band_lo, as IT columns c = j - j0
+      const long long clo = max(i0 + r - ru.band_hi - j0, 0ll);
+      const long long chi = min(i0 + r - ru.band_lo - j0, 7ll);
+      uint32_t b = clo <= chi ? ((0xFFu >> (7 - chi)) & (0xFFu << clo)) : 0u;
+      b |= all_rows | ((grow >> r) & 1u ? 0xFFu : 0u);
+      word |= static_cast<uint64_t>(b) << (8 * r);
+    }
+    words[pb * g.itcols + qc] = word;
+    nnz += __popcll(word);
+  }
+  return nnz;
+}
+
+__global__ void __launch_bounds__(kThreads, 7) encode_rules_kernel(const EncodeParams p,
+                                                                   const __grid_constant__ RuleSet rs) {
+  extern __shared__ uint64_t s_words[];  // [bm/8][nt * bn/8]
+  __shared__ long long s_chunk;
+  __shared__ ChunkState cs;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_chunk = static_cast<long long>(atomicAdd(p.ticket, 1ull));
+    cs.nnz = 0;
+  }
   __syncthreads();
-  classify(s_words, g, cs, warp, lane, kThreads / 32);
-  __syncthreads();
-  if (warp == 0) rank_and_lookback(p, chunk, g, cs, lane);
-  __syncthreads();
-  write_outputs(p, chunk, s_words, g, cs, tid, kThreads);
+  const long long chunk = s_chunk;
+  if (chunk >= p.n_chunks) return;
+  const ChunkGeom g = chunk_geom(p, chunk);
+  const unsigned long long local_nnz = rule_phase(p, g, rs.r[g.m], s_words, tid);
+  finish_chunk(p, chunk, g, cs, s_words, local_nnz, tid);
 }
 
 }  // namespace
@@ -443,6 +508,15 @@ cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream
     encode_kernel<16, false><<<grid, kThreads, g.smem_bytes, s>>>(p);
   else
     encode_kernel<8, false><<<grid, kThreads, g.smem_bytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_rules(const EncodeParams& p, const EncodeGeom& g, const RuleSet& rs, cudaStream_t s) {
+  if (g.smem_bytes > 48 * 1024 &&
+      cudaFuncSetAttribute(encode_rules_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(g.smem_bytes)) != cudaSuccess)
+    return cudaGetLastError();
+  encode_rules_kernel<<<static_cast<unsigned>(g.n_chunks), kThreads, g.smem_bytes, s>>>(p, rs);
   return cudaGetLastError();
 }
 

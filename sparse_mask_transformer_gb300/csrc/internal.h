@@ -59,6 +59,21 @@ struct EncodeParams {
 };
 cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s);
 
+// Parametric masks (stof_encode_rules): one rule per mask, passed to the
+// encoder by value in its kernel parameters.
+constexpr int kMaxRules = 64;
+struct RuleDev {
+  long long band_lo, band_hi;      // valid if band_lo <= i - j <= band_hi
+  const uint32_t* global_rows;     // bitset over query rows, or null
+  const uint32_t* global_cols;     // bitset over key columns, or null
+  const uint32_t* blocks;          // bitset over [lq / block][nbc] blocks, or null
+  int block, nbc;                  // block edge (multiple of 8); blocks per block row
+};
+struct RuleSet {
+  RuleDev r[kMaxRules];
+};
+cudaError_t launch_encode_rules(const EncodeParams& p, const EncodeGeom& g, const RuleSet& rs, cudaStream_t s);
+
 // Scratch of stof_encode_mask_noalloc(): a static device array with room
 // for the ticket and kNoAllocMaxChunks look-back words.  The address is
 // looked up once per device (the current one) and cached.

@@ -81,13 +81,15 @@ size_t stof_encode_workspace_bytes(int n_masks, int lq, int lk, int bm, int bn) 
   return workspace_layout(g).total;
 }
 
-static stof_status encode_impl(const uint8_t* mask, int bits, int n_masks, int lq, int lk, int bm, int bn,
-                               void* workspace, size_t ws_bytes, stof_format* fmt, void* stream) {
-  if (!mask || !workspace || !fmt) return STOF_ERR_INVALID_ARG;
+// Encodes from a dense (bits = 0) or bit-packed (bits = 1) mask, or, with
+// mask = NULL, from the rules in *rules.
+static stof_status encode_impl(const uint8_t* mask, int bits, const RuleSet* rules, int n_masks, int lq, int lk,
+                               int bm, int bn, void* workspace, size_t ws_bytes, stof_format* fmt, void* stream) {
+  if ((!mask && !rules) || !workspace || !fmt) return STOF_ERR_INVALID_ARG;
   if (n_masks < 1 || lq < 1 || lk < 1 || bm < 1 || bn < 1) return STOF_ERR_INVALID_ARG;
   EncodeGeom g;
   if (!encode_geometry(n_masks, lq, lk, bm, bn, &g, bits != 0)) return STOF_ERR_SHAPE;
-  if (!aligned(mask, 8) || !aligned(workspace, 256)) return STOF_ERR_ALIGNMENT;
+  if ((mask && !aligned(mask, 8)) || !aligned(workspace, 256)) return STOF_ERR_ALIGNMENT;
   const WorkspaceLayout w = workspace_layout(g);
   if (ws_bytes < w.total) return STOF_ERR_WORKSPACE;
 
@@ -135,18 +137,47 @@ static stof_status encode_impl(const uint8_t* mask, int bits, int n_masks, int l
   p.counts = f.counts_dev;
   p.ticket = reinterpret_cast<unsigned long long*>(ws + w.ticket);
   p.status = reinterpret_cast<unsigned long long*>(ws + w.status);
-  if (record_cuda(launch_encode(p, g, s)) != cudaSuccess) return STOF_ERR_CUDA;
+  const cudaError_t e = rules ? launch_encode_rules(p, g, *rules, s) : launch_encode(p, g, s);
+  if (record_cuda(e) != cudaSuccess) return STOF_ERR_CUDA;
   return STOF_OK;
 }
 
 stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, int bm, int bn,
                              void* workspace, size_t ws_bytes, stof_format* fmt, void* stream) {
-  return encode_impl(mask, 0, n_masks, lq, lk, bm, bn, workspace, ws_bytes, fmt, stream);
+  if (!mask) return STOF_ERR_INVALID_ARG;
+  return encode_impl(mask, 0, nullptr, n_masks, lq, lk, bm, bn, workspace, ws_bytes, fmt, stream);
 }
 
 stof_status stof_encode_mask_bits(const uint8_t* mask_bits, int n_masks, int lq, int lk, int bm, int bn,
                                   void* workspace, size_t ws_bytes, stof_format* fmt, void* stream) {
-  return encode_impl(mask_bits, 1, n_masks, lq, lk, bm, bn, workspace, ws_bytes, fmt, stream);
+  if (!mask_bits) return STOF_ERR_INVALID_ARG;
+  return encode_impl(mask_bits, 1, nullptr, n_masks, lq, lk, bm, bn, workspace, ws_bytes, fmt, stream);
+}
+
+stof_status stof_encode_rules(const stof_mask_rule* rules, int n_masks, int lq, int lk, int bm, int bn,
+                              void* workspace, size_t ws_bytes, stof_format* fmt, void* stream) {
+  static_assert(STOF_MAX_RULES == kMaxRules, "rule capacity");
+  if (!rules || !workspace || !fmt) return STOF_ERR_INVALID_ARG;
+  if (n_masks < 1 || lq < 1 || lk < 1 || bm < 1 || bn < 1) return STOF_ERR_INVALID_ARG;
+  if (n_masks > kMaxRules) return STOF_ERR_UNSUPPORTED;
+  RuleSet rs;
+  std::memset(&rs, 0, sizeof(rs));
+  for (int m = 0; m < n_masks; ++m) {
+    const stof_mask_rule& u = rules[m];
+    if (!aligned(u.global_rows, 4) || !aligned(u.global_cols, 4) || !aligned(u.blocks, 4))
+      return STOF_ERR_ALIGNMENT;
+    if (u.blocks && (u.block < 8 || u.block % 8 != 0 || lq % u.block != 0 || lk % u.block != 0))
+      return STOF_ERR_SHAPE;
+    RuleDev& r = rs.r[m];
+    r.band_lo = u.band_lo;
+    r.band_hi = u.band_hi;
+    r.global_rows = u.global_rows;
+    r.global_cols = u.global_cols;
+    r.blocks = u.blocks;
+    r.block = u.blocks ? u.block : 8;
+    r.nbc = u.blocks ? lk / u.block : 0;
+  }
+  return encode_impl(nullptr, 0, &rs, n_masks, lq, lk, bm, bn, workspace, ws_bytes, fmt, stream);
 }
 
 // Variant of stof_encode_mask() that allocates nothing and needs no device

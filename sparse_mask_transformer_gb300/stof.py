@@ -42,7 +42,11 @@ STOF_DEVERR_BAD_FORMAT = 0x4
 EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync",
             "stof_select_kernel", "stof_mha_fwd", "stof_status_string", "stof_version",
             "stof_last_cuda_error", "stof_tune_workspace_bytes", "stof_tune", "stof_tune_lookup",
-            "stof_tune_clear", "stof_tune_density_bucket", "stof_encode_mask_bits", "stof_oproj_fwd"]
+            "stof_tune_clear", "stof_tune_density_bucket", "stof_encode_mask_bits", "stof_oproj_fwd",
+            "stof_encode_rules"]
+
+STOF_MAX_RULES = 64
+INT32_MIN, INT32_MAX = -(1 << 31), (1 << 31) - 1
 
 STOF_TUNE_CANDIDATES = 3
 
@@ -66,6 +70,14 @@ class stof_format(ctypes.Structure):
         ("bitmaps", ctypes.c_void_p), ("counts_dev", ctypes.c_void_p), ("scratch", ctypes.c_void_p),
         ("n_full", ctypes.c_int64), ("n_part", ctypes.c_int64), ("nnz", ctypes.c_int64),
         ("device_error", ctypes.c_int64),
+    ]
+
+
+class stof_mask_rule(ctypes.Structure):
+    _fields_ = [
+        ("band_lo", ctypes.c_int32), ("band_hi", ctypes.c_int32),
+        ("global_rows", ctypes.c_void_p), ("global_cols", ctypes.c_void_p), ("blocks", ctypes.c_void_p),
+        ("block", ctypes.c_int32),
     ]
 
 
@@ -95,6 +107,9 @@ def load_library(path: str = LIB_PATH):
         lib.stof_encode_mask.restype = i32
         lib.stof_encode_mask_bits.argtypes = [P, i32, i32, i32, i32, i32, P, sz, ctypes.POINTER(stof_format), P]
         lib.stof_encode_mask_bits.restype = i32
+        lib.stof_encode_rules.argtypes = [ctypes.POINTER(stof_mask_rule), i32, i32, i32, i32, i32, P, sz,
+                                          ctypes.POINTER(stof_format), P]
+        lib.stof_encode_rules.restype = i32
         lib.stof_format_sync.argtypes = [ctypes.POINTER(stof_format), P]
         lib.stof_format_sync.restype = i32
         lib.stof_select_kernel.argtypes = [ctypes.c_double, i32, i32]
@@ -186,6 +201,43 @@ def stof_encode_mask_bits(mask_bits: torch.Tensor, lk: int, bm: int, bn: int, wo
         mask_bits.data_ptr(), n_masks, lq, lk, bm, bn, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), ctypes.byref(fmt), _stream(stream)),
         "stof_encode_mask_bits")
+    return fmt
+
+
+def bitset_words(flags, device="cuda") -> torch.Tensor:
+    """Bool/0-1 array of n flags -> device int32 tensor of ceil(n / 32) words,
+    flag b at bit b % 32 of word b / 32 (the layout of stof_mask_rule's bitsets)."""
+    import numpy as np
+    f = np.asarray(flags, dtype=bool).ravel()
+    packed = np.packbits(f, bitorder="little")
+    packed = np.concatenate([packed, np.zeros((-len(packed)) % 4, dtype=np.uint8)])
+    return torch.from_numpy(np.frombuffer(packed.tobytes(), dtype="<i4").copy()).to(device)
+
+
+class MaskRule:
+    """One parametric mask for stof_encode_rules: a band lo <= i - j <= hi,
+    global rows and columns and a block pattern, each a device bitset
+    (bitset_words) or None."""
+
+    def __init__(self, band_lo: int = 1, band_hi: int = 0, global_rows: torch.Tensor | None = None,
+                 global_cols: torch.Tensor | None = None, blocks: torch.Tensor | None = None, block: int = 0):
+        self.band_lo, self.band_hi = int(band_lo), int(band_hi)
+        self.global_rows, self.global_cols, self.blocks, self.block = global_rows, global_cols, blocks, int(block)
+
+    def as_c(self) -> stof_mask_rule:
+        ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        return stof_mask_rule(self.band_lo, self.band_hi, ptr(self.global_rows), ptr(self.global_cols),
+                              ptr(self.blocks), self.block)
+
+
+def stof_encode_rules(rules: list, lq: int, lk: int, bm: int, bn: int, workspace: torch.Tensor,
+                      fmt: stof_format | None = None, stream=None) -> stof_format:
+    """rules: one MaskRule per mask (its bitsets stay alive until the encode is done)."""
+    arr = (stof_mask_rule * max(1, len(rules)))(*[r.as_c() for r in rules])
+    fmt = fmt if fmt is not None else stof_format()
+    _check(load_library().stof_encode_rules(
+        arr, len(rules), lq, lk, bm, bn, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        ctypes.byref(fmt), _stream(stream)), "stof_encode_rules")
     return fmt
 
 

@@ -29,7 +29,7 @@ from dataclasses import dataclass
 import numpy as np
 
 __all__ = [
-    "Workload", "WORKLOADS", "WORKLOAD_ORDER", "mask_index", "mask_rows", "make_mask",
+    "Workload", "WORKLOADS", "WORKLOAD_ORDER", "mask_index", "mask_rows", "make_mask", "workload_rule",
     "make_qkv", "splitmix64", "bernoulli_threshold", "random_mask", "to_float64",
 ]
 
@@ -163,6 +163,28 @@ def mask_rows(w: Workload, m: int, rows) -> np.ndarray:
     if w.pattern == "causal_bernoulli":
         return _bernoulli_rows(m, rows, L, w.seed, BERNOULLI_P)
     raise ValueError(w.pattern)
+
+
+def workload_rule(w: Workload):
+    """The workload's mask as a rule -- band (lo, hi) on i - j, global rows,
+    global columns, block pattern -- or None when it has no such form (the
+    per-element Bernoulli mask).  Bool arrays, block edge in elements:
+    {"band_lo", "band_hi", "global_rows", "global_cols", "blocks", "block"}."""
+    L = w.L
+    rule = {"band_lo": 1, "band_hi": 0, "global_rows": None, "global_cols": None, "blocks": None, "block": 0}
+    if w.pattern == "window48":
+        rule.update(band_lo=0, band_hi=47)
+    elif w.pattern == "causal":
+        rule.update(band_lo=0, band_hi=(1 << 31) - 1)
+    elif w.pattern == "longformer":
+        g = np.zeros(L, dtype=bool)
+        g[_longformer_globals(L, w.seed)] = True
+        rule.update(band_lo=-256, band_hi=256, global_rows=g, global_cols=g)
+    elif w.pattern == "bigbird64":
+        rule.update(blocks=_bigbird_blocks(L, 64, w.seed).astype(bool), block=64)
+    else:
+        return None
+    return rule
 
 
 def make_mask(w: Workload, max_bytes: int = 1 << 30) -> np.ndarray:

@@ -217,3 +217,30 @@ def test_encode_bits_rejects_bad_arguments(lib):
     assert f(ctypes.c_void_p(257), 1, 256, 256, 128, 128, one, 1 << 30, ctypes.byref(fmt),
              None) == stof.STOF_ERR_ALIGNMENT
     assert f(one, 1, 256, 256, 128, 128, one, 16, ctypes.byref(fmt), None) == stof.STOF_ERR_WORKSPACE
+
+
+def test_encode_rules_rejects_bad_arguments(lib):
+    fmt = stof.stof_format()
+    ws = ctypes.c_void_p(256)
+    f = lib.stof_encode_rules
+
+    def call(rules, n=1, lq=256, lk=256, bm=128, bn=128, wsp=ws, ws_bytes=1 << 30, out=ctypes.byref(fmt)):
+        return f(rules, n, lq, lk, bm, bn, wsp, ws_bytes, out, None)
+
+    one = (stof.stof_mask_rule * 1)(stof.stof_mask_rule(0, 47, None, None, None, 0))
+    assert call(None) == stof.STOF_ERR_INVALID_ARG
+    assert call(one, wsp=None) == stof.STOF_ERR_INVALID_ARG
+    assert call(one, out=None) == stof.STOF_ERR_INVALID_ARG
+    assert call(one, n=0) == stof.STOF_ERR_INVALID_ARG
+    many = (stof.stof_mask_rule * 65)()
+    assert call(many, n=65) == stof.STOF_ERR_UNSUPPORTED
+    assert call(one, lq=250) == stof.STOF_ERR_SHAPE
+    bad_block = (stof.stof_mask_rule * 1)(stof.stof_mask_rule(1, 0, None, None, 256, 12))
+    assert call(bad_block) == stof.STOF_ERR_SHAPE                     # block not a multiple of 8
+    bad_block[0].block = 96
+    assert call(bad_block) == stof.STOF_ERR_SHAPE                     # 96 does not divide 256
+    misaligned = (stof.stof_mask_rule * 1)(stof.stof_mask_rule(1, 0, 258, None, None, 0))
+    assert call(misaligned) == stof.STOF_ERR_ALIGNMENT
+    assert call(one, wsp=ctypes.c_void_p(128)) == stof.STOF_ERR_ALIGNMENT
+    assert call(one, ws_bytes=16) == stof.STOF_ERR_WORKSPACE
+    assert ctypes.sizeof(stof.stof_mask_rule) == 40                   # int32 x 2, 3 pointers, int32 + pad

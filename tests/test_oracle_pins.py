@@ -290,3 +290,47 @@ def test_unpack_bits_inverts_numpy_packbits():
     one[0, 9] = 1                                  # key 9 = bit 1 of byte 1
     assert list(np.packbits(one, axis=-1, bitorder="little")[0]) == [0, 2]
     assert np.array_equal(oracle.unpack_bits(np.array([[0, 2]], np.uint8), 16), one)
+
+
+# ---------------------------------------------------------------- parametric masks
+
+def test_rule_mask_bands_match_numpy_triangles():
+    """A band on i - j is a pair of numpy triangles: causal = tril, a causal
+    window of w keys = tril - tril(-w), a symmetric window = triu(tril(w), -w)."""
+    L = 97
+    ones = np.ones((L, L), np.uint8)
+    assert np.array_equal(oracle.rule_mask(L, L, 0, (1 << 31) - 1), np.tril(ones))
+    assert np.array_equal(oracle.rule_mask(L, L, 0, 47), np.tril(ones) - np.tril(ones, -48))
+    assert np.array_equal(oracle.rule_mask(L, L, -5, 5), np.triu(np.tril(ones, 5), -5))
+    assert np.array_equal(oracle.rule_mask(L, L, -(1 << 31), (1 << 31) - 1), ones)
+    assert not oracle.rule_mask(L, L, 1, 0).any()                     # empty band
+    rect = oracle.rule_mask(40, 72, -3, 10)                            # non-square: i - j on the full grid
+    assert np.array_equal(rect, np.triu(np.tril(np.ones((40, 72), np.uint8), 3), -10))
+
+
+def test_rule_mask_sets_match_their_definitions():
+    rng = np.random.default_rng(5)
+    lq, lk, blk = 64, 128, 16
+    gr, gc = rng.random(lq) < 0.2, rng.random(lk) < 0.1
+    blocks = rng.random((lq // blk, lk // blk)) < 0.3
+    empty = dict(band_lo=1, band_hi=0)
+    assert np.array_equal(oracle.rule_mask(lq, lk, global_rows=gr, **empty),
+                          np.repeat(gr[:, None], lk, 1).astype(np.uint8))
+    assert np.array_equal(oracle.rule_mask(lq, lk, global_cols=gc, **empty),
+                          np.repeat(gc[None, :], lq, 0).astype(np.uint8))
+    assert np.array_equal(oracle.rule_mask(lq, lk, blocks=blocks, block=blk, **empty),
+                          np.kron(blocks, np.ones((blk, blk))).astype(np.uint8))
+    both = oracle.rule_mask(lq, lk, 0, 3, global_rows=gr, global_cols=gc, blocks=blocks, block=blk)
+    union = (oracle.rule_mask(lq, lk, 0, 3) | oracle.rule_mask(lq, lk, global_rows=gr, **empty)
+             | oracle.rule_mask(lq, lk, global_cols=gc, **empty)
+             | oracle.rule_mask(lq, lk, blocks=blocks, block=blk, **empty))
+    assert np.array_equal(both, union)
+
+
+@pytest.mark.parametrize("name", ["window48_L256", "bigbird_L512", "causal_L2048", "longformer_L4096"])
+def test_workload_rules_reproduce_the_workload_masks(name):
+    """The rule form of each structured workload equals its element generator
+    (two independent descriptions of the same mask)."""
+    w = synth.WORKLOADS[name]
+    assert np.array_equal(oracle.rule_mask(w.L, w.L, **synth.workload_rule(w)), synth.make_mask(w)[0])
+    assert synth.workload_rule(synth.WORKLOADS["bernoulli_L16384"]) is None
