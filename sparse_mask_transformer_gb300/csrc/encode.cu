@@ -20,6 +20,10 @@
 //      worked on;
 //   4. writes column indices, row pointers and the bitmaps of its partial
 //      OTs straight into their final slots.
+// Step 1 has three sources: a dense byte mask, a bit-packed mask (one byte
+// of a row is one IT row) and a parametric mask, whose IT words are computed
+// from its rule (band on i - j, global rows and columns, block pattern)
+// without reading any mask.  Steps 2-4 are shared.
 // One CTA per chunk, 256 threads, seven CTAs per SM so that the loads of
 // some CTAs overlap the look-back and writes of others; 16-byte (else
 // 8-byte) coalesced streaming loads.  (A persistent variant that streamed
