@@ -55,9 +55,9 @@ HOST_CODE_MARK = b"// [rows][D] row-major 16-bit matrix"
 
 def kernel_source_hash() -> str:
     """Hash of the block-wise kernel's device code: blockwise.cu up to its
-    host-side launch code, and the PTX wrappers it includes."""
+    host-side launch code, and the headers of device code it includes."""
     h = hashlib.sha256()
-    for f in ("blockwise.cu", "sm100_ptx.cuh"):
+    for f in ("blockwise.cu", "blockwise_common.cuh", "sm100_ptx.cuh"):
         with open(os.path.join(ROOT, "sparse_mask_transformer_gb300", "csrc", f), "rb") as fh:
             text = fh.read()
         h.update(text.split(HOST_CODE_MARK)[0] if f == "blockwise.cu" else text)

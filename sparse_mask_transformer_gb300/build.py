@@ -22,7 +22,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]
 
-STOF_SOURCES = ["stof_api.cu", "encode.cu", "rowwise.cu", "blockwise.cu", "tune.cu", "oproj.cu"]
+STOF_SOURCES = ["stof_api.cu", "encode.cu", "rowwise.cu", "blockwise.cu", "blockwise_persist.cu", "tune.cu",
+                "oproj.cu"]
 SYNTH_SOURCES = ["synth_mask.cu"]
 
 

@@ -48,6 +48,7 @@
 
 #include <mutex>
 
+#include "blockwise_common.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
@@ -56,26 +57,7 @@ namespace stof {
 namespace {
 
 using namespace ptx;
-
-constexpr int kBM = 128;  // query rows per tile (the MMA's M); key columns per OT: BN = 64 or 128
-// 2 producer warps, 2 MMA-issuer warps, 8 softmax warps.  Three warps per
-// SM sub-partition cap a thread at 168 registers.
-constexpr int kThreads = 384;
-constexpr int kStages = 3;                    // K and V ring depth
-constexpr float kRescaleThreshold = 8.0f;     // log2 units
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
-
-// Tiles in shared memory are 128-byte-swizzled: a matrix of R rows is stored
-// as d/64 (or keys/64) atoms of R rows x 128 bytes, 8-row groups 1 KB apart.
-template <int D, int BN>
-struct Cfg {
-  static constexpr int REGIONS = D / 64;            // swizzle atoms along d
-  static constexpr int Q_BYTES = kBM * D * 2;       // the Q tile
-  static constexpr int KV_BYTES = BN * D * 2;       // one K or V tile
-  static constexpr int KV_ATOM = BN * 128;          // one swizzle atom of a K or V tile
-  static constexpr int CHUNKS = BN / 32;            // 32-score chunks of a softmax row
-  static constexpr int BITMAP_WORDS = (kBM / 8) * (BN / 8);
-};
+using namespace bw;
 
 template <int D, int BN>
 struct alignas(1024) Smem {
@@ -99,74 +81,10 @@ struct alignas(1024) Smem {
 };
 static_assert(sizeof(Smem<128, 128>) + 1024 <= 232448, "shared memory");
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float y;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
-  return y;
-}
-
-// d0 = a0 * b0 + c0, d1 = a1 * b1 + c1 in one packed fp32x2 FMA
-__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
-                                      float c0, float c1) {
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.ftz.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-
-// d0 += a0, d1 += a1 in one packed fp32x2 add
-__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) {
-  asm("{\n\t.reg .b64 ra, rd;\n\t"
-      "mov.b64 rd, {%0, %1};\n\tmov.b64 ra, {%2, %3};\n\t"
-      "add.rn.ftz.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "+f"(d0), "+f"(d1)
-      : "f"(a0), "f"(a1));
-}
-
-// s = -inf unless (bits & bit) != 0.  Written as a bit test and a select
-// in PTX: the ternary form measured 2.4% more ALU instructions per tile.
-__device__ __forceinline__ void keep_if_set(uint32_t& s, uint32_t bits, uint32_t bit) {
-  asm("{\n\t.reg .pred p;\n\t.reg .b32 t;\n\t"
-      "and.b32 t, %1, %2;\n\tsetp.eq.u32 p, t, 0;\n\tselp.b32 %0, %3, %0, p;\n\t}"
-      : "+r"(s)
-      : "r"(bits), "r"(bit), "r"(0xFF800000u));
-}
-
 // Barrier over `count` threads (a multiple of 32) under hardware barrier id.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  if constexpr (BF16) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-  } else {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-}
-
-__device__ __forceinline__ void raise_error(int64_t* err, unsigned long long bit) {
-  atomicOr(reinterpret_cast<unsigned long long*>(err), bit);
-}
-
-// Register split: the kernel is launched with kLaunchRegs per thread (the
-// most 384 threads can have); warpgroup 0 (producers, MMA issuers) drops to
-// kProducerRegs, the two softmax warpgroups rise to kSoftmaxRegs.  The host
-// refuses to launch a build whose register count is not kLaunchRegs, since
-// the raise would then wait for registers that are never released.
-constexpr int kLaunchRegs = 168, kProducerRegs = 56, kSoftmaxRegs = 224;
-static_assert(kProducerRegs * 128 + kSoftmaxRegs * 256 <= kLaunchRegs * kThreads, "register split");
-static_assert(kLaunchRegs * kThreads <= 65536, "register file");
 
 template <int D, int BN, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -558,19 +476,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+}  // namespace
+
 // [rows][D] row-major 16-bit matrix, box = 64 columns x box_rows rows, 128-byte swizzle
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_rows, bool bf16) {
+bool make_bw_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_rows, bool bf16) {
   return encode_tensor_map_2d(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                               base, static_cast<uint64_t>(D), rows, static_cast<uint64_t>(D) * 2, 64,
                               static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+namespace {
+
 template <int D, int BN, bool BF16>
 stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.L;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, rows, D, kBM, BF16) || !make_map(&mk, p.k, rows, D, BN, BF16) ||
-      !make_map(&mv, p.v, rows, D, BN, BF16))
+  if (!make_bw_map(&mq, p.q, rows, D, kBM, BF16) || !make_bw_map(&mk, p.k, rows, D, BN, BF16) ||
+      !make_bw_map(&mv, p.v, rows, D, BN, BF16))
     return STOF_ERR_CUDA;
   const size_t smem = sizeof(Smem<D, BN>) + 1024;
   stof_status prep = STOF_OK;
@@ -603,6 +525,9 @@ stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
 stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s) {
   if (p.bm != kBM || (p.bn != 64 && p.bn != 128)) return STOF_ERR_UNSUPPORTED;
   if (static_cast<long long>(p.B) * p.H * p.L >= (1ll << 31)) return STOF_ERR_SHAPE;
+  // d = 64: persistent CTAs (a query tile holds few listed tiles, so start-up
+  // and finish are worth overlapping across tiles)
+  if (p.d == 64) return launch_blockwise_persist64(p, bf16, s);
   if (p.bn == 64) {
     if (p.d == 64) return bf16 ? launch_bw<64, 64, true>(p, s) : launch_bw<64, 64, false>(p, s);
     return bf16 ? launch_bw<128, 64, true>(p, s) : launch_bw<128, 64, false>(p, s);

@@ -1,0 +1,97 @@
+// Pieces shared by the block-wise attention kernels (blockwise.cu: one CTA
+// per query tile; blockwise_persist.cu: persistent CTAs for d = 64): tile
+// sizes, thread layout, register split and the softmax's fp32 helpers.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+namespace stof {
+namespace bw {
+
+constexpr int kBM = 128;  // query rows per tile (the MMA's M); key columns per OT: BN = 64 or 128
+// 2 producer warps, 2 MMA-issuer warps, 8 softmax warps.  Three warps per
+// SM sub-partition cap a thread at 168 registers.
+constexpr int kThreads = 384;
+constexpr int kStages = 3;                    // K and V ring depth
+constexpr float kRescaleThreshold = 8.0f;     // log2 units
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
+
+// Tiles in shared memory are 128-byte-swizzled: a matrix of R rows is stored
+// as d/64 (or keys/64) atoms of R rows x 128 bytes, 8-row groups 1 KB apart.
+template <int D, int BN>
+struct Cfg {
+  static constexpr int REGIONS = D / 64;            // swizzle atoms along d
+  static constexpr int Q_BYTES = kBM * D * 2;       // the Q tile
+  static constexpr int KV_BYTES = BN * D * 2;       // one K or V tile
+  static constexpr int KV_ATOM = BN * 128;          // one swizzle atom of a K or V tile
+  static constexpr int CHUNKS = BN / 32;            // 32-score chunks of a softmax row
+  static constexpr int BITMAP_WORDS = (kBM / 8) * (BN / 8);
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// d0 = a0 * b0 + c0, d1 = a1 * b1 + c1 in one packed fp32x2 FMA
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.ftz.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// d0 += a0, d1 += a1 in one packed fp32x2 add
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rd;\n\t"
+      "mov.b64 rd, {%0, %1};\n\tmov.b64 ra, {%2, %3};\n\t"
+      "add.rn.ftz.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+
+// s = -inf unless (bits & bit) != 0.  Written as a bit test and a select
+// in PTX: the ternary form measured 2.4% more ALU instructions per tile.
+__device__ __forceinline__ void keep_if_set(uint32_t& s, uint32_t bits, uint32_t bit) {
+  asm("{\n\t.reg .pred p;\n\t.reg .b32 t;\n\t"
+      "and.b32 t, %1, %2;\n\tsetp.eq.u32 p, t, 0;\n\tselp.b32 %0, %3, %0, p;\n\t}"
+      : "+r"(s)
+      : "r"(bits), "r"(bit), "r"(0xFF800000u));
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+__device__ __forceinline__ void raise_error(int64_t* err, unsigned long long bit) {
+  atomicOr(reinterpret_cast<unsigned long long*>(err), bit);
+}
+
+// Register split: the kernel is launched with kLaunchRegs per thread (the
+// most 384 threads can have); warpgroup 0 (producers, MMA issuers) drops to
+// kProducerRegs, the two softmax warpgroups rise to kSoftmaxRegs.  The host
+// refuses to launch a build whose register count is not kLaunchRegs, since
+// the raise would then wait for registers that are never released.
+constexpr int kLaunchRegs = 168, kProducerRegs = 56, kSoftmaxRegs = 224;
+static_assert(kProducerRegs * 128 + kSoftmaxRegs * 256 <= kLaunchRegs * kThreads, "register split");
+static_assert(kLaunchRegs * kThreads <= 65536, "register file");
+
+}  // namespace bw
+}  // namespace stof

@@ -455,7 +455,7 @@ WorkspaceLayout workspace_layout(const EncodeGeom& g) {
   WorkspaceLayout w{};
   size_t off = 0;
   w.counts = off;                       // 4 x int64
-  w.ticket = off + 32;                  // 1 x u64
+  w.ticket = off + 32;                  // 1 x u64; off + 40: the persistent attention kernel's work counter
   w.status = off + 64;                  // n_chunks x u64
   w.status_bytes = static_cast<size_t>(g.n_chunks) * 8;
   w.zero_bytes = 64 + w.status_bytes;

@@ -96,11 +96,16 @@ struct AttnParams {
   const int32_t* part_col_idx;
   const uint64_t* bitmaps;
   int64_t* err;                    // device error word (counts[3])
+  unsigned int* work;              // work counter of the persistent kernel, in the format's workspace
 };
 cudaError_t launch_rowwise(const AttnParams& p, bool bf16, cudaStream_t s);
 // Density bucket of the tuning cache.
 int tune_density_bucket(double density);
 // Returns STOF_OK or an error status (tensor-map encoding / launch).
 stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s);
+// The persistent block-wise kernel for d = 64 (blockwise_persist.cu).
+stof_status launch_blockwise_persist64(const AttnParams& p, bool bf16, cudaStream_t s);
+// TMA map of a [rows][D] 16-bit matrix, 64-column x box_rows boxes, 128-byte swizzle.
+bool make_bw_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_rows, bool bf16);
 
 }  // namespace stof

@@ -356,6 +356,8 @@ stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype
   p.part_col_idx = fmt->part_col_idx;
   p.bitmaps = fmt->bitmaps;
   p.err = fmt->counts_dev + 3;
+  // bytes 40..43 of the workspace: a word the encoders zero and never use
+  p.work = reinterpret_cast<unsigned int*>(fmt->counts_dev + 5);
   const bool bf16 = dt == STOF_BF16;
   cudaStream_t s = as_stream(stream);
   if (kern == STOF_KERNEL_ROWWISE)

@@ -113,8 +113,9 @@ def test_rowwise_other_tile_sizes(gpu_lib, bm, bn):
 
 
 @pytest.mark.parametrize("kern,bn", [("row", 128), ("block", 128), ("block", 64)])
-def test_edge_cases(gpu_lib, kern, bn):
-    B, H, L, d = 1, 4, 256, 128
+@pytest.mark.parametrize("d", [64, 128])
+def test_edge_cases(gpu_lib, kern, bn, d):
+    B, H, L = 1, 4, 256
     q, k, v = synth.make_qkv(B, H, L, d, "bf16", seed=6)
     q = (q.float() * 8).to(torch.bfloat16)  # sharp softmax
     masks = np.zeros((4, L, L), np.uint8)
@@ -130,6 +131,32 @@ def test_edge_cases(gpu_lib, kern, bn):
     assert torch.equal(o[0, 2, 128:], v[0, 2, 5].expand(128, d))
     assert torch.all(o[0, 3] == 0)
     _check(o, q, k, v, _mask_of_np(masks, 0, 1), "bf16", heads=[(0, 0)], rel=True)
+
+
+@pytest.mark.parametrize("bn", [128, 64])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_blockwise_many_items_of_every_size(gpu_lib, bn, dtype):
+    """d = 64 runs persistent CTAs that take query tiles from a counter:
+    more query tiles than SMs, with 0, 1, 2, ... listed tiles each (odd and
+    even counts, full and partial tiles), per-head masks."""
+    B, H, L, d = 2, 20, 1024, 64
+    n_tr, n_tc = L // 128, L // bn
+    rng = np.random.default_rng(11 + bn)
+    masks = np.zeros((B * H, L, L), np.uint8)
+    for m in range(B * H):
+        for I in range(n_tr):
+            cnt = (m * n_tr + I) % (n_tc + 1)              # every tile count, 0 .. n_tc
+            for J in rng.choice(n_tc, cnt, replace=False):
+                blk = masks[m, I * 128:(I + 1) * 128, J * bn:(J + 1) * bn]
+                blk[:] = 1 if rng.random() < 0.3 else (rng.random(blk.shape) < 0.3)
+    q, k, v = synth.make_qkv(B, H, L, d, dtype, seed=12)
+    o, fmt = _run(q, k, v, torch.from_numpy(masks).cuda(), 128, bn, H, 1, stof.STOF_KERNEL_BLOCKWISE)
+    assert fmt.n_full > 0 and fmt.n_part > 0
+    assert B * H * n_tr > 152
+    empty = masks.reshape(B, H, L, L).sum(axis=-1) == 0
+    assert torch.all(o[torch.from_numpy(empty)] == 0)  # rows of query tiles without tiles
+    _check(o, q, k, v, _mask_of_np(masks, H, 1), dtype,
+           heads=[(0, 0), (0, 7), (0, 19), (1, 0), (1, 11), (1, 19)])
 
 
 @pytest.mark.parametrize("name", ["bigbird_L512", "longformer_L4096"])
