@@ -241,7 +241,11 @@ stof_kernel stof_select_kernel(double density, int seq_len, int head_dim);
  *               (needs bm == 128 and bn == 64 or 128; else
  *               STOF_ERR_UNSUPPORTED) or STOF_KERNEL_AUTO ([SEL], needs a
  *               synced fmt; falls back to row-wise for other tile sizes).
- * Asynchronous on stream.
+ * Asynchronous on stream.  For d = 64 the block-wise kernel runs persistent
+ * CTAs that take query tiles from a work counter kept in the format's
+ * workspace (a word the encoders leave unused) and zeroed by this call on
+ * stream: calls that use the same format must not overlap on the GPU (one
+ * stream, or streams ordered by events); calls with different formats may.
  */
 stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H,
                          int L, int d, float scale, const stof_format* fmt,
