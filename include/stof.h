@@ -321,6 +321,17 @@ stof_status stof_oproj_fwd(const void* o, const void* w, const void* bias, const
                            stof_dtype dt, int B, int H, int L, int d, int N, void* y,
                            int64_t* device_error, void* stream);
 
+/*
+ * Diagnostic of the failure handling (the paper has no counterpart): every
+ * pipeline wait in this library's kernels is bounded in wall time and, when
+ * it runs out, ORs an error bit into a device error word and lets the
+ * kernel finish instead of hanging.  This call launches one CTA that waits,
+ * through that same bounded wait, on a barrier nothing ever arrives on; after
+ * `seconds` (in (0, 10]) it ORs STOF_DEVERR_PIPE_TIMEOUT into *device_error
+ * (device int64, 8-byte aligned) and exits.  Asynchronous on stream.
+ */
+stof_status stof_check_bounded_wait(int64_t* device_error, double seconds, void* stream);
+
 /* Static description of a status code. */
 const char* stof_status_string(stof_status s);
 

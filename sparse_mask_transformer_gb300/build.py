@@ -23,7 +23,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompil
               "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]
 
 STOF_SOURCES = ["stof_api.cu", "encode.cu", "rowwise.cu", "blockwise.cu", "blockwise_persist.cu", "tune.cu",
-                "oproj.cu"]
+                "oproj.cu", "waitcheck.cu"]
 SYNTH_SOURCES = ["synth_mask.cu"]
 
 

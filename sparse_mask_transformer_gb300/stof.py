@@ -43,7 +43,7 @@ EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync
             "stof_select_kernel", "stof_mha_fwd", "stof_status_string", "stof_version",
             "stof_last_cuda_error", "stof_tune_workspace_bytes", "stof_tune", "stof_tune_lookup",
             "stof_tune_clear", "stof_tune_density_bucket", "stof_encode_mask_bits", "stof_oproj_fwd",
-            "stof_encode_rules"]
+            "stof_encode_rules", "stof_check_bounded_wait"]
 
 STOF_MAX_RULES = 64
 INT32_MIN, INT32_MAX = -(1 << 31), (1 << 31) - 1
@@ -110,6 +110,8 @@ def load_library(path: str = LIB_PATH):
         lib.stof_encode_rules.argtypes = [ctypes.POINTER(stof_mask_rule), i32, i32, i32, i32, i32, P, sz,
                                           ctypes.POINTER(stof_format), P]
         lib.stof_encode_rules.restype = i32
+        lib.stof_check_bounded_wait.argtypes = [P, ctypes.c_double, P]
+        lib.stof_check_bounded_wait.restype = i32
         lib.stof_format_sync.argtypes = [ctypes.POINTER(stof_format), P]
         lib.stof_format_sync.restype = i32
         lib.stof_select_kernel.argtypes = [ctypes.c_double, i32, i32]
@@ -239,6 +241,13 @@ def stof_encode_rules(rules: list, lq: int, lk: int, bm: int, bn: int, workspace
         arr, len(rules), lq, lk, bm, bn, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         ctypes.byref(fmt), _stream(stream)), "stof_encode_rules")
     return fmt
+
+
+def stof_check_bounded_wait(device_error: torch.Tensor, seconds: float, stream=None) -> None:
+    """device_error: device int64 tensor of one element; the call ORs
+    STOF_DEVERR_PIPE_TIMEOUT into it after `seconds` of a wait that never ends."""
+    _check(load_library().stof_check_bounded_wait(device_error.data_ptr(), float(seconds), _stream(stream)),
+           "stof_check_bounded_wait")
 
 
 def stof_format_sync(fmt: stof_format, stream=None) -> stof_format:

@@ -244,3 +244,13 @@ def test_encode_rules_rejects_bad_arguments(lib):
     assert call(one, wsp=ctypes.c_void_p(128)) == stof.STOF_ERR_ALIGNMENT
     assert call(one, ws_bytes=16) == stof.STOF_ERR_WORKSPACE
     assert ctypes.sizeof(stof.stof_mask_rule) == 40                   # int32 x 2, 3 pointers, int32 + pad
+
+
+def test_bounded_wait_check_rejects_bad_arguments(lib):
+    f = lib.stof_check_bounded_wait
+    one = ctypes.c_void_p(256)
+    assert f(None, ctypes.c_double(0.1), None) == stof.STOF_ERR_INVALID_ARG
+    assert f(one, ctypes.c_double(0.0), None) == stof.STOF_ERR_INVALID_ARG
+    assert f(one, ctypes.c_double(11.0), None) == stof.STOF_ERR_INVALID_ARG
+    assert f(one, ctypes.c_double(float("nan")), None) == stof.STOF_ERR_INVALID_ARG
+    assert f(ctypes.c_void_p(260), ctypes.c_double(0.1), None) == stof.STOF_ERR_ALIGNMENT
