@@ -97,6 +97,7 @@ struct AttnParams {
   const uint64_t* bitmaps;
   int64_t* err;                    // device error word (counts[3])
   unsigned int* work;              // work counter of the persistent kernel, in the format's workspace
+  float tiles_per_row;             // mean listed OTs per OT row of the masks (synced format), else -1
 };
 cudaError_t launch_rowwise(const AttnParams& p, bool bf16, cudaStream_t s);
 // Density bucket of the tuning cache.

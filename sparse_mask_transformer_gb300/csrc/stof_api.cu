@@ -358,6 +358,9 @@ stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype
   p.err = fmt->counts_dev + 3;
   // bytes 40..43 of the workspace: a word the encoders zero and never use
   p.work = reinterpret_cast<unsigned int*>(fmt->counts_dev + 5);
+  p.tiles_per_row = fmt->synced ? static_cast<float>(static_cast<double>(fmt->n_full + fmt->n_part) /
+                                                     (static_cast<double>(fmt->n_masks) * fmt->n_tr))
+                                : -1.f;
   const bool bf16 = dt == STOF_BF16;
   cudaStream_t s = as_stream(stream);
   if (kern == STOF_KERNEL_ROWWISE)

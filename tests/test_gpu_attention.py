@@ -159,6 +159,21 @@ def test_blockwise_many_items_of_every_size(gpu_lib, bn, dtype):
            heads=[(0, 0), (0, 7), (0, 19), (1, 0), (1, 11), (1, 19)])
 
 
+def test_blockwise_d64_long_query_tiles_sampled(gpu_lib):
+    """d = 64 with many listed OTs per query tile (about 64 here) runs a CTA
+    per query tile instead of the persistent kernel; sampled rows against
+    the oracle."""
+    B, H, L, d = 1, 2, 16384, 64
+    rng = np.random.default_rng(21)
+    mask = np.tril(rng.integers(0, 2, (L, L), dtype=np.uint8))[None]   # causal, half the keys dropped
+    mask[0, np.arange(L), np.arange(L)] = 1
+    q, k, v = synth.make_qkv(B, H, L, d, "bf16", seed=22)
+    o, fmt = _run(q, k, v, torch.from_numpy(mask).cuda(), 128, 128, 0, 0, stof.STOF_KERNEL_BLOCKWISE)
+    assert (fmt.n_full + fmt.n_part) / (L // 128) >= 48
+    rows = np.unique(np.concatenate([np.arange(64), rng.choice(L, 192, replace=False), np.arange(L - 64, L)]))
+    _check(o, q, k, v, _mask_of_np(mask, 0, 0), "bf16", rows=rows)
+
+
 @pytest.mark.parametrize("name", ["bigbird_L512", "longformer_L4096"])
 def test_blockwise_128x64_tiles_full_size(gpu_lib, name):
     # 128 x 64 OTs: half-width key tiles, 1 KB bitmaps, N = 64 score MMAs
