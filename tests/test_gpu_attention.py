@@ -216,3 +216,26 @@ def test_unsynced_auto_is_refused(gpu_lib):
     with pytest.raises(stof.StofError) as e:
         stof.stof_mha_fwd(q, q, q, fmt, 0.125, 0, 0, stof.STOF_KERNEL_AUTO, q.clone())
     assert e.value.status == stof.STOF_ERR_NOT_SYNCED
+
+
+def test_concurrent_calls_with_different_formats(gpu_lib):
+    """Calls with different formats may overlap on the GPU (each d = 64
+    persistent launch keeps its work counter in its own format's workspace):
+    two heads' worth of work on two streams at once, each against the oracle."""
+    B, H, L, d = 1, 8, 1024, 64
+    masks = [synth.random_mask(1, L, L, p, seed=30 + i) for i, p in enumerate((0.1, 0.6))]
+    encoded = [gpu_encode(torch.from_numpy(m).cuda(), 128, 128) for m in masks]
+    qkv = [tuple(t.cuda() for t in synth.make_qkv(B, H, L, d, "fp16", seed=40 + i)) for i in range(2)]
+    outs = [torch.full_like(qkv[i][0], float("nan")) for i in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                q, k, v = qkv[i]
+                stof.stof_mha_fwd(q, k, v, encoded[i][0], 0.125, 0, 0, stof.STOF_KERNEL_BLOCKWISE, outs[i],
+                                  stream=streams[i])
+    torch.cuda.synchronize()
+    for i in range(2):
+        q, k, v = (t.cpu() for t in qkv[i])
+        _check(outs[i].cpu(), q, k, v, _mask_of_np(masks[i], 0, 0), "fp16", heads=[(0, 0), (0, 7)], scale=0.125)

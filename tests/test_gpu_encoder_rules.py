@@ -141,3 +141,12 @@ def test_rules_differ_per_mask_and_heads_pick_their_mask(gpu_lib):
     for h in range(2):
         ref = oracle.attention(qf[0, h], kf[0, h], vf[0, h], masks[h], 0.125)
         assert np.abs(o[0, h].double().cpu().numpy() - ref).max() <= 2e-3
+
+
+def test_maximum_rule_count(gpu_lib):
+    """STOF_MAX_RULES (64) masks, each with its own rule."""
+    rng = np.random.default_rng(64)
+    L, blk = 256, 32
+    rules = [_random_rule(rng, L, L, blk) for _ in range(stof.STOF_MAX_RULES)]
+    fmt, ws, arrs = _encode_rules(rules, L, L, 64, 64)
+    assert_format_equal(fmt, arrs, oracle.encode(_oracle_masks(rules, L, L), 64, 64))
