@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <cstdint>
 
+#include "sm100_ptx.cuh"
+
 namespace stof {
 namespace bw {
 
@@ -92,6 +94,99 @@ __device__ __forceinline__ void raise_error(int64_t* err, unsigned long long bit
 constexpr int kLaunchRegs = 168, kProducerRegs = 56, kSoftmaxRegs = 224;
 static_assert(kProducerRegs * 128 + kSoftmaxRegs * 256 <= kLaunchRegs * kThreads, "register split");
 static_assert(kLaunchRegs * kThreads <= 65536, "register file");
+
+// ---------------------------------------------------------------- per-tile softmax
+// A softmax thread owns one query row of a tile (= one TMEM lane) and its
+// BN = 32 * CHUNKS scores.
+
+// The row's scores from TMEM into registers.
+template <int CHUNKS>
+__device__ __forceinline__ void load_scores(uint32_t tSr, uint32_t (&sr)[CHUNKS][32]) {
+#pragma unroll
+  for (int cc = 0; cc < CHUNKS; ++cc) ptx::tmem_ld32(tSr + cc * 32, sr[cc]);
+#pragma unroll
+  for (int cc = 0; cc < CHUNKS; ++cc) ptx::tmem_ld_wait(sr[cc]);
+}
+
+// The row's byte of each 8x8 inner tile of an OT (4 * CHUNKS bytes, one per
+// 8 key columns) as CHUNKS words of 32 key bits.
+template <int CHUNKS>
+__device__ __forceinline__ void assemble_bits(const uint32_t (&nb)[CHUNKS * 4], uint32_t (&bits)[CHUNKS]) {
+#pragma unroll
+  for (int cc = 0; cc < CHUNKS; ++cc)
+    bits[cc] = nb[4 * cc] | (nb[4 * cc + 1] << 8) | (nb[4 * cc + 2] << 16) | (nb[4 * cc + 3] << 24);
+}
+
+// -inf at every key whose bit is clear.
+template <int CHUNKS>
+__device__ __forceinline__ void mask_scores(uint32_t (&sr)[CHUNKS][32], const uint32_t (&bits)[CHUNKS]) {
+#pragma unroll
+  for (int cc = 0; cc < CHUNKS; ++cc)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) keep_if_set(sr[cc][i], bits[cc], 1u << i);
+}
+
+// Max of the row's scores (one max3 chain per 32 scores).
+template <int CHUNKS>
+__device__ __forceinline__ float row_max(const uint32_t (&sr)[CHUNKS][32]) {
+  float m4[CHUNKS];
+#pragma unroll
+  for (int cc = 0; cc < CHUNKS; ++cc) {
+    m4[cc] = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+      m4[cc] = max3(m4[cc], __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]));
+      m4[cc] = max3(m4[cc], __uint_as_float(sr[cc][i + 2]), __uint_as_float(sr[cc][i + 3]));
+      m4[cc] = max3(m4[cc], __uint_as_float(sr[cc][i + 4]), __uint_as_float(sr[cc][i + 5]));
+      m4[cc] = max3(m4[cc], __uint_as_float(sr[cc][i + 6]), __uint_as_float(sr[cc][i + 7]));
+    }
+  }
+  float m = m4[0];
+#pragma unroll
+  for (int cc = 1; cc < CHUNKS; ++cc) m = fmaxf(m, m4[cc]);
+  return m;
+}
+
+// P = 2^(c s + nmu) as fp16/bf16 pairs (keys 32 cc + 2 i and + 1 in
+// pk[cc][i]); returns the sum of the fp32 exponentials.
+template <int CHUNKS, bool BF16>
+__device__ __forceinline__ float exp_pack(const uint32_t (&sr)[CHUNKS][32], float c, float nmu,
+                                          uint32_t (&pk)[CHUNKS][16]) {
+  float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int cc = 0; cc < CHUNKS; ++cc)
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float x0, x1;
+      ffma2(x0, x1, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]), c, c, nmu, nmu);
+      const float e0 = ex2(x0), e1 = ex2(x1);
+      fadd2(ls[((i >> 1) & 1) * 2], ls[((i >> 1) & 1) * 2 + 1], e0, e1);
+      pk[cc][i / 2] = pack2<BF16>(e0, e1);
+    }
+  return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+}
+
+// O row (D fp32 columns at tOr) *= alpha, in TMEM.
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t tOr, float alpha) {
+#pragma unroll
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t orr[32];
+    ptx::tmem_ld32(tOr + cc * 32, orr);
+    ptx::tmem_ld_wait(orr);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+    ptx::tmem_st32(tOr + cc * 32, orr);
+  }
+}
+
+// The row's P into TMEM (16 columns of pairs per 32 keys); complete on return.
+template <int CHUNKS>
+__device__ __forceinline__ void store_p(uint32_t tP, const uint32_t (&pk)[CHUNKS][16]) {
+#pragma unroll
+  for (int cc = 0; cc < CHUNKS; ++cc) ptx::tmem_st16(tP + cc * 16, pk[cc]);
+  ptx::tmem_st_wait();
+}
 
 }  // namespace bw
 }  // namespace stof

@@ -400,73 +400,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wwait(&s.s_full[g], J & 1)) { ok = false; break; }
         tc_fence_after();
         uint32_t sr[C::CHUNKS][32];
-#pragma unroll
-        for (int cc = 0; cc < C::CHUNKS; ++cc) tmem_ld32(tSr + cc * 32, sr[cc]);
-#pragma unroll
-        for (int cc = 0; cc < C::CHUNKS; ++cc) tmem_ld_wait(sr[cc]);
+        load_scores(tSr, sr);
         tc_fence_before();
         mbar_arrive(&s.s_free[g]);  // the scores are in registers: S may be overwritten
         const bool partial = t >= nf;
-        uint32_t bits[C::CHUNKS];
-#pragma unroll
-        for (int cc = 0; cc < C::CHUNKS; ++cc)
-          bits[cc] = partial ? nb[4 * cc] | (nb[4 * cc + 1] << 8) | (nb[4 * cc + 2] << 16) | (nb[4 * cc + 3] << 24) : 0u;
-        fetch_bits(t + 2);
-        if (partial) {  // keep only the keys whose bit is set
-#pragma unroll
-          for (int cc = 0; cc < C::CHUNKS; ++cc)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) keep_if_set(sr[cc][i], bits[cc], 1u << i);
-        }
-        float m4[C::CHUNKS];
-#pragma unroll
-        for (int cc = 0; cc < C::CHUNKS; ++cc) {
-          m4[cc] = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) m4[cc] = max3(m4[cc], __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]));
-        }
-        float mt = m4[0];
-#pragma unroll
-        for (int cc = 1; cc < C::CHUNKS; ++cc) mt = fmaxf(mt, m4[cc]);
-        mt *= c;
+        uint32_t bits[C::CHUNKS] = {};
+        if (partial) assemble_bits<C::CHUNKS>(nb, bits);
+        fetch_bits(t + 2);                        // the bytes of this warpgroup's next tile
+        if (partial) mask_scores(sr, bits);       // keep only the keys whose bit is set
+        const float mt = row_max(sr) * c;
         float alpha = 1.f;
         if (mt > m_ref + kRescaleThreshold) {  // also the first finite max
           alpha = ex2(m_ref - mt);             // 0 when m_ref = -inf
           m_ref = mt;
         }
-        l *= alpha;
         const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        l *= alpha;
         uint32_t pk[C::CHUNKS][16];
-#pragma unroll
-        for (int cc = 0; cc < C::CHUNKS; ++cc)
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float x0, x1;
-            ffma2(x0, x1, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]), c, c, nmu, nmu);
-            const float e0 = ex2(x0), e1 = ex2(x1);
-            fadd2(ls[((i >> 1) & 1) * 2], ls[((i >> 1) & 1) * 2 + 1], e0, e1);
-            pk[cc][i / 2] = pack2<BF16>(e0, e1);
-          }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        l += exp_pack<C::CHUNKS, BF16>(sr, c, nmu, pk);
         // P_g is rewritten once the PV of this warpgroup's previous tile (of
         // any item) is done; that also makes O_g current
         if (J > 0 && !wwait(&s.pv_done[g], (J - 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int cc = 0; cc < kD / 32; ++cc) {
-            uint32_t orr[32];
-            tmem_ld32(tOg + cc * 32, orr);
-            tmem_ld_wait(orr);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tmem_st32(tOg + cc * 32, orr);
-          }
-        }
-#pragma unroll
-        for (int cc = 0; cc < C::CHUNKS; ++cc) tmem_st16(tP + cc * 16, pk[cc]);
-        tmem_st_wait();  // P (and a rescaled O) in TMEM before the PV MMA reads them
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) rescale_o<kD>(tOg, alpha);
+        store_p(tP, pk);  // P (and a rescaled O) in TMEM before the PV MMA reads them
         tc_fence_before();
         mbar_arrive(&s.p_full[g]);
         ++J;
