@@ -135,8 +135,9 @@ stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, i
  * uint8 [n_masks][lq][lk / 8], bit c (least significant first) of byte jb
  * of row i being element (i, 8 jb + c) -- numpy's packbits along the key
  * axis with bitorder="little".  One byte of a row is then one IT row, so
- * the encoder reads an eighth of the bytes of the dense mask; the format
- * it produces is identical.  The pages note that STOF keeps working at
+ * the encoder reads an eighth of the bytes of the dense mask (in three
+ * short kernels: classify, scan, fill); the format it produces is
+ * identical.  The pages note that STOF keeps working at
  * sequence lengths where other systems run out of memory (scifaro.com
  * summary, Results, scalability up to 16k); a 16384-long dense mask per
  * head is 256 MB, its bit-packed form 32 MB.  Same sizes, workspace,

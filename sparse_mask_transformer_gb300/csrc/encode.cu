@@ -20,10 +20,11 @@
 //      worked on;
 //   4. writes column indices, row pointers and the bitmaps of its partial
 //      OTs straight into their final slots.
-// Step 1 has three sources: a dense byte mask, a bit-packed mask (one byte
-// of a row is one IT row) and a parametric mask, whose IT words are computed
-// from its rule (band on i - j, global rows and columns, block pattern)
-// without reading any mask.  Steps 2-4 are shared.
+// Step 1 has two sources in this single-pass kernel: a dense byte mask and
+// a parametric mask, whose IT words are computed from its rule (band on
+// i - j, global rows and columns, block pattern) without reading any mask;
+// steps 2-4 are shared.  A bit-packed mask (one byte of a row is one IT row)
+// goes through three short kernels instead (further below).
 // One CTA per chunk, 256 threads, seven CTAs per SM so that the loads of
 // some CTAs overlap the look-back and writes of others; 16-byte (else
 // 8-byte) coalesced streaming loads.  (A persistent variant that streamed
@@ -224,51 +225,43 @@ __device__ __forceinline__ void transpose4(uint32_t a, uint32_t b, uint32_t c, u
   out[3] = __byte_perm(ab23, cd23, 0x7632);
 }
 
-// Phase 1 for a bit-packed mask (bit c of byte jb of a row = column 8 jb + c):
-// one byte of a row is one IT row, so an IT word is the bytes of its eight
-// rows in order.  A unit is VEC bytes (VEC IT columns) of each of the 8 rows
-// of a band.
+// For a bit-packed mask (bit c of byte jb of a row = column 8 jb + c), one
+// byte of a row is one IT row, so an IT word is the bytes of its eight rows
+// in order.  A unit is VEC bytes (VEC IT columns) of 8 consecutive rows at
+// src; it becomes VEC words at dst.  Returns their valid-element count.
 template <int VEC>
-__device__ __forceinline__ unsigned long long pack_bits_phase(const EncodeParams& p, const ChunkGeom& g,
-                                                              const uint8_t* base, long long row_bytes,
-                                                              uint64_t* words, int tid) {
+__device__ __forceinline__ unsigned long long pack_bits_unit(const uint8_t* src, long long row_bytes,
+                                                             uint64_t* dst) {
   unsigned long long nnz = 0;
-  const int upr = g.itcols / VEC;  // units per band
-  const int nunits = g.bands * upr;
-  for (int w = tid; w < nunits; w += kThreads) {
-    const int pb = w / upr, qu = w - pb * upr;
-    const uint8_t* src = base + static_cast<long long>(8 * pb) * row_bytes + VEC * qu;
-    uint64_t* dst = words + pb * g.itcols + qu * VEC;
-    if constexpr (VEC == 1) {
-      uint64_t word = 0;
+  if constexpr (VEC == 1) {
+    uint64_t word = 0;
 #pragma unroll
-      for (int r = 0; r < 8; ++r) word |= static_cast<uint64_t>(__ldcs(src + r * row_bytes)) << (8 * r);
-      dst[0] = word;
-      nnz += __popcll(word);
-    } else {
-      constexpr int G = VEC / 4;  // 4-column groups
-      uint32_t x[8][G];
+    for (int r = 0; r < 8; ++r) word |= static_cast<uint64_t>(__ldcs(src + r * row_bytes)) << (8 * r);
+    dst[0] = word;
+    nnz += __popcll(word);
+  } else {
+    constexpr int G = VEC / 4;  // 4-column groups
+    uint32_t x[8][G];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        if constexpr (VEC == 16) {
-          const uint4 t = __ldcs(reinterpret_cast<const uint4*>(src + r * row_bytes));
-          x[r][0] = t.x; x[r][1] = t.y; x[r][2] = t.z; x[r][3] = t.w;
-        } else {
-          const uint2 t = __ldcs(reinterpret_cast<const uint2*>(src + r * row_bytes));
-          x[r][0] = t.x; x[r][1] = t.y;
-        }
+    for (int r = 0; r < 8; ++r) {
+      if constexpr (VEC == 16) {
+        const uint4 t = __ldcs(reinterpret_cast<const uint4*>(src + r * row_bytes));
+        x[r][0] = t.x; x[r][1] = t.y; x[r][2] = t.z; x[r][3] = t.w;
+      } else {
+        const uint2 t = __ldcs(reinterpret_cast<const uint2*>(src + r * row_bytes));
+        x[r][0] = t.x; x[r][1] = t.y;
       }
+    }
 #pragma unroll
-      for (int cg = 0; cg < G; ++cg) {
-        uint32_t lo[4], hi[4];
-        transpose4(x[0][cg], x[1][cg], x[2][cg], x[3][cg], lo);
-        transpose4(x[4][cg], x[5][cg], x[6][cg], x[7][cg], hi);
+    for (int cg = 0; cg < G; ++cg) {
+      uint32_t lo[4], hi[4];
+      transpose4(x[0][cg], x[1][cg], x[2][cg], x[3][cg], lo);
+      transpose4(x[4][cg], x[5][cg], x[6][cg], x[7][cg], hi);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint64_t word = static_cast<uint64_t>(lo[i]) | (static_cast<uint64_t>(hi[i]) << 32);
-          dst[4 * cg + i] = word;
-          nnz += __popcll(word);
-        }
+      for (int i = 0; i < 4; ++i) {
+        const uint64_t word = static_cast<uint64_t>(lo[i]) | (static_cast<uint64_t>(hi[i]) << 32);
+        dst[4 * cg + i] = word;
+        nnz += __popcll(word);
       }
     }
   }
@@ -293,9 +286,8 @@ __device__ __forceinline__ void finish_chunk(const EncodeParams& p, long long ch
 }
 
 // ---------------------------------------------------------------- kernel 1
-// VEC: bytes per load (dense: 16 when rows and tiles are 16-byte aligned,
-// else 8; bit-packed: 16, 8 or 1).  BITS: the mask is bit-packed.
-template <int VEC, bool BITS>
+// VEC: bytes per load (16 when rows and tiles are 16-byte aligned, else 8).
+template <int VEC>
 __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams p) {
   extern __shared__ uint64_t s_words[];  // [bm/8][nt * bn/8]
   __shared__ long long s_chunk;
@@ -309,15 +301,12 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
   const long long chunk = s_chunk;
   if (chunk >= p.n_chunks) return;
   const ChunkGeom g = chunk_geom(p, chunk);
-  const long long row_bytes = BITS ? (p.lk >> 3) : p.lk;
-  const uint8_t* base = p.mask + (static_cast<long long>(g.m) * p.lq + static_cast<long long>(g.I) * p.bm) * row_bytes +
-                        static_cast<long long>(g.J0) * (BITS ? (p.bn >> 3) : p.bn);
+  const uint8_t* base = p.mask + (static_cast<long long>(g.m) * p.lq + static_cast<long long>(g.I) * p.bm) * p.lk +
+                        static_cast<long long>(g.J0) * p.bn;
 
   // 1. read and pack (each unit = VEC/8 adjacent IT words of one 8-row band)
   unsigned long long local_nnz = 0;
-  if constexpr (BITS) {
-    local_nnz = pack_bits_phase<VEC>(p, g, base, row_bytes, s_words, tid);
-  } else {
+  {
   constexpr int WPU = VEC / 8;                 // IT words per unit
   constexpr int kUnroll = VEC == 16 ? 1 : 2;   // units in flight per thread (128 B)
   const int upr = g.itcols / WPU;              // units per band
@@ -421,6 +410,208 @@ __global__ void __launch_bounds__(kThreads, 7) encode_rules_kernel(const EncodeP
   finish_chunk(p, chunk, g, cs, s_words, local_nnz, tid);
 }
 
+// ---------------------------------------------------------------- bit-packed masks
+// A bit-packed mask is an eighth of the dense one, so reading it twice costs
+// less than the single-pass encoder's wait for its predecessors: three short
+// kernels, none waiting on another CTA.
+//   1. classify: the class of every OT (and the valid-element count), per-row
+//      counts of full and partial OTs;
+//   2. scan: row pointers by an exclusive prefix sum of those counts;
+//   3. fill: column lists and, reading the partial OTs' bytes again, their
+//      IT words, straight into their final slots.
+// Passes 1 and 3 give a CTA 32 consecutive OTs of one OT row band (one per
+// lane, so a warp's load covers 32 * bn / 8 contiguous bytes of a row); the 8
+// warps of pass 1 split the band's rows.  VEC = bytes per load.
+
+constexpr int kGroup = 32;  // OTs per CTA in passes 1 and 3
+
+template <int VEC>
+__global__ void __launch_bounds__(kThreads) bits_classify_kernel(const EncodeParams p) {
+  __shared__ uint32_t s_any[kThreads / 32][kGroup], s_all[kThreads / 32][kGroup];
+  __shared__ unsigned long long s_nnz[kThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ngroups = (p.n_tc + kGroup - 1) / kGroup;
+  const long long row = blockIdx.x / ngroups;  // OT row band, mask-major
+  const int J = static_cast<int>(blockIdx.x % ngroups) * kGroup + lane;
+  const int m = static_cast<int>(row / p.n_tr), I = static_cast<int>(row % p.n_tr);
+  const long long row_bytes = p.lk >> 3;
+  const int tb = p.bn >> 3;  // bytes of one OT row
+  uint32_t any = 0, all = ~0u;
+  unsigned long long nnz = 0;
+  if (J < p.n_tc) {
+    const uint8_t* base =
+        p.mask + (static_cast<long long>(m) * p.lq + static_cast<long long>(I) * p.bm) * row_bytes + static_cast<long long>(J) * tb;
+#pragma unroll 4
+    for (int r = warp; r < p.bm; r += kThreads / 32) {
+      const uint8_t* src = base + r * row_bytes;
+      for (int x = 0; x < tb; x += VEC) {
+        if constexpr (VEC == 16) {
+          const uint4 t = __ldcs(reinterpret_cast<const uint4*>(src + x));
+          any |= t.x | t.y | t.z | t.w;
+          all &= t.x & t.y & t.z & t.w;
+          nnz += __popc(t.x) + __popc(t.y) + __popc(t.z) + __popc(t.w);
+        } else if constexpr (VEC == 8) {
+          const uint2 t = __ldcs(reinterpret_cast<const uint2*>(src + x));
+          any |= t.x | t.y;
+          all &= t.x & t.y;
+          nnz += __popc(t.x) + __popc(t.y);
+        } else {
+          const uint32_t t = __ldcs(src + x);
+          any |= t;
+          all &= t | 0xFFFFFF00u;
+          nnz += __popc(t);
+        }
+      }
+    }
+  }
+  s_any[warp][lane] = any;
+  s_all[warp][lane] = all;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) nnz += __shfl_xor_sync(0xffffffffu, nnz, off);
+  if (lane == 0) s_nnz[warp] = nnz;
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) {
+      any |= s_any[w][lane];
+      all &= s_all[w][lane];
+    }
+    const int cls = J >= p.n_tc ? 0 : (any == 0 ? 0 : (all == ~0u ? 1 : 2));
+    if (J < p.n_tc) p.cls[row * p.n_tc + J] = static_cast<uint8_t>(cls);
+    const int nf = __popc(__ballot_sync(0xffffffffu, cls == 1));
+    const int np = __popc(__ballot_sync(0xffffffffu, cls == 2));
+    if (lane == 0) {
+      if (nf) atomicAdd(&p.rowcnt[row], nf);
+      if (np) atomicAdd(&p.rowcnt[p.n_rows + row], np);
+      unsigned long long t = 0;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) t += s_nnz[w];
+      if (t) atomicAdd(reinterpret_cast<unsigned long long*>(&p.counts[2]), t);
+    }
+  }
+}
+
+// Pass 2, one CTA: row pointers and totals from the per-row counts.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads) bits_scan_kernel(const EncodeParams p) {
+  __shared__ int s_f[kScanThreads / 32], s_p[kScanThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int carry_f = 0, carry_p = 0;
+  for (long long base = 0; base < p.n_rows; base += kScanThreads) {
+    const long long r = base + tid;
+    const int f = r < p.n_rows ? p.rowcnt[r] : 0;
+    const int q = r < p.n_rows ? p.rowcnt[p.n_rows + r] : 0;
+    int xf = f, xq = q;  // inclusive scans inside the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int yf = __shfl_up_sync(0xffffffffu, xf, off), yq = __shfl_up_sync(0xffffffffu, xq, off);
+      if (lane >= off) {
+        xf += yf;
+        xq += yq;
+      }
+    }
+    if (lane == 31) {
+      s_f[warp] = xf;
+      s_p[warp] = xq;
+    }
+    __syncthreads();
+    if (warp == 0) {  // scan of the warp totals
+      int wf = s_f[lane], wq = s_p[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int yf = __shfl_up_sync(0xffffffffu, wf, off), yq = __shfl_up_sync(0xffffffffu, wq, off);
+        if (lane >= off) {
+          wf += yf;
+          wq += yq;
+        }
+      }
+      s_f[lane] = wf;
+      s_p[lane] = wq;
+    }
+    __syncthreads();
+    const int before_f = carry_f + (warp ? s_f[warp - 1] : 0) + xf - f;
+    const int before_p = carry_p + (warp ? s_p[warp - 1] : 0) + xq - q;
+    if (r < p.n_rows) {
+      p.full_row_ptr[r] = before_f;
+      p.part_row_ptr[r] = before_p;
+    }
+    carry_f += s_f[kScanThreads / 32 - 1];
+    carry_p += s_p[kScanThreads / 32 - 1];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    p.full_row_ptr[p.n_rows] = carry_f;
+    p.part_row_ptr[p.n_rows] = carry_p;
+    p.counts[0] = carry_f;
+    p.counts[1] = carry_p;
+  }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kThreads) bits_fill_kernel(const EncodeParams p) {
+  __shared__ int s_before[2][kThreads / 32];
+  __shared__ long long s_slot[kGroup];
+  __shared__ int s_plist[kGroup];
+  __shared__ int s_np;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ngroups = (p.n_tc + kGroup - 1) / kGroup;
+  const long long row = blockIdx.x / ngroups;
+  const int J0 = static_cast<int>(blockIdx.x % ngroups) * kGroup;
+  const uint8_t* crow = p.cls + row * p.n_tc;
+  // full and partial OTs of this row before the group
+  int bf = 0, bp = 0;
+  for (int j = tid; j < J0; j += kThreads) {
+    const int c = crow[j];
+    bf += c == 1;
+    bp += c == 2;
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    bf += __shfl_xor_sync(0xffffffffu, bf, off);
+    bp += __shfl_xor_sync(0xffffffffu, bp, off);
+  }
+  if (lane == 0) {
+    s_before[0][warp] = bf;
+    s_before[1][warp] = bp;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int f0 = 0, p0 = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      f0 += s_before[0][w];
+      p0 += s_before[1][w];
+    }
+    const int J = J0 + lane;
+    const int c = J < p.n_tc ? crow[J] : 0;
+    const unsigned mf = __ballot_sync(0xffffffffu, c == 1), mp = __ballot_sync(0xffffffffu, c == 2);
+    const unsigned lt = (1u << lane) - 1u;
+    if (c == 1) p.full_col_idx[p.full_row_ptr[row] + f0 + __popc(mf & lt)] = J;
+    if (c == 2) {
+      const int rk = __popc(mp & lt);
+      const long long e = static_cast<long long>(p.part_row_ptr[row]) + p0 + rk;
+      p.part_col_idx[e] = J;
+      s_slot[rk] = e;
+      s_plist[rk] = J;
+    }
+    if (lane == 0) s_np = __popc(mp);
+  }
+  __syncthreads();
+  // IT words of the partial OTs, read again from the mask
+  const int np = s_np;
+  const long long row_bytes = p.lk >> 3;
+  const int tb = p.bn >> 3, bands = p.bm >> 3, upr = tb / VEC, wpt = bands * tb;
+  const int m = static_cast<int>(row / p.n_tr), I = static_cast<int>(row % p.n_tr);
+  const uint8_t* band0 = p.mask + (static_cast<long long>(m) * p.lq + static_cast<long long>(I) * p.bm) * row_bytes;
+  const int units = np * bands * upr;
+  for (int u = tid; u < units; u += kThreads) {
+    const int k = u / (bands * upr), rest = u - k * (bands * upr);
+    const int pb = rest / upr, qu = rest - pb * upr;
+    const uint8_t* src = band0 + static_cast<long long>(8 * pb) * row_bytes + static_cast<long long>(s_plist[k]) * tb + VEC * qu;
+    pack_bits_unit<VEC>(src, row_bytes, p.bitmaps + s_slot[k] * wpt + pb * tb + qu * VEC);
+  }
+}
+
 }  // namespace
 
 // Mask columns per chunk.  A bit-packed mask carries an eighth of the bytes
@@ -458,8 +649,11 @@ WorkspaceLayout workspace_layout(const EncodeGeom& g) {
   w.ticket = off + 32;                  // 1 x u64; off + 40: the persistent attention kernel's work counter
   w.status = off + 64;                  // n_chunks x u64
   w.status_bytes = static_cast<size_t>(g.n_chunks) * 8;
-  w.zero_bytes = 64 + w.status_bytes;
-  off = up(w.status + w.status_bytes);
+  w.rowcnt = w.status + w.status_bytes;  // 2 x n_rows x i32 (bit-packed encoder)
+  w.zero_bytes = 64 + w.status_bytes + static_cast<size_t>(g.n_rows) * 8;
+  off = up(w.counts + w.zero_bytes);
+  w.cls = off;                          // n_tiles x u8 (bit-packed encoder)
+  off = up(off + static_cast<size_t>(g.n_tiles));
   w.full_row_ptr = off;
   off = up(off + (static_cast<size_t>(g.n_rows) + 1) * 4);
   w.part_row_ptr = off;
@@ -479,39 +673,26 @@ cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream
   const unsigned grid = static_cast<unsigned>(g.n_chunks);
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.mask);
   if (p.bits) {
-    // a unit of VEC bytes per row must tile every chunk and start aligned
+    // a load of VEC bytes must stay inside one OT row and start aligned
     const int rb = p.lk / 8, tb = p.bn / 8;
-    if (rb % 16 == 0 && tb % 16 == 0 && a % 16 == 0)
-      {
-        if (g.smem_bytes > 48 * 1024 &&
-            cudaFuncSetAttribute(encode_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(g.smem_bytes)) != cudaSuccess)
-          return cudaGetLastError();
-        encode_kernel<16, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
-      }
-    else if (rb % 8 == 0 && tb % 8 == 0 && a % 8 == 0)
-      {
-        if (g.smem_bytes > 48 * 1024 &&
-            cudaFuncSetAttribute(encode_kernel<8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(g.smem_bytes)) != cudaSuccess)
-          return cudaGetLastError();
-        encode_kernel<8, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
-      }
-    else
-      {
-        if (g.smem_bytes > 48 * 1024 &&
-            cudaFuncSetAttribute(encode_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(g.smem_bytes)) != cudaSuccess)
-          return cudaGetLastError();
-        encode_kernel<1, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
-      }
+    const int vec = (rb % 16 == 0 && tb % 16 == 0 && a % 16 == 0) ? 16 : (rb % 8 == 0 && tb % 8 == 0 && a % 8 == 0) ? 8 : 1;
+    const long long groups = g.n_rows * ((g.n_tc + kGroup - 1) / kGroup);
+    if (groups >= (1ll << 31)) return cudaErrorInvalidValue;
+    const unsigned grid2 = static_cast<unsigned>(groups);
+    if (vec == 16) bits_classify_kernel<16><<<grid2, kThreads, 0, s>>>(p);
+    else if (vec == 8) bits_classify_kernel<8><<<grid2, kThreads, 0, s>>>(p);
+    else bits_classify_kernel<1><<<grid2, kThreads, 0, s>>>(p);
+    bits_scan_kernel<<<1, kScanThreads, 0, s>>>(p);
+    if (vec == 16) bits_fill_kernel<16><<<grid2, kThreads, 0, s>>>(p);
+    else if (vec == 8) bits_fill_kernel<8><<<grid2, kThreads, 0, s>>>(p);
+    else bits_fill_kernel<1><<<grid2, kThreads, 0, s>>>(p);
     return cudaGetLastError();
   }
   const bool vec16 = (p.lk % 16 == 0) && (p.bn % 16 == 0) && (a % 16 == 0);
   if (vec16)
-    encode_kernel<16, false><<<grid, kThreads, g.smem_bytes, s>>>(p);
+    encode_kernel<16><<<grid, kThreads, g.smem_bytes, s>>>(p);
   else
-    encode_kernel<8, false><<<grid, kThreads, g.smem_bytes, s>>>(p);
+    encode_kernel<8><<<grid, kThreads, g.smem_bytes, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -38,7 +38,8 @@ bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g,
 
 // Workspace carve-up (byte offsets, 256-byte aligned sections).
 struct WorkspaceLayout {
-  size_t counts, ticket, status, status_bytes, zero_bytes;  // zero_bytes from `counts`
+  size_t counts, ticket, status, status_bytes, rowcnt, zero_bytes;  // zero_bytes from `counts`
+  size_t cls;
   size_t full_row_ptr, part_row_ptr, full_col_idx, part_col_idx, bitmaps, total;
 };
 WorkspaceLayout workspace_layout(const EncodeGeom& g);
@@ -56,6 +57,8 @@ struct EncodeParams {
   int64_t* counts;                 // [0] n_full [1] n_part [2] nnz [3] error word
   unsigned long long* ticket;      // scratch, zero at launch
   unsigned long long* status;      // scratch [n_chunks], zero at launch
+  uint8_t* cls;                    // bit-packed encoder: class of every OT [n_rows][n_tc]
+  int32_t* rowcnt;                 // bit-packed encoder: full, then partial OT counts per row, zero at launch
 };
 cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s);
 

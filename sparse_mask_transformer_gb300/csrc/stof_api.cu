@@ -137,6 +137,8 @@ static stof_status encode_impl(const uint8_t* mask, int bits, const RuleSet* rul
   p.counts = f.counts_dev;
   p.ticket = reinterpret_cast<unsigned long long*>(ws + w.ticket);
   p.status = reinterpret_cast<unsigned long long*>(ws + w.status);
+  p.cls = ws + w.cls;
+  p.rowcnt = reinterpret_cast<int32_t*>(ws + w.rowcnt);
   const cudaError_t e = rules ? launch_encode_rules(p, g, *rules, s) : launch_encode(p, g, s);
   if (record_cuda(e) != cudaSuccess) return STOF_ERR_CUDA;
   return STOF_OK;
@@ -244,6 +246,8 @@ stof_status stof_encode_mask_noalloc(const uint8_t* mask, int n_masks, int lq, i
   p.counts = f.counts_dev;
   p.ticket = scratch;
   p.status = scratch + 1;
+  p.cls = nullptr;     // used by the bit-packed encoder only
+  p.rowcnt = nullptr;
   if (record_cuda(launch_encode(p, g, s)) != cudaSuccess) return STOF_ERR_CUDA;
   return STOF_OK;
 }

@@ -50,10 +50,11 @@ def test_struct_layout_matches_header(lib):
 
 def test_workspace_bytes(lib):
     ws = stof.stof_encode_workspace_bytes
-    # 16384^2 x 32 masks at 128x128: 524288 tiles x (2 KB bitmap + 8 B indices) + row pointers
+    # 16384^2 x 32 masks at 128x128: 524288 tiles x (2 KB bitmap + 8 B indices + 1 class byte)
+    # + row pointers and per-row counts
     n = ws(32, 16384, 16384, 128, 128)
     tiles = 32 * 128 * 128
-    assert tiles * (2048 + 8) <= n <= tiles * (2048 + 8) + (1 << 20)
+    assert tiles * (2048 + 8 + 1) <= n <= tiles * (2048 + 8 + 1) + (1 << 20)
     assert ws(1, 256, 256, 16, 16) > 0
     assert ws(1, 250, 256, 16, 16) == 0      # lq not a multiple of bm
     assert ws(1, 256, 256, 12, 16) == 0      # bm not a multiple of 8
