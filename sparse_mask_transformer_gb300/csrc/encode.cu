@@ -252,17 +252,17 @@ __device__ __forceinline__ unsigned long long pack_bits_unit(const uint8_t* src,
         x[r][0] = t.x; x[r][1] = t.y;
       }
     }
+    // dst is 16-byte aligned for VEC = 8 and 16: the words go out as 16-byte stores
 #pragma unroll
     for (int cg = 0; cg < G; ++cg) {
       uint32_t lo[4], hi[4];
       transpose4(x[0][cg], x[1][cg], x[2][cg], x[3][cg], lo);
       transpose4(x[4][cg], x[5][cg], x[6][cg], x[7][cg], hi);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint64_t word = static_cast<uint64_t>(lo[i]) | (static_cast<uint64_t>(hi[i]) << 32);
-        dst[4 * cg + i] = word;
-        nnz += __popcll(word);
-      }
+      for (int i = 0; i < 4; ++i) nnz += __popc(lo[i]) + __popc(hi[i]);
+      uint4* d4 = reinterpret_cast<uint4*>(dst + 4 * cg);
+      d4[0] = make_uint4(lo[0], hi[0], lo[1], hi[1]);
+      d4[1] = make_uint4(lo[2], hi[2], lo[3], hi[3]);
     }
   }
   return nnz;
