@@ -614,13 +614,11 @@ __global__ void __launch_bounds__(kThreads) bits_fill_kernel(const EncodeParams 
 
 }  // namespace
 
-// Mask columns per chunk.  A bit-packed mask carries an eighth of the bytes
-// per column, so its chunks are wider to keep every thread loading and the
-// per-chunk look-back and barriers rarer.
-constexpr int kChunkColsDense = 1024;
-constexpr int kChunkColsBits = 2048;
+// Mask columns per chunk of the single-pass (dense and rule) encoders.  The
+// bit-packed encoder works on groups of OTs instead and ignores the chunking.
+constexpr int kChunkCols = 1024;
 
-bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g, bool bits) {
+bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g) {
   if (n_masks < 1 || lq < 1 || lk < 1) return false;
   if (bm < 8 || bn < 8 || bm > 256 || bn > 256 || bm % 8 || bn % 8) return false;
   if (lq % bm || lk % bn) return false;
@@ -629,7 +627,7 @@ bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g,
   g->n_rows = static_cast<int64_t>(n_masks) * g->n_tr;
   g->n_tiles = g->n_rows * g->n_tc;
   if (g->n_tiles >= (int64_t(1) << 31) - 1) return false;
-  int ct = (bits ? kChunkColsBits : kChunkColsDense) / bn;
+  int ct = kChunkCols / bn;
   if (ct < 1) ct = 1;
   if (ct > kMaxTilesPerChunk) ct = kMaxTilesPerChunk;
   if (ct > g->n_tc) ct = g->n_tc;

@@ -34,7 +34,7 @@ struct EncodeGeom {
 };
 // chunk_cols: mask columns per chunk (rounded to whole OTs); 0 = the width
 // the encoder uses for a dense (bits = false) or bit-packed mask.
-bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g, bool bits = false);
+bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g);
 
 // Workspace carve-up (byte offsets, 256-byte aligned sections).
 struct WorkspaceLayout {

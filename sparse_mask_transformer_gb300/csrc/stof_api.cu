@@ -88,7 +88,7 @@ static stof_status encode_impl(const uint8_t* mask, int bits, const RuleSet* rul
   if ((!mask && !rules) || !workspace || !fmt) return STOF_ERR_INVALID_ARG;
   if (n_masks < 1 || lq < 1 || lk < 1 || bm < 1 || bn < 1) return STOF_ERR_INVALID_ARG;
   EncodeGeom g;
-  if (!encode_geometry(n_masks, lq, lk, bm, bn, &g, bits != 0)) return STOF_ERR_SHAPE;
+  if (!encode_geometry(n_masks, lq, lk, bm, bn, &g)) return STOF_ERR_SHAPE;
   if ((mask && !aligned(mask, 8)) || !aligned(workspace, 256)) return STOF_ERR_ALIGNMENT;
   const WorkspaceLayout w = workspace_layout(g);
   if (ws_bytes < w.total) return STOF_ERR_WORKSPACE;
