@@ -25,9 +25,10 @@
 // i - j, global rows and columns, block pattern) without reading any mask;
 // steps 2-4 are shared.  A bit-packed mask (one byte of a row is one IT row)
 // goes through three short kernels instead (further below).
-// One CTA per chunk, 256 threads, seven CTAs per SM so that the loads of
-// some CTAs overlap the look-back and writes of others; 16-byte (else
-// 8-byte) coalesced streaming loads.  (A persistent variant that streamed
+// One CTA per chunk, 256 threads, at least seven CTAs per SM (eight are
+// resident at the 32 registers the kernel takes) so that the loads of some
+// CTAs overlap the look-back and writes of others; 16-byte (else 8-byte)
+// coalesced streaming loads.  (A persistent variant that streamed
 // the mask through a TMA ring with a producer warp was measured 3x slower
 // on the 16k workload: one CTA per SM cannot hide each chunk's look-back.)
 // Every wait on another CTA or warp is bounded; on timeout the CTA raises
