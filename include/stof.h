@@ -96,6 +96,11 @@ typedef enum {
  *
  * All pointers are DEVICE memory inside the caller's workspace.  The host
  * counts are valid only after stof_format_sync().
+ *
+ * The attention kernels read the arrays as an stof_encode_* call wrote them.
+ * Row pointers are trusted: a format whose row pointers were changed by the
+ * caller is undefined behaviour.  Column indices are range-checked: an index
+ * outside [0, n_tc) is skipped and reported as STOF_DEVERR_BAD_FORMAT.
  */
 typedef struct {
   int32_t n_masks, lq, lk, bm, bn, n_tr, n_tc;
