@@ -55,3 +55,30 @@ def test_rank_reductions_world_size_2():
     assert all(p.exitcode == 0 for p in procs)
     got = sorted(q.get(timeout=10) for _ in range(2))
     assert got == [(0, 2.0, 30.0), (1, 2.0, 30.0)]
+
+
+def test_traffic_is_reported_only_for_the_profiled_kernel_source(tmp_path, monkeypatch):
+    # roofline.traffic comes from the committed ncu summary only while the
+    # block-wise kernel's device code is the one that was profiled
+    import shutil
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = tmp_path / "sparse_mask_transformer_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("blockwise.cu", "blockwise_common.cuh", "sm100_ptx.cuh"):
+        shutil.copy(os.path.join(ROOT, "sparse_mask_transformer_gb300", "csrc", f), csrc / f)
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.kernel_source_hash()
+    (tmp_path / "profiles" / "blockwise_wl.md").write_text(
+        f"kernel_source_sha256: {h}\ntraffic_bytes_per_launch: 1.5e9\n")
+    assert bench.profiled_traffic("wl") == 1.5e9
+    assert bench.profiled_traffic("other") is None
+    # host launch code below the marker does not change the device-code hash
+    with open(csrc / "blockwise.cu", "a") as fh:
+        fh.write("\n// host-side note\n")
+    assert bench.profiled_traffic("wl") == 1.5e9
+    # a change to the device code does
+    src = (csrc / "blockwise_common.cuh").read_text()
+    (csrc / "blockwise_common.cuh").write_text(src + "\n// device-side change\n")
+    assert bench.profiled_traffic("wl") is None
