@@ -80,7 +80,12 @@ def profiled_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling around the timed region.  The
+    caller keeps the GPU under the step's own load for LEAD_S before and
+    TAIL_S after the timed steps, so that every sample (one per 100 ms) sees
+    the clocks of the loaded GPU, the timed region included."""
+    LEAD_S = 0.4
+    TAIL_S = 0.2
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -96,13 +101,11 @@ class ClockSampler:
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
         return self
 
     def __exit__(self, *exc):
         self.lines = []
         if self.proc is not None:
-            time.sleep(0.15)
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -131,6 +134,15 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def run_for(step, seconds: float) -> int:
+    """Untimed steps for about `seconds` of wall time; returns how many."""
+    n, t_end = 0, time.perf_counter() + seconds
+    while time.perf_counter() < t_end:
+        step()
+        n += 1
+    return n
 
 
 def dist_setup(n_gpus: int):
@@ -232,10 +244,16 @@ def run_gpu(args, w: synth.Workload):
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        run_for(step, clk.LEAD_S)  # untimed: the clocks are sampled under load
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
         start.record(stream)
         for i in range(args.steps):
             step(i)
         end.record(stream)
+        torch.cuda.synchronize()
+        run_for(step, clk.TAIL_S)
         torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()

@@ -82,3 +82,27 @@ def test_traffic_is_reported_only_for_the_profiled_kernel_source(tmp_path, monke
     src = (csrc / "blockwise_common.cuh").read_text()
     (csrc / "blockwise_common.cuh").write_text(src + "\n// device-side change\n")
     assert bench.profiled_traffic("wl") is None
+
+
+def test_run_for_keeps_stepping_for_the_given_time():
+    sys.path.insert(0, ROOT)
+    import time
+    import bench
+    calls = []
+    t0 = time.perf_counter()
+    n = bench.run_for(lambda: (calls.append(1), time.sleep(0.01)), 0.1)
+    assert n == len(calls) >= 5 and time.perf_counter() - t0 >= 0.1
+
+
+def test_clock_summary_reports_median_and_throttle_reasons():
+    sys.path.insert(0, ROOT)
+    import bench
+    clk = bench.ClockSampler(0)
+    act, no = "Active", "Not Active"
+    clk.lines = [f"0, {mhz}, 2070, 900.0, 0x0, {no}, {no}, {no}, {cap}"
+                 for mhz, cap in ((1980, no), (2070, act), (1995, no))] + ["garbage line"]
+    out = clk.summary()
+    assert out["sm_mhz"] == 1995 and out["sm_max_mhz"] == 2070 and out["samples"] == 3
+    assert out["reasons"] == ["sw_power_cap"]
+    clk.lines = []
+    assert clk.summary()["reasons"] == ["unsampled"]
