@@ -106,3 +106,10 @@ def test_clock_summary_reports_median_and_throttle_reasons():
     assert out["reasons"] == ["sw_power_cap"]
     clk.lines = []
     assert clk.summary()["reasons"] == ["unsampled"]
+
+
+def test_l2_note_says_which_case_applies():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.l2_note(8_589_934_592, 402_653_184).startswith("inputs larger than L2")
+    assert "warm L2" in bench.l2_note(65_536, 196_608)
