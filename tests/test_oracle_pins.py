@@ -90,6 +90,44 @@ def test_single_valid_key_returns_that_value_row_exactly():
     assert np.array_equal(o, v[js])  # softmax of one element is exactly 1
 
 
+def test_key_order_does_not_matter():
+    # permuting the keys (rows of K and V with the mask's columns) is a
+    # relabelling of the sum over valid keys: O is unchanged
+    n_q, lk, d = 40, 90, 32
+    q, k, v = _rand((n_q, d), 40), _rand((lk, d), 41), _rand((lk, d), 42)
+    mask = (np.random.default_rng(43).random((n_q, lk)) < 0.3).astype(np.uint8)
+    perm = np.random.default_rng(44).permutation(lk)
+    o = oracle.attention(q, k, v, mask, 0.2)
+    o_p = oracle.attention(q, k[perm], v[perm], mask[:, perm], 0.2)
+    assert np.allclose(o, o_p, rtol=0, atol=1e-13)
+
+
+def test_output_is_linear_in_values():
+    # the softmax weights do not depend on V: O(a V1 + b V2) = a O(V1) + b O(V2)
+    n_q, lk, d = 30, 70, 16
+    q, k = _rand((n_q, d), 45), _rand((lk, d), 46)
+    v1, v2 = _rand((lk, d), 47), _rand((lk, d), 48)
+    mask = (np.random.default_rng(49).random((n_q, lk)) < 0.4).astype(np.uint8)
+    o = oracle.attention(q, k, 2.5 * v1 - 0.75 * v2, mask, 0.3)
+    want = 2.5 * oracle.attention(q, k, v1, mask, 0.3) - 0.75 * oracle.attention(q, k, v2, mask, 0.3)
+    assert np.allclose(o, want, rtol=0, atol=1e-12)
+
+
+def test_shifting_every_key_by_one_vector_changes_nothing():
+    # k_j + c adds scale * q_i . c to every score of row i: softmax is
+    # invariant to a per-row constant, so O is unchanged (shifts of ~1000
+    # and more, beyond exp's fp64 range: only a max-subtracting softmax
+    # survives them)
+    n_q, lk, d = 25, 60, 16
+    q, k, v = _rand((n_q, d), 50) * 4, _rand((lk, d), 51), _rand((lk, d), 52)
+    c = _rand((d,), 53) * 200
+    mask = (np.random.default_rng(54).random((n_q, lk)) < 0.5).astype(np.uint8)
+    o = oracle.attention(q, k, v, mask, 0.5)
+    assert np.abs(0.5 * (q @ c)).max() > 800
+    o_s = oracle.attention(q, k + c, v, mask, 0.5)
+    assert np.allclose(o, o_s, rtol=0, atol=1e-9)
+
+
 def test_fully_masked_rows_are_zero():
     q, k, v = _rand((4, 8), 18), _rand((9, 8), 19), _rand((9, 8), 20)
     o = oracle.attention(q, k, v, np.zeros((4, 9), np.uint8), 1.0)
