@@ -5,6 +5,8 @@ with a status before touching the device."""
 import ctypes
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -255,3 +257,20 @@ def test_bounded_wait_check_rejects_bad_arguments(lib):
     assert f(one, ctypes.c_double(11.0), None) == stof.STOF_ERR_INVALID_ARG
     assert f(one, ctypes.c_double(float("nan")), None) == stof.STOF_ERR_INVALID_ARG
     assert f(ctypes.c_void_p(260), ctypes.c_double(0.1), None) == stof.STOF_ERR_ALIGNMENT
+
+
+def test_missing_library_fails_loudly():
+    # no silent fallback: without the built library the binding raises
+    code = ("import sys; from sparse_mask_transformer_gb300 import stof\n"
+            "try:\n    stof.load_library('/nonexistent/libstof.so')\n"
+            "except RuntimeError as e:\n    print('raised', 'missing' in str(e))\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert r.returncode == 0 and r.stdout.strip() == "raised True", r.stdout + r.stderr
+
+
+def test_product_package_does_not_import_the_oracle(lib):
+    # the oracle is test infrastructure: the package and its binding never load it
+    code = ("import sys; import sparse_mask_transformer_gb300 as p; from sparse_mask_transformer_gb300 import stof, synth\n"
+            "stof.load_library(); print(any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules))\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert r.returncode == 0 and r.stdout.strip() == "False", r.stdout + r.stderr
