@@ -274,3 +274,17 @@ def test_product_package_does_not_import_the_oracle(lib):
             "stof.load_library(); print(any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules))\n")
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert r.returncode == 0 and r.stdout.strip() == "False", r.stdout + r.stderr
+
+
+def test_oracle_and_product_share_no_code():
+    # the C oracle includes system headers only, and no product source
+    # imports, includes or links it
+    src = open(os.path.join(ROOT, "oracle", "stof_oracle.c")).read()
+    assert not re.search(r'#include\s+"', src)
+    for d in ("sparse_mask_transformer_gb300", "include"):
+        for dirpath, _, files in os.walk(os.path.join(ROOT, d)):
+            for f in files:
+                if f.endswith((".py", ".cu", ".cuh", ".h", ".c")):
+                    text = open(os.path.join(dirpath, f)).read()
+                    assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                    assert "stof_oracle" not in text, f
