@@ -64,19 +64,20 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the block-wise kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
+def profiled(workload: str, key: str):
+    """A figure (`key: value` line) of the committed ncu summary of the
+    block-wise kernel on this workload, if it was taken on the current
+    kernel source; else None."""
     path = os.path.join(ROOT, "profiles", f"blockwise_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
-    tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not src or not tr or src.group(1) != kernel_source_hash():
+    val = re.search(rf"{key}:\s*([0-9.eE+]+)", text)
+    if not src or not val or src.group(1) != kernel_source_hash():
         return None
-    return float(tr.group(1))
+    return float(val.group(1))
 
 
 class ClockSampler:
@@ -286,6 +287,10 @@ def run_gpu(args, w: synth.Workload):
     bitmask = None if args.no_bitmask else run_bitmask(args, w, mask, q, k, v, ws, scale, stream, device, dist)
     # the same step from the mask's rule, where the workload has one
     rules = None if args.no_bitmask else run_rules(args, w, q, k, v, ws, scale, stream, device, dist)
+    # kernel-only times of both kernels and the encoder on all five workloads
+    workloads = None
+    if not args.no_workloads and not args.heads:
+        workloads = run_workload_records(args, device, peaks, big=(w, mask, q, k, v))
 
     kern_name = "blockwise" if chosen == stof.STOF_KERNEL_BLOCKWISE else "rowwise"
     if chosen == stof.STOF_KERNEL_BLOCKWISE:
@@ -293,7 +298,9 @@ def run_gpu(args, w: synth.Workload):
         peak = peaks["bf16_tflops"]
         roofline = {"bound": "tensor", "kernel": "blockwise_kernel", "achieved": round(achieved, 2),
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                    "traffic": profiled_traffic(w.name), "peak_source": f"{peak_src} bf16 burst",
+                    "traffic": profiled(w.name, "traffic_bytes_per_launch"),
+                    "tensor_pipe_active_pct": profiled(w.name, "tensor_pipe_active_pct_of_active_cycles"),
+                    "peak_source": f"{peak_src} bf16 burst",
                     "algorithmic": "4*d*128*128 FLOPs per listed outer tile per head"}
     else:
         bytes_alg = 4 * w.B * w.H * w.L * w.d * 2
@@ -305,6 +312,11 @@ def run_gpu(args, w: synth.Workload):
 
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "value_definition": ("4*d*(valid mask elements over all heads) / step time, one step being every row "
+                             "of the hot path on one batch: encode the dense mask, sync the tile counts, "
+                             "select the kernel, stof_mha_fwd.  The same metric over the stof_mha_fwd call "
+                             "alone is breakdown.effective_tflops_mha_only; kernel-only times of both kernels "
+                             "on all five workloads are under workloads"),
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded masks and N(0,1) Q/K/V)",
@@ -324,6 +336,8 @@ def run_gpu(args, w: synth.Workload):
         "e2e": e2e,
         "bitmask": bitmask,
         "rules": rules,
+        "workloads": workloads,
+        "build": {"libstof_srchash": build.built_hash(), "sources_srchash": build.source_hash()},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
@@ -334,6 +348,209 @@ def run_gpu(args, w: synth.Workload):
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- per-workload records
+
+def graph_ms(fn, n: int, flush=None) -> float:
+    """Device time per call of fn() with no host work in it: n calls are
+    captured into one CUDA graph and the replay is timed with events.  With
+    `flush` (a buffer larger than L2), each call is preceded by a write of
+    the buffer and the time of the flushes alone is subtracted, so every
+    call starts with a cold L2."""
+    import torch
+
+    def timed(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(n):
+                body()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    fn()
+    torch.cuda.synchronize()
+    if flush is None:
+        return timed(fn)
+
+    def both():
+        flush.zero_()
+        fn()
+    return timed(both) - timed(flush.zero_)
+
+
+def call_latency(lib_fn, args, reps: int = 15):
+    """One C-ABI call on an idle GPU, timed by events recorded just before and
+    after it on the stream (host argument checks, launch and kernel), median
+    over reps; and the host time of the call alone (median, microseconds)."""
+    import torch
+    dev_ms, host_us = [], []
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        t0 = time.perf_counter_ns()
+        st = lib_fn(*args)
+        t1 = time.perf_counter_ns()
+        b.record()
+        torch.cuda.synchronize()
+        if st != 0:
+            raise RuntimeError(f"status {st}")
+        dev_ms.append(a.elapsed_time(b))
+        host_us.append((t1 - t0) / 1e3)
+    return statistics.median(dev_ms), statistics.median(host_us)
+
+
+def workload_record(w: synth.Workload, mask, q, k, v, peaks, flush) -> dict:
+    """Kernel-only device times of both attention kernels and of the encoder
+    on one workload (CUDA-graph replay, warm and with a cold L2), the latency
+    of one stof_mha_fwd call through the C ABI, and the analytic selector's
+    choice against the measured times."""
+    import ctypes
+
+    import torch
+    from sparse_mask_transformer_gb300 import stof
+    lib = stof.load_library()
+    n_masks = mask.shape[0]
+    ws = torch.empty(stof.stof_encode_workspace_bytes(n_masks, w.L, w.L, 128, 128), dtype=torch.uint8,
+                     device=q.device)
+    fmt = stof.stof_format()
+    enc = lambda: stof.stof_encode_mask(mask, 128, 128, ws, fmt)  # noqa: E731
+    enc_ms = graph_ms(enc, 10)
+    enc()
+    stof.stof_format_sync(fmt)
+    hpm = heads_per_mask(w)
+    density = fmt.nnz / (n_masks * w.L * w.L)
+    tiles = fmt.n_full + fmt.n_part
+    eff_flops = 4.0 * w.d * fmt.nnz * hpm
+    tile_flops = 4.0 * w.d * 128 * 128 * tiles * hpm
+    n_rows = n_masks * (w.L // 128)
+    fmt_bytes = 8 * (n_rows + 1) + 4 * tiles + 2048 * fmt.n_part
+    enc_bytes = n_masks * w.L * w.L + fmt_bytes
+    o = torch.empty_like(q)
+    scale = 1.0 / math.sqrt(w.d)
+    chosen = stof.stof_select_kernel(density, w.L, w.d)
+    rec = {"B": w.B, "H": w.H, "L": w.L, "d": w.d, "dtype": w.dtype, "density": round(density, 6),
+           "tiles_full": fmt.n_full, "tiles_partial": fmt.n_part,
+           "encode": {"ms": round(enc_ms, 5), "gbs": round(enc_bytes / (enc_ms * 1e-3) / 1e9, 1),
+                      "frac_hbm": round(enc_bytes / (enc_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+           "selected": "blockwise" if chosen == stof.STOF_KERNEL_BLOCKWISE else "rowwise"}
+    times = {}
+    for name, which in (("rowwise", stof.STOF_KERNEL_ROWWISE), ("blockwise", stof.STOF_KERNEL_BLOCKWISE)):
+        call = lambda: stof.stof_mha_fwd(q, k, v, fmt, scale, w.stride_b, w.stride_h, which, o)  # noqa: E731
+        once = graph_ms(call, 2)
+        n = max(3, min(40, int(60.0 / max(once, 1e-3))))
+        warm = graph_ms(call, n)
+        cold = graph_ms(call, n, flush=flush) if q.numel() * 6 < L2_BYTES else warm
+        B, H, L, d = q.shape
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), 1 if q.dtype == torch.bfloat16 else 0, B, H, L, d,
+                ctypes.c_float(scale), ctypes.byref(fmt), w.stride_b, w.stride_h, which, o.data_ptr(),
+                torch.cuda.current_stream().cuda_stream)
+        lat_ms, host_us = call_latency(lib.stof_mha_fwd, args)
+        r = {"kernel_ms": round(warm, 5), "kernel_ms_cold_l2": round(cold, 5), "call_ms": round(lat_ms, 5),
+             "call_minus_kernel_us": round((lat_ms - warm) * 1e3, 2), "host_us": round(host_us, 2),
+             "effective_tflops": round(eff_flops / (warm * 1e-3) / 1e12, 3)}
+        if name == "blockwise":
+            r["variant"] = ("persistent" if w.d == 64 and tiles / n_rows < 48 else "cta_per_query_tile")
+            r["tile_tflops"] = round(tile_flops / (warm * 1e-3) / 1e12, 2)
+            r["frac_tensor_peak_tile"] = round(tile_flops / (warm * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)
+        else:
+            alg = 4 * B * H * L * d * 2 + fmt_bytes
+            r["gbs"] = round(alg / (warm * 1e-3) / 1e9, 1)
+            r["frac_hbm"] = round(alg / (warm * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+        rec[name] = r
+        times[name] = warm
+    rec["fastest"] = min(times, key=times.get)
+    rec["selector_picks_fastest"] = rec["fastest"] == rec["selected"]
+    rec["l2"] = ("inputs fit in L2: kernel_ms warm (back to back), kernel_ms_cold_l2 with a 256 MB write "
+                 "before each call" if q.numel() * 6 < L2_BYTES else "inputs larger than L2")
+    del ws
+    return rec
+
+
+def run_workload_records(args, device, peaks, big=None) -> dict:
+    """Sub-records for every workload; `big` = (workload, mask, q, k, v)
+    reuses the headline run's device inputs for that workload."""
+    import torch
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=device)
+    out = {}
+    for name in synth.WORKLOAD_ORDER:
+        w = synth.WORKLOADS[name]
+        if big is not None and big[0].name == name:
+            _, mask, q, k, v = big
+        else:
+            mask, q, k, v = device_inputs(w, device)
+        out[name] = workload_record(w, mask, q, k, v, peaks, flush)
+        del mask, q, k, v
+        torch.cuda.empty_cache()
+    return out
+
+
+SWEEP_L = (128, 256, 512, 1024, 2048)
+SWEEP_DENSITY = (0.01, 0.02, 0.05, 0.1, 0.2, 0.4)
+SWEEP_HEADS = (2, 16, 64)
+
+
+def sweep_mask(pattern: str, L: int, density: float, seed: int):
+    """One shared mask of the sweep: 'random' = i.i.d. Bernoulli(density)
+    elements; 'window' = causal sliding window whose width gives about that
+    density (at least 1 key per row)."""
+    if pattern == "random":
+        m = synth.random_mask(1, L, L, density, seed=seed)
+    else:
+        wdt = max(1, int(round(density * L)))
+        i = np.arange(L)[:, None]
+        j = np.arange(L)[None, :]
+        m = ((i - j >= 0) & (i - j < wdt)).astype(np.uint8)[None]
+    return m
+
+
+def run_sweep(args):
+    """Kernel-only times (CUDA-graph replay, warm L2) of the row-wise and the
+    block-wise kernel over short sequences and low densities, with the
+    analytic selector's choice: one JSON line per case, then a summary."""
+    import torch
+    from sparse_mask_transformer_gb300 import build, stof
+    torch.cuda.set_device(0)
+    build.build()
+    stof.load_library()
+    cases = 0
+    agree = 0
+    for d in (64, 128):
+        for pattern in ("random", "window"):
+            for L in SWEEP_L:
+                for rho in SWEEP_DENSITY:
+                    mask = torch.from_numpy(sweep_mask(pattern, L, rho, seed=L + int(rho * 1000))).cuda()
+                    ws = torch.empty(stof.stof_encode_workspace_bytes(1, L, L, 128, 128), dtype=torch.uint8,
+                                     device="cuda")
+                    fmt = stof.stof_encode_mask(mask, 128, 128, ws)
+                    stof.stof_format_sync(fmt)
+                    density = fmt.nnz / (L * L)
+                    for H in SWEEP_HEADS:
+                        q, k, v = (t.cuda() for t in synth.make_qkv(1, H, L, d, "bf16", seed=H))
+                        o = torch.empty_like(q)
+                        t = {}
+                        for name, which in (("rowwise", stof.STOF_KERNEL_ROWWISE),
+                                            ("blockwise", stof.STOF_KERNEL_BLOCKWISE)):
+                            call = lambda: stof.stof_mha_fwd(q, k, v, fmt, 1 / math.sqrt(d), 0, 0,  # noqa: E731
+                                                             which, o)
+                            t[name] = graph_ms(call, 20) * 1e3
+                        sel = "blockwise" if stof.stof_select_kernel(density, L, d) == stof.STOF_KERNEL_BLOCKWISE \
+                            else "rowwise"
+                        fastest = min(t, key=t.get)
+                        cases += 1
+                        agree += sel == fastest
+                        print(json.dumps({"sweep": pattern, "L": L, "d": d, "H": H, "density": round(density, 5),
+                                          "tiles": fmt.n_full + fmt.n_part, "rowwise_us": round(t["rowwise"], 2),
+                                          "blockwise_us": round(t["blockwise"], 2), "selected": sel,
+                                          "fastest": fastest}), flush=True)
+    print(json.dumps({"sweep_summary": {"cases": cases, "selector_picks_fastest": agree}}), flush=True)
 
 
 def run_bitmask(args, w, mask, q, k, v, ws, scale, stream, device, dist):
@@ -590,6 +807,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-bitmask", action="store_true", help="skip the bit-packed-mask and mask-rule measurements")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the bench line: kernel-only times of both kernels over short, sparse cases")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload kernel-only records of both kernels")
     ap.add_argument("--heads", type=int, default=0,
                     help="profiling only: run the workload with this many heads (one mask per head "
                          "for per-head masks)")
@@ -602,7 +823,9 @@ def main(argv=None):
         per_head = w.n_masks == w.B * w.H
         w = dataclasses.replace(w, H=args.heads, n_masks=w.B * args.heads if per_head else w.n_masks,
                                 stride_b=args.heads if per_head else w.stride_b)
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_gpu(args, w)

@@ -170,8 +170,10 @@ stof_status stof_encode_mask_bits(const uint8_t* mask_bits, int n_masks, int lq,
  *   - The workspace (same size as for stof_encode_mask) receives the
  *     format; its scratch section is not used.
  *   - The first call on a device looks up the static array's device
- *     address (with that device current); make that first call before any
- *     stream capture.
+ *     address (with that device current) and keeps it for the life of the
+ *     process; make that first call before any stream capture.  A device
+ *     reset (cudaDeviceReset) between calls is not supported: the kept
+ *     address would then be stale.
  *   - All calls share the one array, which keeps the last call's contents
  *     (the call clears what must start at zero): calls that may overlap on
  *     the GPU, from several streams or threads, race and must not be made.
@@ -242,6 +244,9 @@ stof_kernel stof_select_kernel(double density, int seq_len, int head_dim);
  * need no mask test, partial OTs are masked through their IT bitmaps.
  *   q, k, v, o  device [B][H][L][d], dt, 16-byte aligned; o is written.
  *   L           == fmt->lq == fmt->lk.   d: 64 or 128.
+ *   scale       any finite value; the softmax is taken over scale * Q.K
+ *               (a negative scale favours the smallest dot products, a zero
+ *               scale averages the valid V rows).
  *   fmt         an encoded format (stof_encode_mask) for masks of size L.
  *   which       STOF_KERNEL_ROWWISE [ROW], STOF_KERNEL_BLOCKWISE [BLK]
  *               (needs bm == 128 and bn == 64 or 128; else

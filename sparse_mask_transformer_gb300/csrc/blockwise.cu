@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<kProducerRegs>();
     if (warp == 0) {
       // ------------------------------------------------------------ K producer
-      if (lane == 0) {  // Q, then K tiles
+      if (lane == 0 && n > 0) {  // Q, then K tiles; a row without listed OTs loads nothing
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
         const int qrow = bh * p.L + I * kBM;
@@ -313,7 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tSr = tS + lane_off;
     const uint32_t tP = tP0 + g * 64 + lane_off;
     const uint32_t tO = tO0 + g * D + lane_off;
-    const float c = p.scale_log2;
+    // c <= 0: the scores are multiplied by c before masking and the max, and
+    // the softmax below runs with a factor of 1
+    const bool prescale = p.scale_log2 <= 0.f;
+    const float c = prescale ? 1.f : p.scale_log2;
     // row r of an OT's bitmaps: byte r % 8 of words (r / 8) * BN / 8 + 0 .. BN / 8 - 1
     const uint8_t* bits_row = reinterpret_cast<const uint8_t*>(p.bitmaps) + (r >> 3) * BN + (r & 7);
     uint32_t nb[BN / 8];  // bitmap bytes of this warpgroup's next partial tile, loaded a tile ahead
@@ -339,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t bits[C::CHUNKS] = {};
       if (partial) assemble_bits<C::CHUNKS>(nb, bits);
       fetch_bits(t + 2);                        // the bytes of this warpgroup's next tile
+      if (prescale) scale_scores(sr, p.scale_log2);
       if (partial) mask_scores(sr, bits);       // keep only the keys whose bit is set
       const float mt = row_max(sr) * c;
       float alpha = 1.f;
@@ -434,11 +438,56 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-// [rows][D] row-major 16-bit matrix, box = 64 columns x box_rows rows, 128-byte swizzle
+// [rows][D] row-major 16-bit matrix, box = 64 columns x box_rows rows, 128-byte swizzle.
+// A tensor map holds only the address, sizes, strides and box of a tensor,
+// so a map made once stays right for every later call with the same key;
+// the cache (round-robin over kMapCache entries) spares the driver call that
+// otherwise dominates a short launch's host time.
+namespace {
+struct MapKey {
+  int dev;
+  const void* base;
+  uint64_t rows;
+  int D, box_rows;
+  bool bf16;
+  bool operator==(const MapKey& o) const {
+    return dev == o.dev && base == o.base && rows == o.rows && D == o.D && box_rows == o.box_rows && bf16 == o.bf16;
+  }
+};
+struct MapEntry {
+  CUtensorMap map;
+  MapKey key;
+  bool used;
+};
+constexpr int kMapCache = 64;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+}  // namespace
+
 bool make_bw_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_rows, bool bf16) {
-  return encode_tensor_map_2d(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                              base, static_cast<uint64_t>(D), rows, static_cast<uint64_t>(D) * 2, 64,
-                              static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  const MapKey key{dev, base, rows, D, box_rows, bf16};
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (const MapEntry& e : g_maps)
+      if (e.used && e.key == key) {
+        *m = e.map;
+        return true;
+      }
+  }
+  if (!encode_tensor_map_2d(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base,
+                            static_cast<uint64_t>(D), rows, static_cast<uint64_t>(D) * 2, 64,
+                            static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B))
+    return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  MapEntry& e = g_maps[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapCache;
+  e.map = *m;
+  e.key = key;
+  e.used = true;
+  return true;
 }
 
 namespace {

@@ -117,6 +117,18 @@ __device__ __forceinline__ void assemble_bits(const uint32_t (&nb)[CHUNKS * 4], 
     bits[cc] = nb[4 * cc] | (nb[4 * cc + 1] << 8) | (nb[4 * cc + 2] << 16) | (nb[4 * cc + 3] << 24);
 }
 
+// Scores times c, in place.  Used when c = scale * log2(e) is not positive:
+// the max of c*s is then not c times the max of s, and a masked score set
+// to -inf before the multiply would become +inf or NaN after it.  With the
+// scores pre-multiplied the softmax runs with c = 1 and masks afterwards.
+template <int CHUNKS>
+__device__ __forceinline__ void scale_scores(uint32_t (&sr)[CHUNKS][32], float c) {
+#pragma unroll
+  for (int cc = 0; cc < CHUNKS; ++cc)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) sr[cc][i] = __float_as_uint(__uint_as_float(sr[cc][i]) * c);
+}
+
 // -inf at every key whose bit is clear.
 template <int CHUNKS>
 __device__ __forceinline__ void mask_scores(uint32_t (&sr)[CHUNKS][32], const uint32_t (&bits)[CHUNKS]) {

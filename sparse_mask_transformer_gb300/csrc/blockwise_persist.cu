@@ -29,8 +29,8 @@
 // leaves its row max and sum in shared memory and moves on.
 // TMEM columns: S [0,BN) P_0 [128,128+BN/2) P_1 [192,192+BN/2)
 // O[item % 2][g] [256 + 128 (item % 2) + 64 g, +64).
-// The work counter lives in the format's workspace and is zeroed before
-// each launch.  Every wait is bounded; on timeout the CTA raises
+// The work counter lives in the format's workspace (zeroed by the encoders)
+// and is zeroed again by the last CTA to finish, ready for the next launch.  Every wait is bounded; on timeout the CTA raises
 // STOF_DEVERR_PIPE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -359,7 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tSr = tS + lane_off;
     const uint32_t tP = tP0 + g * 64 + lane_off;
-    const float c = p.scale_log2;
+    // c <= 0: the scores are multiplied by c before masking and the max, and
+    // the softmax below runs with a factor of 1
+    const bool prescale = p.scale_log2 <= 0.f;
+    const float c = prescale ? 1.f : p.scale_log2;
     const uint8_t* bits_r = reinterpret_cast<const uint8_t*>(p.bitmaps) + (r >> 3) * BN + (r & 7);
     int J = 0;   // tiles of this warpgroup so far, all items
     int e = 0;   // items with tiles so far
@@ -407,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t bits[C::CHUNKS] = {};
         if (partial) assemble_bits<C::CHUNKS>(nb, bits);
         fetch_bits(t + 2);                        // the bytes of this warpgroup's next tile
+        if (prescale) scale_scores(sr, p.scale_log2);
         if (partial) mask_scores(sr, bits);       // keep only the keys whose bit is set
         const float mt = row_max(sr) * c;
         float alpha = 1.f;
@@ -501,6 +505,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  // The CTA's last fetch (thread 0) is done.  The last CTA to get here sees
+  // every fetch of the launch done and zeroes both counters for the next
+  // launch on the stream; so the host needs no reset per call.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.work + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.work, 0u);
+      atomicExch(p.work + 1, 0u);
+    }
+  }
 }
 
 template <int BN, bool BF16>
@@ -537,7 +551,6 @@ stof_status launch_persist(const AttnParams& p, cudaStream_t s) {
   const long long n_items = static_cast<long long>(p.B) * p.H * p.n_tr;
   const long long sms = device_sm_count();
   const long long grid = n_items < sms ? n_items : sms;
-  if (record_cuda(cudaMemsetAsync(p.work, 0, sizeof(unsigned int), s)) != cudaSuccess) return STOF_ERR_CUDA;
   blockwise_persist_kernel<BN, BF16><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(
       mq, mk, mv, p, static_cast<int>(n_items));
   return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;

@@ -99,7 +99,8 @@ struct AttnParams {
   const int32_t* part_col_idx;
   const uint64_t* bitmaps;
   int64_t* err;                    // device error word (counts[3])
-  unsigned int* work;              // work counter of the persistent kernel, in the format's workspace
+  unsigned int* work;              // work counter of the persistent kernel, in the format's workspace:
+                                   // work[0] items taken, work[1] CTAs finished (both zero between launches)
   float tiles_per_row;             // mean listed OTs per OT row of the masks (synced format), else -1
 };
 cudaError_t launch_rowwise(const AttnParams& p, bool bf16, cudaStream_t s);
@@ -110,6 +111,8 @@ stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s);
 // The persistent block-wise kernel for d = 64 (blockwise_persist.cu).
 stof_status launch_blockwise_persist64(const AttnParams& p, bool bf16, cudaStream_t s);
 // TMA map of a [rows][D] 16-bit matrix, 64-column x box_rows boxes, 128-byte swizzle.
+// Maps are kept in a small per-process cache keyed by (device, base, rows,
+// D, box_rows, type), so repeated calls on the same tensors do no driver call.
 bool make_bw_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_rows, bool bf16);
 
 }  // namespace stof

@@ -220,9 +220,10 @@ stof_status stof_encode_mask_noalloc(const uint8_t* mask, int n_masks, int lq, i
   *fmt = f;
 
   cudaStream_t s = as_stream(stream);
-  // the static scratch keeps the previous call's words: the counts, the
-  // ticket and this call's look-back words start at zero
-  if (record_cuda(cudaMemsetAsync(ws + w.counts, 0, 32, s)) != cudaSuccess) return STOF_ERR_CUDA;
+  // the static scratch keeps the previous call's words: the workspace's
+  // 64-byte header (counts and the attention kernel's counters), the ticket
+  // and this call's look-back words start at zero
+  if (record_cuda(cudaMemsetAsync(ws + w.counts, 0, 64, s)) != cudaSuccess) return STOF_ERR_CUDA;
   if (record_cuda(cudaMemsetAsync(scratch, 0, (static_cast<size_t>(g.n_chunks) + 1) * 8, s)) != cudaSuccess)
     return STOF_ERR_CUDA;
   EncodeParams p;
@@ -360,7 +361,8 @@ stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype
   p.part_col_idx = fmt->part_col_idx;
   p.bitmaps = fmt->bitmaps;
   p.err = fmt->counts_dev + 3;
-  // bytes 40..43 of the workspace: a word the encoders zero and never use
+  // bytes 40..47 of the workspace: two words no encoder uses and every
+  // encoder zeroes; the persistent kernel leaves them zero when it ends
   p.work = reinterpret_cast<unsigned int*>(fmt->counts_dev + 5);
   p.tiles_per_row = fmt->synced ? static_cast<float>(static_cast<double>(fmt->n_full + fmt->n_part) /
                                                      (static_cast<double>(fmt->n_masks) * fmt->n_tr))

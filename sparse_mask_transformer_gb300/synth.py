@@ -104,9 +104,9 @@ def bernoulli_threshold(p: float) -> int:
     return int(math.ceil(p * float(1 << 53)))
 
 
-def _bernoulli_rows(h: int, rows: np.ndarray, L: int, seed: int, p: float) -> np.ndarray:
+def _bernoulli_rows(h: int, rows: np.ndarray, L: int, seed: int, p: float, ncols: int | None = None) -> np.ndarray:
     rows = np.asarray(rows, dtype=np.uint64)
-    j = np.arange(L, dtype=np.uint64)
+    j = np.arange(L if ncols is None else ncols, dtype=np.uint64)
     ctr = (np.uint64(h) << np.uint64(48)) | (rows[:, None] << np.uint64(24)) | j[None, :]
     z = splitmix64(np.uint64(seed) ^ ctr)
     keep = (z >> np.uint64(11)) < np.uint64(bernoulli_threshold(p))
@@ -142,26 +142,27 @@ def _longformer_globals(L: int, seed: int) -> np.ndarray:
     return np.sort(np.random.default_rng(seed).choice(L, 32, replace=False))
 
 
-def mask_rows(w: Workload, m: int, rows) -> np.ndarray:
-    """Rows `rows` of mask number m, as uint8 [len(rows), L] of 0/1."""
+def mask_rows(w: Workload, m: int, rows, ncols: int | None = None) -> np.ndarray:
+    """Rows `rows` of mask number m, as uint8 [len(rows), L] of 0/1; with
+    `ncols`, only the first ncols key columns ([len(rows), ncols])."""
     rows = np.asarray(rows, dtype=np.int64)
     L = w.L
     i = rows[:, None]
-    j = np.arange(L, dtype=np.int64)[None, :]
+    j = np.arange(L if ncols is None else ncols, dtype=np.int64)[None, :]
     if w.pattern == "window48":
         return ((i - j >= 0) & (i - j < 48)).astype(np.uint8)
     if w.pattern == "causal":
         return (j <= i).astype(np.uint8)
     if w.pattern == "bigbird64":
         lay = _bigbird_blocks(L, 64, w.seed)
-        return lay[(rows // 64)[:, None], (np.arange(L) // 64)[None, :]].astype(np.uint8)
+        return lay[(rows // 64)[:, None], (j[0] // 64)[None, :]].astype(np.uint8)
     if w.pattern == "longformer":
         g = np.zeros(L, dtype=bool)
         g[_longformer_globals(L, w.seed)] = True
-        out = (np.abs(i - j) <= 256) | g[rows][:, None] | g[None, :]
+        out = (np.abs(i - j) <= 256) | g[rows][:, None] | g[j[0]][None, :]
         return out.astype(np.uint8)
     if w.pattern == "causal_bernoulli":
-        return _bernoulli_rows(m, rows, L, w.seed, BERNOULLI_P)
+        return _bernoulli_rows(m, rows, L, w.seed, BERNOULLI_P, ncols)
     raise ValueError(w.pattern)
 
 

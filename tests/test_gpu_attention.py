@@ -80,9 +80,13 @@ def test_bernoulli_L16384_full_size_sampled(gpu_lib, kern):
     o, fmt = _run(q, k, v, mask, 128, 128, w.stride_b, w.stride_h, KERNELS[kern])
     del mask
     torch.cuda.empty_cache()
+    # 8 heads (the first, the last and 6 seeded others), 1024 query rows of
+    # each: the first 128, the last 128 and 768 seeded others
     rng = np.random.default_rng(2)
-    rows = np.unique(np.concatenate([np.arange(64), rng.integers(0, L, 192), [L - 1]]))
-    heads = [(0, 0), (0, 17), (0, 31)]
+    heads = [(0, 0), (0, 31)] + [(0, int(h)) for h in rng.choice(np.arange(1, 31), 6, replace=False)]
+    mid = rng.choice(np.arange(128, L - 128), 768, replace=False)
+    rows = np.unique(np.concatenate([np.arange(128), mid, np.arange(L - 128, L)]))
+    assert len(rows) == 1024
     _check(o, q, k, v, lambda b, h, r: synth.mask_rows(w, b * w.stride_b + h * w.stride_h, r),
            w.dtype, heads=heads, rows=rows)
 
@@ -239,3 +243,23 @@ def test_concurrent_calls_with_different_formats(gpu_lib):
     for i in range(2):
         q, k, v = (t.cpu() for t in qkv[i])
         _check(outs[i].cpu(), q, k, v, _mask_of_np(masks[i], 0, 0), "fp16", heads=[(0, 0), (0, 7)], scale=0.125)
+
+
+@pytest.mark.parametrize("kern,bn", [("row", 128), ("block", 128), ("block", 64)])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("sign", [-1.0, 0.0])
+def test_nonpositive_scale(gpu_lib, kern, bn, d, sign):
+    """scale <= 0 is a legal softmax temperature: with a negative scale the
+    row max of the scaled scores is the scaled minimum, and a zero scale gives
+    the plain mean of the valid V rows.  Per-head masks with a fully masked
+    row and a query tile without listed OTs."""
+    B, H, L = 1, 3, 384
+    mask = synth.random_mask(B * H, L, L, 0.3, seed=41 + d)
+    mask[1, 5] = 0
+    mask[2, :128] = 0                 # query tile 0 of head 2: no listed OT
+    q, k, v = synth.make_qkv(B, H, L, d, "fp16", seed=43)
+    scale = sign / math.sqrt(d)
+    o, fmt = _run(q, k, v, torch.from_numpy(mask).cuda(), 128, bn, H, 1, KERNELS[kern], scale=scale)
+    assert fmt.device_error == 0
+    _check(o, q, k, v, _mask_of_np(mask, H, 1), "fp16", scale=scale)
+    assert torch.all(o[0, 1, 5] == 0) and torch.all(o[0, 2, :128] == 0)

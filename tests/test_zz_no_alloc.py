@@ -50,13 +50,20 @@ def _assert_same(a_fmt, a, b_fmt, b):
 
 
 def test_noalloc_encoder_matches_regular_encoder_two_calls_in_a_row(gpu_lib):
+    """Masks A, B, A of one geometry (same chunk count) in a row: the
+    look-back words that A leaves in the shared scratch are wrong prefixes
+    for B, so a call that did not clear them would give B a wrong format."""
     cases = [
-        (torch.from_numpy(synth.make_mask(synth.WORKLOADS["causal_L2048"])).cuda(), 128, 128),
-        (torch.from_numpy(synth.random_mask(3, 512, 4096, 0.01, seed=11)).cuda(), 8, 8),  # 768 chunks
+        (torch.from_numpy(synth.make_mask(synth.WORKLOADS["causal_L2048"])).cuda(),
+         torch.from_numpy(synth.random_mask(1, 2048, 2048, 0.5, seed=13)).cuda(), 128, 128),
+        (torch.from_numpy(synth.random_mask(3, 512, 4096, 0.01, seed=11)).cuda(),           # 768 chunks
+         torch.from_numpy(synth.random_mask(3, 512, 4096, 0.3, seed=12)).cuda(), 8, 8),
     ]
-    for mask, bm, bn in cases:
-        ref_fmt, _, ref = gpu_encode(mask, bm, bn)
-        for _ in range(2):
+    for mask_a, mask_b, bm, bn in cases:
+        refs = {id(m): gpu_encode(m, bm, bn) for m in (mask_a, mask_b)}
+        assert refs[id(mask_a)][0].n_part != refs[id(mask_b)][0].n_part
+        for mask in (mask_a, mask_b, mask_a):
+            ref_fmt, _, ref = refs[id(mask)]
             fmt, got = _encode_noalloc(mask, bm, bn)
             _assert_same(fmt, got, ref_fmt, ref)
 
