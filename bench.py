@@ -91,11 +91,16 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, enabled: bool = True):
         self.index = index
         self.proc = None
+        if not enabled:  # profiling runs: no sampler, no untimed lead and tail steps
+            self.LEAD_S = self.TAIL_S = 0.0
+        self.enabled = enabled
 
     def __enter__(self):
+        if not self.enabled:
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
@@ -248,7 +253,8 @@ def run_gpu(args, w: synth.Workload):
         step()
     torch.cuda.synchronize()
     density = fmt.nnz / (w.n_masks * w.L * w.L)
-    chosen = stof.stof_select_kernel(density, w.L, w.d)
+    plan = stof.stof_mha_plan(fmt, w.B, w.H, w.L, w.d, stof.STOF_KERNEL_AUTO)
+    chosen = plan.kernel
     valid = fmt.nnz * heads_per_mask(w)
     tiles = (fmt.n_full + fmt.n_part) * heads_per_mask(w)
 
@@ -256,7 +262,7 @@ def run_gpu(args, w: synth.Workload):
         dist.barrier()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    with ClockSampler(local, enabled=not args.no_clocks) as clk:
         run_for(step, clk.LEAD_S)  # untimed: the clocks are sampled under load
         torch.cuda.synchronize()
         if dist is not None:
@@ -407,6 +413,13 @@ def call_latency(lib_fn, args, reps: int = 15):
     return statistics.median(dev_ms), statistics.median(host_us)
 
 
+def host_time_us(fn, args) -> float:
+    """Host time of one C-ABI call through ctypes (microseconds)."""
+    t0 = time.perf_counter_ns()
+    fn(*args)
+    return (time.perf_counter_ns() - t0) / 1e3
+
+
 def workload_record(w: synth.Workload, mask, q, k, v, peaks, flush) -> dict:
     """Kernel-only device times of both attention kernels and of the encoder
     on one workload (CUDA-graph replay, warm and with a cold L2), the latency
@@ -435,7 +448,7 @@ def workload_record(w: synth.Workload, mask, q, k, v, peaks, flush) -> dict:
     enc_bytes = n_masks * w.L * w.L + fmt_bytes
     o = torch.empty_like(q)
     scale = 1.0 / math.sqrt(w.d)
-    chosen = stof.stof_select_kernel(density, w.L, w.d)
+    chosen = stof.stof_mha_plan(fmt, w.B, w.H, w.L, w.d, stof.STOF_KERNEL_AUTO).kernel
     rec = {"B": w.B, "H": w.H, "L": w.L, "d": w.d, "dtype": w.dtype, "density": round(density, 6),
            "tiles_full": fmt.n_full, "tiles_partial": fmt.n_part,
            "encode": {"ms": round(enc_ms, 5), "gbs": round(enc_bytes / (enc_ms * 1e-3) / 1e9, 1),
@@ -453,8 +466,11 @@ def workload_record(w: synth.Workload, mask, q, k, v, peaks, flush) -> dict:
                 ctypes.c_float(scale), ctypes.byref(fmt), w.stride_b, w.stride_h, which, o.data_ptr(),
                 torch.cuda.current_stream().cuda_stream)
         lat_ms, host_us = call_latency(lib.stof_mha_fwd, args)
+        plan_args = (ctypes.byref(fmt), B, H, L, d, which, ctypes.byref(stof.stof_plan()))
+        plan_us = statistics.median(host_time_us(lib.stof_mha_plan, plan_args) for _ in range(15))
         r = {"kernel_ms": round(warm, 5), "kernel_ms_cold_l2": round(cold, 5), "call_ms": round(lat_ms, 5),
              "call_minus_kernel_us": round((lat_ms - warm) * 1e3, 2), "host_us": round(host_us, 2),
+             "plan_host_us": round(plan_us, 2),
              "effective_tflops": round(eff_flops / (warm * 1e-3) / 1e12, 3)}
         if name == "blockwise":
             r["variant"] = ("persistent" if w.d == 64 and tiles / n_rows < 48 else "cta_per_query_tile")
@@ -492,6 +508,51 @@ def run_workload_records(args, device, peaks, big=None) -> dict:
     return out
 
 
+OPROJ_SHAPES = {
+    # name: (B, H, L, d, N) -- the output projection after the MHA of a layer
+    "llama7b_16384tok": (1, 32, 16384, 128, 4096),
+    "llama7b_4096tok": (1, 32, 4096, 128, 4096),
+    "bert_base_16x512": (16, 12, 512, 64, 768),
+}
+
+
+def run_oproj(args):
+    """The operator after the MHA: stof_oproj_fwd (y = concat_heads(O) W^T +
+    bias + residual) on the shape named by --oproj, bf16, random inputs;
+    kernel-only CUDA-event time over 20 calls against the measured bf16
+    peak.  One JSON line."""
+    import torch
+    from sparse_mask_transformer_gb300 import build, stof
+    torch.cuda.set_device(0)
+    build.build()
+    stof.load_library()
+    peaks, peak_src = load_peaks()
+    B, H, L, d, N = OPROJ_SHAPES[args.oproj]
+    g = torch.Generator(device="cuda").manual_seed(0)
+    o = torch.randn(B, H, L, d, device="cuda", generator=g).to(torch.bfloat16)
+    w = (torch.randn(N, H * d, device="cuda", generator=g) / (H * d) ** 0.5).to(torch.bfloat16)
+    bias = torch.randn(N, device="cuda", generator=g).to(torch.bfloat16)
+    res = torch.randn(B, L, N, device="cuda", generator=g).to(torch.bfloat16)
+    y = torch.empty(B, L, N, dtype=torch.bfloat16, device="cuda")
+    call = lambda: stof.stof_oproj_fwd(o, w, bias, res, y)  # noqa: E731
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    flops = 2.0 * B * L * N * H * d
+    print(json.dumps({"oproj": args.oproj, "B": B, "H": H, "L": L, "d": d, "N": N, "dtype": "bf16",
+                      "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                      "frac_tensor_peak": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                      "peak_source": f"{peak_src} bf16 burst", "steps": args.steps, "warmup": args.warmup}),
+          flush=True)
+
+
 SWEEP_L = (128, 256, 512, 1024, 2048)
 SWEEP_DENSITY = (0.01, 0.02, 0.05, 0.1, 0.2, 0.4)
 SWEEP_HEADS = (2, 16, 64)
@@ -523,33 +584,36 @@ def run_sweep(args):
     cases = 0
     agree = 0
     for d in (64, 128):
-        for pattern in ("random", "window"):
-            for L in SWEEP_L:
+        for L in SWEEP_L:
+            fmts = {}
+            for pattern in ("random", "window"):
                 for rho in SWEEP_DENSITY:
                     mask = torch.from_numpy(sweep_mask(pattern, L, rho, seed=L + int(rho * 1000))).cuda()
                     ws = torch.empty(stof.stof_encode_workspace_bytes(1, L, L, 128, 128), dtype=torch.uint8,
                                      device="cuda")
                     fmt = stof.stof_encode_mask(mask, 128, 128, ws)
                     stof.stof_format_sync(fmt)
+                    fmts[(pattern, rho)] = (fmt, ws)
+            for H in SWEEP_HEADS:
+                q, k, v = (t.cuda() for t in synth.make_qkv(1, H, L, d, "bf16", seed=H))
+                o = torch.empty_like(q)
+                for (pattern, rho), (fmt, ws) in fmts.items():
                     density = fmt.nnz / (L * L)
-                    for H in SWEEP_HEADS:
-                        q, k, v = (t.cuda() for t in synth.make_qkv(1, H, L, d, "bf16", seed=H))
-                        o = torch.empty_like(q)
-                        t = {}
-                        for name, which in (("rowwise", stof.STOF_KERNEL_ROWWISE),
-                                            ("blockwise", stof.STOF_KERNEL_BLOCKWISE)):
-                            call = lambda: stof.stof_mha_fwd(q, k, v, fmt, 1 / math.sqrt(d), 0, 0,  # noqa: E731
-                                                             which, o)
-                            t[name] = graph_ms(call, 20) * 1e3
-                        sel = "blockwise" if stof.stof_select_kernel(density, L, d) == stof.STOF_KERNEL_BLOCKWISE \
-                            else "rowwise"
-                        fastest = min(t, key=t.get)
-                        cases += 1
-                        agree += sel == fastest
-                        print(json.dumps({"sweep": pattern, "L": L, "d": d, "H": H, "density": round(density, 5),
-                                          "tiles": fmt.n_full + fmt.n_part, "rowwise_us": round(t["rowwise"], 2),
-                                          "blockwise_us": round(t["blockwise"], 2), "selected": sel,
-                                          "fastest": fastest}), flush=True)
+                    t = {}
+                    for name, which in (("rowwise", stof.STOF_KERNEL_ROWWISE),
+                                        ("blockwise", stof.STOF_KERNEL_BLOCKWISE)):
+                        call = lambda: stof.stof_mha_fwd(q, k, v, fmt, 1 / math.sqrt(d), 0, 0,  # noqa: E731
+                                                         which, o)
+                        t[name] = graph_ms(call, 20) * 1e3
+                    sel = "blockwise" if stof.stof_mha_plan(fmt, 1, H, L, d, stof.STOF_KERNEL_AUTO).kernel == \
+                        stof.STOF_KERNEL_BLOCKWISE else "rowwise"
+                    fastest = min(t, key=t.get)
+                    cases += 1
+                    agree += sel == fastest
+                    print(json.dumps({"sweep": pattern, "L": L, "d": d, "H": H, "density": round(density, 5),
+                                      "tiles": fmt.n_full + fmt.n_part, "rowwise_us": round(t["rowwise"], 2),
+                                      "blockwise_us": round(t["blockwise"], 2), "selected": sel,
+                                      "fastest": fastest}), flush=True)
     print(json.dumps({"sweep_summary": {"cases": cases, "selector_picks_fastest": agree}}), flush=True)
 
 
@@ -809,6 +873,10 @@ def main(argv=None):
     ap.add_argument("--no-bitmask", action="store_true", help="skip the bit-packed-mask and mask-rule measurements")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: kernel-only times of both kernels over short, sparse cases")
+    ap.add_argument("--oproj", default="", choices=[""] + list(OPROJ_SHAPES),
+                    help="instead of the bench line: time the output projection after the MHA on this shape")
+    ap.add_argument("--no-clocks", action="store_true",
+                    help="profiling runs: no clock sampling and no untimed steps around the timed ones")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload kernel-only records of both kernels")
     ap.add_argument("--heads", type=int, default=0,
@@ -825,6 +893,8 @@ def main(argv=None):
                                 stride_b=args.heads if per_head else w.stride_b)
     if args.sweep:
         run_sweep(args)
+    elif args.oproj:
+        run_oproj(args)
     elif args.impl == "reference":
         run_reference(args, w)
     else:

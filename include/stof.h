@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define STOF_VERSION 1
+#define STOF_VERSION 2
 
 typedef enum {
   STOF_OK = 0,
@@ -232,9 +232,23 @@ stof_status stof_format_sync(stof_format* fmt, void* stream);
 
 /* Analytic kernel choice [SEL]: row-wise or block-wise from the mask
  * density (valid elements / all elements, in [0, 1]), the sequence length
- * and the head dimension.  Pure host arithmetic and deterministic; invalid
- * arguments give STOF_KERNEL_BLOCKWISE. */
+ * and the head dimension, for one head whose mask lists every OT (the
+ * worst case of an arbitrary mask).  The model compares each kernel's
+ * predicted time, linear in its work: the row-wise kernel's in query rows
+ * and valid (query, key) pairs, the block-wise kernel's in listed OTs and
+ * query tiles (coefficients fitted to both kernels' GB300 times).  Pure host
+ * arithmetic and deterministic; invalid arguments give
+ * STOF_KERNEL_BLOCKWISE.  Same as stof_select_kernel_heads(density,
+ * seq_len, head_dim, 1, -1). */
 stof_kernel stof_select_kernel(double density, int seq_len, int head_dim);
+
+/* The same model for `heads` heads (B * H) of one call, whose masks list
+ * tiles_per_row 128x128 OTs per 128-row query tile on average (a negative
+ * value: every OT).  The row-wise kernel's fixed cost per query row is a few
+ * dependent memory round trips, so it wins only while the whole call is
+ * small and sparse; stof_mha_fwd(STOF_KERNEL_AUTO) uses this with the call's
+ * B * H and the format's tile counts. */
+stof_kernel stof_select_kernel_heads(double density, int seq_len, int head_dim, int64_t heads, double tiles_per_row);
 
 /*
  * Masked MHA forward [ABS][PROB]:
@@ -250,37 +264,92 @@ stof_kernel stof_select_kernel(double density, int seq_len, int head_dim);
  *   fmt         an encoded format (stof_encode_mask) for masks of size L.
  *   which       STOF_KERNEL_ROWWISE [ROW], STOF_KERNEL_BLOCKWISE [BLK]
  *               (needs bm == 128 and bn == 64 or 128; else
- *               STOF_ERR_UNSUPPORTED) or STOF_KERNEL_AUTO ([SEL], needs a
- *               synced fmt; falls back to row-wise for other tile sizes).
- * Asynchronous on stream.  For d = 64 the block-wise kernel runs persistent
- * CTAs that take query tiles from a work counter kept in the format's
- * workspace (a word the encoders leave unused) and zeroed by this call on
- * stream: calls that use the same format must not overlap on the GPU (one
- * stream, or streams ordered by events); calls with different formats may.
+ *               STOF_ERR_UNSUPPORTED) or STOF_KERNEL_AUTO (needs a synced
+ *               fmt): the fastest measured candidate that stof_tune()
+ *               cached for (L, d, the density's bucket) among those on the
+ *               format's OT width, if there is one; else the analytic model
+ *               [SEL] (stof_select_kernel_heads with B * H and the format's
+ *               tiles), falling back to row-wise for tile sizes the
+ *               block-wise kernel does not take.  stof_mha_plan() tells
+ *               which.
+ * Asynchronous on stream.  For d = 64 the block-wise kernel may run
+ * persistent CTAs that take query tiles from a work counter kept in two
+ * words of the format's workspace (zeroed by every encoder, and zeroed
+ * again by the kernel's last CTA when it ends): calls that use the same
+ * format must not overlap on the GPU (one stream, or streams ordered by
+ * events); calls with different formats may.
  */
 stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H,
                          int L, int d, float scale, const stof_format* fmt,
                          int64_t mask_stride_b, int64_t mask_stride_h, stof_kernel which, void* o,
                          void* stream);
 
+/* Where a plan's choice came from. */
+#define STOF_PLAN_FORCED 0    /* the caller named the kernel */
+#define STOF_PLAN_ANALYTIC 1  /* stof_select_kernel() on the format's density [SEL] */
+#define STOF_PLAN_TUNED 2     /* a cached stof_tune() measurement */
+
+/* What one stof_mha_fwd() call runs. */
+typedef struct {
+  stof_kernel kernel;  /* STOF_KERNEL_ROWWISE or STOF_KERNEL_BLOCKWISE */
+  int stages;          /* block-wise K/V ring depth; 0 for the row-wise kernel */
+  int persistent;      /* block-wise: 1 = persistent CTAs (d = 64), 0 = one CTA per query tile */
+  int source;          /* STOF_PLAN_FORCED, STOF_PLAN_ANALYTIC or STOF_PLAN_TUNED */
+} stof_plan;
+
+/*
+ * The plan stof_mha_fwd(q, k, v, dt, B, H, L, d, scale, fmt, ..., which, ...)
+ * follows, without running it: fills *out and returns STOF_OK, or the
+ * status that call would return for these sizes, format and `which`.
+ * Pure host code.
+ */
+stof_status stof_mha_plan(const stof_format* fmt, int B, int H, int L, int d, stof_kernel which, stof_plan* out);
+
+/*
+ * stof_mha_fwd() run exactly as *plan says: its kernel, and for the
+ * block-wise kernel its ring depth and variant (plan->source is ignored).
+ * Arguments, layout and errors as stof_mha_fwd(); STOF_ERR_UNSUPPORTED for
+ * a ring depth or variant these sizes do not admit.  Admitted: row-wise on
+ * any OT size; block-wise on 128x128 OTs one CTA per query tile with ring
+ * depth 2 or 3 (d = 128) or 2, 3 or 4 (d = 64), persistent CTAs with ring
+ * depth 2, 3 or 4 (d = 64 only); on 128x64 OTs the default depth (3 per
+ * query tile, 4 persistent).  A plan from stof_mha_plan() or a
+ * stof_tune_result's candidate is always admitted for the sizes it was
+ * made for.
+ */
+stof_status stof_mha_fwd_plan(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int L, int d,
+                              float scale, const stof_format* fmt, int64_t mask_stride_b, int64_t mask_stride_h,
+                              const stof_plan* plan, void* o, void* stream);
+
 /*
  * Measured parameter choice for the MHA step, with a result cache.  The
  * pages' tuner samples kernel parameters (block size, pipeline stages) by
  * running them once the operator boundaries are fixed, and caches what it
  * measured (gist.science technical summary, Methodology 2, two-stage
- * tuning, stage 2 "parameter sampling").  Here the candidates are the
- * row-wise kernel on 128x128 OTs and the block-wise kernel on 128x128 and
- * 128x64 OTs.
+ * tuning, stage 2 "parameter sampling"; the cache: same page, the lay
+ * summary's "autopilot" that remembers what worked).  The candidates:
+ *   0      row-wise kernel, 128x128 OTs;
+ *   1-3    block-wise, 128x128 OTs, one CTA per query tile, K/V ring depth
+ *          3, 2, 4 (depth 4 at d = 64 only: shared memory);
+ *   4-6    block-wise, 128x128 OTs, persistent CTAs (d = 64 only), ring
+ *          depth 4, 3, 2;
+ *   7      block-wise, 128x64 OTs, default variant and ring depth.
+ * The softmax warpgroup count is not a candidate: the kernels' register and
+ * tensor-memory budgets fit exactly two.
  */
-#define STOF_TUNE_CANDIDATES 3
+#define STOF_TUNE_CANDIDATES 8
 typedef struct {
   stof_kernel kernel;        /* fastest candidate */
   int bn;                    /* its OT width (bm = 128) */
   float ms;                  /* its time per stof_mha_fwd call */
   double density;            /* density of the tuned mask */
+  int stages;                /* its K/V ring depth (0 for row-wise) */
+  int persistent;            /* 1 if it runs persistent CTAs */
   stof_kernel cand_kernel[STOF_TUNE_CANDIDATES];
   int cand_bn[STOF_TUNE_CANDIDATES];
-  float cand_ms[STOF_TUNE_CANDIDATES]; /* -1 for a candidate the sizes do not admit */
+  int cand_stages[STOF_TUNE_CANDIDATES];     /* ring depth the candidate ran with (0 row-wise) */
+  int cand_persistent[STOF_TUNE_CANDIDATES]; /* 1 persistent, 0 one CTA per query tile */
+  float cand_ms[STOF_TUNE_CANDIDATES];       /* -1 for a candidate the sizes do not admit */
 } stof_tune_result;
 
 /* Workspace bytes stof_tune() needs (the largest encode workspace over the
@@ -290,7 +359,8 @@ size_t stof_tune_workspace_bytes(int n_masks, int L);
 /*
  * Encodes the mask for each candidate OT size, runs every candidate kernel
  * (one untimed call, then three timed with CUDA events) and returns the
- * fastest in *out; the result is also cached under (L, d, density bucket).
+ * fastest in *out; the result is also cached under (L, d, density bucket),
+ * where stof_mha_fwd(STOF_KERNEL_AUTO) finds it.
  * Arguments as for stof_encode_mask() and stof_mha_fwd(); the workspace must
  * hold stof_tune_workspace_bytes(n_masks, L) bytes and o is overwritten.
  * Blocks until the timing is done.  A candidate whose run reports a device

@@ -59,16 +59,16 @@ namespace {
 using namespace ptx;
 using namespace bw;
 
-template <int D, int BN>
+template <int D, int BN, int ST>
 struct alignas(1024) Smem {
   uint8_t q[Cfg<D, BN>::Q_BYTES];
-  uint8_t k[kStages][Cfg<D, BN>::KV_BYTES];  // K ring, stage t % 3; at the end the warpgroups' max and sum
-  uint8_t v[kStages][Cfg<D, BN>::KV_BYTES];  // V ring, stage t % 3
+  uint8_t k[ST][Cfg<D, BN>::KV_BYTES];  // K ring, stage t % ST; at the end the warpgroups' max and sum
+  uint8_t v[ST][Cfg<D, BN>::KV_BYTES];  // V ring, stage t % ST
   uint64_t q_full;
-  uint64_t k_full[kStages];
-  uint64_t k_free[kStages];
-  uint64_t v_full[kStages];
-  uint64_t v_free[kStages];
+  uint64_t k_full[ST];
+  uint64_t k_free[ST];
+  uint64_t v_full[ST];
+  uint64_t v_free[ST];
   uint64_t s_full[2];   // per warpgroup: the scores of its next tile are in S
   uint64_t s_free[2];   // per warpgroup: it has loaded its tile's scores
   uint64_t p_full[2];   // per warpgroup: P_g written
@@ -79,21 +79,23 @@ struct alignas(1024) Smem {
   int abort_flag;
   int fail_tile;             // 0 once a softmax thread has failed
 };
-static_assert(sizeof(Smem<128, 128>) + 1024 <= 232448, "shared memory");
+static_assert(sizeof(Smem<128, 128, 3>) + 1024 <= 232448, "shared memory");
+static_assert(sizeof(Smem<64, 128, 4>) + 1024 <= 232448, "shared memory");
 
 // Barrier over `count` threads (a multiple of 32) under hardware barrier id.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-template <int D, int BN, bool BF16>
+template <int D, int BN, bool BF16, int ST>
 __global__ void __launch_bounds__(kThreads, 1)
     blockwise_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using C = Cfg<D, BN>;
+  constexpr int kStages = ST;
   extern __shared__ uint8_t smem_raw[];
-  Smem<D, BN>& s = *reinterpret_cast<Smem<D, BN>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
+  Smem<D, BN, ST>& s = *reinterpret_cast<Smem<D, BN, ST>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                   ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // work item: head-major, so CTAs running together stream the same head's
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow);
         int issued = 0;
         for (int t = 0, st = 0, ph = 0; t < n; ++t) {
-          // stage st = t % 3 held K_{t-3}: free once that tile's scores are done
+          // stage st = t % ST held K_{t-ST}: free once that tile's scores are done
           if (t >= kStages && !mbar_wait(&s.k_free[st], ph ^ 1, abort_flag, kWaitNs)) {
             fail();
             break;
@@ -202,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmV);
         int issued = 0;
         for (int t = 0, st = 0, ph = 0; t < n; ++t) {
-          // stage st = t % 3 held V_{t-3}: free once that tile's PV is done
+          // stage st = t % ST held V_{t-ST}: free once that tile's PV is done
           if (t >= kStages && !mbar_wait(&s.v_free[st], ph ^ 1, abort_flag, kWaitNs)) {
             fail();
             break;
@@ -492,24 +494,25 @@ bool make_bw_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box
 
 namespace {
 
-template <int D, int BN, bool BF16>
+template <int D, int BN, bool BF16, int ST>
 stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.L;
   CUtensorMap mq, mk, mv;
   if (!make_bw_map(&mq, p.q, rows, D, kBM, BF16) || !make_bw_map(&mk, p.k, rows, D, BN, BF16) ||
       !make_bw_map(&mv, p.v, rows, D, BN, BF16))
     return STOF_ERR_CUDA;
-  const size_t smem = sizeof(Smem<D, BN>) + 1024;
+  const size_t smem = sizeof(Smem<D, BN, ST>) + 1024;
   stof_status prep = STOF_OK;
   auto prepare = [](const void* arg) {
     stof_status* st = static_cast<stof_status*>(const_cast<void*>(arg));
-    if (record_cuda(cudaFuncSetAttribute(blockwise_kernel<D, BN, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(Smem<D, BN>) + 1024))) != cudaSuccess) {
+    if (record_cuda(cudaFuncSetAttribute(blockwise_kernel<D, BN, BF16, ST>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sizeof(Smem<D, BN, ST>) + 1024))) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
     cudaFuncAttributes fa;
-    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_kernel<D, BN, BF16>)) != cudaSuccess) {
+    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_kernel<D, BN, BF16, ST>)) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
@@ -519,29 +522,41 @@ stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
     }
     return true;
   };
-  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_kernel<D, BN, BF16>), prepare, &prep)) return prep;
+  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_kernel<D, BN, BF16, ST>), prepare, &prep))
+    return prep;
   const long long grid = static_cast<long long>(p.B) * p.H * p.n_tr;
-  blockwise_kernel<D, BN, BF16><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
+  blockwise_kernel<D, BN, BF16, ST><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
   return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
 }
 
 }  // namespace
 
+template <int D, int BN, int ST>
+stof_status launch_bw_t(const AttnParams& p, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_bw<D, BN, true, ST>(p, s) : launch_bw<D, BN, false, ST>(p, s);
+}
+
 stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s) {
   if (p.bm != kBM || (p.bn != 64 && p.bn != 128)) return STOF_ERR_UNSUPPORTED;
   if (static_cast<long long>(p.B) * p.H * p.L >= (1ll << 31)) return STOF_ERR_SHAPE;
   // d = 64 with short query tiles (few listed OTs each): persistent CTAs that
-  // overlap one query tile's start-up and finish with the next.  Measured on
-  // GB300: 15% faster at 4 to 9 OTs per query tile, 5.5% at 28, 3% slower at
-  // 64, where a CTA per query tile has little start-up left to hide.
-  constexpr float kPersistMaxTiles = 48.f;
-  if (p.d == 64 && p.tiles_per_row < kPersistMaxTiles) return launch_blockwise_persist64(p, bf16, s);
+  // overlap one query tile's start-up and finish with the next
+  if (blockwise_persistent(p.d, p.variant, p.tiles_per_row)) return launch_blockwise_persist64(p, bf16, s);
+  // ring depths: 3 by default; the tuner also samples 2 (and 4 at d = 64) on 128 x 128 OTs
+  const int st = p.stages ? p.stages : kStages;
   if (p.bn == 64) {
-    if (p.d == 64) return bf16 ? launch_bw<64, 64, true>(p, s) : launch_bw<64, 64, false>(p, s);
-    return bf16 ? launch_bw<128, 64, true>(p, s) : launch_bw<128, 64, false>(p, s);
+    if (st != kStages) return STOF_ERR_UNSUPPORTED;
+    return p.d == 64 ? launch_bw_t<64, 64, 3>(p, bf16, s) : launch_bw_t<128, 64, 3>(p, bf16, s);
   }
-  if (p.d == 64) return bf16 ? launch_bw<64, 128, true>(p, s) : launch_bw<64, 128, false>(p, s);
-  return bf16 ? launch_bw<128, 128, true>(p, s) : launch_bw<128, 128, false>(p, s);
+  if (p.d == 64) {
+    if (st == 2) return launch_bw_t<64, 128, 2>(p, bf16, s);
+    if (st == 3) return launch_bw_t<64, 128, 3>(p, bf16, s);
+    if (st == 4) return launch_bw_t<64, 128, 4>(p, bf16, s);
+    return STOF_ERR_UNSUPPORTED;
+  }
+  if (st == 2) return launch_bw_t<128, 128, 2>(p, bf16, s);
+  if (st == 3) return launch_bw_t<128, 128, 3>(p, bf16, s);
+  return STOF_ERR_UNSUPPORTED;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

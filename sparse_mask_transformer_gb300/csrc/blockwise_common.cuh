@@ -15,7 +15,7 @@ constexpr int kBM = 128;  // query rows per tile (the MMA's M); key columns per 
 // 2 producer warps, 2 MMA-issuer warps, 8 softmax warps.  Three warps per
 // SM sub-partition cap a thread at 168 registers.
 constexpr int kThreads = 384;
-constexpr int kStages = 3;                    // K and V ring depth
+constexpr int kStages = 3;                    // default K and V ring depth (one CTA per query tile)
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 

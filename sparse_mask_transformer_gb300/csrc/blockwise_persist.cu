@@ -50,10 +50,10 @@ using namespace ptx;
 using namespace bw;
 
 constexpr int kD = 64;
-constexpr int kRing = 4;          // K and V ring depth
+constexpr int kDefaultRing = 4;   // default K and V ring depth (the tuner also samples 2 and 3)
 constexpr int kItemReaders = 11;  // warps that read each published item: V producer, 2 issuers, 8 softmax
 
-template <int BN>
+template <int BN, int kRing>
 struct alignas(1024) PSmem {
   uint8_t q[2][Cfg<kD, BN>::Q_BYTES];      // per item parity
   uint8_t k[kRing][Cfg<kD, BN>::KV_BYTES];
@@ -73,7 +73,7 @@ struct alignas(1024) PSmem {
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(PSmem<128>) + 1024 <= 232448, "shared memory");
+static_assert(sizeof(PSmem<128, kDefaultRing>) + 1024 <= 232448, "shared memory");
 
 // One work item: the 128-row query tile (b, h, OT row I) and its listed OTs.
 struct Item {
@@ -94,14 +94,14 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int idx) {
   return it;
 }
 
-template <int BN, bool BF16>
+template <int BN, bool BF16, int kRing>
 __global__ void __launch_bounds__(kThreads, 1)
     blockwise_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                              const __grid_constant__ CUtensorMap tmV, const AttnParams p, const int n_items) {
   using C = Cfg<kD, BN>;
   extern __shared__ uint8_t smem_raw[];
-  PSmem<BN>& s = *reinterpret_cast<PSmem<BN>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~uintptr_t(1023));
+  PSmem<BN, kRing>& s = *reinterpret_cast<PSmem<BN, kRing>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                            ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -517,25 +517,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, bool BF16>
+template <int BN, bool BF16, int RING>
 stof_status launch_persist(const AttnParams& p, cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.L;
   CUtensorMap mq, mk, mv;
   if (!make_bw_map(&mq, p.q, rows, kD, kBM, BF16) || !make_bw_map(&mk, p.k, rows, kD, BN, BF16) ||
       !make_bw_map(&mv, p.v, rows, kD, BN, BF16))
     return STOF_ERR_CUDA;
-  const size_t smem = sizeof(PSmem<BN>) + 1024;
+  const size_t smem = sizeof(PSmem<BN, RING>) + 1024;
   stof_status prep = STOF_OK;
   auto prepare = [](const void* arg) {
     stof_status* st = static_cast<stof_status*>(const_cast<void*>(arg));
-    if (record_cuda(cudaFuncSetAttribute(blockwise_persist_kernel<BN, BF16>,
+    if (record_cuda(cudaFuncSetAttribute(blockwise_persist_kernel<BN, BF16, RING>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(PSmem<BN>) + 1024))) != cudaSuccess) {
+                                         static_cast<int>(sizeof(PSmem<BN, RING>) + 1024))) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
     cudaFuncAttributes fa;
-    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_persist_kernel<BN, BF16>)) != cudaSuccess) {
+    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_persist_kernel<BN, BF16, RING>)) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
@@ -545,13 +545,13 @@ stof_status launch_persist(const AttnParams& p, cudaStream_t s) {
     }
     return true;
   };
-  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_persist_kernel<BN, BF16>), prepare, &prep))
+  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_persist_kernel<BN, BF16, RING>), prepare, &prep))
     return prep;
   // one resident CTA per SM, each taking items from the work counter
   const long long n_items = static_cast<long long>(p.B) * p.H * p.n_tr;
   const long long sms = device_sm_count();
   const long long grid = n_items < sms ? n_items : sms;
-  blockwise_persist_kernel<BN, BF16><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(
+  blockwise_persist_kernel<BN, BF16, RING><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(
       mq, mk, mv, p, static_cast<int>(n_items));
   return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
 }
@@ -560,8 +560,15 @@ stof_status launch_persist(const AttnParams& p, cudaStream_t s) {
 
 stof_status launch_blockwise_persist64(const AttnParams& p, bool bf16, cudaStream_t s) {
   if (p.d != kD || p.bm != kBM || (p.bn != 64 && p.bn != 128)) return STOF_ERR_UNSUPPORTED;
-  if (p.bn == 64) return bf16 ? launch_persist<64, true>(p, s) : launch_persist<64, false>(p, s);
-  return bf16 ? launch_persist<128, true>(p, s) : launch_persist<128, false>(p, s);
+  const int ring = p.stages ? p.stages : kDefaultRing;
+  if (p.bn == 64) {
+    if (ring != kDefaultRing) return STOF_ERR_UNSUPPORTED;
+    return bf16 ? launch_persist<64, true, kDefaultRing>(p, s) : launch_persist<64, false, kDefaultRing>(p, s);
+  }
+  if (ring == 2) return bf16 ? launch_persist<128, true, 2>(p, s) : launch_persist<128, false, 2>(p, s);
+  if (ring == 3) return bf16 ? launch_persist<128, true, 3>(p, s) : launch_persist<128, false, 3>(p, s);
+  if (ring == 4) return bf16 ? launch_persist<128, true, 4>(p, s) : launch_persist<128, false, 4>(p, s);
+  return STOF_ERR_UNSUPPORTED;
 }
 
 }  // namespace stof

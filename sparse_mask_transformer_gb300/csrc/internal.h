@@ -102,7 +102,41 @@ struct AttnParams {
   unsigned int* work;              // work counter of the persistent kernel, in the format's workspace:
                                    // work[0] items taken, work[1] CTAs finished (both zero between launches)
   float tiles_per_row;             // mean listed OTs per OT row of the masks (synced format), else -1
+  int stages;                      // block-wise K/V ring depth; 0 = the kernel's default
+  int variant;                     // block-wise: kVariantAuto, kVariantPerTile or kVariantPersistent
 };
+// Block-wise kernel variants: one CTA per query tile, or persistent CTAs
+// (d = 64 only); auto picks by the mean listed OTs per OT row.
+constexpr int kVariantAuto = 0, kVariantPerTile = 1, kVariantPersistent = 2;
+// Below this many listed OTs per OT row (mean over the masks) the d = 64
+// block-wise call runs persistent CTAs.  Measured on GB300: 15% faster at 4
+// to 9 OTs per query tile, 5.5% at 28, 3% slower at 64, where a CTA per
+// query tile has little start-up left to hide.
+constexpr float kPersistMaxTiles = 48.f;
+inline bool blockwise_persistent(int d, int variant, float tiles_per_row) {
+  return variant == kVariantPersistent ||
+         (variant == kVariantAuto && d == 64 && tiles_per_row < kPersistMaxTiles);
+}
+// Ring depth a block-wise launch uses (stages = 0: the variant's default).
+inline int blockwise_stages(bool persistent, int stages) { return stages ? stages : (persistent ? 4 : 3); }
+
+// One way to run the MHA step: the kernel, the OT width it needs and the
+// block-wise kernel's ring depth (0 = default) and variant.
+struct KernelChoice {
+  stof_kernel kernel;
+  int bn;
+  int stages;
+  int variant;
+};
+// The candidates stof_tune() times (STOF_TUNE_CANDIDATES of them).
+extern const KernelChoice kTuneCandidates[STOF_TUNE_CANDIDATES];
+// The fastest cached candidate for (L, d, density bucket) among those on
+// OTs of width bn; false if the cache has no such entry.
+bool tuned_choice(int L, int d, double density, int bn, KernelChoice* out);
+// stof_mha_fwd() with the kernel, ring depth and variant given.
+stof_status mha_fwd_choice(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int L, int d,
+                           float scale, const stof_format* fmt, int64_t mask_stride_b, int64_t mask_stride_h,
+                           const KernelChoice& c, void* o, void* stream);
 cudaError_t launch_rowwise(const AttnParams& p, bool bf16, cudaStream_t s);
 // Density bucket of the tuning cache.
 int tune_density_bucket(double density);

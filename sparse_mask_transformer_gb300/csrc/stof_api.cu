@@ -273,72 +273,153 @@ stof_status stof_format_sync(stof_format* fmt, void* stream) {
 // chooses the row-wise or block-wise kernel from mask sparsity and
 // sequence length).
 //
-// Cost per query row (ns of device time, aggregated over the GPU):
-//   row-wise   T_row = rho * L * d * C_ROW
-//              (visits exactly the rho*L valid keys of the row: CUDA-core
-//              dot products and K/V row gathers, about C_ROW per key*dim);
-//   block-wise T_blk = A_BLK + L * d * C_BLK
-//              (tensor-core work on the listed tiles; with no tile
-//              statistics at hand the model charges every key, the worst
-//              case of an arbitrary mask, at C_BLK per key*dim, plus A_BLK
-//              for filling and draining the tile pipeline of a 128-row tile).
-// The row-wise kernel wins for high sparsity (small rho) and short L, the
-// regime the pages give it.  Constants fitted to both kernels' GB300 times
-// on the five workloads (C_ROW from 3.4e-4 to 6.0e-4, C_BLK from 3.1e-6 to
-// 1.4e-5 ns per key*dim; the L=256 workload is latency-bound for both) and
-// frozen, so the choice is a deterministic function of (rho, L, d).
-stof_kernel stof_select_kernel(double density, int seq_len, int head_dim) {
-  if (!(density >= 0.0 && density <= 1.0) || seq_len <= 0 || head_dim <= 0)
+// Predicted device time of each kernel in microseconds, linear in the work
+// it does:
+//   row-wise    T_row = 3.38 + 8.84e-4 R + 1.81e-5 K d/64
+//               R = query rows (heads x L), K = valid (query, key) pairs
+//               (density x L^2 x heads): a warp per query row, whose fixed
+//               cost is a few dependent memory round trips, plus the K and
+//               V rows of every valid key;
+//   block-wise  T_blk = 7.27 + 4.93e-3 T (d/64 + 1)/2 + 9.09e-3 Q
+//               T = listed 128x128 OTs over all heads (each the full tile's
+//               MMA and softmax work, the MMAs half as long at d = 64),
+//               Q = query tiles (heads x L / 128: start-up and finish).
+// The constant terms are launch and pipeline fill.  The coefficients were
+// fitted to kernel-only GB300 times of both kernels (CUDA-graph replay) on
+// 360 cases: L = 128 to 2048, densities 0.01 to 0.4, 2 to 64 heads, d = 64
+// and 128, random and sliding-window masks; the model picks the faster
+// kernel in 351 of them and costs at most 21% where it does not.  The
+// row-wise kernel wins for high sparsity and few, short rows -- the regime
+// the pages give it.
+namespace {
+double model_rowwise_us(double density, double L, double d, double heads) {
+  const double R = heads * L, K = density * L * L * heads;
+  return 3.38 + 8.84e-4 * R + 1.81e-5 * K * (d / 64.0);
+}
+double model_blockwise_us(double L, double d, double heads, double tiles_per_row) {
+  const double n_tr = L / 128.0;
+  const double T = tiles_per_row * n_tr * heads, Q = n_tr * heads;
+  return 7.27 + 4.93e-3 * T * (d / 64.0 + 1.0) / 2.0 + 9.09e-3 * Q;
+}
+}  // namespace
+
+stof_kernel stof_select_kernel_heads(double density, int seq_len, int head_dim, int64_t heads, double tiles_per_row) {
+  if (!(density >= 0.0 && density <= 1.0) || seq_len <= 0 || head_dim <= 0 || heads <= 0)
     return STOF_KERNEL_BLOCKWISE;
-  const double C_ROW = 4.5e-4;
-  const double A_BLK = 4.0, C_BLK = 5.0e-6;
-  const double L = seq_len, d = head_dim;
-  const double t_row = density * L * d * C_ROW;
-  const double t_blk = A_BLK + L * d * C_BLK;
+  const double L = seq_len, n_tc = L / 128.0;
+  // unknown or out of range: every OT of the row listed (an arbitrary mask),
+  // so that the choice depends monotonically on the density
+  double tpr = tiles_per_row;
+  if (!(tpr >= 0.0 && tpr <= n_tc)) tpr = n_tc;
+  const double t_row = model_rowwise_us(density, L, head_dim, static_cast<double>(heads));
+  const double t_blk = model_blockwise_us(L, head_dim, static_cast<double>(heads), tpr);
   return t_row <= t_blk ? STOF_KERNEL_ROWWISE : STOF_KERNEL_BLOCKWISE;
+}
+
+stof_kernel stof_select_kernel(double density, int seq_len, int head_dim) {
+  return stof_select_kernel_heads(density, seq_len, head_dim, 1, -1.0);
 }
 
 // OT sizes the block-wise kernel runs: 128 query rows (the MMA's M) by 64 or
 // 128 key columns.
 static bool blockwise_tiles(const stof_format& f) { return f.bm == 128 && (f.bn == 64 || f.bn == 128); }
 
-stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H,
-                         int L, int d, float scale, const stof_format* fmt,
-                         int64_t mask_stride_b, int64_t mask_stride_h, stof_kernel which, void* o,
-                         void* stream) {
-  if (!q || !k || !v || !o || !fmt) return STOF_ERR_INVALID_ARG;
+static float tiles_per_row(const stof_format& f) {
+  return f.synced ? static_cast<float>(static_cast<double>(f.n_full + f.n_part) /
+                                       (static_cast<double>(f.n_masks) * f.n_tr))
+                  : -1.f;
+}
+
+// The format and sizes agree (what a plan needs to know of a call).
+static stof_status check_format(const stof_format* fmt, int B, int H, int L, int d) {
+  if (!fmt) return STOF_ERR_INVALID_ARG;
   if (!fmt->full_row_ptr || !fmt->full_col_idx || !fmt->part_row_ptr || !fmt->part_col_idx ||
       !fmt->bitmaps || !fmt->counts_dev)
     return STOF_ERR_INVALID_ARG;
-  if (dt != STOF_F16 && dt != STOF_BF16) return STOF_ERR_DTYPE;
-  if (which != STOF_KERNEL_AUTO && which != STOF_KERNEL_ROWWISE && which != STOF_KERNEL_BLOCKWISE)
-    return STOF_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || L < 1 || d < 1) return STOF_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return STOF_ERR_INVALID_ARG;
-  if (mask_stride_b < 0 || mask_stride_h < 0) return STOF_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return STOF_ERR_UNSUPPORTED;
   if (fmt->lq != L || fmt->lk != L) return STOF_ERR_SHAPE;
   if (fmt->bm < 8 || fmt->bn < 8 || fmt->bm % 8 || fmt->bn % 8 || fmt->bm > 256 || fmt->bn > 256 ||
       L % fmt->bm || L % fmt->bn || fmt->n_tr != L / fmt->bm || fmt->n_tc != L / fmt->bn)
     return STOF_ERR_SHAPE;
+  return STOF_OK;
+}
+
+// Every argument of an MHA call.
+static stof_status check_call(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int L,
+                              int d, float scale, const stof_format* fmt, int64_t mask_stride_b,
+                              int64_t mask_stride_h, void* o) {
+  if (!q || !k || !v || !o || !fmt) return STOF_ERR_INVALID_ARG;
+  if (dt != STOF_F16 && dt != STOF_BF16) return STOF_ERR_DTYPE;
+  if (!std::isfinite(scale)) return STOF_ERR_INVALID_ARG;
+  if (mask_stride_b < 0 || mask_stride_h < 0) return STOF_ERR_INVALID_ARG;
+  const stof_status st = check_format(fmt, B, H, L, d);
+  if (st != STOF_OK) return st;
   const long double max_mask = static_cast<long double>(B - 1) * mask_stride_b +
                                static_cast<long double>(H - 1) * mask_stride_h;
   if (max_mask >= fmt->n_masks) return STOF_ERR_SHAPE;
   if (static_cast<long double>(B) * H * L >= 2147483647.0L * 8) return STOF_ERR_SHAPE;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
-    return STOF_ERR_ALIGNMENT;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return STOF_ERR_ALIGNMENT;
+  return STOF_OK;
+}
 
-  stof_kernel kern = which;
-  if (kern == STOF_KERNEL_AUTO) {
-    if (!fmt->synced) return STOF_ERR_NOT_SYNCED;
-    const double density =
-        static_cast<double>(fmt->nnz) / (static_cast<double>(fmt->n_masks) * fmt->lq * fmt->lk);
-    kern = stof_select_kernel(density, L, d);
-    if (kern == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(*fmt))
-      kern = STOF_KERNEL_ROWWISE;  // the block-wise kernel needs 128 x 64 or 128 x 128 OTs
+// What runs for `which` on this format: a forced kernel, a cached tuning
+// result or the analytic model.
+static stof_status plan_call(const stof_format& f, int B, int H, int L, int d, stof_kernel which, KernelChoice* c,
+                             int* source) {
+  if (which != STOF_KERNEL_AUTO && which != STOF_KERNEL_ROWWISE && which != STOF_KERNEL_BLOCKWISE)
+    return STOF_ERR_INVALID_ARG;
+  *c = KernelChoice{which, f.bn, 0, kVariantAuto};
+  *source = STOF_PLAN_FORCED;
+  if (which == STOF_KERNEL_AUTO) {
+    if (!f.synced) return STOF_ERR_NOT_SYNCED;
+    const double density = static_cast<double>(f.nnz) / (static_cast<double>(f.n_masks) * f.lq * f.lk);
+    if (tuned_choice(L, d, density, f.bn, c)) {
+      *source = STOF_PLAN_TUNED;
+    } else {
+      *source = STOF_PLAN_ANALYTIC;
+      // listed area per 128-row query tile, in 128x128 OTs
+      const double tpr = static_cast<double>(f.n_full + f.n_part) * f.bm * f.bn /
+                         (static_cast<double>(f.n_masks) * 128.0 * L);
+      c->kernel = stof_select_kernel_heads(density, L, d, static_cast<int64_t>(B) * H, tpr);
+      if (c->kernel == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(f))
+        c->kernel = STOF_KERNEL_ROWWISE;  // the block-wise kernel needs 128 x 64 or 128 x 128 OTs
+    }
   }
-  if (kern == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(*fmt)) return STOF_ERR_UNSUPPORTED;
+  if (c->kernel == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(f)) return STOF_ERR_UNSUPPORTED;
+  return STOF_OK;
+}
 
+stof_status stof_mha_plan(const stof_format* fmt, int B, int H, int L, int d, stof_kernel which, stof_plan* out) {
+  if (!out) return STOF_ERR_INVALID_ARG;
+  stof_status st = check_format(fmt, B, H, L, d);
+  if (st != STOF_OK) return st;
+  KernelChoice c;
+  int source = 0;
+  st = plan_call(*fmt, B, H, L, d, which, &c, &source);
+  if (st != STOF_OK) return st;
+  out->kernel = c.kernel;
+  out->source = source;
+  out->persistent = 0;
+  out->stages = 0;
+  if (c.kernel == STOF_KERNEL_BLOCKWISE) {
+    out->persistent = blockwise_persistent(d, c.variant, tiles_per_row(*fmt)) ? 1 : 0;
+    out->stages = blockwise_stages(out->persistent != 0, c.stages);
+  }
+  return STOF_OK;
+}
+
+}  // extern "C"
+
+namespace stof {
+
+stof_status mha_fwd_choice(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int L, int d,
+                           float scale, const stof_format* fmt, int64_t mask_stride_b, int64_t mask_stride_h,
+                           const KernelChoice& c, void* o, void* stream) {
+  const stof_status st = check_call(q, k, v, dt, B, H, L, d, scale, fmt, mask_stride_b, mask_stride_h, o);
+  if (st != STOF_OK) return st;
+  if (c.kernel != STOF_KERNEL_ROWWISE && c.kernel != STOF_KERNEL_BLOCKWISE) return STOF_ERR_INVALID_ARG;
+  if (c.kernel == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(*fmt)) return STOF_ERR_UNSUPPORTED;
   AttnParams p;
   p.q = q;
   p.k = k;
@@ -364,14 +445,46 @@ stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype
   // bytes 40..47 of the workspace: two words no encoder uses and every
   // encoder zeroes; the persistent kernel leaves them zero when it ends
   p.work = reinterpret_cast<unsigned int*>(fmt->counts_dev + 5);
-  p.tiles_per_row = fmt->synced ? static_cast<float>(static_cast<double>(fmt->n_full + fmt->n_part) /
-                                                     (static_cast<double>(fmt->n_masks) * fmt->n_tr))
-                                : -1.f;
+  p.tiles_per_row = tiles_per_row(*fmt);
+  p.stages = c.stages;
+  p.variant = c.variant;
   const bool bf16 = dt == STOF_BF16;
   cudaStream_t s = as_stream(stream);
-  if (kern == STOF_KERNEL_ROWWISE)
+  if (c.kernel == STOF_KERNEL_ROWWISE)
     return record_cuda(launch_rowwise(p, bf16, s)) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
   return launch_blockwise(p, bf16, s);
+}
+
+}  // namespace stof
+
+extern "C" {
+
+stof_status stof_mha_fwd_plan(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int L, int d,
+                              float scale, const stof_format* fmt, int64_t mask_stride_b, int64_t mask_stride_h,
+                              const stof_plan* plan, void* o, void* stream) {
+  if (!plan) return STOF_ERR_INVALID_ARG;
+  if (plan->kernel != STOF_KERNEL_ROWWISE && plan->kernel != STOF_KERNEL_BLOCKWISE) return STOF_ERR_INVALID_ARG;
+  if (!fmt) return STOF_ERR_INVALID_ARG;
+  KernelChoice c{plan->kernel, fmt->bn, 0, kVariantAuto};
+  if (plan->kernel == STOF_KERNEL_BLOCKWISE) {
+    if (plan->stages < 0 || plan->stages > 8) return STOF_ERR_INVALID_ARG;
+    c.stages = plan->stages;
+    c.variant = plan->persistent ? kVariantPersistent : kVariantPerTile;
+  }
+  return mha_fwd_choice(q, k, v, dt, B, H, L, d, scale, fmt, mask_stride_b, mask_stride_h, c, o, stream);
+}
+
+stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H,
+                         int L, int d, float scale, const stof_format* fmt,
+                         int64_t mask_stride_b, int64_t mask_stride_h, stof_kernel which, void* o,
+                         void* stream) {
+  stof_status st = check_call(q, k, v, dt, B, H, L, d, scale, fmt, mask_stride_b, mask_stride_h, o);
+  if (st != STOF_OK) return st;
+  KernelChoice c;
+  int source = 0;
+  st = plan_call(*fmt, B, H, L, d, which, &c, &source);
+  if (st != STOF_OK) return st;
+  return mha_fwd_choice(q, k, v, dt, B, H, L, d, scale, fmt, mask_stride_b, mask_stride_h, c, o, stream);
 }
 
 }  // extern "C"

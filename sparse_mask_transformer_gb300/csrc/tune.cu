@@ -6,10 +6,13 @@
 // parameters such as block size and pipeline stages are sampled by running
 // them, and (same page, "autopilot" summary) what was measured is cached so
 // that a configuration is not timed again.  For the masked MHA step the
-// sampled parameters are the kernel (row-wise or block-wise) and the OT width
-// (64 or 128 key columns; 128 query rows).  A result is cached under
-// (sequence length, head dim, density bucket), the bucket being the density
-// rounded to half powers of two.
+// sampled parameters are the kernel (row-wise or block-wise), the OT width
+// (64 or 128 key columns; 128 query rows), the block-wise kernel's K/V ring
+// depth (its pipeline stages) and, at d = 64, whether it runs persistent
+// CTAs.  A result is cached under (sequence length, head dim, density
+// bucket), the bucket being the density rounded to half powers of two;
+// stof_mha_fwd(AUTO) runs the fastest cached candidate on the format's OT
+// width.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -21,14 +24,20 @@
 #include "internal.h"
 
 namespace stof {
+
+const KernelChoice kTuneCandidates[STOF_TUNE_CANDIDATES] = {
+    {STOF_KERNEL_ROWWISE, 128, 0, kVariantAuto},
+    {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPerTile},
+    {STOF_KERNEL_BLOCKWISE, 128, 2, kVariantPerTile},
+    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPerTile},     // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPersistent},  // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPersistent},  // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 128, 2, kVariantPersistent},  // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 64, 0, kVariantAuto},
+};
+
 namespace {
 
-struct Candidate {
-  stof_kernel kernel;
-  int bn;
-};
-constexpr Candidate kCandidates[STOF_TUNE_CANDIDATES] = {
-    {STOF_KERNEL_ROWWISE, 128}, {STOF_KERNEL_BLOCKWISE, 128}, {STOF_KERNEL_BLOCKWISE, 64}};
 constexpr int kTimedCalls = 3;
 
 std::mutex g_mu;
@@ -45,6 +54,19 @@ int tune_density_bucket(double density) {
   return static_cast<int>(std::max(-60.0, b));
 }
 
+bool tuned_choice(int L, int d, double density, int bn, KernelChoice* out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  const auto it = g_cache.find(std::make_tuple(L, d, tune_density_bucket(density)));
+  if (it == g_cache.end()) return false;
+  const stof_tune_result& r = it->second;
+  int best = -1;
+  for (int i = 0; i < STOF_TUNE_CANDIDATES; ++i)
+    if (r.cand_bn[i] == bn && r.cand_ms[i] > 0.f && (best < 0 || r.cand_ms[i] < r.cand_ms[best])) best = i;
+  if (best < 0) return false;
+  *out = kTuneCandidates[best];
+  return true;
+}
+
 }  // namespace stof
 
 using namespace stof;
@@ -53,7 +75,8 @@ extern "C" {
 
 size_t stof_tune_workspace_bytes(int n_masks, int L) {
   size_t best = 0;
-  for (const Candidate& c : kCandidates) best = std::max(best, stof_encode_workspace_bytes(n_masks, L, L, 128, c.bn));
+  for (const KernelChoice& c : kTuneCandidates)
+    best = std::max(best, stof_encode_workspace_bytes(n_masks, L, L, 128, c.bn));
   return best;
 }
 
@@ -77,9 +100,13 @@ stof_status stof_tune(const uint8_t* mask, int n_masks, const void* q, const voi
   r.bn = 0;
   r.ms = -1.f;
   r.density = 0.0;
+  r.stages = 0;
+  r.persistent = 0;
   for (int i = 0; i < STOF_TUNE_CANDIDATES; ++i) {
-    r.cand_kernel[i] = kCandidates[i].kernel;
-    r.cand_bn[i] = kCandidates[i].bn;
+    r.cand_kernel[i] = kTuneCandidates[i].kernel;
+    r.cand_bn[i] = kTuneCandidates[i].bn;
+    r.cand_persistent[i] = 0;
+    r.cand_stages[i] = 0;
     r.cand_ms[i] = -1.f;
   }
   stof_status st = STOF_OK;
@@ -89,18 +116,28 @@ stof_status stof_tune(const uint8_t* mask, int n_masks, const void* q, const voi
     if (st == STOF_OK) st = stof_format_sync(&fmt, stream);
     if (st != STOF_OK) break;
     r.density = static_cast<double>(fmt.nnz) / (static_cast<double>(n_masks) * L * L);
+    const float tpr = static_cast<float>(static_cast<double>(fmt.n_full + fmt.n_part) /
+                                         (static_cast<double>(fmt.n_masks) * fmt.n_tr));
     for (int i = 0; i < STOF_TUNE_CANDIDATES && st == STOF_OK; ++i) {
-      if (kCandidates[i].bn != bn) continue;
-      const stof_kernel kern = kCandidates[i].kernel;
-      st = stof_mha_fwd(q, k, v, dt, B, H, L, d, scale, &fmt, mask_stride_b, mask_stride_h, kern, o, stream);
+      const KernelChoice& cand = kTuneCandidates[i];
+      if (cand.bn != bn) continue;
+      if (cand.kernel == STOF_KERNEL_BLOCKWISE && (cand.variant == kVariantPersistent || cand.stages == 4) &&
+          d != 64)
+        continue;  // persistent CTAs and a 4-deep ring exist for d = 64 only
+      st = mha_fwd_choice(q, k, v, dt, B, H, L, d, scale, &fmt, mask_stride_b, mask_stride_h, cand, o, stream);
       if (st == STOF_ERR_UNSUPPORTED) {  // not a candidate for these sizes
         st = STOF_OK;
         continue;
       }
       if (st != STOF_OK) break;
+      if (cand.kernel == STOF_KERNEL_BLOCKWISE) {  // what the launch ran (an automatic variant resolved)
+        const bool pers = blockwise_persistent(d, cand.variant, tpr);
+        r.cand_persistent[i] = pers ? 1 : 0;
+        r.cand_stages[i] = blockwise_stages(pers, cand.stages);
+      }
       if (record_cuda(cudaEventRecord(ev[0], s)) != cudaSuccess) { st = STOF_ERR_CUDA; break; }
       for (int c = 0; c < kTimedCalls && st == STOF_OK; ++c)
-        st = stof_mha_fwd(q, k, v, dt, B, H, L, d, scale, &fmt, mask_stride_b, mask_stride_h, kern, o, stream);
+        st = mha_fwd_choice(q, k, v, dt, B, H, L, d, scale, &fmt, mask_stride_b, mask_stride_h, cand, o, stream);
       if (st != STOF_OK) break;
       float ms = 0.f;
       if (record_cuda(cudaEventRecord(ev[1], s)) != cudaSuccess ||
@@ -115,8 +152,10 @@ stof_status stof_tune(const uint8_t* mask, int n_masks, const void* q, const voi
       r.cand_ms[i] = ms / kTimedCalls;
       if (r.ms < 0.f || r.cand_ms[i] < r.ms) {
         r.ms = r.cand_ms[i];
-        r.kernel = kern;
+        r.kernel = cand.kernel;
         r.bn = bn;
+        r.stages = r.cand_stages[i];
+        r.persistent = r.cand_persistent[i];
       }
     }
     if (st != STOF_OK) break;

@@ -43,12 +43,17 @@ EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync
             "stof_select_kernel", "stof_mha_fwd", "stof_status_string", "stof_version",
             "stof_last_cuda_error", "stof_tune_workspace_bytes", "stof_tune", "stof_tune_lookup",
             "stof_tune_clear", "stof_tune_density_bucket", "stof_encode_mask_bits", "stof_oproj_fwd",
-            "stof_encode_rules", "stof_check_bounded_wait"]
+            "stof_encode_rules", "stof_check_bounded_wait", "stof_mha_plan", "stof_mha_fwd_plan",
+            "stof_select_kernel_heads"]
 
 STOF_MAX_RULES = 64
 INT32_MIN, INT32_MAX = -(1 << 31), (1 << 31) - 1
 
-STOF_TUNE_CANDIDATES = 3
+STOF_TUNE_CANDIDATES = 8
+
+STOF_PLAN_FORCED = 0
+STOF_PLAN_ANALYTIC = 1
+STOF_PLAN_TUNED = 2
 
 
 class StofError(RuntimeError):
@@ -84,9 +89,17 @@ class stof_mask_rule(ctypes.Structure):
 class stof_tune_result(ctypes.Structure):
     _fields_ = [
         ("kernel", ctypes.c_int), ("bn", ctypes.c_int), ("ms", ctypes.c_float), ("density", ctypes.c_double),
+        ("stages", ctypes.c_int), ("persistent", ctypes.c_int),
         ("cand_kernel", ctypes.c_int * STOF_TUNE_CANDIDATES), ("cand_bn", ctypes.c_int * STOF_TUNE_CANDIDATES),
+        ("cand_stages", ctypes.c_int * STOF_TUNE_CANDIDATES),
+        ("cand_persistent", ctypes.c_int * STOF_TUNE_CANDIDATES),
         ("cand_ms", ctypes.c_float * STOF_TUNE_CANDIDATES),
     ]
+
+
+class stof_plan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("stages", ctypes.c_int), ("persistent", ctypes.c_int),
+                ("source", ctypes.c_int)]
 
 
 _lib = None
@@ -116,9 +129,16 @@ def load_library(path: str = LIB_PATH):
         lib.stof_format_sync.restype = i32
         lib.stof_select_kernel.argtypes = [ctypes.c_double, i32, i32]
         lib.stof_select_kernel.restype = i32
+        lib.stof_select_kernel_heads.argtypes = [ctypes.c_double, i32, i32, i64, ctypes.c_double]
+        lib.stof_select_kernel_heads.restype = i32
         lib.stof_mha_fwd.argtypes = [P, P, P, i32, i32, i32, i32, i32, ctypes.c_float,
                                      ctypes.POINTER(stof_format), i64, i64, i32, P, P]
         lib.stof_mha_fwd.restype = i32
+        lib.stof_mha_plan.argtypes = [ctypes.POINTER(stof_format), i32, i32, i32, i32, i32, ctypes.POINTER(stof_plan)]
+        lib.stof_mha_plan.restype = i32
+        lib.stof_mha_fwd_plan.argtypes = [P, P, P, i32, i32, i32, i32, i32, ctypes.c_float,
+                                          ctypes.POINTER(stof_format), i64, i64, ctypes.POINTER(stof_plan), P, P]
+        lib.stof_mha_fwd_plan.restype = i32
         lib.stof_status_string.argtypes = [i32]
         lib.stof_status_string.restype = ctypes.c_char_p
         lib.stof_version.argtypes = []
@@ -259,6 +279,12 @@ def stof_select_kernel(density: float, seq_len: int, head_dim: int) -> int:
     return int(load_library().stof_select_kernel(float(density), int(seq_len), int(head_dim)))
 
 
+def stof_select_kernel_heads(density: float, seq_len: int, head_dim: int, heads: int,
+                             tiles_per_row: float = -1.0) -> int:
+    return int(load_library().stof_select_kernel_heads(float(density), int(seq_len), int(head_dim), int(heads),
+                                                       float(tiles_per_row)))
+
+
 def stof_mha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: stof_format, scale: float,
                  mask_stride_b: int, mask_stride_h: int, which: int, o: torch.Tensor,
                  stream=None) -> torch.Tensor:
@@ -273,6 +299,31 @@ def stof_mha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: stof_fo
         q.data_ptr(), k.data_ptr(), v.data_ptr(), _dtype_code(q), B, H, L, d, float(scale),
         ctypes.byref(fmt), int(mask_stride_b), int(mask_stride_h), int(which), o.data_ptr(),
         _stream(stream)), "stof_mha_fwd")
+    return o
+
+
+def stof_mha_plan(fmt: stof_format, B: int, H: int, L: int, d: int, which: int) -> stof_plan:
+    """What stof_mha_fwd would run for these sizes, format and kernel request."""
+    plan = stof_plan()
+    _check(load_library().stof_mha_plan(ctypes.byref(fmt), int(B), int(H), int(L), int(d), int(which),
+                                        ctypes.byref(plan)), "stof_mha_plan")
+    return plan
+
+
+def stof_mha_fwd_plan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: stof_format, scale: float,
+                      mask_stride_b: int, mask_stride_h: int, plan: stof_plan, o: torch.Tensor,
+                      stream=None) -> torch.Tensor:
+    """stof_mha_fwd run exactly as `plan` says (kernel, ring depth, variant)."""
+    if q.dim() != 4:
+        raise StofError(STOF_ERR_SHAPE, "stof_mha_fwd_plan: q must be [B, H, L, d]")
+    for t in (q, k, v, o):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise StofError(STOF_ERR_SHAPE, "stof_mha_fwd_plan: q, k, v, o must match and be contiguous")
+    B, H, L, d = q.shape
+    _check(load_library().stof_mha_fwd_plan(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), _dtype_code(q), B, H, L, d, float(scale),
+        ctypes.byref(fmt), int(mask_stride_b), int(mask_stride_h), ctypes.byref(plan), o.data_ptr(),
+        _stream(stream)), "stof_mha_fwd_plan")
     return o
 
 

@@ -72,16 +72,16 @@ def test_traffic_is_reported_only_for_the_profiled_kernel_source(tmp_path, monke
     h = bench.kernel_source_hash()
     (tmp_path / "profiles" / "blockwise_wl.md").write_text(
         f"kernel_source_sha256: {h}\ntraffic_bytes_per_launch: 1.5e9\n")
-    assert bench.profiled_traffic("wl") == 1.5e9
-    assert bench.profiled_traffic("other") is None
+    assert bench.profiled("wl", "traffic_bytes_per_launch") == 1.5e9
+    assert bench.profiled("other", "traffic_bytes_per_launch") is None
     # host launch code below the marker does not change the device-code hash
     with open(csrc / "blockwise.cu", "a") as fh:
         fh.write("\n// host-side note\n")
-    assert bench.profiled_traffic("wl") == 1.5e9
+    assert bench.profiled("wl", "traffic_bytes_per_launch") == 1.5e9
     # a change to the device code does
     src = (csrc / "blockwise_common.cuh").read_text()
     (csrc / "blockwise_common.cuh").write_text(src + "\n// device-side change\n")
-    assert bench.profiled_traffic("wl") is None
+    assert bench.profiled("wl", "traffic_bytes_per_launch") is None
 
 
 def test_run_for_keeps_stepping_for_the_given_time():

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert stof.stof_version() == 1
+    assert stof.stof_version() == 2
     for s in range(10):
         assert stof.stof_status_string(s)
     assert "unknown" in stof.stof_status_string(99)
@@ -288,3 +288,83 @@ def test_oracle_and_product_share_no_code():
                     text = open(os.path.join(dirpath, f)).read()
                     assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                     assert "stof_oracle" not in text, f
+
+
+def _plan_format(L=1024, bm=128, bn=128, n_masks=1, synced=True, nnz=None, tiles=None):
+    """A format struct with non-null (never dereferenced) pointers: the plan
+    is host arithmetic on the sizes and the synced counts."""
+    f = stof.stof_format()
+    f.n_masks, f.lq, f.lk, f.bm, f.bn = n_masks, L, L, bm, bn
+    f.n_tr, f.n_tc = L // bm, L // bn
+    for name in ("full_row_ptr", "full_col_idx", "part_row_ptr", "part_col_idx", "bitmaps", "counts_dev",
+                 "scratch"):
+        setattr(f, name, 1 << 20)
+    f.synced = 1 if synced else 0
+    f.nnz = nnz if nnz is not None else L * L // 2
+    f.n_full = 0
+    f.n_part = tiles if tiles is not None else f.n_tr * f.n_tc // 2
+    return f
+
+
+def test_mha_plan_sources_and_variants(lib):
+    stof.stof_tune_clear()
+    f = _plan_format()
+    p = stof.stof_mha_plan(f, 1, 4, 1024, 64, stof.STOF_KERNEL_ROWWISE)
+    assert (p.kernel, p.stages, p.persistent, p.source) == (stof.STOF_KERNEL_ROWWISE, 0, 0, stof.STOF_PLAN_FORCED)
+    p = stof.stof_mha_plan(f, 1, 4, 1024, 64, stof.STOF_KERNEL_BLOCKWISE)
+    # 32 of 64 OTs listed over 8 OT rows: 4 per row, below the persistent threshold at d = 64
+    assert (p.kernel, p.persistent, p.stages, p.source) == (stof.STOF_KERNEL_BLOCKWISE, 1, 4, stof.STOF_PLAN_FORCED)
+    p = stof.stof_mha_plan(f, 1, 4, 1024, 128, stof.STOF_KERNEL_BLOCKWISE)
+    assert (p.persistent, p.stages) == (0, 3)                       # d = 128: one CTA per query tile
+    p = stof.stof_mha_plan(_plan_format(L=16384, tiles=128 * 100), 1, 1, 16384, 64, stof.STOF_KERNEL_BLOCKWISE)
+    assert (p.persistent, p.stages) == (0, 3)                       # 100 OTs per row: one CTA per query tile
+    p = stof.stof_mha_plan(f, 1, 4, 1024, 64, stof.STOF_KERNEL_AUTO)
+    assert p.source == stof.STOF_PLAN_ANALYTIC
+    assert p.kernel == stof.stof_select_kernel(0.5, 1024, 64)
+
+
+def test_mha_plan_rejects_what_the_call_rejects(lib):
+    f = _plan_format()
+    with pytest.raises(stof.StofError) as e:
+        stof.stof_mha_plan(_plan_format(synced=False), 1, 1, 1024, 64, stof.STOF_KERNEL_AUTO)
+    assert e.value.status == stof.STOF_ERR_NOT_SYNCED
+    with pytest.raises(stof.StofError) as e:
+        stof.stof_mha_plan(_plan_format(bm=64, bn=64), 1, 1, 1024, 64, stof.STOF_KERNEL_BLOCKWISE)
+    assert e.value.status == stof.STOF_ERR_UNSUPPORTED
+    # AUTO on OTs the block-wise kernel does not take falls back to the row-wise kernel
+    p = stof.stof_mha_plan(_plan_format(bm=64, bn=64, nnz=1024 * 1024), 1, 1, 1024, 64, stof.STOF_KERNEL_AUTO)
+    assert p.kernel == stof.STOF_KERNEL_ROWWISE
+    for args, status in [((1, 1, 2048, 64, 0), stof.STOF_ERR_SHAPE),      # L differs from the format's
+                         ((1, 1, 1024, 96, 0), stof.STOF_ERR_UNSUPPORTED),
+                         ((0, 1, 1024, 64, 0), stof.STOF_ERR_INVALID_ARG),
+                         ((1, 1, 1024, 64, 7), stof.STOF_ERR_INVALID_ARG)]:
+        with pytest.raises(stof.StofError) as e:
+            stof.stof_mha_plan(f, *args)
+        assert e.value.status == status, args
+    assert lib.stof_mha_plan(ctypes.byref(f), 1, 1, 1024, 64, 0, None) == stof.STOF_ERR_INVALID_ARG
+
+
+def test_tune_result_layout(lib):
+    # kernel, bn, ms (+pad), density, stages, persistent, then 5 arrays of 8 ints/floats
+    assert ctypes.sizeof(stof.stof_tune_result) == 4 + 4 + 8 + 8 + 4 + 4 + 5 * 8 * 4
+
+
+def test_select_kernel_heads_model(lib):
+    sel = stof.stof_select_kernel_heads
+    row, blk = stof.STOF_KERNEL_ROWWISE, stof.STOF_KERNEL_BLOCKWISE
+    # the window-48 workload (2 heads, L = 256, 3 partial OTs over 2 query tiles) is row-wise territory
+    assert sel(0.1703, 256, 64, 2, 3 / 2) == row
+    # the other workloads are block-wise
+    assert sel(0.969, 512, 64, 16 * 12, 4.0) == blk
+    assert sel(0.5002, 2048, 64, 8 * 12, 136 / 16) == blk
+    assert sel(0.135, 4096, 64, 4 * 16, 884 / 32) == blk
+    assert sel(0.0501, 16384, 128, 32, 8256 / 128) == blk
+    # more heads never turn a block-wise choice into a row-wise one
+    for rho in (0.01, 0.05, 0.2):
+        for L in (128, 512, 2048):
+            ks = [sel(rho, L, 64, h, -1) for h in (1, 2, 4, 16, 64, 256, 4096)]
+            assert ks == sorted(ks), (rho, L, ks)   # ROWWISE (0) before BLOCKWISE (1)
+    # one head, every OT listed: the three-argument form
+    for rho in (0.0, 0.05, 0.5):
+        assert stof.stof_select_kernel(rho, 1024, 128) == sel(rho, 1024, 128, 1, -1)
+    assert sel(0.1, 1024, 64, 0, -1) == blk       # invalid head count
