@@ -605,6 +605,13 @@ def run_sweep(args):
                         call = lambda: stof.stof_mha_fwd(q, k, v, fmt, 1 / math.sqrt(d), 0, 0,  # noqa: E731
                                                          which, o)
                         t[name] = graph_ms(call, 20) * 1e3
+                    rpw_us = {}
+                    for rpw in (1, 2, 4):  # the row-wise kernel with each rows-per-warp setting
+                        plan = stof.stof_plan(stof.STOF_KERNEL_ROWWISE, 0, 0, 0, rpw)
+                        call = lambda: stof.stof_mha_fwd_plan(q, k, v, fmt, 1 / math.sqrt(d), 0, 0,  # noqa: E731
+                                                              plan, o)
+                        rpw_us[rpw] = round(graph_ms(call, 20) * 1e3, 2)
+                    auto_rpw = stof.stof_mha_plan(fmt, 1, H, L, d, stof.STOF_KERNEL_ROWWISE).rows_per_warp
                     sel = "blockwise" if stof.stof_mha_plan(fmt, 1, H, L, d, stof.STOF_KERNEL_AUTO).kernel == \
                         stof.STOF_KERNEL_BLOCKWISE else "rowwise"
                     fastest = min(t, key=t.get)
@@ -613,7 +620,8 @@ def run_sweep(args):
                     print(json.dumps({"sweep": pattern, "L": L, "d": d, "H": H, "density": round(density, 5),
                                       "tiles": fmt.n_full + fmt.n_part, "rowwise_us": round(t["rowwise"], 2),
                                       "blockwise_us": round(t["blockwise"], 2), "selected": sel,
-                                      "fastest": fastest}), flush=True)
+                                      "fastest": fastest, "rowwise_rpw_us": rpw_us, "auto_rpw": auto_rpw}),
+                          flush=True)
     print(json.dumps({"sweep_summary": {"cases": cases, "selector_picks_fastest": agree}}), flush=True)
 
 

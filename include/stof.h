@@ -295,6 +295,7 @@ typedef struct {
   int stages;          /* block-wise K/V ring depth; 0 for the row-wise kernel */
   int persistent;      /* block-wise: 1 = persistent CTAs (d = 64), 0 = one CTA per query tile */
   int source;          /* STOF_PLAN_FORCED, STOF_PLAN_ANALYTIC or STOF_PLAN_TUNED */
+  int rows_per_warp;   /* row-wise: query rows per warp (1, 2 or 4); 0 for the block-wise kernel */
 } stof_plan;
 
 /*
@@ -310,7 +311,8 @@ stof_status stof_mha_plan(const stof_format* fmt, int B, int H, int L, int d, st
  * block-wise kernel its ring depth and variant (plan->source is ignored).
  * Arguments, layout and errors as stof_mha_fwd(); STOF_ERR_UNSUPPORTED for
  * a ring depth or variant these sizes do not admit.  Admitted: row-wise on
- * any OT size; block-wise on 128x128 OTs one CTA per query tile with ring
+ * any OT size with 1, 2 or 4 query rows per warp (0: the library's
+ * choice); block-wise on 128x128 OTs one CTA per query tile with ring
  * depth 2 or 3 (d = 128) or 2, 3 or 4 (d = 64), persistent CTAs with ring
  * depth 2, 3 or 4 (d = 64 only); on 128x64 OTs the default depth (3 per
  * query tile, 4 persistent).  A plan from stof_mha_plan() or a
@@ -328,16 +330,16 @@ stof_status stof_mha_fwd_plan(const void* q, const void* k, const void* v, stof_
  * measured (gist.science technical summary, Methodology 2, two-stage
  * tuning, stage 2 "parameter sampling"; the cache: same page, the lay
  * summary's "autopilot" that remembers what worked).  The candidates:
- *   0      row-wise kernel, 128x128 OTs;
- *   1-3    block-wise, 128x128 OTs, one CTA per query tile, K/V ring depth
+ *   0-2    row-wise kernel, 128x128 OTs, 1, 2, 4 query rows per warp;
+ *   3-5    block-wise, 128x128 OTs, one CTA per query tile, K/V ring depth
  *          3, 2, 4 (depth 4 at d = 64 only: shared memory);
- *   4-6    block-wise, 128x128 OTs, persistent CTAs (d = 64 only), ring
+ *   6-8    block-wise, 128x128 OTs, persistent CTAs (d = 64 only), ring
  *          depth 4, 3, 2;
- *   7      block-wise, 128x64 OTs, default variant and ring depth.
+ *   9      block-wise, 128x64 OTs, default variant and ring depth.
  * The softmax warpgroup count is not a candidate: the kernels' register and
  * tensor-memory budgets fit exactly two.
  */
-#define STOF_TUNE_CANDIDATES 8
+#define STOF_TUNE_CANDIDATES 10
 typedef struct {
   stof_kernel kernel;        /* fastest candidate */
   int bn;                    /* its OT width (bm = 128) */
@@ -345,11 +347,13 @@ typedef struct {
   double density;            /* density of the tuned mask */
   int stages;                /* its K/V ring depth (0 for row-wise) */
   int persistent;            /* 1 if it runs persistent CTAs */
+  int rows_per_warp;         /* row-wise: its query rows per warp (0 for block-wise) */
   stof_kernel cand_kernel[STOF_TUNE_CANDIDATES];
   int cand_bn[STOF_TUNE_CANDIDATES];
-  int cand_stages[STOF_TUNE_CANDIDATES];     /* ring depth the candidate ran with (0 row-wise) */
-  int cand_persistent[STOF_TUNE_CANDIDATES]; /* 1 persistent, 0 one CTA per query tile */
-  float cand_ms[STOF_TUNE_CANDIDATES];       /* -1 for a candidate the sizes do not admit */
+  int cand_stages[STOF_TUNE_CANDIDATES];        /* ring depth the candidate ran with (0 row-wise) */
+  int cand_persistent[STOF_TUNE_CANDIDATES];    /* 1 persistent, 0 one CTA per query tile */
+  int cand_rows_per_warp[STOF_TUNE_CANDIDATES]; /* row-wise rows per warp (0 block-wise) */
+  float cand_ms[STOF_TUNE_CANDIDATES];          /* -1 for a candidate the sizes do not admit */
 } stof_tune_result;
 
 /* Workspace bytes stof_tune() needs (the largest encode workspace over the

@@ -102,7 +102,9 @@ struct AttnParams {
   unsigned int* work;              // work counter of the persistent kernel, in the format's workspace:
                                    // work[0] items taken, work[1] CTAs finished (both zero between launches)
   float tiles_per_row;             // mean listed OTs per OT row of the masks (synced format), else -1
+  float keys_per_row;              // mean valid keys per query row (synced format), else -1
   int stages;                      // block-wise K/V ring depth; 0 = the kernel's default
+  int rows_per_warp;               // row-wise: query rows per warp (1, 2 or 4); 0 = automatic
   int variant;                     // block-wise: kVariantAuto, kVariantPerTile or kVariantPersistent
 };
 // Block-wise kernel variants: one CTA per query tile, or persistent CTAs
@@ -120,13 +122,30 @@ inline bool blockwise_persistent(int d, int variant, float tiles_per_row) {
 // Ring depth a block-wise launch uses (stages = 0: the variant's default).
 inline int blockwise_stages(bool persistent, int stages) { return stages ? stages : (persistent ? 4 : 3); }
 
-// One way to run the MHA step: the kernel, the OT width it needs and the
-// block-wise kernel's ring depth (0 = default) and variant.
+// Row-wise kernel: query rows per warp.  A whole warp per row while the
+// call has few rows (the GPU holds them all at once and the shortest
+// dependent chain wins); for more rows with few valid keys, 2 or 4 rows per
+// warp so that more rows are in flight.  `requested` (1, 2 or 4) overrides.
+// Thresholds from kernel-only GB300 times of the three settings on 360
+// short, sparse cases: within 3% of the best setting on average.
+constexpr long long kRowwiseFewRows = 2048;
+inline int rowwise_rows_per_warp(long long rows, float keys_per_row, int requested) {
+  if (requested == 1 || requested == 2 || requested == 4) return requested;
+  if (rows <= kRowwiseFewRows || keys_per_row < 0.f) return 1;
+  if (keys_per_row <= 32.f) return 4;
+  if (keys_per_row <= 256.f) return 2;
+  return 1;
+}
+
+// One way to run the MHA step: the kernel, the OT width it needs, the
+// block-wise kernel's ring depth (0 = default) and variant, and the
+// row-wise kernel's rows per warp (0 = automatic).
 struct KernelChoice {
   stof_kernel kernel;
   int bn;
   int stages;
   int variant;
+  int rows_per_warp;
 };
 // The candidates stof_tune() times (STOF_TUNE_CANDIDATES of them).
 extern const KernelChoice kTuneCandidates[STOF_TUNE_CANDIDATES];

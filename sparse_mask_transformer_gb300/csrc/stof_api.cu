@@ -275,12 +275,14 @@ stof_status stof_format_sync(stof_format* fmt, void* stream) {
 //
 // Predicted device time of each kernel in microseconds, linear in the work
 // it does:
-//   row-wise    T_row = 3.38 + 8.84e-4 R + 1.81e-5 K d/64
-//               R = query rows (heads x L), K = valid (query, key) pairs
-//               (density x L^2 x heads): a warp per query row, whose fixed
-//               cost is a few dependent memory round trips, plus the K and
-//               V rows of every valid key;
-//   block-wise  T_blk = 7.27 + 4.93e-3 T (d/64 + 1)/2 + 9.09e-3 Q
+//   row-wise    T_row = 3.80 + 4.65e-4 R / r + 1.754e-5 K d/64 + 6.34e-5 P
+//               R = query rows (heads x L) and r the kernel's rows per warp
+//               (a warp's fixed cost is a few dependent memory round
+//               trips), K = valid (query, key) pairs (density x L^2 x
+//               heads: the K and V rows of every valid key), P = (query
+//               row, listed OT) pairs (heads x L x listed OTs per query
+//               tile: the bitmap bytes and column indices fetched per row);
+//   block-wise  T_blk = 7.19 + 4.94e-3 T (d/64 + 1)/2 + 9.43e-3 Q
 //               T = listed 128x128 OTs over all heads (each the full tile's
 //               MMA and softmax work, the MMAs half as long at d = 64),
 //               Q = query tiles (heads x L / 128: start-up and finish).
@@ -288,18 +290,19 @@ stof_status stof_format_sync(stof_format* fmt, void* stream) {
 // fitted to kernel-only GB300 times of both kernels (CUDA-graph replay) on
 // 360 cases: L = 128 to 2048, densities 0.01 to 0.4, 2 to 64 heads, d = 64
 // and 128, random and sliding-window masks; the model picks the faster
-// kernel in 351 of them and costs at most 21% where it does not.  The
-// row-wise kernel wins for high sparsity and few, short rows -- the regime
-// the pages give it.
+// kernel in 343 of them, costs 0.6% on average and at most 47% where it
+// does not.  The row-wise kernel wins for high sparsity and few, short
+// rows -- the regime the pages give it.
 namespace {
-double model_rowwise_us(double density, double L, double d, double heads) {
-  const double R = heads * L, K = density * L * L * heads;
-  return 3.38 + 8.84e-4 * R + 1.81e-5 * K * (d / 64.0);
+double model_rowwise_us(double density, double L, double d, double heads, double tiles_per_row) {
+  const double R = heads * L, K = density * L * L * heads, P = R * tiles_per_row;
+  const double r = rowwise_rows_per_warp(static_cast<long long>(R), static_cast<float>(density * L), 0);
+  return 3.80 + 4.65e-4 * R / r + 1.754e-5 * K * (d / 64.0) + 6.34e-5 * P;
 }
 double model_blockwise_us(double L, double d, double heads, double tiles_per_row) {
   const double n_tr = L / 128.0;
   const double T = tiles_per_row * n_tr * heads, Q = n_tr * heads;
-  return 7.27 + 4.93e-3 * T * (d / 64.0 + 1.0) / 2.0 + 9.09e-3 * Q;
+  return 7.19 + 4.94e-3 * T * (d / 64.0 + 1.0) / 2.0 + 9.43e-3 * Q;
 }
 }  // namespace
 
@@ -311,7 +314,7 @@ stof_kernel stof_select_kernel_heads(double density, int seq_len, int head_dim, 
   // so that the choice depends monotonically on the density
   double tpr = tiles_per_row;
   if (!(tpr >= 0.0 && tpr <= n_tc)) tpr = n_tc;
-  const double t_row = model_rowwise_us(density, L, head_dim, static_cast<double>(heads));
+  const double t_row = model_rowwise_us(density, L, head_dim, static_cast<double>(heads), tpr);
   const double t_blk = model_blockwise_us(L, head_dim, static_cast<double>(heads), tpr);
   return t_row <= t_blk ? STOF_KERNEL_ROWWISE : STOF_KERNEL_BLOCKWISE;
 }
@@ -323,6 +326,10 @@ stof_kernel stof_select_kernel(double density, int seq_len, int head_dim) {
 // OT sizes the block-wise kernel runs: 128 query rows (the MMA's M) by 64 or
 // 128 key columns.
 static bool blockwise_tiles(const stof_format& f) { return f.bm == 128 && (f.bn == 64 || f.bn == 128); }
+
+static float keys_per_row(const stof_format& f) {
+  return f.synced ? static_cast<float>(static_cast<double>(f.nnz) / (static_cast<double>(f.n_masks) * f.lq)) : -1.f;
+}
 
 static float tiles_per_row(const stof_format& f) {
   return f.synced ? static_cast<float>(static_cast<double>(f.n_full + f.n_part) /
@@ -369,7 +376,7 @@ static stof_status plan_call(const stof_format& f, int B, int H, int L, int d, s
                              int* source) {
   if (which != STOF_KERNEL_AUTO && which != STOF_KERNEL_ROWWISE && which != STOF_KERNEL_BLOCKWISE)
     return STOF_ERR_INVALID_ARG;
-  *c = KernelChoice{which, f.bn, 0, kVariantAuto};
+  *c = KernelChoice{which, f.bn, 0, kVariantAuto, 0};
   *source = STOF_PLAN_FORCED;
   if (which == STOF_KERNEL_AUTO) {
     if (!f.synced) return STOF_ERR_NOT_SYNCED;
@@ -402,9 +409,13 @@ stof_status stof_mha_plan(const stof_format* fmt, int B, int H, int L, int d, st
   out->source = source;
   out->persistent = 0;
   out->stages = 0;
+  out->rows_per_warp = 0;
   if (c.kernel == STOF_KERNEL_BLOCKWISE) {
     out->persistent = blockwise_persistent(d, c.variant, tiles_per_row(*fmt)) ? 1 : 0;
     out->stages = blockwise_stages(out->persistent != 0, c.stages);
+  } else {
+    out->rows_per_warp = rowwise_rows_per_warp(static_cast<long long>(B) * H * L, keys_per_row(*fmt),
+                                               c.rows_per_warp);
   }
   return STOF_OK;
 }
@@ -446,6 +457,8 @@ stof_status mha_fwd_choice(const void* q, const void* k, const void* v, stof_dty
   // encoder zeroes; the persistent kernel leaves them zero when it ends
   p.work = reinterpret_cast<unsigned int*>(fmt->counts_dev + 5);
   p.tiles_per_row = tiles_per_row(*fmt);
+  p.keys_per_row = keys_per_row(*fmt);
+  p.rows_per_warp = c.rows_per_warp;
   p.stages = c.stages;
   p.variant = c.variant;
   const bool bf16 = dt == STOF_BF16;
@@ -465,11 +478,15 @@ stof_status stof_mha_fwd_plan(const void* q, const void* k, const void* v, stof_
   if (!plan) return STOF_ERR_INVALID_ARG;
   if (plan->kernel != STOF_KERNEL_ROWWISE && plan->kernel != STOF_KERNEL_BLOCKWISE) return STOF_ERR_INVALID_ARG;
   if (!fmt) return STOF_ERR_INVALID_ARG;
-  KernelChoice c{plan->kernel, fmt->bn, 0, kVariantAuto};
+  KernelChoice c{plan->kernel, fmt->bn, 0, kVariantAuto, 0};
   if (plan->kernel == STOF_KERNEL_BLOCKWISE) {
     if (plan->stages < 0 || plan->stages > 8) return STOF_ERR_INVALID_ARG;
     c.stages = plan->stages;
     c.variant = plan->persistent ? kVariantPersistent : kVariantPerTile;
+  } else {
+    const int r = plan->rows_per_warp;
+    if (r != 0 && r != 1 && r != 2 && r != 4) return STOF_ERR_UNSUPPORTED;
+    c.rows_per_warp = r;
   }
   return mha_fwd_choice(q, k, v, dt, B, H, L, d, scale, fmt, mask_stride_b, mask_stride_h, c, o, stream);
 }

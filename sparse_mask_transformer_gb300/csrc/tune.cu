@@ -26,14 +26,16 @@
 namespace stof {
 
 const KernelChoice kTuneCandidates[STOF_TUNE_CANDIDATES] = {
-    {STOF_KERNEL_ROWWISE, 128, 0, kVariantAuto},
-    {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPerTile},
-    {STOF_KERNEL_BLOCKWISE, 128, 2, kVariantPerTile},
-    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPerTile},     // d = 64 only
-    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPersistent},  // d = 64 only
-    {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPersistent},  // d = 64 only
-    {STOF_KERNEL_BLOCKWISE, 128, 2, kVariantPersistent},  // d = 64 only
-    {STOF_KERNEL_BLOCKWISE, 64, 0, kVariantAuto},
+    {STOF_KERNEL_ROWWISE, 128, 0, kVariantAuto, 1},
+    {STOF_KERNEL_ROWWISE, 128, 0, kVariantAuto, 2},
+    {STOF_KERNEL_ROWWISE, 128, 0, kVariantAuto, 4},
+    {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPerTile, 0},
+    {STOF_KERNEL_BLOCKWISE, 128, 2, kVariantPerTile, 0},
+    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPerTile, 0},     // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPersistent, 0},  // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPersistent, 0},  // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 128, 2, kVariantPersistent, 0},  // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 64, 0, kVariantAuto, 0},
 };
 
 namespace {
@@ -102,11 +104,13 @@ stof_status stof_tune(const uint8_t* mask, int n_masks, const void* q, const voi
   r.density = 0.0;
   r.stages = 0;
   r.persistent = 0;
+  r.rows_per_warp = 0;
   for (int i = 0; i < STOF_TUNE_CANDIDATES; ++i) {
     r.cand_kernel[i] = kTuneCandidates[i].kernel;
     r.cand_bn[i] = kTuneCandidates[i].bn;
     r.cand_persistent[i] = 0;
     r.cand_stages[i] = 0;
+    r.cand_rows_per_warp[i] = kTuneCandidates[i].rows_per_warp;
     r.cand_ms[i] = -1.f;
   }
   stof_status st = STOF_OK;
@@ -156,6 +160,7 @@ stof_status stof_tune(const uint8_t* mask, int n_masks, const void* q, const voi
         r.bn = bn;
         r.stages = r.cand_stages[i];
         r.persistent = r.cand_persistent[i];
+        r.rows_per_warp = r.cand_rows_per_warp[i];
       }
     }
     if (st != STOF_OK) break;

@@ -49,7 +49,7 @@ EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync
 STOF_MAX_RULES = 64
 INT32_MIN, INT32_MAX = -(1 << 31), (1 << 31) - 1
 
-STOF_TUNE_CANDIDATES = 8
+STOF_TUNE_CANDIDATES = 10
 
 STOF_PLAN_FORCED = 0
 STOF_PLAN_ANALYTIC = 1
@@ -89,17 +89,18 @@ class stof_mask_rule(ctypes.Structure):
 class stof_tune_result(ctypes.Structure):
     _fields_ = [
         ("kernel", ctypes.c_int), ("bn", ctypes.c_int), ("ms", ctypes.c_float), ("density", ctypes.c_double),
-        ("stages", ctypes.c_int), ("persistent", ctypes.c_int),
+        ("stages", ctypes.c_int), ("persistent", ctypes.c_int), ("rows_per_warp", ctypes.c_int),
         ("cand_kernel", ctypes.c_int * STOF_TUNE_CANDIDATES), ("cand_bn", ctypes.c_int * STOF_TUNE_CANDIDATES),
         ("cand_stages", ctypes.c_int * STOF_TUNE_CANDIDATES),
         ("cand_persistent", ctypes.c_int * STOF_TUNE_CANDIDATES),
+        ("cand_rows_per_warp", ctypes.c_int * STOF_TUNE_CANDIDATES),
         ("cand_ms", ctypes.c_float * STOF_TUNE_CANDIDATES),
     ]
 
 
 class stof_plan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("stages", ctypes.c_int), ("persistent", ctypes.c_int),
-                ("source", ctypes.c_int)]
+                ("source", ctypes.c_int), ("rows_per_warp", ctypes.c_int)]
 
 
 _lib = None

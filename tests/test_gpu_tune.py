@@ -30,11 +30,13 @@ def test_tune_picks_the_fastest_candidate_and_caches_it(gpu_lib):
     res = stof.stof_tune(mdev, qd, kd, vd, 1 / math.sqrt(d), 0, 0, ws, o)
     ms = list(res.cand_ms)
     assert all(t > 0 for t in ms)                            # d = 64 admits every candidate
-    assert list(res.cand_stages) == [0, 3, 2, 4, 4, 3, 2, 4]
-    assert list(res.cand_persistent) == [0, 0, 0, 0, 1, 1, 1, 1]  # 128x64: 4 OTs per row -> persistent
+    assert list(res.cand_stages) == [0, 0, 0, 3, 2, 4, 4, 3, 2, 4]
+    assert list(res.cand_persistent) == [0, 0, 0, 0, 0, 0, 1, 1, 1, 1]  # 128x64: 9 OTs per row -> persistent
+    assert list(res.cand_rows_per_warp) == [1, 2, 4, 0, 0, 0, 0, 0, 0, 0]
     best = int(np.argmin(ms))
     assert res.kernel == res.cand_kernel[best] and res.bn == res.cand_bn[best]
     assert res.stages == res.cand_stages[best] and res.persistent == res.cand_persistent[best]
+    assert res.rows_per_warp == res.cand_rows_per_warp[best]
     assert res.ms == pytest.approx(ms[best])
     assert res.density == pytest.approx((L + 1) / (2 * L))
     hit = stof.stof_tune_lookup(L, d, res.density * 1.05)    # same half-octave bucket
@@ -77,12 +79,14 @@ def test_auto_runs_the_cached_measurement(gpu_lib, d):
     ms = [t if (t > 0 and res.cand_bn[i] == 128) else float("inf") for i, t in enumerate(res.cand_ms)]
     best = int(np.argmin(ms))
     if d == 128:
-        assert all(res.cand_ms[i] < 0 for i in (3, 4, 5, 6))    # d = 64-only candidates
+        assert all(res.cand_ms[i] < 0 for i in (5, 6, 7, 8))    # d = 64-only candidates
     plan = stof.stof_mha_plan(fmt, B, H, L, d, stof.STOF_KERNEL_AUTO)
     assert plan.source == stof.STOF_PLAN_TUNED
     assert plan.kernel == res.cand_kernel[best]
     if plan.kernel == stof.STOF_KERNEL_BLOCKWISE:
         assert (plan.stages, plan.persistent) == (res.cand_stages[best], res.cand_persistent[best])
+    else:
+        assert plan.rows_per_warp == res.cand_rows_per_warp[best]
     o2 = torch.full_like(qd, float("nan"))
     stof.stof_mha_fwd(qd, kd, vd, fmt, scale, 0, 0, stof.STOF_KERNEL_AUTO, o2)
     torch.cuda.synchronize()
@@ -109,7 +113,7 @@ def test_every_tuned_configuration_matches_the_oracle(gpu_lib, d, stages, persis
     masks[1, :128] = 0
     q, k, v = synth.make_qkv(B, H, L, d, "bf16", seed=91)
     fmt, ws, _ = gpu_encode(torch.from_numpy(masks).cuda(), 128, 128)
-    plan = stof.stof_plan(stof.STOF_KERNEL_BLOCKWISE, stages, persistent, 0)
+    plan = stof.stof_plan(stof.STOF_KERNEL_BLOCKWISE, stages, persistent, 0, 0)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o = torch.full_like(qd, float("nan"))
     scale = 1 / math.sqrt(d)
@@ -131,5 +135,35 @@ def test_configurations_the_sizes_do_not_admit_are_refused(gpu_lib):
     q = torch.zeros(1, 1, L, 128, dtype=torch.bfloat16, device="cuda")
     for stages, persistent in ((4, 0), (2, 1), (5, 0)):
         with pytest.raises(stof.StofError) as e:
-            stof.stof_mha_fwd_plan(q, q, q, fmt, 0.1, 0, 0, stof.stof_plan(1, stages, persistent, 0), q.clone())
+            stof.stof_mha_fwd_plan(q, q, q, fmt, 0.1, 0, 0, stof.stof_plan(1, stages, persistent, 0, 0), q.clone())
         assert e.value.status == stof.STOF_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("rpw", [1, 2, 4])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("bm,bn,L,density", [(128, 128, 384, 0.05), (128, 128, 512, 0.6), (8, 8, 136, 0.2),
+                                             (64, 32, 320, 0.02)])
+def test_rowwise_rows_per_warp_match_the_oracle(gpu_lib, rpw, d, bm, bn, L, density):
+    """The row-wise kernel with 1, 2 or 4 query rows per warp (the rows of a
+    warp have different OT and key counts; with 3 heads and L = 136 the last
+    warp is ragged), per-head masks with a fully masked row and empty tile
+    columns."""
+    B, H = 1, 3
+    masks = synth.random_mask(B * H, L, L, density, seed=L + rpw + d)
+    masks[1, 5] = 0
+    masks[2, :, : L // 3] = 0
+    masks[0, 7, :] = 1                                  # one dense row among sparse ones
+    q, k, v = synth.make_qkv(B, H, L, d, "fp16", seed=12)
+    fmt, ws, _ = gpu_encode(torch.from_numpy(masks).cuda(), bm, bn)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full_like(qd, float("nan"))
+    scale = 1 / math.sqrt(d)
+    stof.stof_mha_fwd_plan(qd, kd, vd, fmt, scale, H, 1, stof.stof_plan(stof.STOF_KERNEL_ROWWISE, 0, 0, 0, rpw), o)
+    torch.cuda.synchronize()
+    stof.stof_format_sync(fmt)
+    assert fmt.device_error == 0
+    q64, k64, v64 = (synth.to_float64(t) for t in (q, k, v))
+    ref = oracle.attention_bhld(q64, k64, v64, lambda b, h, rows: masks[b * H + h][rows], scale)
+    for (b, h), o_ref in ref.items():
+        assert np.abs(o[b, h].double().cpu().numpy() - o_ref).max() <= TOL["fp16"]
+    assert torch.all(o[0, 1, 5] == 0)

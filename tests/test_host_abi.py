@@ -311,6 +311,13 @@ def test_mha_plan_sources_and_variants(lib):
     f = _plan_format()
     p = stof.stof_mha_plan(f, 1, 4, 1024, 64, stof.STOF_KERNEL_ROWWISE)
     assert (p.kernel, p.stages, p.persistent, p.source) == (stof.STOF_KERNEL_ROWWISE, 0, 0, stof.STOF_PLAN_FORCED)
+    assert p.rows_per_warp == 1                                      # 512 keys per row: a warp each
+    assert stof.stof_mha_plan(_plan_format(nnz=20 * 1024), 1, 2, 1024, 64, 0).rows_per_warp == 1  # 2048 rows
+    # more rows: rows per warp by the mean valid keys per row
+    assert stof.stof_mha_plan(_plan_format(nnz=20 * 1024), 1, 64, 1024, 64, 0).rows_per_warp == 4
+    assert stof.stof_mha_plan(_plan_format(nnz=200 * 1024), 1, 64, 1024, 64, 0).rows_per_warp == 2
+    assert stof.stof_mha_plan(_plan_format(nnz=512 * 1024), 1, 64, 1024, 64, 0).rows_per_warp == 1
+    assert stof.stof_mha_plan(_plan_format(nnz=20 * 1024, synced=False), 1, 64, 1024, 64, 0).rows_per_warp == 1
     p = stof.stof_mha_plan(f, 1, 4, 1024, 64, stof.STOF_KERNEL_BLOCKWISE)
     # 32 of 64 OTs listed over 8 OT rows: 4 per row, below the persistent threshold at d = 64
     assert (p.kernel, p.persistent, p.stages, p.source) == (stof.STOF_KERNEL_BLOCKWISE, 1, 4, stof.STOF_PLAN_FORCED)
@@ -344,9 +351,26 @@ def test_mha_plan_rejects_what_the_call_rejects(lib):
     assert lib.stof_mha_plan(ctypes.byref(f), 1, 1, 1024, 64, 0, None) == stof.STOF_ERR_INVALID_ARG
 
 
-def test_tune_result_layout(lib):
-    # kernel, bn, ms (+pad), density, stages, persistent, then 5 arrays of 8 ints/floats
-    assert ctypes.sizeof(stof.stof_tune_result) == 4 + 4 + 8 + 8 + 4 + 4 + 5 * 8 * 4
+def test_python_structs_match_the_header(tmp_path):
+    """The binding's ctypes mirrors against the C compiler's layout of the
+    header's structs (sizes and every field offset)."""
+    structs = {"stof_format": stof.stof_format, "stof_plan": stof.stof_plan,
+               "stof_tune_result": stof.stof_tune_result, "stof_mask_rule": stof.stof_mask_rule}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "stof.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'  printf("{name} %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'  printf("{name}.{field} %zu\\n", offsetof({name}, {field}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c11", f"-I{os.path.join(ROOT, 'include')}", str(src), "-o", str(exe)])
+    got = dict(ln.split() for ln in subprocess.check_output([str(exe)], text=True).splitlines())
+    for name, cls in structs.items():
+        assert int(got[name]) == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert int(got[f"{name}.{field}"]) == getattr(cls, field).offset, (name, field)
 
 
 def test_select_kernel_heads_model(lib):
