@@ -20,6 +20,11 @@ GPU", gist.science technical summary):
     module: fusion carried past the MHA layer): heads concatenated along
     the reduction axis, y = O_cat W^T + bias + residual.  A numpy matmul is
     its one library step.
+  - ``layer_norm`` / ``oproj_ln``: the LayerNorm that closes a post-norm
+    transformer sublayer (the operator after the projection and residual),
+    by its definition in fp64: per token, subtract the mean over the
+    features, divide by sqrt(population variance + eps), scale by gamma and
+    add beta; ``oproj_ln`` is ``layer_norm(oproj(...))``.
   - ``unpack_bits``: a bit-packed mask (least significant bit first along
     the key axis) back to bytes, by explicit shifts.
   - ``rule_mask``: the dense mask a parametric rule stands for, by its
@@ -184,6 +189,28 @@ def oproj(o, w, bias=None, residual=None) -> np.ndarray:
     if residual is not None:
         y = y + np.asarray(residual, np.float64)
     return y
+
+
+def layer_norm(x, gamma=None, beta=None, eps: float = 1e-5) -> np.ndarray:
+    """LayerNorm over the last axis, fp64: (x - mean) / sqrt(var + eps) * gamma
+    + beta, with mean and var (population variance, divisor n) of each row;
+    gamma, beta: [n] or None (1 and 0)."""
+    x = np.asarray(x, np.float64)
+    n = x.shape[-1]
+    mean = x.sum(axis=-1, keepdims=True) / n
+    dev = x - mean
+    var = (dev * dev).sum(axis=-1, keepdims=True) / n
+    y = dev / np.sqrt(var + eps)
+    if gamma is not None:
+        y = y * np.asarray(gamma, np.float64)
+    if beta is not None:
+        y = y + np.asarray(beta, np.float64)
+    return y
+
+
+def oproj_ln(o, w, bias=None, residual=None, gamma=None, beta=None, eps: float = 1e-5) -> np.ndarray:
+    """layer_norm(oproj(o, w, bias, residual), gamma, beta, eps), fp64."""
+    return layer_norm(oproj(o, w, bias, residual), gamma, beta, eps)
 
 
 def unpack_bits(bits, lk: int) -> np.ndarray:

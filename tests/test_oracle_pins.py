@@ -372,3 +372,51 @@ def test_workload_rules_reproduce_the_workload_masks(name):
     w = synth.WORKLOADS[name]
     assert np.array_equal(oracle.rule_mask(w.L, w.L, **synth.workload_rule(w)), synth.make_mask(w)[0])
     assert synth.workload_rule(synth.WORKLOADS["bernoulli_L16384"]) is None
+
+
+# ---------------------------------------------------------------- LayerNorm after the projection
+
+def test_layer_norm_matches_the_library_routine():
+    import torch
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((7, 96)) * 3 + 5
+    g, b = rng.standard_normal(96), rng.standard_normal(96)
+    for eps in (1e-5, 1e-12, 0.3):
+        want = torch.nn.functional.layer_norm(torch.from_numpy(x), (96,), torch.from_numpy(g),
+                                              torch.from_numpy(b), eps).numpy()
+        assert np.allclose(oracle.layer_norm(x, g, b, eps), want, rtol=0, atol=1e-12)
+
+
+def test_layer_norm_closed_forms():
+    # a constant row has zero deviation: the output is beta
+    b = np.arange(6.0)
+    assert np.array_equal(oracle.layer_norm(np.full((1, 6), 4.25), np.ones(6), b, 1e-5)[0], b)
+    # +a, -a alternating: mean 0, variance a^2, so y = +-a / sqrt(a^2 + eps)
+    a, eps = 2.0, 0.25
+    x = np.array([[a, -a, a, -a]])
+    want = np.array([a, -a, a, -a]) / np.sqrt(a * a + eps)
+    assert np.allclose(oracle.layer_norm(x, None, None, eps)[0], want, rtol=1e-15, atol=0)
+    # gamma scales and beta shifts each feature
+    g = np.array([1.0, 2.0, -1.0, 0.5])
+    assert np.allclose(oracle.layer_norm(x, g, np.ones(4), eps)[0], want * g + 1, rtol=1e-15, atol=0)
+
+
+def test_layer_norm_invariances():
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((3, 64))
+    y = oracle.layer_norm(x, None, None, 0.0)
+    # shift invariance, positive scale invariance (eps = 0), zero mean and unit variance
+    assert np.allclose(oracle.layer_norm(x + 7.5, None, None, 0.0), y, atol=1e-12)
+    assert np.allclose(oracle.layer_norm(x * 3.0, None, None, 0.0), y, atol=1e-12)
+    assert np.allclose(y.mean(axis=-1), 0, atol=1e-14)
+    assert np.allclose((y * y).mean(axis=-1), 1, atol=1e-12)
+
+
+def test_oproj_ln_is_layer_norm_of_the_projection():
+    rng = np.random.default_rng(33)
+    o = rng.standard_normal((2, 3, 4, 8))
+    w = rng.standard_normal((16, 24))
+    bias, res = rng.standard_normal(16), rng.standard_normal((2, 4, 16))
+    g, b = rng.standard_normal(16), rng.standard_normal(16)
+    z = oracle.oproj(o, w, bias, res)
+    assert np.array_equal(oracle.oproj_ln(o, w, bias, res, g, b, 1e-5), oracle.layer_norm(z, g, b, 1e-5))
