@@ -533,22 +533,32 @@ def run_oproj(args):
     w = (torch.randn(N, H * d, device="cuda", generator=g) / (H * d) ** 0.5).to(torch.bfloat16)
     bias = torch.randn(N, device="cuda", generator=g).to(torch.bfloat16)
     res = torch.randn(B, L, N, device="cuda", generator=g).to(torch.bfloat16)
+    gamma = (1 + 0.1 * torch.randn(N, device="cuda", generator=g)).to(torch.bfloat16)
+    beta = (0.1 * torch.randn(N, device="cuda", generator=g)).to(torch.bfloat16)
     y = torch.empty(B, L, N, dtype=torch.bfloat16, device="cuda")
-    call = lambda: stof.stof_oproj_fwd(o, w, bias, res, y)  # noqa: E731
-    for _ in range(args.warmup):
-        call()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(args.steps):
-        call()
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.steps
+    ws = torch.empty(stof.stof_oproj_ln_workspace_bytes(B, L, N), dtype=torch.uint8, device="cuda")
+
+    def timed(call):
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            call()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    ms = timed(lambda: stof.stof_oproj_fwd(o, w, bias, res, y))
+    ms_ln = timed(lambda: stof.stof_oproj_ln_fwd(o, w, bias, res, gamma, beta, 1e-5, y, ws))
     flops = 2.0 * B * L * N * H * d
+    ln_bytes = 2 * B * L * N * 2  # the normalising pass reads and writes y
     print(json.dumps({"oproj": args.oproj, "B": B, "H": H, "L": L, "d": d, "N": N, "dtype": "bf16",
                       "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
                       "frac_tensor_peak": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                      "with_layernorm": {"ms": round(ms_ln, 4), "ln_pass_ms": round(ms_ln - ms, 4),
+                                         "ln_pass_gbs": round(ln_bytes / max(ms_ln - ms, 1e-6) / 1e6, 1)},
                       "peak_source": f"{peak_src} bf16 burst", "steps": args.steps, "warmup": args.warmup}),
           flush=True)
 

@@ -407,6 +407,31 @@ stof_status stof_oproj_fwd(const void* o, const void* w, const void* bias, const
                            int64_t* device_error, void* stream);
 
 /*
+ * stof_oproj_fwd() followed by a LayerNorm over the N output features of
+ * each token -- the operator that closes a post-norm transformer sublayer,
+ * fused the same way (gist.science technical summary, Methodology 2):
+ *   z = concat_heads(O) W^T + bias + residual
+ *   y[b, l, :] = (z - mean) / sqrt(var + eps) * gamma + beta
+ * with mean and var (population variance) of z[b, l, :] as rounded to dt.
+ * The GEMM's epilogue writes z and each (token, 256-feature tile)'s mean and
+ * sum of squared deviations to `workspace`; a second pass merges them and
+ * normalises y in place.
+ *   gamma, beta  device [N] or NULL (1 and 0), dt, 16-byte aligned.
+ *   eps          > 0, finite.
+ *   workspace    device, >= stof_oproj_ln_workspace_bytes(B, L, N) bytes,
+ *                16-byte aligned; caller-owned scratch.
+ * Other arguments, requirements and errors as stof_oproj_fwd().
+ * Asynchronous on stream.
+ */
+stof_status stof_oproj_ln_fwd(const void* o, const void* w, const void* bias, const void* residual, const void* gamma,
+                              const void* beta, float eps, stof_dtype dt, int B, int H, int L, int d, int N, void* y,
+                              void* workspace, size_t ws_bytes, int64_t* device_error, void* stream);
+
+/* Workspace bytes of stof_oproj_ln_fwd(): 8 per (token, 256-feature tile);
+ * 0 for invalid sizes. */
+size_t stof_oproj_ln_workspace_bytes(int B, int L, int N);
+
+/*
  * Diagnostic of the failure handling (the paper has no counterpart): every
  * pipeline wait in this library's kernels is bounded in wall time and, when
  * it runs out, ORs an error bit into a device error word and lets the

@@ -223,15 +223,17 @@ def unpack_bits(bits, lk: int) -> np.ndarray:
 
 
 def rule_mask(lq: int, lk: int, band_lo: int, band_hi: int, global_rows=None, global_cols=None,
-              blocks=None, block: int = 0) -> np.ndarray:
+              blocks=None, block: int = 0, rows=None) -> np.ndarray:
     """uint8 [lq, lk]: element (i, j) is 1 iff band_lo <= i - j <= band_hi,
     or global_rows[i], or global_cols[j], or blocks[i // block, j // block]
-    (bool arrays; None for an empty set)."""
-    i = np.arange(lq, dtype=np.int64)[:, None]
+    (bool arrays; None for an empty set).  With `rows`, only those query
+    rows ([len(rows), lk])."""
+    rows = np.arange(lq, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    i = rows[:, None]
     j = np.arange(lk, dtype=np.int64)[None, :]
     m = (i - j >= band_lo) & (i - j <= band_hi)
     if global_rows is not None:
-        m = m | np.asarray(global_rows, bool)[:, None]
+        m = m | np.asarray(global_rows, bool)[rows][:, None]
     if global_cols is not None:
         m = m | np.asarray(global_cols, bool)[None, :]
     if blocks is not None:

@@ -28,11 +28,23 @@
 //               next.
 // Every wait is bounded; on timeout the CTA raises STOF_DEVERR_PIPE_TIMEOUT
 // in the caller's error word (if given), drains and exits.
+//
+// LayerNorm after the projection (stof_oproj_ln_fwd, a post-norm sublayer's
+// last operator): a token's normalisation needs all N of its features, which
+// span N / 256 output tiles computed by different CTAs.  The epilogue
+// therefore also reduces each (token, tile) row of rounded outputs to its
+// mean and sum of squared deviations (shifted by the row's first value, so
+// no cancellation), written to a small workspace; a second, memory-bound
+// pass merges a token's tile statistics (Chan, Golub and LeVeque's pairwise
+// update) and normalises y in place: (y - mean) / sqrt(var + eps) * gamma +
+// beta in fp32, rounded once.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+
+#include <cmath>
 
 #include "internal.h"
 #include "sm100_ptx.cuh"
@@ -67,9 +79,20 @@ struct OpParams {
   const void* bias;      // [N] or null
   const void* residual;  // [B][L][N] or null
   void* y;               // [B][L][N]
+  float2* stats;         // [B*L][n_tiles] (mean, sum of squared deviations) of each tile row, or null
   int64_t* err;          // device error word or null
   int B, H, L, d, N;
   int m_tiles, n_tiles, k_blocks;
+};
+
+struct LnParams {
+  const float2* stats;   // [rows][n_tiles]
+  void* y;               // [rows][N], normalised in place
+  const void* gamma;     // [N] or null
+  const void* beta;      // [N] or null
+  float eps;
+  long long rows;
+  int N, n_tiles;
 };
 
 template <bool BF16>
@@ -220,6 +243,7 @@ __global__ void __launch_bounds__(kThreadsOP, 1)
       const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
       const long long row = static_cast<long long>(mt) * kTM + r;
       const int n0 = nt * kTN;
+      float x0 = 0.f, s1 = 0.f, s2 = 0.f;  // LayerNorm statistics of the row's rounded outputs
 #pragma unroll 1
       for (int cc = 0; cc < kTN / 32; ++cc) {
         uint32_t acc[32];
@@ -255,12 +279,25 @@ __global__ void __launch_bounds__(kThreadsOP, 1)
             }
           }
         }
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) pk[q] = pack2f<BF16>(v[2 * q], v[2 * q + 1]);
         uint4* dst = reinterpret_cast<uint4*>(y + row * p.N + n);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          dst[q] = make_uint4(pack2f<BF16>(v[8 * q], v[8 * q + 1]), pack2f<BF16>(v[8 * q + 2], v[8 * q + 3]),
-                              pack2f<BF16>(v[8 * q + 4], v[8 * q + 5]), pack2f<BF16>(v[8 * q + 6], v[8 * q + 7]));
+        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        if (p.stats) {
+          if (cc == 0) x0 = to_f32<BF16>(static_cast<uint16_t>(pk[0] & 0xFFFFu));
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float lo = to_f32<BF16>(static_cast<uint16_t>(pk[q] & 0xFFFFu)) - x0;
+            const float hi = to_f32<BF16>(static_cast<uint16_t>(pk[q] >> 16)) - x0;
+            s1 += lo + hi;
+            s2 = fmaf(lo, lo, fmaf(hi, hi, s2));
+          }
+        }
       }
+      if (p.stats)
+        p.stats[row * p.n_tiles + nt] = make_float2(x0 + s1 / kTN, s2 - s1 * s1 / kTN);
       tc_fence_before();
       mbar_arrive(&s.acc_empty[a]);
     }
@@ -271,6 +308,68 @@ __global__ void __launch_bounds__(kThreadsOP, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
+  }
+}
+
+// ---------------------------------------------------------------- LayerNorm pass
+// One warp per token row of y (N features, N % 256 == 0): the row's
+// per-tile statistics (mean and sum of squared deviations of the rounded
+// outputs of each 256-wide tile) are merged by Chan et al.'s pairwise
+// update, then y is normalised in place: (y - mean) / sqrt(var + eps) *
+// gamma + beta, in fp32, rounded once.
+template <bool BF16>
+__global__ void __launch_bounds__(256) layernorm_kernel(const LnParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= p.rows) return;  // warp-uniform
+  // merge the row's n_tiles statistics: lanes take tiles, then a shuffle tree
+  float cnt = 0.f, mean = 0.f, m2 = 0.f;
+  for (int t = lane; t < p.n_tiles; t += 32) {
+    const float2 st = p.stats[row * p.n_tiles + t];
+    const float nb = static_cast<float>(kTN);
+    const float n = cnt + nb;
+    const float delta = st.x - mean;
+    mean += delta * (nb / n);
+    m2 += st.y + delta * delta * (cnt * nb / n);
+    cnt = n;
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const float cb = __shfl_xor_sync(0xffffffffu, cnt, off);
+    const float mb = __shfl_xor_sync(0xffffffffu, mean, off);
+    const float qb = __shfl_xor_sync(0xffffffffu, m2, off);
+    const float n = cnt + cb;
+    if (n > 0.f) {
+      const float delta = mb - mean;
+      mean += delta * (cb / n);
+      m2 += qb + delta * delta * (cnt * cb / n);
+      cnt = n;
+    }
+  }
+  const float var = m2 / static_cast<float>(p.N);
+  const float rstd = 1.f / sqrtf(var + p.eps);
+  uint16_t* y = static_cast<uint16_t*>(p.y) + row * p.N;
+  const uint16_t* gamma = static_cast<const uint16_t*>(p.gamma);
+  const uint16_t* beta = static_cast<const uint16_t*>(p.beta);
+  for (int c = lane * 8; c < p.N; c += 256) {  // 8 features (16 bytes) per lane per step
+    const uint4 yv = *reinterpret_cast<const uint4*>(y + c);
+    const uint4 gv = gamma ? __ldg(reinterpret_cast<const uint4*>(gamma + c)) : make_uint4(0, 0, 0, 0);
+    const uint4 bv = beta ? __ldg(reinterpret_cast<const uint4*>(beta + c)) : make_uint4(0, 0, 0, 0);
+    const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float v[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint16_t ys = static_cast<uint16_t>(yw[e] >> (16 * hh));
+        const float g = gamma ? to_f32<BF16>(static_cast<uint16_t>(gw[e] >> (16 * hh))) : 1.f;
+        const float bb = beta ? to_f32<BF16>(static_cast<uint16_t>(bw[e] >> (16 * hh))) : 0.f;
+        v[hh] = fmaf((to_f32<BF16>(ys) - mean) * rstd, g, bb);
+      }
+      out[e] = pack2f<BF16>(v[0], v[1]);
+    }
+    *reinterpret_cast<uint4*>(y + c) = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
 
@@ -297,14 +396,16 @@ stof_status launch_op(const void* o, const void* w, const OpParams& p, cudaStrea
   return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
 }
 
-}  // namespace
-}  // namespace stof
+template <bool BF16>
+stof_status launch_ln(const LnParams& lp, cudaStream_t s) {
+  const long long blocks = (lp.rows + 7) / 8;
+  layernorm_kernel<BF16><<<static_cast<unsigned>(blocks), 256, 0, s>>>(lp);
+  return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
+}
 
-using namespace stof;
-
-extern "C" stof_status stof_oproj_fwd(const void* o, const void* w, const void* bias, const void* residual,
-                                      stof_dtype dt, int B, int H, int L, int d, int N, void* y,
-                                      int64_t* device_error, void* stream) {
+// Argument checks shared by both entry points; fills p.
+stof_status check_op(const void* o, const void* w, const void* bias, const void* residual, stof_dtype dt, int B,
+                     int H, int L, int d, int N, void* y, int64_t* device_error, OpParams* p) {
   if (!o || !w || !y) return STOF_ERR_INVALID_ARG;
   if (dt != STOF_F16 && dt != STOF_BF16) return STOF_ERR_DTYPE;
   if (B < 1 || H < 1 || L < 1 || d < 1 || N < 1) return STOF_ERR_INVALID_ARG;
@@ -316,19 +417,65 @@ extern "C" stof_status stof_oproj_fwd(const void* o, const void* w, const void* 
   auto al16 = [](const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; };
   if (!al16(o) || !al16(w) || !al16(y) || (bias && !al16(bias)) || (residual && !al16(residual)))
     return STOF_ERR_ALIGNMENT;
+  p->bias = bias;
+  p->residual = residual;
+  p->y = y;
+  p->stats = nullptr;
+  p->err = device_error;
+  p->B = B;
+  p->H = H;
+  p->L = L;
+  p->d = d;
+  p->N = N;
+  p->m_tiles = B * L / kTM;
+  p->n_tiles = N / kTN;
+  p->k_blocks = H * d / kTK;
+  return STOF_OK;
+}
+
+}  // namespace
+}  // namespace stof
+
+using namespace stof;
+
+extern "C" stof_status stof_oproj_fwd(const void* o, const void* w, const void* bias, const void* residual,
+                                      stof_dtype dt, int B, int H, int L, int d, int N, void* y,
+                                      int64_t* device_error, void* stream) {
   OpParams p;
-  p.bias = bias;
-  p.residual = residual;
-  p.y = y;
-  p.err = device_error;
-  p.B = B;
-  p.H = H;
-  p.L = L;
-  p.d = d;
-  p.N = N;
-  p.m_tiles = B * L / kTM;
-  p.n_tiles = N / kTN;
-  p.k_blocks = H * d / kTK;
+  const stof_status st = check_op(o, w, bias, residual, dt, B, H, L, d, N, y, device_error, &p);
+  if (st != STOF_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return dt == STOF_BF16 ? launch_op<true>(o, w, p, s) : launch_op<false>(o, w, p, s);
+}
+
+extern "C" size_t stof_oproj_ln_workspace_bytes(int B, int L, int N) {
+  if (B < 1 || L < 1 || N < 1 || N % kTN) return 0;
+  return static_cast<size_t>(B) * L * (N / kTN) * sizeof(float2);
+}
+
+extern "C" stof_status stof_oproj_ln_fwd(const void* o, const void* w, const void* bias, const void* residual,
+                                         const void* gamma, const void* beta, float eps, stof_dtype dt, int B,
+                                         int H, int L, int d, int N, void* y, void* workspace, size_t ws_bytes,
+                                         int64_t* device_error, void* stream) {
+  OpParams p;
+  stof_status st = check_op(o, w, bias, residual, dt, B, H, L, d, N, y, device_error, &p);
+  if (st != STOF_OK) return st;
+  if (!workspace || !(eps > 0.f) || !std::isfinite(eps)) return STOF_ERR_INVALID_ARG;
+  if (ws_bytes < stof_oproj_ln_workspace_bytes(B, L, N)) return STOF_ERR_WORKSPACE;
+  auto al16 = [](const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; };
+  if (!al16(workspace) || (gamma && !al16(gamma)) || (beta && !al16(beta))) return STOF_ERR_ALIGNMENT;
+  p.stats = static_cast<float2*>(workspace);
+  LnParams lp;
+  lp.stats = p.stats;
+  lp.y = y;
+  lp.gamma = gamma;
+  lp.beta = beta;
+  lp.eps = eps;
+  lp.rows = static_cast<long long>(B) * L;
+  lp.N = N;
+  lp.n_tiles = N / kTN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = dt == STOF_BF16 ? launch_op<true>(o, w, p, s) : launch_op<false>(o, w, p, s);
+  if (st != STOF_OK) return st;
+  return dt == STOF_BF16 ? launch_ln<true>(lp, s) : launch_ln<false>(lp, s);
 }

@@ -44,7 +44,7 @@ EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync
             "stof_last_cuda_error", "stof_tune_workspace_bytes", "stof_tune", "stof_tune_lookup",
             "stof_tune_clear", "stof_tune_density_bucket", "stof_encode_mask_bits", "stof_oproj_fwd",
             "stof_encode_rules", "stof_check_bounded_wait", "stof_mha_plan", "stof_mha_fwd_plan",
-            "stof_select_kernel_heads"]
+            "stof_select_kernel_heads", "stof_oproj_ln_fwd", "stof_oproj_ln_workspace_bytes"]
 
 STOF_MAX_RULES = 64
 INT32_MIN, INT32_MAX = -(1 << 31), (1 << 31) - 1
@@ -148,6 +148,11 @@ def load_library(path: str = LIB_PATH):
         lib.stof_last_cuda_error.restype = ctypes.c_char_p
         lib.stof_oproj_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]
         lib.stof_oproj_fwd.restype = i32
+        lib.stof_oproj_ln_fwd.argtypes = [P, P, P, P, P, P, ctypes.c_float, i32, i32, i32, i32, i32, i32, P, P, sz,
+                                          P, P]
+        lib.stof_oproj_ln_fwd.restype = i32
+        lib.stof_oproj_ln_workspace_bytes.argtypes = [i32, i32, i32]
+        lib.stof_oproj_ln_workspace_bytes.restype = sz
         lib.stof_tune_workspace_bytes.argtypes = [i32, i32]
         lib.stof_tune_workspace_bytes.restype = sz
         lib.stof_tune.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, i32, ctypes.c_float, i64, i64, P, sz, P,
@@ -349,6 +354,37 @@ def stof_oproj_fwd(o: torch.Tensor, w: torch.Tensor, bias: torch.Tensor | None, 
     _check(load_library().stof_oproj_fwd(
         o.data_ptr(), w.data_ptr(), ptr(bias), ptr(residual), _dtype_code(o), B, H, L, d, N, y.data_ptr(),
         ptr(device_error), _stream(stream)), "stof_oproj_fwd")
+    return y
+
+
+def stof_oproj_ln_workspace_bytes(B: int, L: int, N: int) -> int:
+    return int(load_library().stof_oproj_ln_workspace_bytes(int(B), int(L), int(N)))
+
+
+def stof_oproj_ln_fwd(o: torch.Tensor, w: torch.Tensor, bias: torch.Tensor | None, residual: torch.Tensor | None,
+                      gamma: torch.Tensor | None, beta: torch.Tensor | None, eps: float, y: torch.Tensor,
+                      workspace: torch.Tensor, device_error: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """stof_oproj_fwd followed by a LayerNorm over the N features (gamma, beta: [N] or None);
+    workspace: device tensor of at least stof_oproj_ln_workspace_bytes(B, L, N) bytes."""
+    if o.dim() != 4:
+        raise StofError(STOF_ERR_SHAPE, "stof_oproj_ln_fwd: o must be [B, H, L, d]")
+    B, H, L, d = o.shape
+    N = w.shape[0]
+    if w.shape != (N, H * d) or y.shape != (B, L, N):
+        raise StofError(STOF_ERR_SHAPE, "stof_oproj_ln_fwd: w must be [N, H*d] and y [B, L, N]")
+    for t in (o, w, y, bias, residual, gamma, beta):
+        if t is not None and (t.dtype != o.dtype or not t.is_contiguous()):
+            raise StofError(STOF_ERR_SHAPE, "stof_oproj_ln_fwd: tensors must share o's dtype and be contiguous")
+    for t in (bias, gamma, beta):
+        if t is not None and t.shape != (N,):
+            raise StofError(STOF_ERR_SHAPE, "stof_oproj_ln_fwd: bias, gamma and beta must be [N]")
+    if residual is not None and residual.shape != (B, L, N):
+        raise StofError(STOF_ERR_SHAPE, "stof_oproj_ln_fwd: residual must be [B, L, N]")
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    _check(load_library().stof_oproj_ln_fwd(
+        o.data_ptr(), w.data_ptr(), ptr(bias), ptr(residual), ptr(gamma), ptr(beta), float(eps), _dtype_code(o),
+        B, H, L, d, N, y.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        ptr(device_error), _stream(stream)), "stof_oproj_ln_fwd")
     return y
 
 

@@ -150,3 +150,38 @@ def test_maximum_rule_count(gpu_lib):
     rules = [_random_rule(rng, L, L, blk) for _ in range(stof.STOF_MAX_RULES)]
     fmt, ws, arrs = _encode_rules(rules, L, L, 64, 64)
     assert_format_equal(fmt, arrs, oracle.encode(_oracle_masks(rules, L, L), 64, 64))
+
+
+@pytest.mark.parametrize("kern", ["block", "row"])
+def test_64k_tokens_from_a_rule(gpu_lib, kern):
+    """A 65,536-token causal sliding window (4096 keys) with 16 global
+    tokens, two heads, d = 128: the mask would be 4 GB as bytes and is never
+    materialised.  Sampled OT rows of the format bit-exact against the
+    oracle's encoding of the same rows; sampled query rows of O against the
+    oracle (the first, the last and seeded others)."""
+    L, H, d = 65536, 2, 128
+    rng = np.random.default_rng(64)
+    g = np.zeros(L, bool)
+    g[rng.choice(L, 16, replace=False)] = True
+    rule = {"band_lo": 0, "band_hi": 4095, "global_rows": g, "global_cols": g, "blocks": None, "block": 0}
+    fmt, ws, arrs = _encode_rules([rule], L, L, 128, 128)
+    frp, prp = arrs["full_row_ptr"], arrs["part_row_ptr"]
+    for I in [0, 1, 31, 32, 511] + [int(x) for x in rng.choice(512, 4, replace=False)]:
+        want = oracle.encode(oracle.rule_mask(L, L, rows=np.arange(I * 128, I * 128 + 128), **rule)[None], 128, 128)
+        assert frp[I + 1] - frp[I] == want["n_full"] and prp[I + 1] - prp[I] == want["n_part"]
+        assert np.array_equal(arrs["full_col_idx"][frp[I]:frp[I + 1]], want["full_col_idx"])
+        assert np.array_equal(arrs["part_col_idx"][prp[I]:prp[I + 1]], want["part_col_idx"])
+        assert np.array_equal(arrs["bitmaps"][prp[I]:prp[I + 1]], want["bitmaps"])
+    q, k, v = synth.make_qkv(1, H, L, d, "bf16", seed=65)
+    o = torch.full((1, H, L, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    which = stof.STOF_KERNEL_BLOCKWISE if kern == "block" else stof.STOF_KERNEL_ROWWISE
+    stof.stof_mha_fwd(q.cuda(), k.cuda(), v.cuda(), fmt, 1 / math.sqrt(d), 0, 0, which, o)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.arange(32), rng.choice(L, 96, replace=False), np.arange(L - 32, L),
+                                     np.flatnonzero(g)]))
+    q64, k64, v64 = (synth.to_float64(t) for t in (q, k, v))
+    ref = oracle.attention_bhld(q64, k64, v64, lambda b, h, r: oracle.rule_mask(L, L, rows=r, **rule),
+                                1 / math.sqrt(d), rows=rows)
+    og = o.double().cpu().numpy()
+    for (b, h), o_ref in ref.items():
+        assert np.abs(og[b, h, rows] - o_ref).max() <= 1.5e-2

@@ -82,3 +82,90 @@ def test_shape_errors(gpu_lib):
     with pytest.raises(stof.StofError) as e:
         stof.stof_oproj_fwd(o, w, None, None, y)
     assert e.value.status == stof.STOF_ERR_SHAPE          # N not a multiple of 256
+
+
+# ---------------------------------------------------------------- with the LayerNorm that follows
+
+def _ln_case(B, H, L, d, N, dtype, affine=True, offset=0.0, eps=1e-5, seed=0):
+    """stof_oproj_ln_fwd against oracle.oproj_ln.  Error bound from the
+    arithmetic: the pre-norm value z is rounded once to the input type
+    (relative error u = 2^-8 for bf16, 2^-11 for fp16) before its statistics
+    are taken, which moves a normalised value by at most
+    u (|z_i| + mean|z| (1 + |y'_i|)) / sigma (y' = (z_i - mean) / sigma),
+    scaled by |gamma_i|; the output's own rounding adds u |y|.  The test
+    allows twice that sum."""
+    u = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11}[dtype]
+    g = torch.Generator().manual_seed(seed)
+    o = torch.randn(B, H, L, d, generator=g).to(DT[dtype])
+    w = (torch.randn(N, H * d, generator=g) / (H * d) ** 0.5).to(DT[dtype])
+    b = (0.1 * torch.randn(N, generator=g)).to(DT[dtype])
+    r = (torch.randn(B, L, N, generator=g) + offset).to(DT[dtype])
+    gamma = (1 + 0.5 * torch.randn(N, generator=g)).to(DT[dtype]) if affine else None
+    beta = (0.2 * torch.randn(N, generator=g)).to(DT[dtype]) if affine else None
+    err = torch.zeros(1, dtype=torch.int64, device="cuda")
+    y = torch.full((B, L, N), float("nan"), dtype=DT[dtype], device="cuda")
+    ws = torch.empty(stof.stof_oproj_ln_workspace_bytes(B, L, N), dtype=torch.uint8, device="cuda")
+    cuda = lambda t: None if t is None else t.cuda()  # noqa: E731
+    stof.stof_oproj_ln_fwd(o.cuda(), w.cuda(), b.cuda(), r.cuda(), cuda(gamma), cuda(beta), eps, y, ws, err)
+    torch.cuda.synchronize()
+    f64 = lambda t: None if t is None else t.double().numpy()  # noqa: E731
+    z = oracle.oproj(f64(o), f64(w), f64(b), f64(r))
+    want = oracle.oproj_ln(f64(o), f64(w), f64(b), f64(r), f64(gamma), f64(beta), eps)
+    got = y.double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    mean = z.mean(axis=-1, keepdims=True)
+    sigma = np.sqrt(z.var(axis=-1, keepdims=True) + eps)
+    m_abs = np.abs(z).mean(axis=-1, keepdims=True)
+    g_abs = np.abs(f64(gamma)) if gamma is not None else 1.0
+    bound = 2 * u * (np.abs(want) + g_abs * (np.abs(z) + m_abs * (1 + np.abs((z - mean) / sigma))) / sigma)
+    assert np.all(np.abs(got - want) <= bound), float(np.max(np.abs(got - want) / bound))
+    assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_ln_bert_base_layer_shape(gpu_lib, dtype):
+    _ln_case(16, 12, 512, 64, 768, dtype, seed=5)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("affine", [True, False])
+def test_ln_llama_width(gpu_lib, dtype, affine):
+    _ln_case(1, 32, 256, 128, 4096, dtype, affine=affine, seed=6)
+
+
+def test_ln_rows_far_from_zero_mean(gpu_lib):
+    # residual stream offset by 40: the statistics must not cancel
+    _ln_case(2, 4, 128, 64, 512, "fp16", offset=40.0, seed=7)
+
+
+def test_ln_constant_row_gives_beta(gpu_lib):
+    """O = 0 and no bias: z is the residual; a constant residual row has no
+    deviation, so its output is beta exactly."""
+    B, H, L, d, N = 1, 2, 128, 64, 256
+    o = torch.zeros(B, H, L, d, dtype=torch.bfloat16, device="cuda")
+    w = torch.randn(N, H * d, device="cuda").to(torch.bfloat16)
+    r = torch.randn(B, L, N, device="cuda").to(torch.bfloat16)
+    r[0, 3] = 2.5
+    beta = torch.randn(N, device="cuda").to(torch.bfloat16)
+    gamma = torch.randn(N, device="cuda").to(torch.bfloat16)
+    y = torch.empty(B, L, N, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(stof.stof_oproj_ln_workspace_bytes(B, L, N), dtype=torch.uint8, device="cuda")
+    stof.stof_oproj_ln_fwd(o, w, None, r, gamma, beta, 1e-5, y, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y[0, 3], beta)
+
+
+def test_ln_argument_errors(gpu_lib):
+    B, H, L, d, N = 1, 2, 128, 64, 256
+    o = torch.zeros(B, H, L, d, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(N, H * d, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(B, L, N, dtype=torch.bfloat16, device="cuda")
+    need = stof.stof_oproj_ln_workspace_bytes(B, L, N)
+    big = torch.empty(need + 16, dtype=torch.uint8, device="cuda")
+    ws = big[:need]
+    for eps, wsp, status in ((0.0, ws, stof.STOF_ERR_INVALID_ARG), (float("nan"), ws, stof.STOF_ERR_INVALID_ARG),
+                             (1e-5, ws[:-8], stof.STOF_ERR_WORKSPACE),
+                             (1e-5, big[8:8 + need], stof.STOF_ERR_ALIGNMENT)):
+        with pytest.raises(stof.StofError) as e:
+            stof.stof_oproj_ln_fwd(o, w, None, None, None, None, eps, y, wsp)
+        assert e.value.status == status

@@ -420,3 +420,12 @@ def test_oproj_ln_is_layer_norm_of_the_projection():
     g, b = rng.standard_normal(16), rng.standard_normal(16)
     z = oracle.oproj(o, w, bias, res)
     assert np.array_equal(oracle.oproj_ln(o, w, bias, res, g, b, 1e-5), oracle.layer_norm(z, g, b, 1e-5))
+
+
+def test_rule_mask_rows_are_rows_of_the_whole_mask():
+    rng = np.random.default_rng(34)
+    L = 96
+    r = dict(band_lo=-5, band_hi=9, global_rows=rng.random(L) < 0.1, global_cols=rng.random(L) < 0.1,
+             blocks=rng.random((L // 8, L // 8)) < 0.2, block=8)
+    rows = np.array([0, 7, 8, 50, 95])
+    assert np.array_equal(oracle.rule_mask(L, L, rows=rows, **r), oracle.rule_mask(L, L, **r)[rows])
