@@ -413,6 +413,24 @@ def call_latency(lib_fn, args, reps: int = 15):
     return statistics.median(dev_ms), statistics.median(host_us)
 
 
+def back_to_back(lib_fn, args, n: int = 20):
+    """n C-ABI calls issued back to back (no synchronisation between them, as
+    a pipeline issues them): event time per call on the stream and host time
+    per call (microseconds)."""
+    import torch
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    t0 = time.perf_counter_ns()
+    for _ in range(n):
+        if lib_fn(*args) != 0:
+            raise RuntimeError("call failed")
+    t1 = time.perf_counter_ns()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n, (t1 - t0) / 1e3 / n
+
+
 def host_time_us(fn, args) -> float:
     """Host time of one C-ABI call through ctypes (microseconds)."""
     t0 = time.perf_counter_ns()
@@ -466,11 +484,14 @@ def workload_record(w: synth.Workload, mask, q, k, v, peaks, flush) -> dict:
                 ctypes.c_float(scale), ctypes.byref(fmt), w.stride_b, w.stride_h, which, o.data_ptr(),
                 torch.cuda.current_stream().cuda_stream)
         lat_ms, host_us = call_latency(lib.stof_mha_fwd, args)
+        b2b_ms, b2b_host_us = back_to_back(lib.stof_mha_fwd, args, max(5, min(40, int(40.0 / max(warm, 1e-3)))))
         plan_args = (ctypes.byref(fmt), B, H, L, d, which, ctypes.byref(stof.stof_plan()))
         plan_us = statistics.median(host_time_us(lib.stof_mha_plan, plan_args) for _ in range(15))
         r = {"kernel_ms": round(warm, 5), "kernel_ms_cold_l2": round(cold, 5), "call_ms": round(lat_ms, 5),
              "call_minus_kernel_us": round((lat_ms - warm) * 1e3, 2), "host_us": round(host_us, 2),
              "plan_host_us": round(plan_us, 2),
+             "back_to_back_ms_per_call": round(b2b_ms, 5), "back_to_back_host_us": round(b2b_host_us, 2),
+             "back_to_back_minus_kernel_us": round((b2b_ms - warm) * 1e3, 2),
              "effective_tflops": round(eff_flops / (warm * 1e-3) / 1e12, 3)}
         if name == "blockwise":
             r["variant"] = ("persistent" if w.d == 64 and tiles / n_rows < 48 else "cta_per_query_tile")

@@ -87,7 +87,10 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-template <int D, int BN, bool BF16, int ST>
+// NEG: the softmax scale is not positive (the scores are multiplied by it
+// before masking and the row max); a separate instance, so that the usual
+// positive scale pays no test.
+template <int D, int BN, bool BF16, int ST, bool NEG>
 __global__ void __launch_bounds__(kThreads, 1)
     blockwise_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -315,10 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tSr = tS + lane_off;
     const uint32_t tP = tP0 + g * 64 + lane_off;
     const uint32_t tO = tO0 + g * D + lane_off;
-    // c <= 0: the scores are multiplied by c before masking and the max, and
+    // NEG: the scores are multiplied by c before masking and the max, and
     // the softmax below runs with a factor of 1
-    const bool prescale = p.scale_log2 <= 0.f;
-    const float c = prescale ? 1.f : p.scale_log2;
+    const float c = NEG ? 1.f : p.scale_log2;
     // row r of an OT's bitmaps: byte r % 8 of words (r / 8) * BN / 8 + 0 .. BN / 8 - 1
     const uint8_t* bits_row = reinterpret_cast<const uint8_t*>(p.bitmaps) + (r >> 3) * BN + (r & 7);
     uint32_t nb[BN / 8];  // bitmap bytes of this warpgroup's next partial tile, loaded a tile ahead
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t bits[C::CHUNKS] = {};
       if (partial) assemble_bits<C::CHUNKS>(nb, bits);
       fetch_bits(t + 2);                        // the bytes of this warpgroup's next tile
-      if (prescale) scale_scores(sr, p.scale_log2);
+      if constexpr (NEG) scale_scores(sr, p.scale_log2);
       if (partial) mask_scores(sr, bits);       // keep only the keys whose bit is set
       const float mt = row_max(sr) * c;
       float alpha = 1.f;
@@ -494,7 +496,7 @@ bool make_bw_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box
 
 namespace {
 
-template <int D, int BN, bool BF16, int ST>
+template <int D, int BN, bool BF16, int ST, bool NEG>
 stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.L;
   CUtensorMap mq, mk, mv;
@@ -505,14 +507,14 @@ stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
   stof_status prep = STOF_OK;
   auto prepare = [](const void* arg) {
     stof_status* st = static_cast<stof_status*>(const_cast<void*>(arg));
-    if (record_cuda(cudaFuncSetAttribute(blockwise_kernel<D, BN, BF16, ST>,
+    if (record_cuda(cudaFuncSetAttribute(blockwise_kernel<D, BN, BF16, ST, NEG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sizeof(Smem<D, BN, ST>) + 1024))) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
     cudaFuncAttributes fa;
-    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_kernel<D, BN, BF16, ST>)) != cudaSuccess) {
+    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_kernel<D, BN, BF16, ST, NEG>)) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
@@ -522,10 +524,10 @@ stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
     }
     return true;
   };
-  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_kernel<D, BN, BF16, ST>), prepare, &prep))
+  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_kernel<D, BN, BF16, ST, NEG>), prepare, &prep))
     return prep;
   const long long grid = static_cast<long long>(p.B) * p.H * p.n_tr;
-  blockwise_kernel<D, BN, BF16, ST><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
+  blockwise_kernel<D, BN, BF16, ST, NEG><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
   return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
 }
 
@@ -533,7 +535,9 @@ stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
 
 template <int D, int BN, int ST>
 stof_status launch_bw_t(const AttnParams& p, bool bf16, cudaStream_t s) {
-  return bf16 ? launch_bw<D, BN, true, ST>(p, s) : launch_bw<D, BN, false, ST>(p, s);
+  if (p.scale_log2 > 0.f)
+    return bf16 ? launch_bw<D, BN, true, ST, false>(p, s) : launch_bw<D, BN, false, ST, false>(p, s);
+  return bf16 ? launch_bw<D, BN, true, ST, true>(p, s) : launch_bw<D, BN, false, ST, true>(p, s);
 }
 
 stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s) {

@@ -94,7 +94,8 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int idx) {
   return it;
 }
 
-template <int BN, bool BF16, int kRing>
+// NEG: the softmax scale is not positive (see blockwise.cu).
+template <int BN, bool BF16, int kRing, bool NEG>
 __global__ void __launch_bounds__(kThreads, 1)
     blockwise_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                              const __grid_constant__ CUtensorMap tmV, const AttnParams p, const int n_items) {
@@ -359,10 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tSr = tS + lane_off;
     const uint32_t tP = tP0 + g * 64 + lane_off;
-    // c <= 0: the scores are multiplied by c before masking and the max, and
+    // NEG: the scores are multiplied by c before masking and the max, and
     // the softmax below runs with a factor of 1
-    const bool prescale = p.scale_log2 <= 0.f;
-    const float c = prescale ? 1.f : p.scale_log2;
+    const float c = NEG ? 1.f : p.scale_log2;
     const uint8_t* bits_r = reinterpret_cast<const uint8_t*>(p.bitmaps) + (r >> 3) * BN + (r & 7);
     int J = 0;   // tiles of this warpgroup so far, all items
     int e = 0;   // items with tiles so far
@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t bits[C::CHUNKS] = {};
         if (partial) assemble_bits<C::CHUNKS>(nb, bits);
         fetch_bits(t + 2);                        // the bytes of this warpgroup's next tile
-        if (prescale) scale_scores(sr, p.scale_log2);
+        if constexpr (NEG) scale_scores(sr, p.scale_log2);
         if (partial) mask_scores(sr, bits);       // keep only the keys whose bit is set
         const float mt = row_max(sr) * c;
         float alpha = 1.f;
@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, bool BF16, int RING>
+template <int BN, bool BF16, int RING, bool NEG>
 stof_status launch_persist(const AttnParams& p, cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.L;
   CUtensorMap mq, mk, mv;
@@ -528,14 +528,14 @@ stof_status launch_persist(const AttnParams& p, cudaStream_t s) {
   stof_status prep = STOF_OK;
   auto prepare = [](const void* arg) {
     stof_status* st = static_cast<stof_status*>(const_cast<void*>(arg));
-    if (record_cuda(cudaFuncSetAttribute(blockwise_persist_kernel<BN, BF16, RING>,
+    if (record_cuda(cudaFuncSetAttribute(blockwise_persist_kernel<BN, BF16, RING, NEG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sizeof(PSmem<BN, RING>) + 1024))) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
     cudaFuncAttributes fa;
-    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_persist_kernel<BN, BF16, RING>)) != cudaSuccess) {
+    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_persist_kernel<BN, BF16, RING, NEG>)) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
@@ -545,15 +545,22 @@ stof_status launch_persist(const AttnParams& p, cudaStream_t s) {
     }
     return true;
   };
-  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_persist_kernel<BN, BF16, RING>), prepare, &prep))
+  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_persist_kernel<BN, BF16, RING, NEG>), prepare, &prep))
     return prep;
   // one resident CTA per SM, each taking items from the work counter
   const long long n_items = static_cast<long long>(p.B) * p.H * p.n_tr;
   const long long sms = device_sm_count();
   const long long grid = n_items < sms ? n_items : sms;
-  blockwise_persist_kernel<BN, BF16, RING><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(
+  blockwise_persist_kernel<BN, BF16, RING, NEG><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(
       mq, mk, mv, p, static_cast<int>(n_items));
   return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
+}
+
+template <int BN, int RING>
+stof_status launch_persist_t(const AttnParams& p, bool bf16, cudaStream_t s) {
+  if (p.scale_log2 > 0.f)
+    return bf16 ? launch_persist<BN, true, RING, false>(p, s) : launch_persist<BN, false, RING, false>(p, s);
+  return bf16 ? launch_persist<BN, true, RING, true>(p, s) : launch_persist<BN, false, RING, true>(p, s);
 }
 
 }  // namespace
@@ -563,11 +570,11 @@ stof_status launch_blockwise_persist64(const AttnParams& p, bool bf16, cudaStrea
   const int ring = p.stages ? p.stages : kDefaultRing;
   if (p.bn == 64) {
     if (ring != kDefaultRing) return STOF_ERR_UNSUPPORTED;
-    return bf16 ? launch_persist<64, true, kDefaultRing>(p, s) : launch_persist<64, false, kDefaultRing>(p, s);
+    return launch_persist_t<64, kDefaultRing>(p, bf16, s);
   }
-  if (ring == 2) return bf16 ? launch_persist<128, true, 2>(p, s) : launch_persist<128, false, 2>(p, s);
-  if (ring == 3) return bf16 ? launch_persist<128, true, 3>(p, s) : launch_persist<128, false, 3>(p, s);
-  if (ring == 4) return bf16 ? launch_persist<128, true, 4>(p, s) : launch_persist<128, false, 4>(p, s);
+  if (ring == 2) return launch_persist_t<128, 2>(p, bf16, s);
+  if (ring == 3) return launch_persist_t<128, 3>(p, bf16, s);
+  if (ring == 4) return launch_persist_t<128, 4>(p, bf16, s);
   return STOF_ERR_UNSUPPORTED;
 }
 
