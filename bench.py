@@ -505,6 +505,19 @@ def workload_record(w: synth.Workload, mask, q, k, v, peaks, flush) -> dict:
         times[name] = warm
     rec["fastest"] = min(times, key=times.get)
     rec["selector_picks_fastest"] = rec["fastest"] == rec["selected"]
+    # the measured choice (stof_tune: every candidate, cached) and what AUTO then runs
+    wst = torch.empty(stof.stof_tune_workspace_bytes(n_masks, w.L), dtype=torch.uint8, device=q.device)
+    stof.stof_tune_clear()
+    tr = stof.stof_tune(mask, q, k, v, scale, w.stride_b, w.stride_h, wst, o)
+    del wst
+    names = ["rowwise_rpw1", "rowwise_rpw2", "rowwise_rpw4", "blockwise_st3", "blockwise_st2", "blockwise_st4",
+             "blockwise_persistent_st4", "blockwise_persistent_st3", "blockwise_persistent_st2", "blockwise_128x64"]
+    plan = stof.stof_mha_plan(fmt, w.B, w.H, w.L, w.d, stof.STOF_KERNEL_AUTO)
+    rec["tuned"] = {"candidates_ms": {nm: round(float(t), 5) for nm, t in zip(names, tr.cand_ms) if t > 0},
+                    "auto_after_tuning": {"kernel": "blockwise" if plan.kernel == stof.STOF_KERNEL_BLOCKWISE
+                                          else "rowwise", "stages": plan.stages, "persistent": plan.persistent,
+                                          "rows_per_warp": plan.rows_per_warp, "source": plan.source}}
+    stof.stof_tune_clear()
     rec["l2"] = ("inputs fit in L2: kernel_ms warm (back to back), kernel_ms_cold_l2 with a 256 MB write "
                  "before each call" if q.numel() * 6 < L2_BYTES else "inputs larger than L2")
     del ws
