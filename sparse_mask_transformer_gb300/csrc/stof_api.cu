@@ -381,9 +381,12 @@ static stof_status plan_call(const stof_format& f, int B, int H, int L, int d, s
   if (which == STOF_KERNEL_AUTO) {
     if (!f.synced) return STOF_ERR_NOT_SYNCED;
     const double density = static_cast<double>(f.nnz) / (static_cast<double>(f.n_masks) * f.lq * f.lk);
-    if (tuned_choice(L, d, density, f.bn, c)) {
+    // a cached measurement counts only if its kernel runs on this format
+    // (the block-wise kernel needs 128-row OTs)
+    if (tuned_choice(L, d, density, f.bn, c) && (c->kernel == STOF_KERNEL_ROWWISE || blockwise_tiles(f))) {
       *source = STOF_PLAN_TUNED;
     } else {
+      *c = KernelChoice{which, f.bn, 0, kVariantAuto, 0};
       *source = STOF_PLAN_ANALYTIC;
       // listed area per 128-row query tile, in 128x128 OTs
       const double tpr = static_cast<double>(f.n_full + f.n_part) * f.bm * f.bn /

@@ -167,3 +167,29 @@ def test_rowwise_rows_per_warp_match_the_oracle(gpu_lib, rpw, d, bm, bn, L, dens
     for (b, h), o_ref in ref.items():
         assert np.abs(o[b, h].double().cpu().numpy() - o_ref).max() <= TOL["fp16"]
     assert torch.all(o[0, 1, 5] == 0)
+
+
+def test_auto_ignores_a_cached_kernel_the_format_cannot_run(gpu_lib):
+    """A tuned entry for (L, d, density bucket) made on 128x128 OTs does not
+    apply to a format of 64x128 OTs when it names the block-wise kernel: AUTO
+    then follows the analytic model (which falls back to the row-wise kernel
+    for such OTs) instead of failing."""
+    B, H, L, d = 1, 2, 512, 64
+    mask = np.tril(np.ones((L, L), np.uint8))[None]
+    q, k, v = (t.cuda() for t in synth.make_qkv(B, H, L, d, "bf16", seed=5))
+    mdev = torch.from_numpy(mask).cuda()
+    wst = torch.empty(stof.stof_tune_workspace_bytes(1, L), dtype=torch.uint8, device="cuda")
+    stof.stof_tune_clear()
+    res = stof.stof_tune(mdev, q, k, v, 0.125, 0, 0, wst, torch.empty_like(q))
+    f128, _, _ = gpu_encode(mdev, 128, 128)
+    f64, _, _ = gpu_encode(mdev, 64, 128)
+    p128 = stof.stof_mha_plan(f128, B, H, L, d, stof.STOF_KERNEL_AUTO)
+    p64 = stof.stof_mha_plan(f64, B, H, L, d, stof.STOF_KERNEL_AUTO)
+    assert p128.source == stof.STOF_PLAN_TUNED
+    if p128.kernel == stof.STOF_KERNEL_BLOCKWISE:
+        assert p64.source == stof.STOF_PLAN_ANALYTIC and p64.kernel == stof.STOF_KERNEL_ROWWISE
+    o = torch.full_like(q, float("nan"))
+    stof.stof_mha_fwd(q, k, v, f64, 0.125, 0, 0, stof.STOF_KERNEL_AUTO, o)   # runs, does not raise
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all()
+    stof.stof_tune_clear()
