@@ -392,3 +392,46 @@ def test_select_kernel_heads_model(lib):
     for rho in (0.0, 0.05, 0.5):
         assert stof.stof_select_kernel(rho, 1024, 128) == sel(rho, 1024, 128, 1, -1)
     assert sel(0.1, 1024, 64, 0, -1) == blk       # invalid head count
+
+
+def _plan_call(lib, plan, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dt=stof.STOF_BF16, B=1, H=2, L=256, d=64, scale=0.125, sb=0, sh=0, o=FAKE)
+    a.update(kw)
+    fmt = _fake_format()
+    return lib.stof_mha_fwd_plan(a["q"], a["k"], a["v"], a["dt"], a["B"], a["H"], a["L"], a["d"], a["scale"],
+                                 ctypes.byref(fmt), a["sb"], a["sh"], None if plan is None else ctypes.byref(plan),
+                                 a["o"], None)
+
+
+def test_mha_fwd_plan_rejects_bad_plans_before_launch(lib):
+    P = stof.stof_plan
+    assert _plan_call(lib, None) == stof.STOF_ERR_INVALID_ARG
+    assert _plan_call(lib, P(5, 0, 0, 0, 0)) == stof.STOF_ERR_INVALID_ARG              # unknown kernel
+    assert _plan_call(lib, P(stof.STOF_KERNEL_AUTO, 0, 0, 0, 0)) == stof.STOF_ERR_INVALID_ARG
+    assert _plan_call(lib, P(stof.STOF_KERNEL_ROWWISE, 0, 0, 0, 3)) == stof.STOF_ERR_UNSUPPORTED  # rows per warp
+    assert _plan_call(lib, P(stof.STOF_KERNEL_BLOCKWISE, 9, 0, 0, 0)) == stof.STOF_ERR_INVALID_ARG
+    assert _plan_call(lib, P(stof.STOF_KERNEL_ROWWISE, 0, 0, 0, 1), q=None) == stof.STOF_ERR_INVALID_ARG
+    assert _plan_call(lib, P(stof.STOF_KERNEL_ROWWISE, 0, 0, 0, 1), d=96) == stof.STOF_ERR_UNSUPPORTED
+
+
+def test_oproj_ln_sizes_and_argument_errors(lib):
+    assert stof.stof_oproj_ln_workspace_bytes(2, 256, 512) == 2 * 256 * 2 * 8
+    assert stof.stof_oproj_ln_workspace_bytes(1, 128, 300) == 0      # N not a multiple of 256
+    assert stof.stof_oproj_ln_workspace_bytes(0, 128, 256) == 0
+
+    def call(**kw):
+        a = dict(o=FAKE, w=FAKE, bias=None, res=None, gamma=None, beta=None, eps=1e-5, dt=stof.STOF_BF16, B=1, H=2,
+                 L=128, d=64, N=256, y=FAKE, ws=FAKE, ws_bytes=1 << 20)
+        a.update(kw)
+        return lib.stof_oproj_ln_fwd(a["o"], a["w"], a["bias"], a["res"], a["gamma"], a["beta"], a["eps"], a["dt"],
+                                     a["B"], a["H"], a["L"], a["d"], a["N"], a["y"], a["ws"], a["ws_bytes"], None,
+                                     None)
+    assert call(o=None) == stof.STOF_ERR_INVALID_ARG
+    assert call(ws=None) == stof.STOF_ERR_INVALID_ARG
+    assert call(eps=0.0) == stof.STOF_ERR_INVALID_ARG
+    assert call(eps=float("inf")) == stof.STOF_ERR_INVALID_ARG
+    assert call(ws_bytes=100) == stof.STOF_ERR_WORKSPACE
+    assert call(gamma=FAKE + 4) == stof.STOF_ERR_ALIGNMENT
+    assert call(N=300) == stof.STOF_ERR_SHAPE
+    assert call(d=96) == stof.STOF_ERR_UNSUPPORTED
+    assert call(dt=5) == stof.STOF_ERR_DTYPE
