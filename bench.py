@@ -597,9 +597,15 @@ def run_oproj(args):
           flush=True)
 
 
-SWEEP_L = (128, 256, 512, 1024, 2048)
-SWEEP_DENSITY = (0.01, 0.02, 0.05, 0.1, 0.2, 0.4)
-SWEEP_HEADS = (2, 16, 64)
+# The grid the selector's coefficients were fitted to ("fit") and a held-out
+# grid of other lengths, densities, head counts and a block-sparse pattern
+# ("holdout") that checks the fitted model out of sample.
+SWEEPS = {
+    "fit": {"L": (128, 256, 512, 1024, 2048), "density": (0.01, 0.02, 0.05, 0.1, 0.2, 0.4),
+            "heads": (2, 16, 64), "patterns": ("random", "window")},
+    "holdout": {"L": (384, 768, 1536, 3072), "density": (0.03, 0.07, 0.15, 0.3),
+                "heads": (1, 8, 32), "patterns": ("random", "window", "blocks")},
+}
 
 
 def sweep_mask(pattern: str, L: int, density: float, seed: int):
@@ -608,6 +614,10 @@ def sweep_mask(pattern: str, L: int, density: float, seed: int):
     density (at least 1 key per row)."""
     if pattern == "random":
         m = synth.random_mask(1, L, L, density, seed=seed)
+    elif pattern == "blocks":  # 64 x 64 blocks kept with probability density (BigBird-like random blocks)
+        nb = L // 64
+        keep = np.random.default_rng(seed).random((nb, nb)) < density
+        m = np.kron(keep, np.ones((64, 64), bool)).astype(np.uint8)[None]
     else:
         wdt = max(1, int(round(density * L)))
         i = np.arange(L)[:, None]
@@ -625,20 +635,22 @@ def run_sweep(args):
     torch.cuda.set_device(0)
     build.build()
     stof.load_library()
+    grid = SWEEPS[args.sweep_set]
     cases = 0
     agree = 0
+    losses = []
     for d in (64, 128):
-        for L in SWEEP_L:
+        for L in grid["L"]:
             fmts = {}
-            for pattern in ("random", "window"):
-                for rho in SWEEP_DENSITY:
+            for pattern in grid["patterns"]:
+                for rho in grid["density"]:
                     mask = torch.from_numpy(sweep_mask(pattern, L, rho, seed=L + int(rho * 1000))).cuda()
                     ws = torch.empty(stof.stof_encode_workspace_bytes(1, L, L, 128, 128), dtype=torch.uint8,
                                      device="cuda")
                     fmt = stof.stof_encode_mask(mask, 128, 128, ws)
                     stof.stof_format_sync(fmt)
                     fmts[(pattern, rho)] = (fmt, ws)
-            for H in SWEEP_HEADS:
+            for H in grid["heads"]:
                 q, k, v = (t.cuda() for t in synth.make_qkv(1, H, L, d, "bf16", seed=H))
                 o = torch.empty_like(q)
                 for (pattern, rho), (fmt, ws) in fmts.items():
@@ -661,12 +673,15 @@ def run_sweep(args):
                     fastest = min(t, key=t.get)
                     cases += 1
                     agree += sel == fastest
+                    losses.append(t[sel] / t[fastest])
                     print(json.dumps({"sweep": pattern, "L": L, "d": d, "H": H, "density": round(density, 5),
                                       "tiles": fmt.n_full + fmt.n_part, "rowwise_us": round(t["rowwise"], 2),
                                       "blockwise_us": round(t["blockwise"], 2), "selected": sel,
                                       "fastest": fastest, "rowwise_rpw_us": rpw_us, "auto_rpw": auto_rpw}),
                           flush=True)
-    print(json.dumps({"sweep_summary": {"cases": cases, "selector_picks_fastest": agree}}), flush=True)
+    print(json.dumps({"sweep_summary": {"set": args.sweep_set, "cases": cases, "selector_picks_fastest": agree,
+                                        "mean_time_over_fastest": round(float(np.mean(losses)), 4),
+                                        "worst_time_over_fastest": round(float(np.max(losses)), 3)}}), flush=True)
 
 
 def run_bitmask(args, w, mask, q, k, v, ws, scale, stream, device, dist):
@@ -925,6 +940,8 @@ def main(argv=None):
     ap.add_argument("--no-bitmask", action="store_true", help="skip the bit-packed-mask and mask-rule measurements")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: kernel-only times of both kernels over short, sparse cases")
+    ap.add_argument("--sweep-set", default="fit", choices=list(SWEEPS),
+                    help="the grid the selector was fitted to, or a held-out grid")
     ap.add_argument("--oproj", default="", choices=[""] + list(OPROJ_SHAPES),
                     help="instead of the bench line: time the output projection after the MHA on this shape")
     ap.add_argument("--no-clocks", action="store_true",

@@ -103,6 +103,7 @@ struct AttnParams {
                                    // work[0] items taken, work[1] CTAs finished (both zero between launches)
   float tiles_per_row;             // mean listed OTs per OT row of the masks (synced format), else -1
   float keys_per_row;              // mean valid keys per query row (synced format), else -1
+  float listed128_per_row;         // listed OT area per 128-row query tile, in 128x128 OTs (synced), else -1
   int stages;                      // block-wise K/V ring depth; 0 = the kernel's default
   int rows_per_warp;               // row-wise: query rows per warp (1, 2 or 4); 0 = automatic
   int variant;                     // block-wise: kVariantAuto, kVariantPerTile or kVariantPersistent
@@ -125,15 +126,20 @@ inline int blockwise_stages(bool persistent, int stages) { return stages ? stage
 // Row-wise kernel: query rows per warp.  A whole warp per row while the
 // call has few rows (the GPU holds them all at once and the shortest
 // dependent chain wins); for more rows with few valid keys, 2 or 4 rows per
-// warp so that more rows are in flight.  `requested` (1, 2 or 4) overrides.
-// Thresholds from kernel-only GB300 times of the three settings on 360
+// warp so that more rows are in flight.  A warp's loops run at the pace of
+// its row with the most keys, so a mask whose keys come in blocks (few keys
+// on average, many in the rows that have any) keeps one row per warp: the
+// second test bounds the valid keys per (row, listed 128-column OT).
+// Thresholds from kernel-only GB300 times of the three settings on 648
 // short, sparse cases: within 3% of the best setting on average.
+// `requested` (1, 2 or 4) overrides; negative statistics mean unknown.
 constexpr long long kRowwiseFewRows = 2048;
-inline int rowwise_rows_per_warp(long long rows, float keys_per_row, int requested) {
+inline int rowwise_rows_per_warp(long long rows, float keys_per_row, float listed128_per_row, int requested) {
   if (requested == 1 || requested == 2 || requested == 4) return requested;
-  if (rows <= kRowwiseFewRows || keys_per_row < 0.f) return 1;
-  if (keys_per_row <= 32.f) return 4;
-  if (keys_per_row <= 256.f) return 2;
+  if (rows <= kRowwiseFewRows || keys_per_row < 0.f || listed128_per_row <= 0.f) return 1;
+  const float keys_per_listed = keys_per_row / listed128_per_row;
+  if (keys_per_row <= 24.f && keys_per_listed <= 32.f) return 4;
+  if (keys_per_row <= 128.f && keys_per_listed <= 64.f) return 2;
   return 1;
 }
 

@@ -345,7 +345,8 @@ cudaError_t launch_rw(const AttnParams& p, cudaStream_t s) {
 
 template <int D, bool BF16>
 cudaError_t launch_rw_d(const AttnParams& p, cudaStream_t s) {
-  const int rpw = rowwise_rows_per_warp(static_cast<long long>(p.B) * p.H * p.L, p.keys_per_row, p.rows_per_warp);
+  const int rpw = rowwise_rows_per_warp(static_cast<long long>(p.B) * p.H * p.L, p.keys_per_row,
+                                        p.listed128_per_row, p.rows_per_warp);
   if (rpw == 4) return launch_rw<D, BF16, 8>(p, s);
   if (rpw == 2) return launch_rw<D, BF16, 16>(p, s);
   return launch_rw<D, BF16, 32>(p, s);

@@ -275,34 +275,37 @@ stof_status stof_format_sync(stof_format* fmt, void* stream) {
 //
 // Predicted device time of each kernel in microseconds, linear in the work
 // it does:
-//   row-wise    T_row = 3.80 + 4.65e-4 R / r + 1.754e-5 K d/64 + 6.34e-5 P
+//   row-wise    T_row = 4.08 + 4.52e-4 R / r + 1.770e-5 K d/64 + 6.13e-5 P
 //               R = query rows (heads x L) and r the kernel's rows per warp
 //               (a warp's fixed cost is a few dependent memory round
 //               trips), K = valid (query, key) pairs (density x L^2 x
 //               heads: the K and V rows of every valid key), P = (query
 //               row, listed OT) pairs (heads x L x listed OTs per query
 //               tile: the bitmap bytes and column indices fetched per row);
-//   block-wise  T_blk = 7.19 + 4.94e-3 T (d/64 + 1)/2 + 9.43e-3 Q
+//   block-wise  T_blk = 7.48 + 5.24e-3 T (d/64 + 1)/2 + 8.16e-3 Q
 //               T = listed 128x128 OTs over all heads (each the full tile's
 //               MMA and softmax work, the MMAs half as long at d = 64),
 //               Q = query tiles (heads x L / 128: start-up and finish).
 // The constant terms are launch and pipeline fill.  The coefficients were
 // fitted to kernel-only GB300 times of both kernels (CUDA-graph replay) on
-// 360 cases: L = 128 to 2048, densities 0.01 to 0.4, 2 to 64 heads, d = 64
-// and 128, random and sliding-window masks; the model picks the faster
-// kernel in 343 of them, costs 0.6% on average and at most 47% where it
-// does not.  The row-wise kernel wins for high sparsity and few, short
-// rows -- the regime the pages give it.
+// 648 cases: L = 128 to 3072, densities 0.01 to 0.4, 1 to 64 heads, d = 64
+// and 128, random, sliding-window and block-sparse masks (fitted to the 360
+// cases of L = 128 to 2048 alone, it picked the faster kernel in 268 of the
+// other 288).  Timed again with these coefficients, it picks the faster
+// kernel in 612 of the 648 cases and costs 1.0% on average; where it
+// misses, both kernels take under 30 us.  The row-wise kernel wins for high
+// sparsity and few, short rows -- the regime the pages give it.
 namespace {
 double model_rowwise_us(double density, double L, double d, double heads, double tiles_per_row) {
   const double R = heads * L, K = density * L * L * heads, P = R * tiles_per_row;
-  const double r = rowwise_rows_per_warp(static_cast<long long>(R), static_cast<float>(density * L), 0);
-  return 3.80 + 4.65e-4 * R / r + 1.754e-5 * K * (d / 64.0) + 6.34e-5 * P;
+  const double r = rowwise_rows_per_warp(static_cast<long long>(R), static_cast<float>(density * L),
+                                         static_cast<float>(tiles_per_row), 0);
+  return 4.08 + 4.52e-4 * R / r + 1.770e-5 * K * (d / 64.0) + 6.13e-5 * P;
 }
 double model_blockwise_us(double L, double d, double heads, double tiles_per_row) {
   const double n_tr = L / 128.0;
   const double T = tiles_per_row * n_tr * heads, Q = n_tr * heads;
-  return 7.19 + 4.94e-3 * T * (d / 64.0 + 1.0) / 2.0 + 9.43e-3 * Q;
+  return 7.48 + 5.24e-3 * T * (d / 64.0 + 1.0) / 2.0 + 8.16e-3 * Q;
 }
 }  // namespace
 
@@ -329,6 +332,13 @@ static bool blockwise_tiles(const stof_format& f) { return f.bm == 128 && (f.bn 
 
 static float keys_per_row(const stof_format& f) {
   return f.synced ? static_cast<float>(static_cast<double>(f.nnz) / (static_cast<double>(f.n_masks) * f.lq)) : -1.f;
+}
+
+// Listed OT area per 128-row query tile, in 128x128 OTs (synced format), else -1.
+static float listed128_per_row(const stof_format& f) {
+  return f.synced ? static_cast<float>(static_cast<double>(f.n_full + f.n_part) * f.bm * f.bn /
+                                       (static_cast<double>(f.n_masks) * 128.0 * f.lq))
+                  : -1.f;
 }
 
 static float tiles_per_row(const stof_format& f) {
@@ -388,10 +398,7 @@ static stof_status plan_call(const stof_format& f, int B, int H, int L, int d, s
     } else {
       *c = KernelChoice{which, f.bn, 0, kVariantAuto, 0};
       *source = STOF_PLAN_ANALYTIC;
-      // listed area per 128-row query tile, in 128x128 OTs
-      const double tpr = static_cast<double>(f.n_full + f.n_part) * f.bm * f.bn /
-                         (static_cast<double>(f.n_masks) * 128.0 * L);
-      c->kernel = stof_select_kernel_heads(density, L, d, static_cast<int64_t>(B) * H, tpr);
+      c->kernel = stof_select_kernel_heads(density, L, d, static_cast<int64_t>(B) * H, listed128_per_row(f));
       if (c->kernel == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(f))
         c->kernel = STOF_KERNEL_ROWWISE;  // the block-wise kernel needs 128 x 64 or 128 x 128 OTs
     }
@@ -418,7 +425,7 @@ stof_status stof_mha_plan(const stof_format* fmt, int B, int H, int L, int d, st
     out->stages = blockwise_stages(out->persistent != 0, c.stages);
   } else {
     out->rows_per_warp = rowwise_rows_per_warp(static_cast<long long>(B) * H * L, keys_per_row(*fmt),
-                                               c.rows_per_warp);
+                                               listed128_per_row(*fmt), c.rows_per_warp);
   }
   return STOF_OK;
 }
@@ -461,6 +468,7 @@ stof_status mha_fwd_choice(const void* q, const void* k, const void* v, stof_dty
   p.work = reinterpret_cast<unsigned int*>(fmt->counts_dev + 5);
   p.tiles_per_row = tiles_per_row(*fmt);
   p.keys_per_row = keys_per_row(*fmt);
+  p.listed128_per_row = listed128_per_row(*fmt);
   p.rows_per_warp = c.rows_per_warp;
   p.stages = c.stages;
   p.variant = c.variant;

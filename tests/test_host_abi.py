@@ -315,7 +315,9 @@ def test_mha_plan_sources_and_variants(lib):
     assert stof.stof_mha_plan(_plan_format(nnz=20 * 1024), 1, 2, 1024, 64, 0).rows_per_warp == 1  # 2048 rows
     # more rows: rows per warp by the mean valid keys per row
     assert stof.stof_mha_plan(_plan_format(nnz=20 * 1024), 1, 64, 1024, 64, 0).rows_per_warp == 4
-    assert stof.stof_mha_plan(_plan_format(nnz=200 * 1024), 1, 64, 1024, 64, 0).rows_per_warp == 2
+    assert stof.stof_mha_plan(_plan_format(nnz=100 * 1024), 1, 64, 1024, 64, 0).rows_per_warp == 2
+    # few keys on average but many per listed OT (keys in blocks): one row per warp
+    assert stof.stof_mha_plan(_plan_format(nnz=20 * 1024, tiles=2), 1, 64, 1024, 64, 0).rows_per_warp == 1
     assert stof.stof_mha_plan(_plan_format(nnz=512 * 1024), 1, 64, 1024, 64, 0).rows_per_warp == 1
     assert stof.stof_mha_plan(_plan_format(nnz=20 * 1024, synced=False), 1, 64, 1024, 64, 0).rows_per_warp == 1
     p = stof.stof_mha_plan(f, 1, 4, 1024, 64, stof.STOF_KERNEL_BLOCKWISE)
