@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define STOF_VERSION 2
+#define STOF_VERSION 3
 
 typedef enum {
   STOF_OK = 0,
@@ -296,6 +296,9 @@ typedef struct {
   int persistent;      /* block-wise: 1 = persistent CTAs (d = 64), 0 = one CTA per query tile */
   int source;          /* STOF_PLAN_FORCED, STOF_PLAN_ANALYTIC or STOF_PLAN_TUNED */
   int rows_per_warp;   /* row-wise: query rows per warp (1, 2 or 4); 0 for the block-wise kernel */
+  int exp_split;       /* block-wise: 1 = one key pair in eight takes its exponentials on the FMA pipe
+                          (a Remez-fitted polynomial) instead of the special-function unit; else 0 */
+  int softmax_warpgroups; /* block-wise softmax warpgroups: 2, or 4 (persistent, d = 64); 0 row-wise */
 } stof_plan;
 
 /*
@@ -308,14 +311,19 @@ stof_status stof_mha_plan(const stof_format* fmt, int B, int H, int L, int d, st
 
 /*
  * stof_mha_fwd() run exactly as *plan says: its kernel, and for the
- * block-wise kernel its ring depth and variant (plan->source is ignored).
- * Arguments, layout and errors as stof_mha_fwd(); STOF_ERR_UNSUPPORTED for
- * a ring depth or variant these sizes do not admit.  Admitted: row-wise on
- * any OT size with 1, 2 or 4 query rows per warp (0: the library's
- * choice); block-wise on 128x128 OTs one CTA per query tile with ring
- * depth 2 or 3 (d = 128) or 2, 3 or 4 (d = 64), persistent CTAs with ring
- * depth 2, 3 or 4 (d = 64 only); on 128x64 OTs the default depth (3 per
- * query tile, 4 persistent).  A plan from stof_mha_plan() or a
+ * block-wise kernel its ring depth, variant, exp split and softmax
+ * warpgroup count (plan->source is ignored).  Arguments, layout and errors
+ * as stof_mha_fwd(); STOF_ERR_UNSUPPORTED for a setting these sizes do not
+ * admit, STOF_ERR_INVALID_ARG for exp_split other than 0 or 1 or a ring
+ * depth outside 0..8.  Admitted: row-wise on any OT size with 1, 2 or 4
+ * query rows per warp (0: the library's choice) and exp_split and
+ * softmax_warpgroups 0; block-wise on 128x128 OTs one CTA per query tile
+ * with ring depth 2 or 3 (d = 128) or 2, 3 or 4 (d = 64), persistent CTAs
+ * with ring depth 2, 3 or 4 (d = 64 only); on 128x64 OTs the default depth
+ * (3 per query tile, 4 persistent); the exp split on 128x128 OTs at the
+ * default depth (3 per query tile, 4 persistent); four softmax warpgroups
+ * on 128x128 OTs, persistent, ring depth 4, d = 64, without the exp split
+ * (softmax_warpgroups 0 means 2).  A plan from stof_mha_plan() or a
  * stof_tune_result's candidate is always admitted for the sizes it was
  * made for.
  */
@@ -335,11 +343,15 @@ stof_status stof_mha_fwd_plan(const void* q, const void* k, const void* v, stof_
  *          3, 2, 4 (depth 4 at d = 64 only: shared memory);
  *   6-8    block-wise, 128x128 OTs, persistent CTAs (d = 64 only), ring
  *          depth 4, 3, 2;
- *   9      block-wise, 128x64 OTs, default variant and ring depth.
- * The softmax warpgroup count is not a candidate: the kernels' register and
- * tensor-memory budgets fit exactly two.
+ *   9      block-wise, 128x64 OTs, default variant and ring depth;
+ *   10     block-wise, 128x128 OTs, one CTA per query tile, ring depth 3,
+ *          exp split;
+ *   11     block-wise, 128x128 OTs, persistent (d = 64 only), ring depth 4,
+ *          exp split;
+ *   12     block-wise, 128x128 OTs, persistent (d = 64 only), ring depth 4,
+ *          four softmax warpgroups.
  */
-#define STOF_TUNE_CANDIDATES 10
+#define STOF_TUNE_CANDIDATES 13
 typedef struct {
   stof_kernel kernel;        /* fastest candidate */
   int bn;                    /* its OT width (bm = 128) */
@@ -348,11 +360,15 @@ typedef struct {
   int stages;                /* its K/V ring depth (0 for row-wise) */
   int persistent;            /* 1 if it runs persistent CTAs */
   int rows_per_warp;         /* row-wise: its query rows per warp (0 for block-wise) */
+  int exp_split;             /* block-wise: 1 if its exp split is on */
+  int softmax_warpgroups;    /* block-wise: its softmax warpgroups (2 or 4; 0 row-wise) */
   stof_kernel cand_kernel[STOF_TUNE_CANDIDATES];
   int cand_bn[STOF_TUNE_CANDIDATES];
   int cand_stages[STOF_TUNE_CANDIDATES];        /* ring depth the candidate ran with (0 row-wise) */
   int cand_persistent[STOF_TUNE_CANDIDATES];    /* 1 persistent, 0 one CTA per query tile */
   int cand_rows_per_warp[STOF_TUNE_CANDIDATES]; /* row-wise rows per warp (0 block-wise) */
+  int cand_exp_split[STOF_TUNE_CANDIDATES];     /* 1 exp split on */
+  int cand_softmax_warpgroups[STOF_TUNE_CANDIDATES]; /* block-wise softmax warpgroups (0 row-wise) */
   float cand_ms[STOF_TUNE_CANDIDATES];          /* -1 for a candidate the sizes do not admit */
 } stof_tune_result;
 
@@ -441,6 +457,17 @@ size_t stof_oproj_ln_workspace_bytes(int B, int L, int N);
  * (device int64, 8-byte aligned) and exits.  Asynchronous on stream.
  */
 stof_status stof_check_bounded_wait(int64_t* device_error, double seconds, void* stream);
+
+/*
+ * The block-wise kernels' FMA-pipe exp2 (the exp split's polynomial) on n
+ * inputs: y[i] = 2^x[i] computed as 2^rint(x) * p(x - rint(x)) with a
+ * degree-4 polynomial p (p(0) = 1; relative error at most 2.9e-6 on
+ * [-1/2, 1/2]); 0 for x < -125 and at -inf.  For x <= 127.  x and y are
+ * device fp32 arrays (4-byte aligned, may be the same array).  Lets a test
+ * check the polynomial against exp2.  STOF_ERR_INVALID_ARG for n < 0 or a
+ * NULL array with n > 0.  Asynchronous on stream.
+ */
+stof_status stof_ex2_fma(const float* x, float* y, int64_t n, void* stream);
 
 /* Static description of a status code. */
 const char* stof_status_string(stof_status s);

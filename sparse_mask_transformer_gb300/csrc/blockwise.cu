@@ -46,6 +46,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "blockwise_common.cuh"
@@ -89,8 +90,9 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 
 // NEG: the softmax scale is not positive (the scores are multiplied by it
 // before masking and the row max); a separate instance, so that the usual
-// positive scale pays no test.
-template <int D, int BN, bool BF16, int ST, bool NEG>
+// positive scale pays no test.  ESPLIT: one key pair in eight takes its
+// exponentials on the FMA pipe (ex2_fma).
+template <int D, int BN, bool BF16, int ST, bool NEG, bool ESPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     blockwise_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
       l *= alpha;
       uint32_t pk[C::CHUNKS][16];
-      l += exp_pack<C::CHUNKS, BF16>(sr, c, nmu, pk);
+      l += exp_pack<C::CHUNKS, BF16, ESPLIT>(sr, c, nmu, pk);
       if (j > 0) {
         // P_g is rewritten and O_g rescaled once the PV of this warpgroup's
         // previous tile is done
@@ -496,7 +498,7 @@ bool make_bw_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box
 
 namespace {
 
-template <int D, int BN, bool BF16, int ST, bool NEG>
+template <int D, int BN, bool BF16, int ST, bool NEG, bool ESPLIT>
 stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.L;
   CUtensorMap mq, mk, mv;
@@ -507,14 +509,14 @@ stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
   stof_status prep = STOF_OK;
   auto prepare = [](const void* arg) {
     stof_status* st = static_cast<stof_status*>(const_cast<void*>(arg));
-    if (record_cuda(cudaFuncSetAttribute(blockwise_kernel<D, BN, BF16, ST, NEG>,
+    if (record_cuda(cudaFuncSetAttribute(blockwise_kernel<D, BN, BF16, ST, NEG, ESPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sizeof(Smem<D, BN, ST>) + 1024))) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
     cudaFuncAttributes fa;
-    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_kernel<D, BN, BF16, ST, NEG>)) != cudaSuccess) {
+    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_kernel<D, BN, BF16, ST, NEG, ESPLIT>)) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
@@ -524,21 +526,29 @@ stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
     }
     return true;
   };
-  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_kernel<D, BN, BF16, ST, NEG>), prepare, &prep))
+  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_kernel<D, BN, BF16, ST, NEG, ESPLIT>), prepare, &prep))
     return prep;
   const long long grid = static_cast<long long>(p.B) * p.H * p.n_tr;
-  blockwise_kernel<D, BN, BF16, ST, NEG><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
+  blockwise_kernel<D, BN, BF16, ST, NEG, ESPLIT><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(mq, mk, mv, p);
   return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
 }
 
 }  // namespace
 
-template <int D, int BN, int ST>
+template <int D, int BN, int ST, bool ESPLIT = false>
 stof_status launch_bw_t(const AttnParams& p, bool bf16, cudaStream_t s) {
   if (p.scale_log2 > 0.f)
-    return bf16 ? launch_bw<D, BN, true, ST, false>(p, s) : launch_bw<D, BN, false, ST, false>(p, s);
-  return bf16 ? launch_bw<D, BN, true, ST, true>(p, s) : launch_bw<D, BN, false, ST, true>(p, s);
+    return bf16 ? launch_bw<D, BN, true, ST, false, ESPLIT>(p, s) : launch_bw<D, BN, false, ST, false, ESPLIT>(p, s);
+  return bf16 ? launch_bw<D, BN, true, ST, true, ESPLIT>(p, s) : launch_bw<D, BN, false, ST, true, ESPLIT>(p, s);
 }
+
+namespace {
+__global__ void ex2_fma_kernel(const float* x, float* y, long long n) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    y[i] = bw::ex2_fma(x[i]);
+}
+}  // namespace
 
 stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s) {
   if (p.bm != kBM || (p.bn != 64 && p.bn != 128)) return STOF_ERR_UNSUPPORTED;
@@ -548,6 +558,11 @@ stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s) {
   if (blockwise_persistent(p.d, p.variant, p.tiles_per_row)) return launch_blockwise_persist64(p, bf16, s);
   // ring depths: 3 by default; the tuner also samples 2 (and 4 at d = 64) on 128 x 128 OTs
   const int st = p.stages ? p.stages : kStages;
+  if (p.softmax_wg != 0 && p.softmax_wg != 2) return STOF_ERR_UNSUPPORTED;
+  if (p.exp_split) {  // sampled on 128 x 128 OTs at the default ring depth
+    if (p.bn != 128 || st != kStages) return STOF_ERR_UNSUPPORTED;
+    return p.d == 64 ? launch_bw_t<64, 128, 3, true>(p, bf16, s) : launch_bw_t<128, 128, 3, true>(p, bf16, s);
+  }
   if (p.bn == 64) {
     if (st != kStages) return STOF_ERR_UNSUPPORTED;
     return p.d == 64 ? launch_bw_t<64, 64, 3>(p, bf16, s) : launch_bw_t<128, 64, 3>(p, bf16, s);
@@ -603,3 +618,11 @@ int device_sm_count() {
 }
 
 }  // namespace stof
+
+extern "C" stof_status stof_ex2_fma(const float* x, float* y, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!x || !y))) return STOF_ERR_INVALID_ARG;
+  if (n == 0) return STOF_OK;
+  const long long blocks = std::min<long long>((n + 255) / 256, 16ll * stof::device_sm_count());
+  stof::ex2_fma_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y, n);
+  return stof::record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
+}

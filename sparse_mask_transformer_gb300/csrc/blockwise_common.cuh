@@ -71,6 +71,25 @@ __device__ __forceinline__ void keep_if_set(uint32_t& s, uint32_t bits, uint32_t
       : "r"(bits), "r"(bit), "r"(0xFF800000u));
 }
 
+// 2^x on the FMA pipe, for the exp split: x = n + f with n = rint(x)
+// (adding and subtracting 1.5 * 2^23 rounds to an integer), 2^f by
+// p(f) = 1 + f (c1 + f (c2 + f (c3 + f c4))), whose coefficients minimise
+// the maximum relative error on [-1/2, 1/2] (Remez exchange; derived and
+// checked by ex2_poly.py: at most 2.9e-6), and n added to p's exponent field.
+// Exactly 1 at 0; 0 below -125, at -inf included.  For x <= 127.
+__device__ __forceinline__ float ex2_fma(float x) {
+  constexpr float kRound = 12582912.f;  // 1.5 * 2^23
+  const float t = x + kRound;
+  const float n = t - kRound;
+  const float f = x - n;
+  float p = fmaf(f, 0x1.3a02ccp-7f, 0x1.c9fc46p-5f);
+  p = fmaf(p, f, 0x1.ec0378p-3f);
+  p = fmaf(p, f, 0x1.62e12cp-1f);
+  p = fmaf(p, f, 1.f);
+  const float y = __uint_as_float(__float_as_uint(p) + (__float_as_uint(t) << 23));
+  return x < -125.f ? 0.f : y;
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (BF16) {
@@ -160,8 +179,10 @@ __device__ __forceinline__ float row_max(const uint32_t (&sr)[CHUNKS][32]) {
 }
 
 // P = 2^(c s + nmu) as fp16/bf16 pairs (keys 32 cc + 2 i and + 1 in
-// pk[cc][i]); returns the sum of the fp32 exponentials.
-template <int CHUNKS, bool BF16>
+// pk[cc][i]); returns the sum of the fp32 exponentials.  ESPLIT: one pair
+// of keys in eight takes its exponentials on the FMA pipe (ex2_fma), the
+// rest on the special-function unit.
+template <int CHUNKS, bool BF16, bool ESPLIT = false>
 __device__ __forceinline__ float exp_pack(const uint32_t (&sr)[CHUNKS][32], float c, float nmu,
                                           uint32_t (&pk)[CHUNKS][16]) {
   float ls[4] = {0.f, 0.f, 0.f, 0.f};
@@ -171,10 +192,26 @@ __device__ __forceinline__ float exp_pack(const uint32_t (&sr)[CHUNKS][32], floa
     for (int i = 0; i < 32; i += 2) {
       float x0, x1;
       ffma2(x0, x1, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]), c, c, nmu, nmu);
-      const float e0 = ex2(x0), e1 = ex2(x1);
+      const bool fma_pipe = ESPLIT && (i / 2) % 8 == 7;
+      const float e0 = fma_pipe ? ex2_fma(x0) : ex2(x0), e1 = fma_pipe ? ex2_fma(x1) : ex2(x1);
       fadd2(ls[((i >> 1) & 1) * 2], ls[((i >> 1) & 1) * 2 + 1], e0, e1);
       pk[cc][i / 2] = pack2<BF16>(e0, e1);
     }
+  return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+}
+
+// exp_pack for one chunk of 32 scores.
+template <bool BF16>
+__device__ __forceinline__ float exp_pack32(const uint32_t (&sr)[32], float c, float nmu, uint32_t (&pk)[16]) {
+  float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    float x0, x1;
+    ffma2(x0, x1, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]), c, c, nmu, nmu);
+    const float e0 = ex2(x0), e1 = ex2(x1);
+    fadd2(ls[((i >> 1) & 1) * 2], ls[((i >> 1) & 1) * 2 + 1], e0, e1);
+    pk[i / 2] = pack2<BF16>(e0, e1);
+  }
   return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 

@@ -29,6 +29,16 @@
 // leaves its row max and sum in shared memory and moves on.
 // TMEM columns: S [0,BN) P_0 [128,128+BN/2) P_1 [192,192+BN/2)
 // O[item % 2][g] [256 + 128 (item % 2) + 64 g, +64).
+//
+// A second softmax layout (SWG = 4), one of the tuner's candidates: four
+// softmax warpgroups, two per tile parity, each taking one half of a tile's
+// key columns for all 128 rows (so each thread holds 64 scores, not 128,
+// and 16 softmax warps share the SM instead of 8).  The two warps that hold
+// the same rows of the same tile swap their halves' row max through shared
+// memory (one mbarrier per pair of warps, bounded wait); both halves then
+// take the same rescale decision, write their halves of P, rescale their
+// halves of O and keep their own partial sums, which the epilogue adds.
+// Same TMEM columns; 640 threads at 96 registers, split 32 / 112.
 // The work counter lives in the format's workspace (zeroed by the encoders)
 // and is zeroed again by the last CTA to finish, ready for the next launch.  Every wait is bounded; on timeout the CTA raises
 // STOF_DEVERR_PIPE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
@@ -51,7 +61,18 @@ using namespace bw;
 
 constexpr int kD = 64;
 constexpr int kDefaultRing = 4;   // default K and V ring depth (the tuner also samples 2 and 3)
-constexpr int kItemReaders = 11;  // warps that read each published item: V producer, 2 issuers, 8 softmax
+// warps that read each published item: V producer, 2 issuers, the softmax warps
+template <int SWG>
+constexpr int kItemReaders = 3 + 4 * SWG;
+// With four softmax warpgroups: 4 producer / issuer warps and 16 softmax
+// warps.  Five warps per SM sub-partition cap a thread at 96 registers at
+// launch; the producers drop to 32 and the softmax warps rise to 112.
+constexpr int kThreads4 = 640;
+constexpr int kLaunchRegs4 = 96, kProducerRegs4 = 32, kSoftmaxRegs4 = 112;
+static_assert(kProducerRegs4 * 128 + kSoftmaxRegs4 * 512 <= kLaunchRegs4 * kThreads4, "register split");
+static_assert(kLaunchRegs4 * kThreads4 <= 65536, "register file");
+template <int SWG>
+constexpr int threads_of = SWG == 4 ? kThreads4 : kThreads;
 
 template <int BN, int kRing>
 struct alignas(1024) PSmem {
@@ -64,10 +85,13 @@ struct alignas(1024) PSmem {
   uint64_t s_full[2], s_free[2];           // per warpgroup
   uint64_t p_full[2], pv_done[2];          // per warpgroup
   uint64_t item_full[2], item_free[2];     // ring of work items
-  uint64_t xchg[2];                        // per item parity: the early warpgroup's max and sum are in xml
+  uint64_t xchg[2];                        // per item parity: the max and sum for the epilogue are in
   uint64_t x_free[2];                      // per item parity: the epilogue has read them
   uint64_t o_free[2];                      // per O set: its item's epilogue is done with it
+  uint64_t mx[2][4];                       // four warpgroups: per pair and row quarter, both half maxima in xm
   float xml[2][2][kBM];                    // per item parity: max, sum of the early warpgroup per row
+  float xml4[2][2][2][2][kBM];             // four warpgroups: [item parity][pair][half][max, sum][row]
+  float xm[2][2][2][kBM];                  // four warpgroups: [pair][tile parity][half][row], half-row max
   uint64_t drain, drain_qk;
   int item[2];
   uint32_t tmem_base;
@@ -94,12 +118,17 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int idx) {
   return it;
 }
 
-// NEG: the softmax scale is not positive (see blockwise.cu).
-template <int BN, bool BF16, int kRing, bool NEG>
-__global__ void __launch_bounds__(kThreads, 1)
+// NEG: the softmax scale is not positive (see blockwise.cu).  ESPLIT: one
+// key pair in eight takes its exponentials on the FMA pipe (two softmax
+// warpgroups only).  SWG: softmax warpgroups, 2 or 4.
+template <int BN, bool BF16, int kRing, bool NEG, bool ESPLIT, int SWG>
+__global__ void __launch_bounds__(threads_of<SWG>, 1)
     blockwise_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                              const __grid_constant__ CUtensorMap tmV, const AttnParams p, const int n_items) {
   using C = Cfg<kD, BN>;
+  static_assert(SWG == 2 || (SWG == 4 && !ESPLIT), "softmax layout");
+  constexpr int HB = BN / 2;    // four warpgroups: keys per half tile
+  constexpr int HCH = HB / 32;  // and 32-key chunks per half
   extern __shared__ uint8_t smem_raw[];
   PSmem<BN, kRing>& s = *reinterpret_cast<PSmem<BN, kRing>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                             ~uintptr_t(1023));
@@ -110,14 +139,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.q_full[i], 1);
       mbar_init(&s.q_free[i], 1);
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.s_free[i], 128);
-      mbar_init(&s.p_full[i], 128);
+      mbar_init(&s.s_free[i], 64 * SWG);  // every softmax thread of the tile's warpgroup(s)
+      mbar_init(&s.p_full[i], 64 * SWG);
       mbar_init(&s.pv_done[i], 1);
       mbar_init(&s.item_full[i], 1);
-      mbar_init(&s.item_free[i], kItemReaders);
-      mbar_init(&s.o_free[i], 4);
-      mbar_init(&s.xchg[i], 4);
-      mbar_init(&s.x_free[i], 4);
+      mbar_init(&s.item_free[i], kItemReaders<SWG>);
+      mbar_init(&s.o_free[i], 2 * SWG);   // the epilogue's warps
+      mbar_init(&s.xchg[i], SWG == 4 ? 16 : 4);
+      mbar_init(&s.x_free[i], 2 * SWG);
+      for (int q = 0; q < 4; ++q) mbar_init(&s.mx[i][q], 2);
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&s.k_full[i], 1);
@@ -167,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp < 4) {
-    regs_dec<kProducerRegs>();
+    regs_dec<SWG == 4 ? kProducerRegs4 : kProducerRegs>();
     if (warp == 0) {
       // ------------------------------------------------------------ Q/K producer
       if (lane == 0) {
@@ -351,6 +381,168 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  } else if constexpr (SWG == 4) {
+    regs_inc<kSoftmaxRegs4>();
+    // ------------------------------------------------------------ softmax
+    const int sw = warp - 4;
+    const int quarter = warp & 3;
+    const int g = (sw >> 2) & 1;        // pair: tiles t with t % 2 == g
+    const int hh = sw >> 3;             // key half: columns [HB hh, HB hh + HB) of each tile
+    const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c = NEG ? 1.f : p.scale_log2;
+    const int bits_off = (r >> 3) * BN + (r & 7) + hh * (HB / 8) * 8;  // this row's byte in an OT's bitmaps
+    int J = 0;   // tiles of this pair so far, all items
+    int e = 0;   // items with tiles so far
+    int T0 = 0;  // tiles of the items before this one
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      int idx;
+      if (!read_item(k, idx)) { ok = false; break; }
+      if (idx >= n_items) break;
+      const Item it = decode_item(p, idx);
+      const int n = it.n, nf = it.nf, p0 = it.p0;
+      // this thread's output row (recomputed where it is used)
+      auto out_row = [&]() {
+        const int bh = idx / p.n_tr, I = p.n_tr - 1 - idx % p.n_tr;
+        return static_cast<uint8_t*>(p.o) +
+               (static_cast<size_t>(bh) * p.L + static_cast<size_t>(I) * kBM + r) * (kD * 2);
+      };
+      if (n == 0) {  // no listed tile: the rows of this query tile are 0 (a quarter of each row per warpgroup)
+        uint4* z = reinterpret_cast<uint4*>(out_row() + (2 * g + hh) * (kD / 2));
+        z[0] = make_uint4(0u, 0u, 0u, 0u);
+        z[1] = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
+      const int t_first = (g ^ T0) & 1;
+      const uint32_t tO_item = tO + (e & 1) * 128 + lane_off;  // this item's O set
+      uint32_t nb[HB / 8];  // bitmap bytes of this half of a partial tile, loaded before its scores' wait
+      auto fetch_bits = [&](int t) {
+        if (t >= nf) {
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(p.bitmaps) + bits_off +
+                               static_cast<long long>(p0 + (t - nf)) * (C::BITMAP_WORDS * 8);
+#pragma unroll
+          for (int w = 0; w < HB / 8; ++w) nb[w] = __ldg(src + w * 8);
+        }
+      };
+      float m_ref = -INFINITY, l = 0.f;
+      for (int t = t_first; t < n; t += 2) {
+        const int j = t >> 1;  // this pair's j-th tile of the item
+        fetch_bits(t);
+        if (!wwait(&s.s_full[g], J & 1)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[HCH][32];
+        load_scores(tS + lane_off + hh * HB, sr);
+        tc_fence_before();
+        mbar_arrive(&s.s_free[g]);  // this half's scores are in registers
+        const bool partial = t >= nf;
+        uint32_t bits[HCH] = {};
+        if (partial) assemble_bits<HCH>(nb, bits);
+        if constexpr (NEG) scale_scores(sr, p.scale_log2);
+        if (partial) mask_scores(sr, bits);
+        // The row max over both halves: each warp leaves its half's max and
+        // reads the other half's, written by the warp of the other
+        // warpgroup of the pair that holds the same rows.
+        const float m_half = row_max(sr);
+        const int xs = J & 1;
+        s.xm[g][xs][hh][r] = m_half;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.mx[g][quarter]);
+        if (!wwait(&s.mx[g][quarter], J & 1)) { ok = false; break; }
+        const float mt = fmaxf(m_half, s.xm[g][xs][hh ^ 1][r]) * c;
+        float alpha = 1.f;
+        if (mt > m_ref + kRescaleThreshold) {  // also the first finite max; the same decision in both halves
+          alpha = ex2(m_ref - mt);
+          m_ref = mt;
+        }
+        const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
+        l *= alpha;
+        // P_g is rewritten once the PV of this pair's previous tile (of any
+        // item) is done; that also makes O_g current
+        if (J > 0 && !wwait(&s.pv_done[g], (J - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        // this half's P, 32 keys at a time, and its half of a rescaled O,
+        // before the PV MMA reads them
+#pragma unroll
+        for (int cc = 0; cc < HCH; ++cc) {
+          uint32_t pk[16];
+          l += exp_pack32<BF16>(sr[cc], c, nmu, pk);
+          tmem_st16(tP0 + g * 64 + hh * (HB / 2) + lane_off + cc * 16, pk);
+        }
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) rescale_o<kD / 2>(tO_item + g * kD + hh * (kD / 2), alpha);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&s.p_full[g]);
+        ++J;
+      }
+      const int slot = e & 1;  // exchange slot and O set of this item
+      // Every warpgroup leaves its row max and its half's sum; the pair
+      // that took the item's last tile merges and stores.  The slot held
+      // item e - 2's values: wait until they were read.
+      if (ok && e >= 2 && !wwait(&s.x_free[slot], ((e >> 1) & 1) ^ 1)) ok = false;
+      s.xml4[slot][g][hh][0][r] = m_ref;
+      s.xml4[slot][g][hh][1][r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.xchg[slot]);
+      if (!ok) {
+        if (quarter == 0 && lane == 0) fail();
+        break;
+      }
+      if (g == ((T0 + n - 1) & 1)) {  // this pair took the item's last tile
+        // O = (a_me O_me + a_ot O_ot) / (a_me l_me + a_ot l_ot) over this
+        // half's kD / 2 columns, once the pair's last PV (the item's last)
+        // is done and every warpgroup's max and sum are in.
+        const bool good = wwait(&s.pv_done[g], (J - 1) & 1) && wwait(&s.xchg[slot], (e >> 1) & 1);
+        if (!good) {
+          if (quarter == 0 && lane == 0) fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float mo = s.xml4[slot][g ^ 1][0][0][r];
+        const float lo = s.xml4[slot][g ^ 1][0][1][r] + s.xml4[slot][g ^ 1][1][1][r];
+        const float lme = s.xml4[slot][g][0][1][r] + s.xml4[slot][g][1][1][r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.x_free[slot]);
+        const float m = fmaxf(m_ref, mo);
+        const float a_me = m_ref != -INFINITY ? ex2(m_ref - m) : 0.f;
+        const float a_ot = (n > 1 && mo != -INFINITY) ? ex2(mo - m) : 0.f;
+        const float lt = a_me * lme + a_ot * lo;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        const float w_me = a_me * inv, w_ot = a_ot * inv;
+#pragma unroll
+        for (int cc = 0; cc < kD / 32; ++cc) {  // 16 columns at a time
+          const uint32_t col = hh * (kD / 2) + cc * 16;
+          uint32_t om[16], oo[16];
+          tmem_ld16(tO_item + g * kD + col, om);
+          tmem_ld_wait(om);
+          if (n > 1) {  // the other pair's partial exists only with two tiles or more
+            tmem_ld16(tO_item + (g ^ 1) * kD + col, oo);
+            tmem_ld_wait(oo);
+          }
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float v0 = w_me * __uint_as_float(om[2 * i]);
+            float v1 = w_me * __uint_as_float(om[2 * i + 1]);
+            if (n > 1) {
+              v0 = fmaf(w_ot, __uint_as_float(oo[2 * i]), v0);
+              v1 = fmaf(w_ot, __uint_as_float(oo[2 * i + 1]), v1);
+            }
+            w[i] = pack2<BF16>(v0, v1);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(out_row() + col * 2);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        // done with this item's O set: the item after next may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.o_free[slot]);
+      }
+      T0 += n;
+      ++e;
+    }
   } else {
     regs_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
@@ -421,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
         l *= alpha;
         uint32_t pk[C::CHUNKS][16];
-        l += exp_pack<C::CHUNKS, BF16>(sr, c, nmu, pk);
+        l += exp_pack<C::CHUNKS, BF16, ESPLIT>(sr, c, nmu, pk);
         // P_g is rewritten once the PV of this warpgroup's previous tile (of
         // any item) is done; that also makes O_g current
         if (J > 0 && !wwait(&s.pv_done[g], (J - 1) & 1)) { ok = false; break; }
@@ -517,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, bool BF16, int RING, bool NEG>
+template <int BN, bool BF16, int RING, bool NEG, bool ESPLIT, int SWG>
 stof_status launch_persist(const AttnParams& p, cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.L;
   CUtensorMap mq, mk, mv;
@@ -528,39 +720,41 @@ stof_status launch_persist(const AttnParams& p, cudaStream_t s) {
   stof_status prep = STOF_OK;
   auto prepare = [](const void* arg) {
     stof_status* st = static_cast<stof_status*>(const_cast<void*>(arg));
-    if (record_cuda(cudaFuncSetAttribute(blockwise_persist_kernel<BN, BF16, RING, NEG>,
+    if (record_cuda(cudaFuncSetAttribute(blockwise_persist_kernel<BN, BF16, RING, NEG, ESPLIT, SWG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sizeof(PSmem<BN, RING>) + 1024))) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
     cudaFuncAttributes fa;
-    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_persist_kernel<BN, BF16, RING, NEG>)) != cudaSuccess) {
+    if (record_cuda(cudaFuncGetAttributes(&fa, blockwise_persist_kernel<BN, BF16, RING, NEG, ESPLIT, SWG>)) != cudaSuccess) {
       *st = STOF_ERR_CUDA;
       return false;
     }
-    if (fa.numRegs != kLaunchRegs) {  // the register split needs exactly this
+    if (fa.numRegs != (SWG == 4 ? kLaunchRegs4 : kLaunchRegs)) {  // the register split needs exactly this
       *st = STOF_ERR_UNSUPPORTED;
       return false;
     }
     return true;
   };
-  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_persist_kernel<BN, BF16, RING, NEG>), prepare, &prep))
+  if (!once_per_device(reinterpret_cast<const void*>(&blockwise_persist_kernel<BN, BF16, RING, NEG, ESPLIT, SWG>), prepare, &prep))
     return prep;
   // one resident CTA per SM, each taking items from the work counter
   const long long n_items = static_cast<long long>(p.B) * p.H * p.n_tr;
   const long long sms = device_sm_count();
   const long long grid = n_items < sms ? n_items : sms;
-  blockwise_persist_kernel<BN, BF16, RING, NEG><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(
+  blockwise_persist_kernel<BN, BF16, RING, NEG, ESPLIT, SWG><<<static_cast<unsigned>(grid), threads_of<SWG>, smem, s>>>(
       mq, mk, mv, p, static_cast<int>(n_items));
   return record_cuda(cudaGetLastError()) == cudaSuccess ? STOF_OK : STOF_ERR_CUDA;
 }
 
-template <int BN, int RING>
+template <int BN, int RING, bool ESPLIT = false, int SWG = 2>
 stof_status launch_persist_t(const AttnParams& p, bool bf16, cudaStream_t s) {
   if (p.scale_log2 > 0.f)
-    return bf16 ? launch_persist<BN, true, RING, false>(p, s) : launch_persist<BN, false, RING, false>(p, s);
-  return bf16 ? launch_persist<BN, true, RING, true>(p, s) : launch_persist<BN, false, RING, true>(p, s);
+    return bf16 ? launch_persist<BN, true, RING, false, ESPLIT, SWG>(p, s)
+                : launch_persist<BN, false, RING, false, ESPLIT, SWG>(p, s);
+  return bf16 ? launch_persist<BN, true, RING, true, ESPLIT, SWG>(p, s)
+              : launch_persist<BN, false, RING, true, ESPLIT, SWG>(p, s);
 }
 
 }  // namespace
@@ -568,6 +762,15 @@ stof_status launch_persist_t(const AttnParams& p, bool bf16, cudaStream_t s) {
 stof_status launch_blockwise_persist64(const AttnParams& p, bool bf16, cudaStream_t s) {
   if (p.d != kD || p.bm != kBM || (p.bn != 64 && p.bn != 128)) return STOF_ERR_UNSUPPORTED;
   const int ring = p.stages ? p.stages : kDefaultRing;
+  const int swg = p.softmax_wg ? p.softmax_wg : 2;
+  if (swg != 2 && swg != 4) return STOF_ERR_UNSUPPORTED;
+  // the exp split and four softmax warpgroups (tuner candidates, not both
+  // at once) on 128 x 128 OTs at the default ring depth
+  if (p.exp_split || swg == 4) {
+    if (p.bn != 128 || ring != kDefaultRing || (p.exp_split && swg == 4)) return STOF_ERR_UNSUPPORTED;
+    return p.exp_split ? launch_persist_t<128, kDefaultRing, true, 2>(p, bf16, s)
+                       : launch_persist_t<128, kDefaultRing, false, 4>(p, bf16, s);
+  }
   if (p.bn == 64) {
     if (ring != kDefaultRing) return STOF_ERR_UNSUPPORTED;
     return launch_persist_t<64, kDefaultRing>(p, bf16, s);

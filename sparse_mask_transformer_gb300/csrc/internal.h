@@ -107,6 +107,8 @@ struct AttnParams {
   int stages;                      // block-wise K/V ring depth; 0 = the kernel's default
   int rows_per_warp;               // row-wise: query rows per warp (1, 2 or 4); 0 = automatic
   int variant;                     // block-wise: kVariantAuto, kVariantPerTile or kVariantPersistent
+  int exp_split;                   // block-wise: 1 = one key pair in eight exponentiated on the FMA pipe
+  int softmax_wg;                  // block-wise softmax warpgroups: 2, or 4 (persistent, d = 64); 0 = 2
 };
 // Block-wise kernel variants: one CTA per query tile, or persistent CTAs
 // (d = 64 only); auto picks by the mean listed OTs per OT row.
@@ -152,6 +154,8 @@ struct KernelChoice {
   int stages;
   int variant;
   int rows_per_warp;
+  int exp_split;   // block-wise: 1 = one key pair in eight exponentiated on the FMA pipe
+  int softmax_wg;  // block-wise softmax warpgroups: 0 (= 2), 2 or 4
 };
 // The candidates stof_tune() times (STOF_TUNE_CANDIDATES of them).
 extern const KernelChoice kTuneCandidates[STOF_TUNE_CANDIDATES];

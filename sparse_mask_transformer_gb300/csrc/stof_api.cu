@@ -386,7 +386,7 @@ static stof_status plan_call(const stof_format& f, int B, int H, int L, int d, s
                              int* source) {
   if (which != STOF_KERNEL_AUTO && which != STOF_KERNEL_ROWWISE && which != STOF_KERNEL_BLOCKWISE)
     return STOF_ERR_INVALID_ARG;
-  *c = KernelChoice{which, f.bn, 0, kVariantAuto, 0};
+  *c = KernelChoice{which, f.bn, 0, kVariantAuto, 0, 0, 0};
   *source = STOF_PLAN_FORCED;
   if (which == STOF_KERNEL_AUTO) {
     if (!f.synced) return STOF_ERR_NOT_SYNCED;
@@ -396,7 +396,7 @@ static stof_status plan_call(const stof_format& f, int B, int H, int L, int d, s
     if (tuned_choice(L, d, density, f.bn, c) && (c->kernel == STOF_KERNEL_ROWWISE || blockwise_tiles(f))) {
       *source = STOF_PLAN_TUNED;
     } else {
-      *c = KernelChoice{which, f.bn, 0, kVariantAuto, 0};
+      *c = KernelChoice{which, f.bn, 0, kVariantAuto, 0, 0, 0};
       *source = STOF_PLAN_ANALYTIC;
       c->kernel = stof_select_kernel_heads(density, L, d, static_cast<int64_t>(B) * H, listed128_per_row(f));
       if (c->kernel == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(f))
@@ -420,9 +420,13 @@ stof_status stof_mha_plan(const stof_format* fmt, int B, int H, int L, int d, st
   out->persistent = 0;
   out->stages = 0;
   out->rows_per_warp = 0;
+  out->exp_split = 0;
+  out->softmax_warpgroups = 0;
   if (c.kernel == STOF_KERNEL_BLOCKWISE) {
     out->persistent = blockwise_persistent(d, c.variant, tiles_per_row(*fmt)) ? 1 : 0;
     out->stages = blockwise_stages(out->persistent != 0, c.stages);
+    out->exp_split = c.exp_split;
+    out->softmax_warpgroups = c.softmax_wg ? c.softmax_wg : 2;
   } else {
     out->rows_per_warp = rowwise_rows_per_warp(static_cast<long long>(B) * H * L, keys_per_row(*fmt),
                                                listed128_per_row(*fmt), c.rows_per_warp);
@@ -472,6 +476,8 @@ stof_status mha_fwd_choice(const void* q, const void* k, const void* v, stof_dty
   p.rows_per_warp = c.rows_per_warp;
   p.stages = c.stages;
   p.variant = c.variant;
+  p.exp_split = c.exp_split;
+  p.softmax_wg = c.softmax_wg;
   const bool bf16 = dt == STOF_BF16;
   cudaStream_t s = as_stream(stream);
   if (c.kernel == STOF_KERNEL_ROWWISE)
@@ -489,14 +495,20 @@ stof_status stof_mha_fwd_plan(const void* q, const void* k, const void* v, stof_
   if (!plan) return STOF_ERR_INVALID_ARG;
   if (plan->kernel != STOF_KERNEL_ROWWISE && plan->kernel != STOF_KERNEL_BLOCKWISE) return STOF_ERR_INVALID_ARG;
   if (!fmt) return STOF_ERR_INVALID_ARG;
-  KernelChoice c{plan->kernel, fmt->bn, 0, kVariantAuto, 0};
+  KernelChoice c{plan->kernel, fmt->bn, 0, kVariantAuto, 0, 0, 0};
   if (plan->kernel == STOF_KERNEL_BLOCKWISE) {
     if (plan->stages < 0 || plan->stages > 8) return STOF_ERR_INVALID_ARG;
+    if (plan->exp_split != 0 && plan->exp_split != 1) return STOF_ERR_INVALID_ARG;
+    const int w = plan->softmax_warpgroups;
+    if (w != 0 && w != 2 && w != 4) return STOF_ERR_UNSUPPORTED;
     c.stages = plan->stages;
     c.variant = plan->persistent ? kVariantPersistent : kVariantPerTile;
+    c.exp_split = plan->exp_split;
+    c.softmax_wg = w;
   } else {
     const int r = plan->rows_per_warp;
     if (r != 0 && r != 1 && r != 2 && r != 4) return STOF_ERR_UNSUPPORTED;
+    if (plan->exp_split != 0 || plan->softmax_warpgroups != 0) return STOF_ERR_UNSUPPORTED;
     c.rows_per_warp = r;
   }
   return mha_fwd_choice(q, k, v, dt, B, H, L, d, scale, fmt, mask_stride_b, mask_stride_h, c, o, stream);

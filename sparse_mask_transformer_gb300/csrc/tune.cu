@@ -7,9 +7,11 @@
 // them, and (same page, "autopilot" summary) what was measured is cached so
 // that a configuration is not timed again.  For the masked MHA step the
 // sampled parameters are the kernel (row-wise or block-wise), the OT width
-// (64 or 128 key columns; 128 query rows), the block-wise kernel's K/V ring
-// depth (its pipeline stages) and, at d = 64, whether it runs persistent
-// CTAs.  A result is cached under (sequence length, head dim, density
+// (64 or 128 key columns; 128 query rows), the row-wise kernel's rows per
+// warp, the block-wise kernel's K/V ring depth (its pipeline stages), its
+// exp split (a share of the exponentials on the FMA pipe), its softmax
+// warpgroup count (2, or 4 on the persistent kernel) and, at d = 64,
+// whether it runs persistent CTAs.  A result is cached under (sequence length, head dim, density
 // bucket), the bucket being the density rounded to half powers of two;
 // stof_mha_fwd(AUTO) runs the fastest cached candidate on the format's OT
 // width.
@@ -36,6 +38,9 @@ const KernelChoice kTuneCandidates[STOF_TUNE_CANDIDATES] = {
     {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPersistent, 0},  // d = 64 only
     {STOF_KERNEL_BLOCKWISE, 128, 2, kVariantPersistent, 0},  // d = 64 only
     {STOF_KERNEL_BLOCKWISE, 64, 0, kVariantAuto, 0},
+    {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPerTile, 0, 1, 0},     // exp split
+    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPersistent, 0, 1, 0},  // exp split, d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPersistent, 0, 0, 4},  // four softmax warpgroups, d = 64 only
 };
 
 namespace {
@@ -105,12 +110,18 @@ stof_status stof_tune(const uint8_t* mask, int n_masks, const void* q, const voi
   r.stages = 0;
   r.persistent = 0;
   r.rows_per_warp = 0;
+  r.exp_split = 0;
+  r.softmax_warpgroups = 0;
   for (int i = 0; i < STOF_TUNE_CANDIDATES; ++i) {
-    r.cand_kernel[i] = kTuneCandidates[i].kernel;
-    r.cand_bn[i] = kTuneCandidates[i].bn;
+    const KernelChoice& cand = kTuneCandidates[i];
+    r.cand_kernel[i] = cand.kernel;
+    r.cand_bn[i] = cand.bn;
     r.cand_persistent[i] = 0;
     r.cand_stages[i] = 0;
-    r.cand_rows_per_warp[i] = kTuneCandidates[i].rows_per_warp;
+    r.cand_rows_per_warp[i] = cand.rows_per_warp;
+    r.cand_exp_split[i] = cand.exp_split;
+    r.cand_softmax_warpgroups[i] =
+        cand.kernel == STOF_KERNEL_BLOCKWISE ? (cand.softmax_wg ? cand.softmax_wg : 2) : 0;
     r.cand_ms[i] = -1.f;
   }
   stof_status st = STOF_OK;
@@ -161,6 +172,8 @@ stof_status stof_tune(const uint8_t* mask, int n_masks, const void* q, const voi
         r.stages = r.cand_stages[i];
         r.persistent = r.cand_persistent[i];
         r.rows_per_warp = r.cand_rows_per_warp[i];
+        r.exp_split = r.cand_exp_split[i];
+        r.softmax_warpgroups = r.cand_softmax_warpgroups[i];
       }
     }
     if (st != STOF_OK) break;

@@ -44,12 +44,12 @@ EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync
             "stof_last_cuda_error", "stof_tune_workspace_bytes", "stof_tune", "stof_tune_lookup",
             "stof_tune_clear", "stof_tune_density_bucket", "stof_encode_mask_bits", "stof_oproj_fwd",
             "stof_encode_rules", "stof_check_bounded_wait", "stof_mha_plan", "stof_mha_fwd_plan",
-            "stof_select_kernel_heads", "stof_oproj_ln_fwd", "stof_oproj_ln_workspace_bytes"]
+            "stof_select_kernel_heads", "stof_oproj_ln_fwd", "stof_oproj_ln_workspace_bytes", "stof_ex2_fma"]
 
 STOF_MAX_RULES = 64
 INT32_MIN, INT32_MAX = -(1 << 31), (1 << 31) - 1
 
-STOF_TUNE_CANDIDATES = 10
+STOF_TUNE_CANDIDATES = 13
 
 STOF_PLAN_FORCED = 0
 STOF_PLAN_ANALYTIC = 1
@@ -90,17 +90,21 @@ class stof_tune_result(ctypes.Structure):
     _fields_ = [
         ("kernel", ctypes.c_int), ("bn", ctypes.c_int), ("ms", ctypes.c_float), ("density", ctypes.c_double),
         ("stages", ctypes.c_int), ("persistent", ctypes.c_int), ("rows_per_warp", ctypes.c_int),
+        ("exp_split", ctypes.c_int), ("softmax_warpgroups", ctypes.c_int),
         ("cand_kernel", ctypes.c_int * STOF_TUNE_CANDIDATES), ("cand_bn", ctypes.c_int * STOF_TUNE_CANDIDATES),
         ("cand_stages", ctypes.c_int * STOF_TUNE_CANDIDATES),
         ("cand_persistent", ctypes.c_int * STOF_TUNE_CANDIDATES),
         ("cand_rows_per_warp", ctypes.c_int * STOF_TUNE_CANDIDATES),
+        ("cand_exp_split", ctypes.c_int * STOF_TUNE_CANDIDATES),
+        ("cand_softmax_warpgroups", ctypes.c_int * STOF_TUNE_CANDIDATES),
         ("cand_ms", ctypes.c_float * STOF_TUNE_CANDIDATES),
     ]
 
 
 class stof_plan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("stages", ctypes.c_int), ("persistent", ctypes.c_int),
-                ("source", ctypes.c_int), ("rows_per_warp", ctypes.c_int)]
+                ("source", ctypes.c_int), ("rows_per_warp", ctypes.c_int), ("exp_split", ctypes.c_int),
+                ("softmax_warpgroups", ctypes.c_int)]
 
 
 _lib = None
@@ -126,6 +130,8 @@ def load_library(path: str = LIB_PATH):
         lib.stof_encode_rules.restype = i32
         lib.stof_check_bounded_wait.argtypes = [P, ctypes.c_double, P]
         lib.stof_check_bounded_wait.restype = i32
+        lib.stof_ex2_fma.argtypes = [P, P, i64, P]
+        lib.stof_ex2_fma.restype = i32
         lib.stof_format_sync.argtypes = [ctypes.POINTER(stof_format), P]
         lib.stof_format_sync.restype = i32
         lib.stof_select_kernel.argtypes = [ctypes.c_double, i32, i32]
@@ -274,6 +280,13 @@ def stof_check_bounded_wait(device_error: torch.Tensor, seconds: float, stream=N
     STOF_DEVERR_PIPE_TIMEOUT into it after `seconds` of a wait that never ends."""
     _check(load_library().stof_check_bounded_wait(device_error.data_ptr(), float(seconds), _stream(stream)),
            "stof_check_bounded_wait")
+
+
+def stof_ex2_fma(x: torch.Tensor, y: torch.Tensor, stream=None) -> None:
+    """y = the block-wise kernels' FMA-pipe exp2 of x (device fp32, same length)."""
+    if x.dtype != torch.float32 or y.dtype != torch.float32 or x.numel() != y.numel():
+        raise ValueError("x and y must be fp32 tensors of the same size")
+    _check(load_library().stof_ex2_fma(x.data_ptr(), y.data_ptr(), x.numel(), _stream(stream)), "stof_ex2_fma")
 
 
 def stof_format_sync(fmt: stof_format, stream=None) -> stof_format:

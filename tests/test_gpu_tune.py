@@ -1,10 +1,11 @@
 """Measured parameter choice with a result cache (gist.science technical
 summary, Methodology 2, two-stage tuning, stage 2 "parameter sampling":
 kernel parameters are sampled by running them and the outcomes cached).
-The candidates are the row-wise kernel on 128x128 OTs and the block-wise
-kernel on 128x128 OTs with ring depths 2-4, one CTA per query tile or
-persistent CTAs (d = 64), and on 128x64 OTs; the chosen one must also be
-correct, and stof_mha_fwd(AUTO) must run it once it is cached."""
+The candidates are the row-wise kernel on 128x128 OTs with 1, 2 or 4 rows
+per warp and the block-wise kernel on 128x128 OTs with ring depths 2-4, one
+CTA per query tile or persistent CTAs (d = 64), the exp split, four softmax
+warpgroups (persistent, d = 64), and on 128x64 OTs; the chosen one must also
+be correct, and stof_mha_fwd(AUTO) must run it once it is cached."""
 import math
 
 import numpy as np
@@ -30,13 +31,18 @@ def test_tune_picks_the_fastest_candidate_and_caches_it(gpu_lib):
     res = stof.stof_tune(mdev, qd, kd, vd, 1 / math.sqrt(d), 0, 0, ws, o)
     ms = list(res.cand_ms)
     assert all(t > 0 for t in ms)                            # d = 64 admits every candidate
-    assert list(res.cand_stages) == [0, 0, 0, 3, 2, 4, 4, 3, 2, 4]
-    assert list(res.cand_persistent) == [0, 0, 0, 0, 0, 0, 1, 1, 1, 1]  # 128x64: 9 OTs per row -> persistent
-    assert list(res.cand_rows_per_warp) == [1, 2, 4, 0, 0, 0, 0, 0, 0, 0]
+    assert list(res.cand_stages) == [0, 0, 0, 3, 2, 4, 4, 3, 2, 4, 3, 4, 4]
+    # 128x64: 9 OTs per row -> persistent
+    assert list(res.cand_persistent) == [0, 0, 0, 0, 0, 0, 1, 1, 1, 1, 0, 1, 1]
+    assert list(res.cand_rows_per_warp) == [1, 2, 4] + [0] * 10
+    assert list(res.cand_exp_split) == [0] * 10 + [1, 1, 0]
+    assert list(res.cand_softmax_warpgroups) == [0, 0, 0] + [2] * 9 + [4]
     best = int(np.argmin(ms))
     assert res.kernel == res.cand_kernel[best] and res.bn == res.cand_bn[best]
     assert res.stages == res.cand_stages[best] and res.persistent == res.cand_persistent[best]
     assert res.rows_per_warp == res.cand_rows_per_warp[best]
+    assert res.exp_split == res.cand_exp_split[best]
+    assert res.softmax_warpgroups == res.cand_softmax_warpgroups[best]
     assert res.ms == pytest.approx(ms[best])
     assert res.density == pytest.approx((L + 1) / (2 * L))
     hit = stof.stof_tune_lookup(L, d, res.density * 1.05)    # same half-octave bucket
@@ -79,12 +85,14 @@ def test_auto_runs_the_cached_measurement(gpu_lib, d):
     ms = [t if (t > 0 and res.cand_bn[i] == 128) else float("inf") for i, t in enumerate(res.cand_ms)]
     best = int(np.argmin(ms))
     if d == 128:
-        assert all(res.cand_ms[i] < 0 for i in (5, 6, 7, 8))    # d = 64-only candidates
+        assert all(res.cand_ms[i] < 0 for i in (5, 6, 7, 8, 11, 12))    # d = 64-only candidates
     plan = stof.stof_mha_plan(fmt, B, H, L, d, stof.STOF_KERNEL_AUTO)
     assert plan.source == stof.STOF_PLAN_TUNED
     assert plan.kernel == res.cand_kernel[best]
     if plan.kernel == stof.STOF_KERNEL_BLOCKWISE:
         assert (plan.stages, plan.persistent) == (res.cand_stages[best], res.cand_persistent[best])
+        assert (plan.exp_split, plan.softmax_warpgroups) == (res.cand_exp_split[best],
+                                                             res.cand_softmax_warpgroups[best])
     else:
         assert plan.rows_per_warp == res.cand_rows_per_warp[best]
     o2 = torch.full_like(qd, float("nan"))
@@ -98,22 +106,25 @@ def test_auto_runs_the_cached_measurement(gpu_lib, d):
     assert stof.stof_mha_plan(fmt, B, H, L, d, stof.STOF_KERNEL_AUTO).source == stof.STOF_PLAN_ANALYTIC
 
 
-@pytest.mark.parametrize("d,stages,persistent", [(64, 2, 0), (64, 3, 0), (64, 4, 0), (64, 2, 1), (64, 3, 1),
-                                                  (64, 4, 1), (128, 2, 0), (128, 3, 0)])
-def test_every_tuned_configuration_matches_the_oracle(gpu_lib, d, stages, persistent):
-    """Each block-wise configuration the tuner samples (ring depth, variant),
-    run through stof_mha_fwd_plan: per-head causal masks with random holes,
-    a fully masked row and a query tile without listed OTs, more query tiles
-    than SMs for d = 64."""
+@pytest.mark.parametrize("d,stages,persistent,esplit,swg", [
+    (64, 2, 0, 0, 0), (64, 3, 0, 0, 0), (64, 4, 0, 0, 0), (64, 2, 1, 0, 0), (64, 3, 1, 0, 0), (64, 4, 1, 0, 0),
+    (128, 2, 0, 0, 0), (128, 3, 0, 0, 0),
+    (64, 3, 0, 1, 0), (64, 4, 1, 1, 0), (128, 3, 0, 1, 0),       # exp split
+    (64, 4, 1, 0, 4)])                                           # four softmax warpgroups
+def test_every_tuned_configuration_matches_the_oracle(gpu_lib, d, stages, persistent, esplit, swg):
+    """Each block-wise configuration the tuner samples (ring depth, variant,
+    exp split, softmax warpgroups), run through stof_mha_fwd_plan: per-head
+    causal masks with random holes, a fully masked row and a query tile
+    without listed OTs, more query tiles than SMs for d = 64."""
     B, H, L = (2, 10, 1024) if d == 64 else (1, 4, 512)
-    rng = np.random.default_rng(90 + stages + 10 * persistent + d)
+    rng = np.random.default_rng(90 + stages + 10 * persistent + d + 100 * esplit + swg)
     masks = (rng.random((B * H, L, L)) < 0.2).astype(np.uint8) * np.tril(np.ones((L, L), np.uint8))[None]
     masks[:, np.arange(L), np.arange(L)] = 1
     masks[3, 300] = 0
     masks[1, :128] = 0
     q, k, v = synth.make_qkv(B, H, L, d, "bf16", seed=91)
     fmt, ws, _ = gpu_encode(torch.from_numpy(masks).cuda(), 128, 128)
-    plan = stof.stof_plan(stof.STOF_KERNEL_BLOCKWISE, stages, persistent, 0, 0)
+    plan = stof.stof_plan(stof.STOF_KERNEL_BLOCKWISE, stages, persistent, 0, 0, esplit, swg)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o = torch.full_like(qd, float("nan"))
     scale = 1 / math.sqrt(d)
@@ -133,9 +144,19 @@ def test_configurations_the_sizes_do_not_admit_are_refused(gpu_lib):
     L = 256
     fmt, ws, _ = gpu_encode(torch.ones(1, L, L, dtype=torch.uint8, device="cuda"), 128, 128)
     q = torch.zeros(1, 1, L, 128, dtype=torch.bfloat16, device="cuda")
-    for stages, persistent in ((4, 0), (2, 1), (5, 0)):
+    # d = 128: ring depth 4, persistent CTAs, four softmax warpgroups, the exp split off its ring depth
+    for stages, persistent, esplit, swg in ((4, 0, 0, 0), (2, 1, 0, 0), (5, 0, 0, 0), (3, 0, 0, 4), (4, 1, 0, 4),
+                                            (2, 0, 1, 0)):
         with pytest.raises(stof.StofError) as e:
-            stof.stof_mha_fwd_plan(q, q, q, fmt, 0.1, 0, 0, stof.stof_plan(1, stages, persistent, 0, 0), q.clone())
+            stof.stof_mha_fwd_plan(q, q, q, fmt, 0.1, 0, 0,
+                                   stof.stof_plan(1, stages, persistent, 0, 0, esplit, swg), q.clone())
+        assert e.value.status == stof.STOF_ERR_UNSUPPORTED
+    # d = 64: four warpgroups only persistent at ring depth 4 and without the exp split
+    q64 = torch.zeros(1, 1, L, 64, dtype=torch.bfloat16, device="cuda")
+    for stages, persistent, esplit, swg in ((4, 0, 0, 4), (3, 1, 0, 4), (4, 1, 1, 4), (3, 1, 1, 0)):
+        with pytest.raises(stof.StofError) as e:
+            stof.stof_mha_fwd_plan(q64, q64, q64, fmt, 0.1, 0, 0,
+                                   stof.stof_plan(1, stages, persistent, 0, 0, esplit, swg), q64.clone())
         assert e.value.status == stof.STOF_ERR_UNSUPPORTED
 
 

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert stof.stof_version() == 2
+    assert stof.stof_version() == 3
     for s in range(10):
         assert stof.stof_status_string(s)
     assert "unknown" in stof.stof_status_string(99)
@@ -414,6 +414,12 @@ def test_mha_fwd_plan_rejects_bad_plans_before_launch(lib):
     assert _plan_call(lib, P(stof.STOF_KERNEL_BLOCKWISE, 9, 0, 0, 0)) == stof.STOF_ERR_INVALID_ARG
     assert _plan_call(lib, P(stof.STOF_KERNEL_ROWWISE, 0, 0, 0, 1), q=None) == stof.STOF_ERR_INVALID_ARG
     assert _plan_call(lib, P(stof.STOF_KERNEL_ROWWISE, 0, 0, 0, 1), d=96) == stof.STOF_ERR_UNSUPPORTED
+    blk = stof.STOF_KERNEL_BLOCKWISE
+    assert _plan_call(lib, P(blk, 0, 1, 0, 0, 2, 0)) == stof.STOF_ERR_INVALID_ARG        # exp split is 0 or 1
+    assert _plan_call(lib, P(blk, 0, 1, 0, 0, 0, 3)) == stof.STOF_ERR_UNSUPPORTED        # 2 or 4 warpgroups
+    assert _plan_call(lib, P(blk, 0, 1, 0, 0, 0, 8)) == stof.STOF_ERR_UNSUPPORTED
+    assert _plan_call(lib, P(stof.STOF_KERNEL_ROWWISE, 0, 0, 0, 1, 1, 0)) == stof.STOF_ERR_UNSUPPORTED
+    assert _plan_call(lib, P(stof.STOF_KERNEL_ROWWISE, 0, 0, 0, 1, 0, 4)) == stof.STOF_ERR_UNSUPPORTED
 
 
 def test_oproj_ln_sizes_and_argument_errors(lib):
