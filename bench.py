@@ -50,7 +50,7 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-HOST_CODE_MARK = b"// [rows][D] row-major 16-bit matrix"
+HOST_CODE_MARK = b"// ---------------------------------------------------------------- host side"
 
 
 def kernel_source_hash() -> str:

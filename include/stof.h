@@ -60,7 +60,7 @@ extern "C" {
 typedef enum {
   STOF_OK = 0,
   STOF_ERR_INVALID_ARG = 1,  /* null pointer, negative size, unknown enum value */
-  STOF_ERR_SHAPE = 2,        /* sizes inconsistent, not tile-divisible, or too large */
+  STOF_ERR_SHAPE = 2,        /* sizes inconsistent, not tile-divisible where required, or too large */
   STOF_ERR_DTYPE = 3,        /* unknown element type */
   STOF_ERR_ALIGNMENT = 4,    /* a pointer is not aligned as required */
   STOF_ERR_WORKSPACE = 5,    /* workspace smaller than stof_encode_workspace_bytes() */
@@ -125,7 +125,11 @@ size_t stof_encode_workspace_bytes(int n_masks, int lq, int lk, int bm, int bn);
  * as empty / full / partial, builds the two CSR pointer arrays by a prefix
  * sum, and packs the IT bitmaps of partial OTs, in one pass over the mask.
  *   mask       device, uint8 [n_masks][lq][lk]; 8-byte aligned.
- *   bm, bn     OT size: multiples of 8 in [8, 256]; lq % bm == 0, lk % bn == 0.
+ *   bm, bn     OT size: multiples of 8 in [8, 256].  lq and lk need not be
+ *              multiples of bm and bn: a side that is not a whole number of
+ *              OTs is encoded as padded to one with invalid elements, so
+ *              n_tr = ceil(lq / bm), n_tc = ceil(lk / bn), and an OT that
+ *              reaches past a side is partial or empty, never full.
  *   workspace  device, >= stof_encode_workspace_bytes(...) bytes, 256-byte
  *              aligned; owned by the caller and must outlive every use of fmt.
  *   fmt        host struct, overwritten; its pointers alias the workspace.
@@ -145,8 +149,9 @@ stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, i
  * identical.  The pages note that STOF keeps working at
  * sequence lengths where other systems run out of memory (scifaro.com
  * summary, Results, scalability up to 16k); a 16384-long dense mask per
- * head is 256 MB, its bit-packed form 32 MB.  Same sizes, workspace,
- * alignment (8 bytes) and errors as stof_encode_mask().
+ * head is 256 MB, its bit-packed form 32 MB.  Same workspace, alignment
+ * (8 bytes) and errors as stof_encode_mask(), but lq and lk must be
+ * multiples of bm and bn (STOF_ERR_SHAPE otherwise).
  */
 stof_status stof_encode_mask_bits(const uint8_t* mask_bits, int n_masks, int lq, int lk, int bm, int bn,
                                   void* workspace, size_t ws_bytes, stof_format* fmt, void* stream);
@@ -257,7 +262,9 @@ stof_kernel stof_select_kernel_heads(double density, int seq_len, int head_dim, 
  * rows without valid keys give 0.  Only listed OTs are touched; full OTs
  * need no mask test, partial OTs are masked through their IT bitmaps.
  *   q, k, v, o  device [B][H][L][d], dt, 16-byte aligned; o is written.
- *   L           == fmt->lq == fmt->lk.   d: 64 or 128.
+ *   L           == fmt->lq == fmt->lk, any length (a last OT row and column
+ *               that reach past L are padded: rows past L are computed and
+ *               not stored, keys past L are never valid).   d: 64 or 128.
  *   scale       any finite value; the softmax is taken over scale * Q.K
  *               (a negative scale favours the smallest dot products, a zero
  *               scale averages the valid V rows).

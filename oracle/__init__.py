@@ -108,10 +108,28 @@ def attention(q, k, v, mask, scale: float, n_threads: int | None = None) -> np.n
     return o
 
 
-def encode_count(mask, bm: int, bn: int):
-    """(n_full, n_part, nnz) of mask [n_masks, lq, lk]."""
-    lib = _load()
+def _padded(mask, bm: int, bn: int) -> np.ndarray:
+    """mask [n_masks, lq, lk] extended with invalid (0) elements to whole
+    OTs on both sides.  The two-level format tiles the whole matrix with
+    BM x BN outer tiles ("Accelerating Sparse Transformer Inference on
+    GPU", gist.science technical summary, Methodology 1, two-level storage
+    format); the pages only use sides that are whole numbers of tiles, and
+    for other sides this is the plain reading: the last OT row and column
+    are padded, and padding is never a valid element."""
     mask = np.ascontiguousarray(mask, dtype=np.uint8)
+    n_masks, lq, lk = mask.shape
+    lqp, lkp = -(-lq // bm) * bm, -(-lk // bn) * bn
+    if (lqp, lkp) == (lq, lk):
+        return mask
+    out = np.zeros((n_masks, lqp, lkp), dtype=np.uint8)
+    out[:, :lq, :lk] = mask
+    return out
+
+
+def encode_count(mask, bm: int, bn: int):
+    """(n_full, n_part, nnz) of mask [n_masks, lq, lk] (sides padded to whole OTs)."""
+    lib = _load()
+    mask = _padded(mask, bm, bn)
     n_masks, lq, lk = mask.shape
     counts = np.zeros(3, dtype=np.int64)
     if lib.stof_oracle_encode_count(_ptr(mask), n_masks, lq, lk, bm, bn, _ptr(counts)) != 0:
@@ -120,9 +138,12 @@ def encode_count(mask, bm: int, bn: int):
 
 
 def encode(mask, bm: int, bn: int) -> dict:
-    """Brute-force two-level encoding of mask [n_masks, lq, lk]."""
+    """Brute-force two-level encoding of mask [n_masks, lq, lk]; sides that
+    are not whole numbers of OTs are padded to one with invalid elements
+    (_padded); lq and lk of the result are the mask's own."""
     lib = _load()
-    mask = np.ascontiguousarray(mask, dtype=np.uint8)
+    lq0, lk0 = np.shape(mask)[1:]
+    mask = _padded(mask, bm, bn)
     n_masks, lq, lk = mask.shape
     n_full, n_part, nnz = encode_count(mask, bm, bn)
     n_rows = n_masks * (lq // bm)
@@ -143,13 +164,15 @@ def encode(mask, bm: int, bn: int) -> dict:
     fmt["full_col_idx"] = fmt["full_col_idx"][:n_full]
     fmt["part_col_idx"] = fmt["part_col_idx"][:n_part]
     fmt["bitmaps"] = fmt["bitmaps"][:n_part]
+    fmt["lq"], fmt["lk"] = lq0, lk0
     return fmt
 
 
 def decode(fmt: dict) -> np.ndarray:
     """Dense 0/1 mask [n_masks, lq, lk] rebuilt from a format dict."""
     lib = _load()
-    n_masks, lq, lk, bm, bn = (fmt[x] for x in ("n_masks", "lq", "lk", "bm", "bn"))
+    n_masks, lq0, lk0, bm, bn = (fmt[x] for x in ("n_masks", "lq", "lk", "bm", "bn"))
+    lq, lk = -(-lq0 // bm) * bm, -(-lk0 // bn) * bn     # decoded on the padded sides, then cropped
     out = np.empty((n_masks, lq, lk), dtype=np.uint8)
     arrs = [np.ascontiguousarray(fmt[x], dtype=t) for x, t in (
         ("full_row_ptr", np.int32), ("full_col_idx", np.int32), ("part_row_ptr", np.int32),
@@ -158,7 +181,7 @@ def decode(fmt: dict) -> np.ndarray:
     rc = lib.stof_oracle_decode(n_masks, lq, lk, bm, bn, *[_ptr(a) for a in arrs], _ptr(out))
     if rc != 0:
         raise ValueError("oracle decode: bad shape")
-    return out
+    return out[:, :lq0, :lk0]
 
 
 def attention_bhld(q, k, v, mask_of, scale: float, heads=None, rows=None,

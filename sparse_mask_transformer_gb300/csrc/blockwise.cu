@@ -176,10 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && n > 0) {  // Q, then K tiles; a row without listed OTs loads nothing
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
-        const int qrow = bh * p.L + I * kBM;
+        const int qrow = I * kBM;  // row of head bh
         mbar_arrive_expect_tx(&s.q_full, C::Q_BYTES);
 #pragma unroll
-        for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow);
+        for (int r = 0; r < C::REGIONS; ++r) tma_load_3d(s.q + r * 16384, &tmQ, &s.q_full, 64 * r, qrow, bh);
         int issued = 0;
         for (int t = 0, st = 0, ph = 0; t < n; ++t) {
           // stage st = t % ST held K_{t-ST}: free once that tile's scores are done
@@ -187,10 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             fail();
             break;
           }
-          const int krow = bh * p.L + column_of(t) * BN;
+          const int krow = column_of(t) * BN;
           mbar_arrive_expect_tx(&s.k_full[st], C::KV_BYTES);
 #pragma unroll
-          for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.k[st] + r * C::KV_ATOM, &tmK, &s.k_full[st], 64 * r, krow);
+          for (int r = 0; r < C::REGIONS; ++r)
+            tma_load_3d(s.k[st] + r * C::KV_ATOM, &tmK, &s.k_full[st], 64 * r, krow, bh);
           issued = t + 1;
           if (++st == kStages) {
             st = 0;
@@ -214,10 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             fail();
             break;
           }
-          const int vrow = bh * p.L + column_of(t) * BN;
+          const int vrow = column_of(t) * BN;
           mbar_arrive_expect_tx(&s.v_full[st], C::KV_BYTES);
 #pragma unroll
-          for (int r = 0; r < C::REGIONS; ++r) tma_load_2d(s.v[st] + r * C::KV_ATOM, &tmV, &s.v_full[st], 64 * r, vrow);
+          for (int r = 0; r < C::REGIONS; ++r)
+            tma_load_3d(s.v[st] + r * C::KV_ATOM, &tmV, &s.v_full[st], 64 * r, vrow, bh);
           issued = t + 1;
           if (++st == kStages) {
             st = 0;
@@ -399,6 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lt = a0 * x0[kBM + r] + a1 * x1[kBM + r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float w0 = a0 * inv, w1 = a1 * inv;
+      // a query tile of a padded last OT row has rows past L: computed, not stored
+      const bool row_in = I * kBM + r < p.L;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
                       (static_cast<size_t>(bh) * p.L + static_cast<size_t>(I) * kBM + r) * (D * 2) + g * D;
 #pragma unroll
@@ -428,8 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           w[i] = pack2<BF16>(v0, v1);
         }
         uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
+        if (row_in) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
       }
     }
   }
@@ -444,7 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-// [rows][D] row-major 16-bit matrix, box = 64 columns x box_rows rows, 128-byte swizzle.
+// ---------------------------------------------------------------- host side
+// [heads][L][D] row-major 16-bit tensor (one [L][D] matrix per head, as
+// Q, K and V are), box = 64 columns x box_rows rows of one head, 128-byte
+// swizzle; a box that runs past row L of its head reads zeros there.
 // A tensor map holds only the address, sizes, strides and box of a tensor,
 // so a map made once stays right for every later call with the same key;
 // the cache (round-robin over kMapCache entries) spares the driver call that
@@ -453,11 +462,12 @@ namespace {
 struct MapKey {
   int dev;
   const void* base;
-  uint64_t rows;
+  uint64_t heads, L;
   int D, box_rows;
   bool bf16;
   bool operator==(const MapKey& o) const {
-    return dev == o.dev && base == o.base && rows == o.rows && D == o.D && box_rows == o.box_rows && bf16 == o.bf16;
+    return dev == o.dev && base == o.base && heads == o.heads && L == o.L && D == o.D && box_rows == o.box_rows &&
+           bf16 == o.bf16;
   }
 };
 struct MapEntry {
@@ -471,10 +481,10 @@ MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 }  // namespace
 
-bool make_bw_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_rows, bool bf16) {
+bool make_bw_map(CUtensorMap* m, const void* base, uint64_t heads, uint64_t L, int D, int box_rows, bool bf16) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
-  const MapKey key{dev, base, rows, D, box_rows, bf16};
+  const MapKey key{dev, base, heads, L, D, box_rows, bf16};
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (const MapEntry& e : g_maps)
@@ -483,9 +493,10 @@ bool make_bw_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box
         return true;
       }
   }
-  if (!encode_tensor_map_2d(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base,
-                            static_cast<uint64_t>(D), rows, static_cast<uint64_t>(D) * 2, 64,
-                            static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_tensor_map_3d(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base,
+                            static_cast<uint64_t>(D), L, heads, static_cast<uint64_t>(D) * 2,
+                            L * static_cast<uint64_t>(D) * 2, 64, static_cast<uint32_t>(box_rows),
+                            CU_TENSOR_MAP_SWIZZLE_128B))
     return false;
   std::lock_guard<std::mutex> lock(g_map_mu);
   MapEntry& e = g_maps[g_map_next];
@@ -500,10 +511,10 @@ namespace {
 
 template <int D, int BN, bool BF16, int ST, bool NEG, bool ESPLIT>
 stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
-  const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.L;
+  const uint64_t heads = static_cast<uint64_t>(p.B) * p.H;
   CUtensorMap mq, mk, mv;
-  if (!make_bw_map(&mq, p.q, rows, D, kBM, BF16) || !make_bw_map(&mk, p.k, rows, D, BN, BF16) ||
-      !make_bw_map(&mv, p.v, rows, D, BN, BF16))
+  if (!make_bw_map(&mq, p.q, heads, p.L, D, kBM, BF16) || !make_bw_map(&mk, p.k, heads, p.L, D, BN, BF16) ||
+      !make_bw_map(&mv, p.v, heads, p.L, D, BN, BF16))
     return STOF_ERR_CUDA;
   const size_t smem = sizeof(Smem<D, BN, ST>) + 1024;
   stof_status prep = STOF_OK;
@@ -590,6 +601,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   });
   return fn;
+}
+
+// [planes][rows][inner] with `row_bytes` between rows and `plane_bytes`
+// between planes; boxes of box_inner x box_rows x 1; zeros outside.
+bool encode_tensor_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t rows, uint64_t planes, uint64_t row_bytes, uint64_t plane_bytes,
+                          uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, rows, planes};
+  cuuint64_t strides[2] = {row_bytes, plane_bytes};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,

@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(threads_of<SWG>, 1)
             break;
           }
           mbar_arrive_expect_tx(&s.q_full[qb], C::Q_BYTES);
-          tma_load_2d(s.q[qb], &tmQ, &s.q_full[qb], 0, it.bh * p.L + it.I * kBM);
+          tma_load_3d(s.q[qb], &tmQ, &s.q_full[qb], 0, it.I * kBM, it.bh);
           ++e;
           bool ok = true;
           for (int t = 0; t < it.n; ++t) {
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(threads_of<SWG>, 1)
               break;
             }
             mbar_arrive_expect_tx(&s.k_full[st], C::KV_BYTES);
-            tma_load_2d(s.k[st], &tmK, &s.k_full[st], 0, it.bh * p.L + column_of(it, t) * BN);
+            tma_load_3d(s.k[st], &tmK, &s.k_full[st], 0, column_of(it, t) * BN, it.bh);
             ++issued;
             if (++st == kRing) {
               st = 0;
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(threads_of<SWG>, 1)
               break;
             }
             mbar_arrive_expect_tx(&s.v_full[st], C::KV_BYTES);
-            tma_load_2d(s.v[st], &tmV, &s.v_full[st], 0, it.bh * p.L + column_of(it, t) * BN);
+            tma_load_3d(s.v[st], &tmV, &s.v_full[st], 0, column_of(it, t) * BN, it.bh);
             ++issued;
             if (++st == kRing) {
               st = 0;
@@ -408,10 +408,14 @@ __global__ void __launch_bounds__(threads_of<SWG>, 1)
         return static_cast<uint8_t*>(p.o) +
                (static_cast<size_t>(bh) * p.L + static_cast<size_t>(I) * kBM + r) * (kD * 2);
       };
+      // rows past L (a padded last OT row) are computed, not stored
+      const bool row_in = (p.n_tr - 1 - idx % p.n_tr) * kBM + r < p.L;
       if (n == 0) {  // no listed tile: the rows of this query tile are 0 (a quarter of each row per warpgroup)
-        uint4* z = reinterpret_cast<uint4*>(out_row() + (2 * g + hh) * (kD / 2));
-        z[0] = make_uint4(0u, 0u, 0u, 0u);
-        z[1] = make_uint4(0u, 0u, 0u, 0u);
+        if (row_in) {
+          uint4* z = reinterpret_cast<uint4*>(out_row() + (2 * g + hh) * (kD / 2));
+          z[0] = make_uint4(0u, 0u, 0u, 0u);
+          z[1] = make_uint4(0u, 0u, 0u, 0u);
+        }
         continue;
       }
       const int t_first = (g ^ T0) & 1;
@@ -531,9 +535,11 @@ __global__ void __launch_bounds__(threads_of<SWG>, 1)
             }
             w[i] = pack2<BF16>(v0, v1);
           }
-          uint4* dst = reinterpret_cast<uint4*>(out_row() + col * 2);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          if (row_in) {
+            uint4* dst = reinterpret_cast<uint4*>(out_row() + col * 2);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
         }
         // done with this item's O set: the item after next may overwrite it
         tc_fence_before();
@@ -568,9 +574,12 @@ __global__ void __launch_bounds__(threads_of<SWG>, 1)
       const int n = it.n, nf = it.nf;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
                       (static_cast<size_t>(it.bh) * p.L + static_cast<size_t>(it.I) * kBM + r) * (kD * 2);
+      const bool row_in = it.I * kBM + r < p.L;  // rows past L (a padded last OT row): computed, not stored
       if (n == 0) {  // no listed tile: the rows of this query tile are 0
+        if (row_in) {
 #pragma unroll
-        for (int i = 0; i < kD / 16; ++i) reinterpret_cast<uint4*>(orow + g * kD)[i] = make_uint4(0u, 0u, 0u, 0u);
+          for (int i = 0; i < kD / 16; ++i) reinterpret_cast<uint4*>(orow + g * kD)[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
         continue;
       }
       // tile t of the item is the warpgroup's iff (T0 + t) % 2 == g: tiles
@@ -678,8 +687,10 @@ __global__ void __launch_bounds__(threads_of<SWG>, 1)
             w[i] = pack2<BF16>(v0, v1);
           }
           uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
+          if (row_in) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
         }
         // done with this item's O set: the item after next may overwrite it
         tc_fence_before();
@@ -711,10 +722,10 @@ __global__ void __launch_bounds__(threads_of<SWG>, 1)
 
 template <int BN, bool BF16, int RING, bool NEG, bool ESPLIT, int SWG>
 stof_status launch_persist(const AttnParams& p, cudaStream_t s) {
-  const uint64_t rows = static_cast<uint64_t>(p.B) * p.H * p.L;
+  const uint64_t heads = static_cast<uint64_t>(p.B) * p.H;
   CUtensorMap mq, mk, mv;
-  if (!make_bw_map(&mq, p.q, rows, kD, kBM, BF16) || !make_bw_map(&mk, p.k, rows, kD, BN, BF16) ||
-      !make_bw_map(&mv, p.v, rows, kD, BN, BF16))
+  if (!make_bw_map(&mq, p.q, heads, p.L, kD, kBM, BF16) || !make_bw_map(&mk, p.k, heads, p.L, kD, BN, BF16) ||
+      !make_bw_map(&mv, p.v, heads, p.L, kD, BN, BF16))
     return STOF_ERR_CUDA;
   const size_t smem = sizeof(PSmem<BN, RING>) + 1024;
   stof_status prep = STOF_OK;

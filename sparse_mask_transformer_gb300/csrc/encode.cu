@@ -286,9 +286,25 @@ __device__ __forceinline__ void finish_chunk(const EncodeParams& p, long long ch
   write_outputs(p, chunk, s_words, g, cs, tid, kThreads);
 }
 
+// n bytes (n <= VEC; none if n <= 0) from src into the low bytes of a uint4,
+// the rest 0: the part of an 8-row band's unit that lies inside the mask at
+// its lower and right edges, or anywhere when rows are not VEC-aligned.
+template <int VEC>
+__device__ __forceinline__ uint4 load_partial(const uint8_t* src, int n) {
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int b = 0; b < VEC; ++b)
+    if (b < n) w[b >> 2] |= static_cast<uint32_t>(src[b]) << (8 * (b & 3));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // ---------------------------------------------------------------- kernel 1
 // VEC: bytes per load (16 when rows and tiles are 16-byte aligned, else 8).
-template <int VEC>
+// ALIGNED: mask rows start on VEC-byte boundaries, so whole units are read
+// with vector loads; else byte by byte.  A mask whose sides are not whole
+// OTs is encoded as its zero-padded extension: nothing outside lq x lk is
+// read, and those elements count as invalid.
+template <int VEC, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams p) {
   extern __shared__ uint64_t s_words[];  // [bm/8][nt * bn/8]
   __shared__ long long s_chunk;
@@ -320,14 +336,23 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
       if (w < nunits) {
         const int pb = w / upr, qu = w - pb * upr;
         const uint8_t* src = base + static_cast<long long>(8 * pb) * p.lk + VEC * qu;
+        // rows and columns of the unit inside the mask (all but at its edges)
+        const int rows_in = min(8, p.lq - (g.I * p.bm + 8 * pb));
+        const int cols_in = min(VEC, p.lk - (g.J0 * p.bn + VEC * qu));
+        if (ALIGNED && rows_in == 8 && cols_in == VEC) {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          if constexpr (VEC == 16) {
-            v[u][r] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * p.lk));
-          } else {
-            const uint2 x = __ldcs(reinterpret_cast<const uint2*>(src + static_cast<long long>(r) * p.lk));
-            v[u][r] = make_uint4(x.x, x.y, 0u, 0u);
+          for (int r = 0; r < 8; ++r) {
+            if constexpr (VEC == 16) {
+              v[u][r] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * p.lk));
+            } else {
+              const uint2 x = __ldcs(reinterpret_cast<const uint2*>(src + static_cast<long long>(r) * p.lk));
+              v[u][r] = make_uint4(x.x, x.y, 0u, 0u);
+            }
           }
+        } else {
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            v[u][r] = load_partial<VEC>(src + static_cast<long long>(r) * p.lk, r < rows_in ? cols_in : 0);
         }
       }
     }
@@ -370,6 +395,10 @@ __device__ __forceinline__ unsigned long long rule_phase(const EncodeParams& p, 
   for (int w = tid; w < nw; w += kThreads) {
     const int pb = w / g.itcols, qc = w - pb * g.itcols;
     const long long i0 = i_base + 8 * pb, j0 = j_base + 8 * qc;
+    if (i0 >= p.lq || j0 >= p.lk) {  // an IT wholly in the padding of a side: invalid, nothing read
+      words[pb * g.itcols + qc] = 0;
+      continue;
+    }
     uint32_t all_rows = 0;  // bits valid in every row of the IT
     if (ru.global_cols) all_rows |= (__ldg(ru.global_cols + (j0 >> 5)) >> (j0 & 31)) & 0xFFu;
     if (ru.blocks) {
@@ -377,15 +406,19 @@ __device__ __forceinline__ unsigned long long rule_phase(const EncodeParams& p, 
       if ((__ldg(ru.blocks + (bi >> 5)) >> (bi & 31)) & 1u) all_rows = 0xFFu;
     }
     const uint32_t grow = ru.global_rows ? (__ldg(ru.global_rows + (i0 >> 5)) >> (i0 & 31)) & 0xFFu : 0u;
+    // columns j0 .. j0 + 7 inside the matrix (an edge IT of a padded side has fewer)
+    const long long ncols = min(max(static_cast<long long>(p.lk) - j0, 0ll), 8ll);
+    const uint32_t in_cols = ncols == 8 ? 0xFFu : (1u << ncols) - 1u;
     uint64_t word = 0;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
+      if (i0 + r >= p.lq) break;  // rows beyond the matrix: invalid
       // band: i - band_hi <= j <= i - band_lo, as IT columns c = j - j0
       const long long clo = max(i0 + r - ru.band_hi - j0, 0ll);
       const long long chi = min(i0 + r - ru.band_lo - j0, 7ll);
       uint32_t b = clo <= chi ? ((0xFFu >> (7 - chi)) & (0xFFu << clo)) : 0u;
       b |= all_rows | ((grow >> r) & 1u ? 0xFFu : 0u);
-      word |= static_cast<uint64_t>(b) << (8 * r);
+      word |= static_cast<uint64_t>(b & in_cols) << (8 * r);
     }
     words[pb * g.itcols + qc] = word;
     nnz += __popcll(word);
@@ -622,9 +655,9 @@ constexpr int kChunkCols = 1024;
 bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g) {
   if (n_masks < 1 || lq < 1 || lk < 1) return false;
   if (bm < 8 || bn < 8 || bm > 256 || bn > 256 || bm % 8 || bn % 8) return false;
-  if (lq % bm || lk % bn) return false;
-  g->n_tr = lq / bm;
-  g->n_tc = lk / bn;
+  // a side that is not a whole number of OTs is padded to one (with invalid elements)
+  g->n_tr = (lq + bm - 1) / bm;
+  g->n_tc = (lk + bn - 1) / bn;
   g->n_rows = static_cast<int64_t>(n_masks) * g->n_tr;
   g->n_tiles = g->n_rows * g->n_tc;
   if (g->n_tiles >= (int64_t(1) << 31) - 1) return false;
@@ -688,10 +721,13 @@ cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream
     return cudaGetLastError();
   }
   const bool vec16 = (p.lk % 16 == 0) && (p.bn % 16 == 0) && (a % 16 == 0);
+  const bool vec8 = (p.lk % 8 == 0) && (a % 8 == 0);
   if (vec16)
-    encode_kernel<16><<<grid, kThreads, g.smem_bytes, s>>>(p);
+    encode_kernel<16, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
+  else if (vec8)
+    encode_kernel<8, true><<<grid, kThreads, g.smem_bytes, s>>>(p);
   else
-    encode_kernel<8><<<grid, kThreads, g.smem_bytes, s>>>(p);
+    encode_kernel<8, false><<<grid, kThreads, g.smem_bytes, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,10 @@ cudaError_t record_cuda(cudaError_t e);
 bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
                           uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                           CUtensorMapSwizzle swizzle);
+// [planes][rows][inner] tensor, boxes of box_inner x box_rows x 1 (zeros outside the tensor).
+bool encode_tensor_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t rows, uint64_t planes, uint64_t row_bytes, uint64_t plane_bytes,
+                          uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
@@ -173,9 +177,10 @@ int tune_density_bucket(double density);
 stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s);
 // The persistent block-wise kernel for d = 64 (blockwise_persist.cu).
 stof_status launch_blockwise_persist64(const AttnParams& p, bool bf16, cudaStream_t s);
-// TMA map of a [rows][D] 16-bit matrix, 64-column x box_rows boxes, 128-byte swizzle.
+// TMA map of a [heads][L][D] 16-bit tensor, boxes of 64 columns x box_rows rows of
+// one head (zeros past row L), 128-byte swizzle.
 // Maps are kept in a small per-process cache keyed by (device, base, rows,
 // D, box_rows, type), so repeated calls on the same tensors do no driver call.
-bool make_bw_map(CUtensorMap* m, const void* base, uint64_t rows, int D, int box_rows, bool bf16);
+bool make_bw_map(CUtensorMap* m, const void* base, uint64_t heads, uint64_t L, int D, int box_rows, bool bf16);
 
 }  // namespace stof

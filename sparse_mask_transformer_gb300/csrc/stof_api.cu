@@ -89,6 +89,7 @@ static stof_status encode_impl(const uint8_t* mask, int bits, const RuleSet* rul
   if (n_masks < 1 || lq < 1 || lk < 1 || bm < 1 || bn < 1) return STOF_ERR_INVALID_ARG;
   EncodeGeom g;
   if (!encode_geometry(n_masks, lq, lk, bm, bn, &g)) return STOF_ERR_SHAPE;
+  if (bits && (lq % bm || lk % bn)) return STOF_ERR_SHAPE;  // the bit-packed encoder takes whole OTs only
   if ((mask && !aligned(mask, 8)) || !aligned(workspace, 256)) return STOF_ERR_ALIGNMENT;
   const WorkspaceLayout w = workspace_layout(g);
   if (ws_bytes < w.total) return STOF_ERR_WORKSPACE;
@@ -356,8 +357,9 @@ static stof_status check_format(const stof_format* fmt, int B, int H, int L, int
   if (B < 1 || H < 1 || L < 1 || d < 1) return STOF_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return STOF_ERR_UNSUPPORTED;
   if (fmt->lq != L || fmt->lk != L) return STOF_ERR_SHAPE;
+  // L need not be a whole number of OTs: the last OT row and column are padded
   if (fmt->bm < 8 || fmt->bn < 8 || fmt->bm % 8 || fmt->bn % 8 || fmt->bm > 256 || fmt->bn > 256 ||
-      L % fmt->bm || L % fmt->bn || fmt->n_tr != L / fmt->bm || fmt->n_tc != L / fmt->bn)
+      fmt->n_tr != (L + fmt->bm - 1) / fmt->bm || fmt->n_tc != (L + fmt->bn - 1) / fmt->bn)
     return STOF_ERR_SHAPE;
   return STOF_OK;
 }

@@ -58,7 +58,7 @@ def test_workspace_bytes(lib):
     tiles = 32 * 128 * 128
     assert tiles * (2048 + 8 + 1) <= n <= tiles * (2048 + 8 + 1) + (1 << 20)
     assert ws(1, 256, 256, 16, 16) > 0
-    assert ws(1, 250, 256, 16, 16) == 0      # lq not a multiple of bm
+    assert ws(1, 250, 256, 16, 16) == ws(1, 256, 256, 16, 16)  # a side not a whole number of OTs is padded
     assert ws(1, 256, 256, 12, 16) == 0      # bm not a multiple of 8
     assert ws(1, 512, 512, 512, 128) == 0    # bm above 256
     assert ws(0, 256, 256, 16, 16) == 0
@@ -98,7 +98,7 @@ def test_encode_rejects_bad_arguments(lib):
     assert _encode(lib, mask=None) == stof.STOF_ERR_INVALID_ARG
     assert _encode(lib, ws=None) == stof.STOF_ERR_INVALID_ARG
     assert _encode(lib, n_masks=0) == stof.STOF_ERR_INVALID_ARG
-    assert _encode(lib, lq=200) == stof.STOF_ERR_SHAPE
+    assert _encode(lib, lk=0) == stof.STOF_ERR_INVALID_ARG
     assert _encode(lib, bm=12) == stof.STOF_ERR_SHAPE
     assert _encode(lib, bn=512) == stof.STOF_ERR_SHAPE
     assert _encode(lib, mask=FAKE + 4) == stof.STOF_ERR_ALIGNMENT
@@ -197,7 +197,8 @@ def test_tune_cache_host_side(lib):
     assert stof.stof_tune_lookup(16384, 128, 0.05) is None
     assert stof.stof_tune_workspace_bytes(32, 16384) == max(
         stof.stof_encode_workspace_bytes(32, 16384, 16384, 128, bn) for bn in (64, 128))
-    assert stof.stof_tune_workspace_bytes(1, 100) == 0
+    assert stof.stof_tune_workspace_bytes(1, 100) == stof.stof_tune_workspace_bytes(1, 128)  # padded to a tile
+    assert stof.stof_tune_workspace_bytes(0, 128) == 0
 
 
 def test_tune_rejects_bad_arguments(lib):
@@ -237,7 +238,8 @@ def test_encode_rules_rejects_bad_arguments(lib):
     assert call(one, n=0) == stof.STOF_ERR_INVALID_ARG
     many = (stof.stof_mask_rule * 65)()
     assert call(many, n=65) == stof.STOF_ERR_UNSUPPORTED
-    assert call(one, lq=250) == stof.STOF_ERR_SHAPE
+    blocks_ragged = (stof.stof_mask_rule * 1)(stof.stof_mask_rule(1, 0, None, None, 256, 8))
+    assert call(blocks_ragged, lq=250) == stof.STOF_ERR_SHAPE         # a block pattern needs whole blocks
     bad_block = (stof.stof_mask_rule * 1)(stof.stof_mask_rule(1, 0, None, None, 256, 12))
     assert call(bad_block) == stof.STOF_ERR_SHAPE                     # block not a multiple of 8
     bad_block[0].block = 96

@@ -429,3 +429,22 @@ def test_rule_mask_rows_are_rows_of_the_whole_mask():
              blocks=rng.random((L // 8, L // 8)) < 0.2, block=8)
     rows = np.array([0, 7, 8, 50, 95])
     assert np.array_equal(oracle.rule_mask(L, L, rows=rows, **r), oracle.rule_mask(L, L, **r)[rows])
+
+
+@pytest.mark.parametrize("lq,lk,bm,bn", [(250, 256, 128, 128), (77, 130, 16, 24), (1, 1, 8, 8), (129, 200, 64, 128)])
+def test_padded_sides_closed_forms(lq, lk, bm, bn):
+    """A side that is not a whole number of OTs is read as padded with invalid
+    elements: an all-valid lq x lk mask then has floor(lq/bm) * floor(lk/bn)
+    full OTs, every other OT of the ceil(lq/bm) x ceil(lk/bn) grid partial,
+    and lq * lk valid elements; decoding gives the mask back."""
+    mask = np.ones((1, lq, lk), np.uint8)
+    f = oracle.encode(mask, bm, bn)
+    n_tr, n_tc = -(-lq // bm), -(-lk // bn)
+    assert (f["n_tr"], f["n_tc"], f["lq"], f["lk"]) == (n_tr, n_tc, lq, lk)
+    assert f["n_full"] == (lq // bm) * (lk // bn)
+    assert f["n_part"] == n_tr * n_tc - f["n_full"]
+    assert f["nnz"] == lq * lk
+    assert np.array_equal(oracle.decode(f), mask)
+    rng = np.random.default_rng(lq + lk)
+    m2 = (rng.random((2, lq, lk)) < 0.3).astype(np.uint8)
+    assert np.array_equal(oracle.decode(oracle.encode(m2, bm, bn)), m2)
