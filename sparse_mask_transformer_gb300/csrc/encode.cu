@@ -287,8 +287,7 @@ __device__ __forceinline__ void finish_chunk(const EncodeParams& p, long long ch
 }
 
 // n bytes (n <= VEC; none if n <= 0) from src into the low bytes of a uint4,
-// the rest 0: the part of an 8-row band's unit that lies inside the mask at
-// its lower and right edges, or anywhere when rows are not VEC-aligned.
+// the rest 0: the part of an IT row that lies inside the mask.
 template <int VEC>
 __device__ __forceinline__ uint4 load_partial(const uint8_t* src, int n) {
   uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -323,7 +322,11 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
 
   // 1. read and pack (each unit = VEC/8 adjacent IT words of one 8-row band)
   unsigned long long local_nnz = 0;
-  {
+  // a chunk wholly inside the mask, with VEC-aligned rows: vector loads;
+  // else (a chunk at the lower or right edge of a padded side, or rows not
+  // aligned) byte-guarded loads, one IT word per unit
+  const bool interior = ALIGNED && (g.I + 1) * p.bm <= p.lq && (g.J0 + g.nt) * p.bn <= p.lk;
+  if (interior) {
   constexpr int WPU = VEC / 8;                 // IT words per unit
   constexpr int kUnroll = VEC == 16 ? 1 : 2;   // units in flight per thread (128 B)
   const int upr = g.itcols / WPU;              // units per band
@@ -336,23 +339,14 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
       if (w < nunits) {
         const int pb = w / upr, qu = w - pb * upr;
         const uint8_t* src = base + static_cast<long long>(8 * pb) * p.lk + VEC * qu;
-        // rows and columns of the unit inside the mask (all but at its edges)
-        const int rows_in = min(8, p.lq - (g.I * p.bm + 8 * pb));
-        const int cols_in = min(VEC, p.lk - (g.J0 * p.bn + VEC * qu));
-        if (ALIGNED && rows_in == 8 && cols_in == VEC) {
 #pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            if constexpr (VEC == 16) {
-              v[u][r] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * p.lk));
-            } else {
-              const uint2 x = __ldcs(reinterpret_cast<const uint2*>(src + static_cast<long long>(r) * p.lk));
-              v[u][r] = make_uint4(x.x, x.y, 0u, 0u);
-            }
+        for (int r = 0; r < 8; ++r) {
+          if constexpr (VEC == 16) {
+            v[u][r] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * p.lk));
+          } else {
+            const uint2 x = __ldcs(reinterpret_cast<const uint2*>(src + static_cast<long long>(r) * p.lk));
+            v[u][r] = make_uint4(x.x, x.y, 0u, 0u);
           }
-        } else {
-#pragma unroll
-          for (int r = 0; r < 8; ++r)
-            v[u][r] = load_partial<VEC>(src + static_cast<long long>(r) * p.lk, r < rows_in ? cols_in : 0);
         }
       }
     }
@@ -376,6 +370,21 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
       }
     }
   }
+  } else {
+    const int nunits = g.bands * g.itcols;
+    for (int w = tid; w < nunits; w += kThreads) {
+      const int pb = w / g.itcols, qc = w - pb * g.itcols;
+      const uint8_t* src = base + static_cast<long long>(8 * pb) * p.lk + 8 * qc;
+      const int rows_in = min(8, p.lq - (g.I * p.bm + 8 * pb));
+      const int cols_in = min(8, p.lk - (g.J0 * p.bn + 8 * qc));
+      uint64_t word = 0;
+      for (int r = 0; r < rows_in; ++r) {
+        const uint4 x = load_partial<8>(src + static_cast<long long>(r) * p.lk, cols_in);
+        word |= static_cast<uint64_t>(pack_word4(x.x) | (pack_word4(x.y) << 4)) << (8 * r);
+      }
+      s_words[pb * g.itcols + qc] = word;
+      local_nnz += __popcll(word);
+    }
   }
   finish_chunk(p, chunk, g, cs, s_words, local_nnz, tid);
 }
