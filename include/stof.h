@@ -149,9 +149,9 @@ stof_status stof_encode_mask(const uint8_t* mask, int n_masks, int lq, int lk, i
  * identical.  The pages note that STOF keeps working at
  * sequence lengths where other systems run out of memory (scifaro.com
  * summary, Results, scalability up to 16k); a 16384-long dense mask per
- * head is 256 MB, its bit-packed form 32 MB.  Same workspace, alignment
- * (8 bytes) and errors as stof_encode_mask(), but lq and lk must be
- * multiples of bm and bn (STOF_ERR_SHAPE otherwise).
+ * head is 256 MB, its bit-packed form 32 MB.  Same sizes (sides that are
+ * not whole OTs padded), workspace, alignment (8 bytes) and errors as
+ * stof_encode_mask(); lk must be a multiple of 8 (STOF_ERR_SHAPE otherwise).
  */
 stof_status stof_encode_mask_bits(const uint8_t* mask_bits, int n_masks, int lq, int lk, int bm, int bn,
                                   void* workspace, size_t ws_bytes, stof_format* fmt, void* stream);

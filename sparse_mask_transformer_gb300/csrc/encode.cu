@@ -481,11 +481,25 @@ __global__ void __launch_bounds__(kThreads) bits_classify_kernel(const EncodePar
   const int tb = p.bn >> 3;  // bytes of one OT row
   uint32_t any = 0, all = ~0u;
   unsigned long long nnz = 0;
-  if (J < p.n_tc) {
+  // an OT reaching past a padded side: only its rows < lq and bytes < lk / 8
+  // are read, and it is never full
+  const bool edge_c = (J + 1) * tb > row_bytes;
+  const int rows = min(p.bm, p.lq - I * p.bm);
+  if (J < p.n_tc && edge_c) {
+    const uint8_t* base =
+        p.mask + (static_cast<long long>(m) * p.lq + static_cast<long long>(I) * p.bm) * row_bytes + static_cast<long long>(J) * tb;
+    const int bytes = static_cast<int>(row_bytes - static_cast<long long>(J) * tb);
+    for (int r = warp; r < rows; r += kThreads / 32)
+      for (int x = 0; x < bytes; ++x) {
+        const uint32_t t = __ldcs(base + r * row_bytes + x);
+        any |= t;
+        nnz += __popc(t);
+      }
+  } else if (J < p.n_tc) {
     const uint8_t* base =
         p.mask + (static_cast<long long>(m) * p.lq + static_cast<long long>(I) * p.bm) * row_bytes + static_cast<long long>(J) * tb;
 #pragma unroll 4
-    for (int r = warp; r < p.bm; r += kThreads / 32) {
+    for (int r = warp; r < rows; r += kThreads / 32) {
       const uint8_t* src = base + r * row_bytes;
       for (int x = 0; x < tb; x += VEC) {
         if constexpr (VEC == 16) {
@@ -507,6 +521,7 @@ __global__ void __launch_bounds__(kThreads) bits_classify_kernel(const EncodePar
       }
     }
   }
+  if (edge_c || rows < p.bm) all = 0;
   s_any[warp][lane] = any;
   s_all[warp][lane] = all;
 #pragma unroll
@@ -651,7 +666,21 @@ __global__ void __launch_bounds__(kThreads) bits_fill_kernel(const EncodeParams 
     const int k = u / (bands * upr), rest = u - k * (bands * upr);
     const int pb = rest / upr, qu = rest - pb * upr;
     const uint8_t* src = band0 + static_cast<long long>(8 * pb) * row_bytes + static_cast<long long>(s_plist[k]) * tb + VEC * qu;
-    pack_bits_unit<VEC>(src, row_bytes, p.bitmaps + s_slot[k] * wpt + pb * tb + qu * VEC);
+    uint64_t* dst = p.bitmaps + s_slot[k] * wpt + pb * tb + qu * VEC;
+    // rows and bytes of the unit inside the mask (fewer at the edge of a padded side)
+    const int rows_in = min(8, p.lq - (I * p.bm + 8 * pb));
+    const long long bytes_left = row_bytes - (static_cast<long long>(s_plist[k]) * tb + VEC * qu);
+    const int bytes_in = bytes_left < VEC ? static_cast<int>(bytes_left) : VEC;
+    if (rows_in == 8 && bytes_in == VEC) {
+      pack_bits_unit<VEC>(src, row_bytes, dst);
+    } else {
+      for (int c = 0; c < VEC; ++c) {
+        uint64_t word = 0;
+        if (c < bytes_in)
+          for (int r = 0; r < rows_in; ++r) word |= static_cast<uint64_t>(src[r * row_bytes + c]) << (8 * r);
+        dst[c] = word;
+      }
+    }
   }
 }
 

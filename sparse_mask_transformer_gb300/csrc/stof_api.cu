@@ -89,7 +89,7 @@ static stof_status encode_impl(const uint8_t* mask, int bits, const RuleSet* rul
   if (n_masks < 1 || lq < 1 || lk < 1 || bm < 1 || bn < 1) return STOF_ERR_INVALID_ARG;
   EncodeGeom g;
   if (!encode_geometry(n_masks, lq, lk, bm, bn, &g)) return STOF_ERR_SHAPE;
-  if (bits && (lq % bm || lk % bn)) return STOF_ERR_SHAPE;  // the bit-packed encoder takes whole OTs only
+  if (bits && lk % 8) return STOF_ERR_SHAPE;  // a bit-packed row is lk / 8 whole bytes
   if ((mask && !aligned(mask, 8)) || !aligned(workspace, 256)) return STOF_ERR_ALIGNMENT;
   const WorkspaceLayout w = workspace_layout(g);
   if (ws_bytes < w.total) return STOF_ERR_WORKSPACE;

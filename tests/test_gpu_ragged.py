@@ -67,11 +67,28 @@ def test_rule_encoder_pads_to_whole_tiles(gpu_lib, lq, lk):
     assert_format_equal(fmt, arrs, want)
 
 
-def test_bit_packed_encoder_takes_whole_tiles_only(gpu_lib):
-    bits = torch.zeros(1, 250, 32, dtype=torch.uint8, device="cuda")
-    ws = torch.empty(stof.stof_encode_workspace_bytes(1, 250, 256, 128, 128), dtype=torch.uint8, device="cuda")
+@pytest.mark.parametrize("lq,lk", [(250, 256), (1000, 1000), (77, 136), (1, 8), (129, 2056)])
+@pytest.mark.parametrize("bm,bn", [(128, 128), (64, 128), (16, 16)])
+def test_bit_packed_encoder_pads_to_whole_tiles(gpu_lib, lq, lk, bm, bn):
+    """The bit-packed encoder on sides that are not whole OTs (lk a multiple
+    of 8, so a row is lk / 8 whole bytes): the same format as the oracle's
+    encoding of the padded dense mask."""
+    rng = np.random.default_rng(lq + lk + bm)
+    masks = (rng.random((2, lq, lk)) < 0.4).astype(np.uint8)
+    masks[0] = 1
+    bits = torch.from_numpy(np.packbits(masks, axis=2, bitorder="little")).cuda()
+    ws = torch.empty(stof.stof_encode_workspace_bytes(2, lq, lk, bm, bn), dtype=torch.uint8, device="cuda")
+    fmt = stof.stof_encode_mask_bits(bits, lk, bm, bn, ws)
+    stof.stof_format_sync(fmt)
+    arrs = {k: v.cpu().numpy() for k, v in stof.format_arrays(fmt, ws).items()}
+    arrs["bitmaps"] = arrs["bitmaps"].view("uint64")
+    assert_format_equal(fmt, arrs, oracle.encode(masks, bm, bn))
+
+
+def test_bit_packed_rows_must_be_whole_bytes(gpu_lib):
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
     with pytest.raises(stof.StofError) as e:
-        stof.stof_encode_mask_bits(bits, 256, 128, 128, ws)
+        stof.stof_encode_mask_bits(torch.zeros(1, 64, 9, dtype=torch.uint8, device="cuda"), 77, 16, 16, ws)
     assert e.value.status == stof.STOF_ERR_SHAPE
 
 
