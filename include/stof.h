@@ -422,8 +422,8 @@ int stof_tune_density_bucket(double density);
  *   device_error  device int64 word that a pipeline timeout ORs
  *             STOF_DEVERR_PIPE_TIMEOUT into, or NULL.
  * fp32 accumulation; bias and residual are added in fp32 and y is rounded
- * once to nearest even.  Requires d = 64 or 128, L % 128 == 0,
- * N % 256 == 0 and 16-byte aligned pointers.  Asynchronous on stream.
+ * once to nearest even.  Requires d = 64 or 128, N % 256 == 0 and 16-byte
+ * aligned pointers; any L.  Asynchronous on stream.
  */
 stof_status stof_oproj_fwd(const void* o, const void* w, const void* bias, const void* residual,
                            stof_dtype dt, int B, int H, int L, int d, int N, void* y,

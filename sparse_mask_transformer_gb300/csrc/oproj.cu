@@ -83,6 +83,7 @@ struct OpParams {
   int64_t* err;          // device error word or null
   int B, H, L, d, N;
   int m_tiles, n_tiles, k_blocks;
+  int m_per_b;           // token tiles per batch element: ceil(L / 128)
 };
 
 struct LnParams {
@@ -159,8 +160,8 @@ __global__ void __launch_bounds__(kThreadsOP, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x) {
         const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
-        const int tok0 = mt * kTM;                      // token index b * L + l
-        const int b = tok0 / p.L, l0 = tok0 - b * p.L;  // a tile never straddles a batch (L % 128 == 0)
+        // token tiles are per batch element (the last may run past L: zeros there)
+        const int b = mt / p.m_per_b, l0 = (mt - b * p.m_per_b) * kTM;
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const int st = it % kStages;
           if (it >= kStages && !mbar_wait(&s.empty[st], ((it / kStages) - 1) & 1, abort_flag, kWaitNsOP)) {
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kThreadsOP, 1)
           }
           const int h = kb / kb_per_head, c0 = (kb - h * kb_per_head) * kTK;
           mbar_arrive_expect_tx(&s.full[st], kABytes + kBBytes);
-          tma_load_2d(s.a[st], &tmO, &s.full[st], c0, (b * p.H + h) * p.L + l0);
+          tma_load_3d(s.a[st], &tmO, &s.full[st], c0, l0, b * p.H + h);
           tma_load_2d(s.b[st], &tmW, &s.full[st], kb * kTK, nt * kTN);
           issued = it + 1;
         }
@@ -241,7 +242,9 @@ __global__ void __launch_bounds__(kThreadsOP, 1)
       }
       tc_fence_after();
       const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
-      const long long row = static_cast<long long>(mt) * kTM + r;
+      const int b = mt / p.m_per_b, l = (mt - b * p.m_per_b) * kTM + r;
+      const bool row_in = l < p.L;  // rows past L: computed, not read or stored
+      const long long row = static_cast<long long>(b) * p.L + l;
       const int n0 = nt * kTN;
       float x0 = 0.f, s1 = 0.f, s2 = 0.f;  // LayerNorm statistics of the row's rounded outputs
 #pragma unroll 1
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kThreadsOP, 1)
             }
           }
         }
-        if (res) {
+        if (res && row_in) {
           const uint4* rv = reinterpret_cast<const uint4*>(res + row * p.N + n);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -283,8 +286,10 @@ __global__ void __launch_bounds__(kThreadsOP, 1)
 #pragma unroll
         for (int q = 0; q < 16; ++q) pk[q] = pack2f<BF16>(v[2 * q], v[2 * q + 1]);
         uint4* dst = reinterpret_cast<uint4*>(y + row * p.N + n);
+        if (row_in) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
         if (p.stats) {
           if (cc == 0) x0 = to_f32<BF16>(static_cast<uint16_t>(pk[0] & 0xFFFFu));
 #pragma unroll
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(kThreadsOP, 1)
           }
         }
       }
-      if (p.stats)
+      if (p.stats && row_in)
         p.stats[row * p.n_tiles + nt] = make_float2(x0 + s1 / kTN, s2 - s1 * s1 / kTN);
       tc_fence_before();
       mbar_arrive(&s.acc_empty[a]);
@@ -378,9 +383,11 @@ stof_status launch_op(const void* o, const void* w, const OpParams& p, cudaStrea
   const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const uint64_t K = static_cast<uint64_t>(p.H) * p.d;
   CUtensorMap mo, mw;
-  // O viewed as [B*H*L][d]; W as [N][K]; boxes of 64 columns (one swizzle atom)
-  if (!encode_tensor_map_2d(&mo, dt, o, static_cast<uint64_t>(p.d), static_cast<uint64_t>(p.B) * p.H * p.L,
-                            static_cast<uint64_t>(p.d) * 2, kTK, kTM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  // O viewed as [B*H][L][d] (a token tile past L reads zeros); W as [N][K];
+  // boxes of 64 columns (one swizzle atom)
+  if (!encode_tensor_map_3d(&mo, dt, o, static_cast<uint64_t>(p.d), static_cast<uint64_t>(p.L),
+                            static_cast<uint64_t>(p.B) * p.H, static_cast<uint64_t>(p.d) * 2,
+                            static_cast<uint64_t>(p.L) * p.d * 2, kTK, kTM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_2d(&mw, dt, w, K, static_cast<uint64_t>(p.N), K * 2, kTK, kTN,
                             CU_TENSOR_MAP_SWIZZLE_128B))
     return STOF_ERR_CUDA;
@@ -410,7 +417,7 @@ stof_status check_op(const void* o, const void* w, const void* bias, const void*
   if (dt != STOF_F16 && dt != STOF_BF16) return STOF_ERR_DTYPE;
   if (B < 1 || H < 1 || L < 1 || d < 1 || N < 1) return STOF_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return STOF_ERR_UNSUPPORTED;
-  if (L % kTM || N % kTN) return STOF_ERR_SHAPE;
+  if (N % kTN) return STOF_ERR_SHAPE;  // any L: the last token tile of a batch element may run past it
   if (static_cast<long long>(B) * H * L >= (1ll << 31) || static_cast<long long>(B) * L * N >= (1ll << 40) ||
       static_cast<long long>(H) * d > (1 << 20))
     return STOF_ERR_SHAPE;
@@ -427,7 +434,8 @@ stof_status check_op(const void* o, const void* w, const void* bias, const void*
   p->L = L;
   p->d = d;
   p->N = N;
-  p->m_tiles = B * L / kTM;
+  p->m_per_b = (L + kTM - 1) / kTM;
+  p->m_tiles = B * p->m_per_b;
   p->n_tiles = N / kTN;
   p->k_blocks = H * d / kTK;
   return STOF_OK;

@@ -182,7 +182,7 @@ def test_oproj_rejects_bad_arguments(lib):
     assert f(None, one, None, None, 0, 1, 2, 128, 64, 256, one, None, None) == stof.STOF_ERR_INVALID_ARG
     assert f(one, one, None, None, 7, 1, 2, 128, 64, 256, one, None, None) == stof.STOF_ERR_DTYPE
     assert f(one, one, None, None, 0, 1, 2, 128, 96, 256, one, None, None) == stof.STOF_ERR_UNSUPPORTED
-    assert f(one, one, None, None, 0, 1, 2, 100, 64, 256, one, None, None) == stof.STOF_ERR_SHAPE
+    assert f(one, one, None, None, 0, 1, 2, 0, 64, 256, one, None, None) == stof.STOF_ERR_INVALID_ARG
     assert f(one, one, None, None, 0, 1, 2, 128, 64, 200, one, None, None) == stof.STOF_ERR_SHAPE
     assert f(ctypes.c_void_p(8), one, None, None, 0, 1, 2, 128, 64, 256, one, None,
              None) == stof.STOF_ERR_ALIGNMENT
