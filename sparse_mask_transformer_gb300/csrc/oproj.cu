@@ -15,8 +15,8 @@
 // GB300 design: a persistent kernel, one CTA per SM, 192 threads:
 //   warp 0      TMA producer: for every (128-token, 256-feature) output
 //               tile and every 64-wide slice of the reduction, the O slice
-//               (128 tokens of one head, 64 of its d columns: rows of O
-//               viewed as [B*H*L][d]) and the W slice (256 rows x 64) into a
+//               (128 tokens of one head, 64 of its d columns, O viewed as
+//               [B*H][L][d]: zeros past L) and the W slice (256 rows x 64) into a
 //               four-stage ring;
 //   warp 1      allocates TMEM and issues the tcgen05 MMAs (M = 128,
 //               N = 256, K = 16; both operands K-major, 128-byte swizzle)

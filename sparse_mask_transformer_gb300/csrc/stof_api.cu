@@ -63,7 +63,7 @@ const char* stof_status_string(stof_status s) {
   switch (s) {
     case STOF_OK: return "ok";
     case STOF_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or bad enum)";
-    case STOF_ERR_SHAPE: return "bad shape (inconsistent sizes, not tile-divisible, or too large)";
+    case STOF_ERR_SHAPE: return "bad shape (inconsistent sizes, not tile-divisible where required, or too large)";
     case STOF_ERR_DTYPE: return "unknown element type";
     case STOF_ERR_ALIGNMENT: return "pointer not aligned as required";
     case STOF_ERR_WORKSPACE: return "workspace too small";
