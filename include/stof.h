@@ -291,6 +291,19 @@ stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype
                          int64_t mask_stride_b, int64_t mask_stride_h, stof_kernel which, void* o,
                          void* stream);
 
+/*
+ * stof_mha_fwd() with Lq query rows and Lk keys per head (attention of one
+ * sequence over another, e.g. a decoder over an encoder's output):
+ *   q, o      device [B][H][Lq][d];  k, v  device [B][H][Lk][d].
+ *   fmt       encodes masks of Lq rows and Lk columns (fmt->lq == Lq,
+ *             fmt->lk == Lk); the masks, kernels and errors are those of
+ *             stof_mha_fwd(), which is this call with Lq = Lk = L.  AUTO
+ *             uses a stof_tune() result only when Lq == Lk.
+ */
+stof_status stof_mha_fwd_cross(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int Lq,
+                               int Lk, int d, float scale, const stof_format* fmt, int64_t mask_stride_b,
+                               int64_t mask_stride_h, stof_kernel which, void* o, void* stream);
+
 /* Where a plan's choice came from. */
 #define STOF_PLAN_FORCED 0    /* the caller named the kernel */
 #define STOF_PLAN_ANALYTIC 1  /* stof_select_kernel() on the format's density [SEL] */

@@ -513,8 +513,8 @@ template <int D, int BN, bool BF16, int ST, bool NEG, bool ESPLIT>
 stof_status launch_bw(const AttnParams& p, cudaStream_t s) {
   const uint64_t heads = static_cast<uint64_t>(p.B) * p.H;
   CUtensorMap mq, mk, mv;
-  if (!make_bw_map(&mq, p.q, heads, p.L, D, kBM, BF16) || !make_bw_map(&mk, p.k, heads, p.L, D, BN, BF16) ||
-      !make_bw_map(&mv, p.v, heads, p.L, D, BN, BF16))
+  if (!make_bw_map(&mq, p.q, heads, p.L, D, kBM, BF16) || !make_bw_map(&mk, p.k, heads, p.Lk, D, BN, BF16) ||
+      !make_bw_map(&mv, p.v, heads, p.Lk, D, BN, BF16))
     return STOF_ERR_CUDA;
   const size_t smem = sizeof(Smem<D, BN, ST>) + 1024;
   stof_status prep = STOF_OK;
@@ -563,7 +563,7 @@ __global__ void ex2_fma_kernel(const float* x, float* y, long long n) {
 
 stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s) {
   if (p.bm != kBM || (p.bn != 64 && p.bn != 128)) return STOF_ERR_UNSUPPORTED;
-  if (static_cast<long long>(p.B) * p.H * p.L >= (1ll << 31)) return STOF_ERR_SHAPE;
+  if (static_cast<long long>(p.B) * p.H * (p.L > p.Lk ? p.L : p.Lk) >= (1ll << 31)) return STOF_ERR_SHAPE;
   // d = 64 with short query tiles (few listed OTs each): persistent CTAs that
   // overlap one query tile's start-up and finish with the next
   if (blockwise_persistent(p.d, p.variant, p.tiles_per_row)) return launch_blockwise_persist64(p, bf16, s);

@@ -724,8 +724,8 @@ template <int BN, bool BF16, int RING, bool NEG, bool ESPLIT, int SWG>
 stof_status launch_persist(const AttnParams& p, cudaStream_t s) {
   const uint64_t heads = static_cast<uint64_t>(p.B) * p.H;
   CUtensorMap mq, mk, mv;
-  if (!make_bw_map(&mq, p.q, heads, p.L, kD, kBM, BF16) || !make_bw_map(&mk, p.k, heads, p.L, kD, BN, BF16) ||
-      !make_bw_map(&mv, p.v, heads, p.L, kD, BN, BF16))
+  if (!make_bw_map(&mq, p.q, heads, p.L, kD, kBM, BF16) || !make_bw_map(&mk, p.k, heads, p.Lk, kD, BN, BF16) ||
+      !make_bw_map(&mv, p.v, heads, p.Lk, kD, BN, BF16))
     return STOF_ERR_CUDA;
   const size_t smem = sizeof(PSmem<BN, RING>) + 1024;
   stof_status prep = STOF_OK;

@@ -93,7 +93,8 @@ struct AttnParams {
   const void* k;
   const void* v;
   void* o;
-  int B, H, L, d;
+  int B, H, L, d;                 // L: query rows per head
+  int Lk;                          // keys per head (L for self-attention)
   float scale_log2;                // scale * log2(e)
   int bm, bn, n_tr, n_tc;
   int64_t stride_b, stride_h;
@@ -167,8 +168,8 @@ extern const KernelChoice kTuneCandidates[STOF_TUNE_CANDIDATES];
 // OTs of width bn; false if the cache has no such entry.
 bool tuned_choice(int L, int d, double density, int bn, KernelChoice* out);
 // stof_mha_fwd() with the kernel, ring depth and variant given.
-stof_status mha_fwd_choice(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int L, int d,
-                           float scale, const stof_format* fmt, int64_t mask_stride_b, int64_t mask_stride_h,
+stof_status mha_fwd_choice(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int L, int Lk,
+                           int d, float scale, const stof_format* fmt, int64_t mask_stride_b, int64_t mask_stride_h,
                            const KernelChoice& c, void* o, void* stream);
 cudaError_t launch_rowwise(const AttnParams& p, bool bf16, cudaStream_t s);
 // Density bucket of the tuning cache.

@@ -140,8 +140,8 @@ __global__ void __launch_bounds__(kWarps * 32, 5) rowwise_kernel(const AttnParam
   const int g = sl / G;            // key group
   const int sub = sl % G;          // 16-dim slice
   const size_t row_bytes = static_cast<size_t>(D) * 2;
-  const uint8_t* kbase = static_cast<const uint8_t*>(p.k) + bh * p.L * row_bytes + sub * 32;
-  const uint8_t* vbase = static_cast<const uint8_t*>(p.v) + bh * p.L * row_bytes + sub * 32;
+  const uint8_t* kbase = static_cast<const uint8_t*>(p.k) + bh * p.Lk * row_bytes + sub * 32;
+  const uint8_t* vbase = static_cast<const uint8_t*>(p.v) + bh * p.Lk * row_bytes + sub * 32;
 
   float qf[16];
   widen16<BF16>(load_raw16(static_cast<const uint8_t*>(p.q) + row * row_bytes + sub * 32), qf);

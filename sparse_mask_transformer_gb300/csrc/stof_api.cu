@@ -349,43 +349,44 @@ static float tiles_per_row(const stof_format& f) {
 }
 
 // The format and sizes agree (what a plan needs to know of a call).
-static stof_status check_format(const stof_format* fmt, int B, int H, int L, int d) {
+// L query rows, Lk keys per head (Lk = L for self-attention).
+static stof_status check_format(const stof_format* fmt, int B, int H, int L, int Lk, int d) {
   if (!fmt) return STOF_ERR_INVALID_ARG;
   if (!fmt->full_row_ptr || !fmt->full_col_idx || !fmt->part_row_ptr || !fmt->part_col_idx ||
       !fmt->bitmaps || !fmt->counts_dev)
     return STOF_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || L < 1 || d < 1) return STOF_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || L < 1 || Lk < 1 || d < 1) return STOF_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return STOF_ERR_UNSUPPORTED;
-  if (fmt->lq != L || fmt->lk != L) return STOF_ERR_SHAPE;
-  // L need not be a whole number of OTs: the last OT row and column are padded
+  if (fmt->lq != L || fmt->lk != Lk) return STOF_ERR_SHAPE;
+  // the lengths need not be whole numbers of OTs: the last OT row and column are padded
   if (fmt->bm < 8 || fmt->bn < 8 || fmt->bm % 8 || fmt->bn % 8 || fmt->bm > 256 || fmt->bn > 256 ||
-      fmt->n_tr != (L + fmt->bm - 1) / fmt->bm || fmt->n_tc != (L + fmt->bn - 1) / fmt->bn)
+      fmt->n_tr != (L + fmt->bm - 1) / fmt->bm || fmt->n_tc != (Lk + fmt->bn - 1) / fmt->bn)
     return STOF_ERR_SHAPE;
   return STOF_OK;
 }
 
 // Every argument of an MHA call.
 static stof_status check_call(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int L,
-                              int d, float scale, const stof_format* fmt, int64_t mask_stride_b,
+                              int Lk, int d, float scale, const stof_format* fmt, int64_t mask_stride_b,
                               int64_t mask_stride_h, void* o) {
   if (!q || !k || !v || !o || !fmt) return STOF_ERR_INVALID_ARG;
   if (dt != STOF_F16 && dt != STOF_BF16) return STOF_ERR_DTYPE;
   if (!std::isfinite(scale)) return STOF_ERR_INVALID_ARG;
   if (mask_stride_b < 0 || mask_stride_h < 0) return STOF_ERR_INVALID_ARG;
-  const stof_status st = check_format(fmt, B, H, L, d);
+  const stof_status st = check_format(fmt, B, H, L, Lk, d);
   if (st != STOF_OK) return st;
   const long double max_mask = static_cast<long double>(B - 1) * mask_stride_b +
                                static_cast<long double>(H - 1) * mask_stride_h;
   if (max_mask >= fmt->n_masks) return STOF_ERR_SHAPE;
-  if (static_cast<long double>(B) * H * L >= 2147483647.0L * 8) return STOF_ERR_SHAPE;
+  if (static_cast<long double>(B) * H * (L > Lk ? L : Lk) >= 2147483647.0L * 8) return STOF_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return STOF_ERR_ALIGNMENT;
   return STOF_OK;
 }
 
 // What runs for `which` on this format: a forced kernel, a cached tuning
 // result or the analytic model.
-static stof_status plan_call(const stof_format& f, int B, int H, int L, int d, stof_kernel which, KernelChoice* c,
-                             int* source) {
+static stof_status plan_call(const stof_format& f, int B, int H, int L, int Lk, int d, stof_kernel which,
+                             KernelChoice* c, int* source) {
   if (which != STOF_KERNEL_AUTO && which != STOF_KERNEL_ROWWISE && which != STOF_KERNEL_BLOCKWISE)
     return STOF_ERR_INVALID_ARG;
   *c = KernelChoice{which, f.bn, 0, kVariantAuto, 0, 0, 0};
@@ -395,12 +396,16 @@ static stof_status plan_call(const stof_format& f, int B, int H, int L, int d, s
     const double density = static_cast<double>(f.nnz) / (static_cast<double>(f.n_masks) * f.lq * f.lk);
     // a cached measurement counts only if its kernel runs on this format
     // (the block-wise kernel needs 128-row OTs)
-    if (tuned_choice(L, d, density, f.bn, c) && (c->kernel == STOF_KERNEL_ROWWISE || blockwise_tiles(f))) {
+    // (the tuner measures self-attention: its cache applies when Lk = L)
+    if (L == Lk && tuned_choice(L, d, density, f.bn, c) &&
+        (c->kernel == STOF_KERNEL_ROWWISE || blockwise_tiles(f))) {
       *source = STOF_PLAN_TUNED;
     } else {
       *c = KernelChoice{which, f.bn, 0, kVariantAuto, 0, 0, 0};
       *source = STOF_PLAN_ANALYTIC;
-      c->kernel = stof_select_kernel_heads(density, L, d, static_cast<int64_t>(B) * H, listed128_per_row(f));
+      // the model's length: L, or for Lk != L the one with L * L = L * Lk valid-key positions
+      const int len = L == Lk ? L : static_cast<int>(std::lround(std::sqrt(static_cast<double>(L) * Lk)));
+      c->kernel = stof_select_kernel_heads(density, len, d, static_cast<int64_t>(B) * H, listed128_per_row(f));
       if (c->kernel == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(f))
         c->kernel = STOF_KERNEL_ROWWISE;  // the block-wise kernel needs 128 x 64 or 128 x 128 OTs
     }
@@ -411,11 +416,11 @@ static stof_status plan_call(const stof_format& f, int B, int H, int L, int d, s
 
 stof_status stof_mha_plan(const stof_format* fmt, int B, int H, int L, int d, stof_kernel which, stof_plan* out) {
   if (!out) return STOF_ERR_INVALID_ARG;
-  stof_status st = check_format(fmt, B, H, L, d);
+  stof_status st = check_format(fmt, B, H, L, L, d);
   if (st != STOF_OK) return st;
   KernelChoice c;
   int source = 0;
-  st = plan_call(*fmt, B, H, L, d, which, &c, &source);
+  st = plan_call(*fmt, B, H, L, L, d, which, &c, &source);
   if (st != STOF_OK) return st;
   out->kernel = c.kernel;
   out->source = source;
@@ -440,10 +445,11 @@ stof_status stof_mha_plan(const stof_format* fmt, int B, int H, int L, int d, st
 
 namespace stof {
 
-stof_status mha_fwd_choice(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int L, int d,
+stof_status mha_fwd_choice(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int L, int Lk,
+                           int d,
                            float scale, const stof_format* fmt, int64_t mask_stride_b, int64_t mask_stride_h,
                            const KernelChoice& c, void* o, void* stream) {
-  const stof_status st = check_call(q, k, v, dt, B, H, L, d, scale, fmt, mask_stride_b, mask_stride_h, o);
+  const stof_status st = check_call(q, k, v, dt, B, H, L, Lk, d, scale, fmt, mask_stride_b, mask_stride_h, o);
   if (st != STOF_OK) return st;
   if (c.kernel != STOF_KERNEL_ROWWISE && c.kernel != STOF_KERNEL_BLOCKWISE) return STOF_ERR_INVALID_ARG;
   if (c.kernel == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(*fmt)) return STOF_ERR_UNSUPPORTED;
@@ -455,6 +461,7 @@ stof_status mha_fwd_choice(const void* q, const void* k, const void* v, stof_dty
   p.B = B;
   p.H = H;
   p.L = L;
+  p.Lk = Lk;
   p.d = d;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.bm = fmt->bm;
@@ -513,20 +520,26 @@ stof_status stof_mha_fwd_plan(const void* q, const void* k, const void* v, stof_
     if (plan->exp_split != 0 || plan->softmax_warpgroups != 0) return STOF_ERR_UNSUPPORTED;
     c.rows_per_warp = r;
   }
-  return mha_fwd_choice(q, k, v, dt, B, H, L, d, scale, fmt, mask_stride_b, mask_stride_h, c, o, stream);
+  return mha_fwd_choice(q, k, v, dt, B, H, L, L, d, scale, fmt, mask_stride_b, mask_stride_h, c, o, stream);
+}
+
+stof_status stof_mha_fwd_cross(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H, int Lq,
+                               int Lk, int d, float scale, const stof_format* fmt, int64_t mask_stride_b,
+                               int64_t mask_stride_h, stof_kernel which, void* o, void* stream) {
+  stof_status st = check_call(q, k, v, dt, B, H, Lq, Lk, d, scale, fmt, mask_stride_b, mask_stride_h, o);
+  if (st != STOF_OK) return st;
+  KernelChoice c;
+  int source = 0;
+  st = plan_call(*fmt, B, H, Lq, Lk, d, which, &c, &source);
+  if (st != STOF_OK) return st;
+  return mha_fwd_choice(q, k, v, dt, B, H, Lq, Lk, d, scale, fmt, mask_stride_b, mask_stride_h, c, o, stream);
 }
 
 stof_status stof_mha_fwd(const void* q, const void* k, const void* v, stof_dtype dt, int B, int H,
                          int L, int d, float scale, const stof_format* fmt,
                          int64_t mask_stride_b, int64_t mask_stride_h, stof_kernel which, void* o,
                          void* stream) {
-  stof_status st = check_call(q, k, v, dt, B, H, L, d, scale, fmt, mask_stride_b, mask_stride_h, o);
-  if (st != STOF_OK) return st;
-  KernelChoice c;
-  int source = 0;
-  st = plan_call(*fmt, B, H, L, d, which, &c, &source);
-  if (st != STOF_OK) return st;
-  return mha_fwd_choice(q, k, v, dt, B, H, L, d, scale, fmt, mask_stride_b, mask_stride_h, c, o, stream);
+  return stof_mha_fwd_cross(q, k, v, dt, B, H, L, L, d, scale, fmt, mask_stride_b, mask_stride_h, which, o, stream);
 }
 
 }  // extern "C"

@@ -139,7 +139,7 @@ stof_status stof_tune(const uint8_t* mask, int n_masks, const void* q, const voi
       if (cand.kernel == STOF_KERNEL_BLOCKWISE && (cand.variant == kVariantPersistent || cand.stages == 4) &&
           d != 64)
         continue;  // persistent CTAs and a 4-deep ring exist for d = 64 only
-      st = mha_fwd_choice(q, k, v, dt, B, H, L, d, scale, &fmt, mask_stride_b, mask_stride_h, cand, o, stream);
+      st = mha_fwd_choice(q, k, v, dt, B, H, L, L, d, scale, &fmt, mask_stride_b, mask_stride_h, cand, o, stream);
       if (st == STOF_ERR_UNSUPPORTED) {  // not a candidate for these sizes
         st = STOF_OK;
         continue;
@@ -152,7 +152,7 @@ stof_status stof_tune(const uint8_t* mask, int n_masks, const void* q, const voi
       }
       if (record_cuda(cudaEventRecord(ev[0], s)) != cudaSuccess) { st = STOF_ERR_CUDA; break; }
       for (int c = 0; c < kTimedCalls && st == STOF_OK; ++c)
-        st = mha_fwd_choice(q, k, v, dt, B, H, L, d, scale, &fmt, mask_stride_b, mask_stride_h, cand, o, stream);
+        st = mha_fwd_choice(q, k, v, dt, B, H, L, L, d, scale, &fmt, mask_stride_b, mask_stride_h, cand, o, stream);
       if (st != STOF_OK) break;
       float ms = 0.f;
       if (record_cuda(cudaEventRecord(ev[1], s)) != cudaSuccess ||

@@ -44,7 +44,8 @@ EXPORTED = ["stof_encode_workspace_bytes", "stof_encode_mask", "stof_format_sync
             "stof_last_cuda_error", "stof_tune_workspace_bytes", "stof_tune", "stof_tune_lookup",
             "stof_tune_clear", "stof_tune_density_bucket", "stof_encode_mask_bits", "stof_oproj_fwd",
             "stof_encode_rules", "stof_check_bounded_wait", "stof_mha_plan", "stof_mha_fwd_plan",
-            "stof_select_kernel_heads", "stof_oproj_ln_fwd", "stof_oproj_ln_workspace_bytes", "stof_ex2_fma"]
+            "stof_select_kernel_heads", "stof_oproj_ln_fwd", "stof_oproj_ln_workspace_bytes", "stof_ex2_fma",
+            "stof_mha_fwd_cross"]
 
 STOF_MAX_RULES = 64
 INT32_MIN, INT32_MAX = -(1 << 31), (1 << 31) - 1
@@ -141,6 +142,9 @@ def load_library(path: str = LIB_PATH):
         lib.stof_mha_fwd.argtypes = [P, P, P, i32, i32, i32, i32, i32, ctypes.c_float,
                                      ctypes.POINTER(stof_format), i64, i64, i32, P, P]
         lib.stof_mha_fwd.restype = i32
+        lib.stof_mha_fwd_cross.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, ctypes.c_float,
+                                           ctypes.POINTER(stof_format), i64, i64, i32, P, P]
+        lib.stof_mha_fwd_cross.restype = i32
         lib.stof_mha_plan.argtypes = [ctypes.POINTER(stof_format), i32, i32, i32, i32, i32, ctypes.POINTER(stof_plan)]
         lib.stof_mha_plan.restype = i32
         lib.stof_mha_fwd_plan.argtypes = [P, P, P, i32, i32, i32, i32, i32, ctypes.c_float,
@@ -318,6 +322,24 @@ def stof_mha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: stof_fo
         q.data_ptr(), k.data_ptr(), v.data_ptr(), _dtype_code(q), B, H, L, d, float(scale),
         ctypes.byref(fmt), int(mask_stride_b), int(mask_stride_h), int(which), o.data_ptr(),
         _stream(stream)), "stof_mha_fwd")
+    return o
+
+
+def stof_mha_fwd_cross(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: stof_format, scale: float,
+                       mask_stride_b: int, mask_stride_h: int, which: int, o: torch.Tensor,
+                       stream=None) -> torch.Tensor:
+    """q, o: device [B, H, Lq, d]; k, v: device [B, H, Lk, d]; fp16/bf16, contiguous."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise StofError(STOF_ERR_SHAPE, "stof_mha_fwd_cross: q, k must be [B, H, L, d]")
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    if (o.shape != q.shape or k.shape != (B, H, Lk, d) or v.shape != k.shape
+            or any(t.dtype != q.dtype or not t.is_contiguous() for t in (k, v, o)) or not q.is_contiguous()):
+        raise StofError(STOF_ERR_SHAPE, "stof_mha_fwd_cross: q, o [B, H, Lq, d] and k, v [B, H, Lk, d], contiguous")
+    _check(load_library().stof_mha_fwd_cross(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), _dtype_code(q), B, H, Lq, Lk, d, float(scale),
+        ctypes.byref(fmt), int(mask_stride_b), int(mask_stride_h), int(which), o.data_ptr(),
+        _stream(stream)), "stof_mha_fwd_cross")
     return o
 
 
