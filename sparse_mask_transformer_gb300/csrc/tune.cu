@@ -28,16 +28,17 @@
 namespace stof {
 
 const KernelChoice kTuneCandidates[STOF_TUNE_CANDIDATES] = {
-    {STOF_KERNEL_ROWWISE, 128, 0, kVariantAuto, 1},
-    {STOF_KERNEL_ROWWISE, 128, 0, kVariantAuto, 2},
-    {STOF_KERNEL_ROWWISE, 128, 0, kVariantAuto, 4},
-    {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPerTile, 0},
-    {STOF_KERNEL_BLOCKWISE, 128, 2, kVariantPerTile, 0},
-    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPerTile, 0},     // d = 64 only
-    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPersistent, 0},  // d = 64 only
-    {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPersistent, 0},  // d = 64 only
-    {STOF_KERNEL_BLOCKWISE, 128, 2, kVariantPersistent, 0},  // d = 64 only
-    {STOF_KERNEL_BLOCKWISE, 64, 0, kVariantAuto, 0},
+    // kernel, OT width, ring depth, variant, rows per warp, exp split, softmax warpgroups
+    {STOF_KERNEL_ROWWISE, 128, 0, kVariantAuto, 1, 0, 0},
+    {STOF_KERNEL_ROWWISE, 128, 0, kVariantAuto, 2, 0, 0},
+    {STOF_KERNEL_ROWWISE, 128, 0, kVariantAuto, 4, 0, 0},
+    {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPerTile, 0, 0, 0},
+    {STOF_KERNEL_BLOCKWISE, 128, 2, kVariantPerTile, 0, 0, 0},
+    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPerTile, 0, 0, 0},     // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPersistent, 0, 0, 0},  // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPersistent, 0, 0, 0},  // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 128, 2, kVariantPersistent, 0, 0, 0},  // d = 64 only
+    {STOF_KERNEL_BLOCKWISE, 64, 0, kVariantAuto, 0, 0, 0},
     {STOF_KERNEL_BLOCKWISE, 128, 3, kVariantPerTile, 0, 1, 0},     // exp split
     {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPersistent, 0, 1, 0},  // exp split, d = 64 only
     {STOF_KERNEL_BLOCKWISE, 128, 4, kVariantPersistent, 0, 0, 4},  // four softmax warpgroups, d = 64 only
