@@ -68,6 +68,15 @@ def test_noalloc_encoder_matches_regular_encoder_two_calls_in_a_row(gpu_lib):
             _assert_same(fmt, got, ref_fmt, ref)
 
 
+def test_noalloc_encoder_on_sides_that_are_not_whole_tiles(gpu_lib):
+    """A 1000 x 777 mask (edge chunks with byte-guarded loads, rows not
+    8-byte aligned) gives the regular encoder's format."""
+    mask = torch.from_numpy(synth.random_mask(2, 1000, 777, 0.2, seed=21)).cuda()
+    ref_fmt, _, ref = gpu_encode(mask, 128, 128)
+    fmt, got = _encode_noalloc(mask, 128, 128)
+    _assert_same(fmt, got, ref_fmt, ref)
+
+
 def test_noalloc_encoder_rejects_sizes_beyond_its_scratch(gpu_lib):
     # 5 masks of 65536^2 at 128x128 need 5 * 512 * 64 = 163840 chunks > 131072;
     # rejected on the host before any device access (the pointers are never used)
