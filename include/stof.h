@@ -28,7 +28,8 @@
  *
  * Conventions of this library (the pages leave them open):
  *   - Q, K, V, O are [B][H][L][d] row-major, contiguous, fp16 or bf16,
- *     16-byte aligned device memory.  d is 64 or 128.
+ *     16-byte aligned device memory.  d is 32, 64, 128 or 256 (the
+ *     block-wise kernels take 64 and 128).
  *   - A mask is uint8 [n_masks][L][L] (query row i, key column j); an
  *     element is valid iff its byte is non-zero.  Head (b, h) uses mask
  *     number b * mask_stride_b + h * mask_stride_h.
@@ -264,7 +265,11 @@ stof_kernel stof_select_kernel_heads(double density, int seq_len, int head_dim, 
  *   q, k, v, o  device [B][H][L][d], dt, 16-byte aligned; o is written.
  *   L           == fmt->lq == fmt->lk, any length (a last OT row and column
  *               that reach past L are padded: rows past L are computed and
- *               not stored, keys past L are never valid).   d: 64 or 128.
+ *               not stored, keys past L are never valid).
+ *   d           32, 64, 128 or 256; the block-wise kernel takes 64 and 128
+ *               (STOF_ERR_UNSUPPORTED if forced on another), AUTO runs the
+ *               row-wise kernel for 32 and 256 (at most 2 query rows per
+ *               warp at d = 256).
  *   scale       any finite value; the softmax is taken over scale * Q.K
  *               (a negative scale favours the smallest dot products, a zero
  *               scale averages the valid V rows).

@@ -562,7 +562,7 @@ __global__ void ex2_fma_kernel(const float* x, float* y, long long n) {
 }  // namespace
 
 stof_status launch_blockwise(const AttnParams& p, bool bf16, cudaStream_t s) {
-  if (p.bm != kBM || (p.bn != 64 && p.bn != 128)) return STOF_ERR_UNSUPPORTED;
+  if (p.bm != kBM || (p.bn != 64 && p.bn != 128) || (p.d != 64 && p.d != 128)) return STOF_ERR_UNSUPPORTED;
   if (static_cast<long long>(p.B) * p.H * (p.L > p.Lk ? p.L : p.Lk) >= (1ll << 31)) return STOF_ERR_SHAPE;
   // d = 64 with short query tiles (few listed OTs each): persistent CTAs that
   // overlap one query tile's start-up and finish with the next

@@ -347,7 +347,12 @@ template <int D, bool BF16>
 cudaError_t launch_rw_d(const AttnParams& p, cudaStream_t s) {
   const int rpw = rowwise_rows_per_warp(static_cast<long long>(p.B) * p.H * p.L, p.keys_per_row,
                                         p.listed128_per_row, p.rows_per_warp);
-  if (rpw == 4) return launch_rw<D, BF16, 8>(p, s);
+  // a key needs D / 16 lanes: d = 256 fits 2 rows per warp at most
+  if constexpr (D / 16 <= 8) {
+    if (rpw == 4) return launch_rw<D, BF16, 8>(p, s);
+  } else {
+    if (rpw == 4) return launch_rw<D, BF16, 16>(p, s);
+  }
   if (rpw == 2) return launch_rw<D, BF16, 16>(p, s);
   return launch_rw<D, BF16, 32>(p, s);
 }
@@ -355,8 +360,13 @@ cudaError_t launch_rw_d(const AttnParams& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_rowwise(const AttnParams& p, bool bf16, cudaStream_t s) {
-  if (p.d == 64) return bf16 ? launch_rw_d<64, true>(p, s) : launch_rw_d<64, false>(p, s);
-  return bf16 ? launch_rw_d<128, true>(p, s) : launch_rw_d<128, false>(p, s);
+  switch (p.d) {
+    case 32: return bf16 ? launch_rw_d<32, true>(p, s) : launch_rw_d<32, false>(p, s);
+    case 64: return bf16 ? launch_rw_d<64, true>(p, s) : launch_rw_d<64, false>(p, s);
+    case 128: return bf16 ? launch_rw_d<128, true>(p, s) : launch_rw_d<128, false>(p, s);
+    case 256: return bf16 ? launch_rw_d<256, true>(p, s) : launch_rw_d<256, false>(p, s);
+    default: return cudaErrorInvalidValue;  // the host checks d first
+  }
 }
 
 }  // namespace stof

@@ -356,7 +356,7 @@ static stof_status check_format(const stof_format* fmt, int B, int H, int L, int
       !fmt->bitmaps || !fmt->counts_dev)
     return STOF_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || L < 1 || Lk < 1 || d < 1) return STOF_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return STOF_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return STOF_ERR_UNSUPPORTED;
   if (fmt->lq != L || fmt->lk != Lk) return STOF_ERR_SHAPE;
   // the lengths need not be whole numbers of OTs: the last OT row and column are padded
   if (fmt->bm < 8 || fmt->bn < 8 || fmt->bm % 8 || fmt->bn % 8 || fmt->bm > 256 || fmt->bn > 256 ||
@@ -391,6 +391,7 @@ static stof_status plan_call(const stof_format& f, int B, int H, int L, int Lk, 
     return STOF_ERR_INVALID_ARG;
   *c = KernelChoice{which, f.bn, 0, kVariantAuto, 0, 0, 0};
   *source = STOF_PLAN_FORCED;
+  const bool blk_d = d == 64 || d == 128;  // head dims of the block-wise kernels; the row-wise one takes 32-256
   if (which == STOF_KERNEL_AUTO) {
     if (!f.synced) return STOF_ERR_NOT_SYNCED;
     const double density = static_cast<double>(f.nnz) / (static_cast<double>(f.n_masks) * f.lq * f.lk);
@@ -398,7 +399,7 @@ static stof_status plan_call(const stof_format& f, int B, int H, int L, int Lk, 
     // (the block-wise kernel needs 128-row OTs)
     // (the tuner measures self-attention: its cache applies when Lk = L)
     if (L == Lk && tuned_choice(L, d, density, f.bn, c) &&
-        (c->kernel == STOF_KERNEL_ROWWISE || blockwise_tiles(f))) {
+        (c->kernel == STOF_KERNEL_ROWWISE || (blockwise_tiles(f) && blk_d))) {
       *source = STOF_PLAN_TUNED;
     } else {
       *c = KernelChoice{which, f.bn, 0, kVariantAuto, 0, 0, 0};
@@ -406,11 +407,11 @@ static stof_status plan_call(const stof_format& f, int B, int H, int L, int Lk, 
       // the model's length: L, or for Lk != L the one with L * L = L * Lk valid-key positions
       const int len = L == Lk ? L : static_cast<int>(std::lround(std::sqrt(static_cast<double>(L) * Lk)));
       c->kernel = stof_select_kernel_heads(density, len, d, static_cast<int64_t>(B) * H, listed128_per_row(f));
-      if (c->kernel == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(f))
-        c->kernel = STOF_KERNEL_ROWWISE;  // the block-wise kernel needs 128 x 64 or 128 x 128 OTs
+      if (c->kernel == STOF_KERNEL_BLOCKWISE && (!blockwise_tiles(f) || !blk_d))
+        c->kernel = STOF_KERNEL_ROWWISE;  // the block-wise kernel needs 128 x 64 or 128 x 128 OTs, d 64 or 128
     }
   }
-  if (c->kernel == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(f)) return STOF_ERR_UNSUPPORTED;
+  if (c->kernel == STOF_KERNEL_BLOCKWISE && (!blockwise_tiles(f) || !blk_d)) return STOF_ERR_UNSUPPORTED;
   return STOF_OK;
 }
 
@@ -437,6 +438,7 @@ stof_status stof_mha_plan(const stof_format* fmt, int B, int H, int L, int d, st
   } else {
     out->rows_per_warp = rowwise_rows_per_warp(static_cast<long long>(B) * H * L, keys_per_row(*fmt),
                                                listed128_per_row(*fmt), c.rows_per_warp);
+    if (d == 256 && out->rows_per_warp > 2) out->rows_per_warp = 2;  // 16 lanes per key
   }
   return STOF_OK;
 }
@@ -452,7 +454,10 @@ stof_status mha_fwd_choice(const void* q, const void* k, const void* v, stof_dty
   const stof_status st = check_call(q, k, v, dt, B, H, L, Lk, d, scale, fmt, mask_stride_b, mask_stride_h, o);
   if (st != STOF_OK) return st;
   if (c.kernel != STOF_KERNEL_ROWWISE && c.kernel != STOF_KERNEL_BLOCKWISE) return STOF_ERR_INVALID_ARG;
-  if (c.kernel == STOF_KERNEL_BLOCKWISE && !blockwise_tiles(*fmt)) return STOF_ERR_UNSUPPORTED;
+  if (c.kernel == STOF_KERNEL_BLOCKWISE && (!blockwise_tiles(*fmt) || (d != 64 && d != 128)))
+    return STOF_ERR_UNSUPPORTED;
+  if (c.kernel == STOF_KERNEL_ROWWISE && d == 256 && c.rows_per_warp == 4)
+    return STOF_ERR_UNSUPPORTED;  // a d = 256 key needs 16 lanes: 2 rows per warp at most
   AttnParams p;
   p.q = q;
   p.k = k;

@@ -1,6 +1,6 @@
 """Seeded random configurations of the whole attention path against the fp64
-oracle: lengths (whole tiles or not, Lq != Lk), OT sizes, kernels and
-variants, dtypes, the scale's sign, mask densities and how masks are shared
+oracle: lengths (whole tiles or not, Lq != Lk), head sizes 32-256, OT sizes,
+kernels and variants, dtypes, the scale's sign, mask densities and how masks are shared
 between batch elements and heads (mask strides).  Each case encodes its
 masks on the GPU, runs the attention and compares every output row with
 "Accelerating Sparse Transformer Inference on GPU" (gist.science technical
@@ -24,13 +24,13 @@ TILES = [(128, 128), (128, 64), (64, 64), (16, 16), (8, 24), (32, 128)]
 
 def _case(seed):
     rng = np.random.default_rng(1000 + seed)
-    c = dict(B=int(rng.integers(1, 3)), H=int(rng.integers(1, 4)), d=int(rng.choice([64, 128])),
+    c = dict(B=int(rng.integers(1, 3)), H=int(rng.integers(1, 4)), d=int(rng.choice([32, 64, 64, 128, 128, 256])),
              dtype=str(rng.choice(["bf16", "fp16"])), sign=float(rng.choice([1.0, 1.0, -1.0])),
              density=float(rng.choice([0.02, 0.2, 0.6, 1.0])))
     c["Lq"] = int(rng.integers(1, 700))
     c["Lk"] = c["Lq"] if rng.random() < 0.6 else int(rng.integers(1, 700))
     c["bm"], c["bn"] = TILES[int(rng.integers(len(TILES)))]
-    blockwise_ok = c["bm"] == 128 and c["bn"] in (64, 128)
+    blockwise_ok = c["bm"] == 128 and c["bn"] in (64, 128) and c["d"] in (64, 128)
     kinds = ["row", "auto"] + (["block", "persist", "persist4", "esplit"] if blockwise_ok else [])
     c["kind"] = str(rng.choice(kinds))
     if c["kind"] in ("persist", "persist4") and c["d"] != 64:

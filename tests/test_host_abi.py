@@ -445,3 +445,18 @@ def test_oproj_ln_sizes_and_argument_errors(lib):
     assert call(N=300) == stof.STOF_ERR_SHAPE
     assert call(d=96) == stof.STOF_ERR_UNSUPPORTED
     assert call(dt=5) == stof.STOF_ERR_DTYPE
+
+
+def test_head_dims_outside_the_block_wise_kernels_plan_row_wise(lib):
+    """d = 32 and 256 are the row-wise kernel's alone: AUTO plans it (at most
+    2 query rows per warp at d = 256, whose key needs 16 lanes), and a forced
+    block-wise call is refused before any launch."""
+    for d in (32, 256):
+        p = stof.stof_mha_plan(_plan_format(L=1024, nnz=1024 * 1024), 1, 64, 1024, d, stof.STOF_KERNEL_AUTO)
+        assert p.kernel == stof.STOF_KERNEL_ROWWISE
+        assert p.rows_per_warp in ((1, 2, 4) if d == 32 else (1, 2))
+        with pytest.raises(stof.StofError) as e:
+            stof.stof_mha_plan(_plan_format(L=1024), 1, 1, 1024, d, stof.STOF_KERNEL_BLOCKWISE)
+        assert e.value.status == stof.STOF_ERR_UNSUPPORTED
+    few = stof.stof_mha_plan(_plan_format(L=1024, nnz=20 * 1024), 1, 64, 1024, 256, stof.STOF_KERNEL_AUTO)
+    assert few.rows_per_warp <= 2
