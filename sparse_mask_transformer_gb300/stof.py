@@ -9,6 +9,7 @@ and raises StofError on a non-OK status.  The library must have been built
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 import torch
@@ -341,6 +342,61 @@ def stof_mha_fwd_cross(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt: s
         ctypes.byref(fmt), int(mask_stride_b), int(mask_stride_h), int(which), o.data_ptr(),
         _stream(stream)), "stof_mha_fwd_cross")
     return o
+
+
+class MaskedAttention:
+    """The usual sequence of library calls for one attention with a dense
+    mask, for PyTorch callers: stof_encode_mask into a workspace this object
+    keeps (and grows when a larger one is needed), stof_format_sync, then
+    stof_mha_fwd_cross.  No arithmetic here; every step is a library call.
+    Reuse one object per stream: its workspace holds the last format."""
+
+    def __init__(self, bm: int = 128, bn: int = 128):
+        self.bm, self.bn = bm, bn
+        self.workspace = None
+        self.fmt = None
+
+    def encode(self, mask: torch.Tensor, stream=None) -> stof_format:
+        """mask: device [n_masks, Lq, Lk], nonzero = valid."""
+        n_masks, lq, lk = mask.shape
+        need = stof_encode_workspace_bytes(n_masks, lq, lk, self.bm, self.bn)
+        if need == 0:
+            raise StofError(STOF_ERR_SHAPE, "MaskedAttention: bad mask or tile sizes")
+        if self.workspace is None or self.workspace.numel() < need or self.workspace.device != mask.device:
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=mask.device)
+        m = mask if mask.dtype in (torch.uint8, torch.bool) and mask.is_contiguous() else \
+            mask.to(torch.uint8).contiguous()
+        self.fmt = stof_encode_mask(m, self.bm, self.bn, self.workspace, stream=stream)
+        return stof_format_sync(self.fmt, stream)
+
+    def __call__(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor | None = None,
+                 scale: float | None = None, mask_stride_b: int | None = None, mask_stride_h: int | None = None,
+                 which: int = STOF_KERNEL_AUTO, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """q [B, H, Lq, d], k and v [B, H, Lk, d]; mask [n_masks, Lq, Lk]
+        (None: the last encoded one).  Head (b, h) uses mask
+        b * mask_stride_b + h * mask_stride_h; by default one mask per
+        (b, h) if there are B * H, one per head if H, one for all if 1.
+        scale defaults to 1 / sqrt(d)."""
+        if mask is not None:
+            self.encode(mask, stream)
+        if self.fmt is None:
+            raise StofError(STOF_ERR_INVALID_ARG, "MaskedAttention: no mask encoded")
+        B, H, _, d = q.shape
+        if mask_stride_b is None or mask_stride_h is None:
+            n = self.fmt.n_masks
+            if n == B * H:
+                sb, sh = H, 1
+            elif n == H:
+                sb, sh = 0, 1
+            elif n == 1:
+                sb, sh = 0, 0
+            else:
+                raise StofError(STOF_ERR_SHAPE, "MaskedAttention: give the mask strides for this mask count")
+            mask_stride_b = sb if mask_stride_b is None else mask_stride_b
+            mask_stride_h = sh if mask_stride_h is None else mask_stride_h
+        o = out if out is not None else torch.empty_like(q)
+        scale = 1.0 / math.sqrt(d) if scale is None else scale
+        return stof_mha_fwd_cross(q, k, v, self.fmt, scale, mask_stride_b, mask_stride_h, which, o, stream)
 
 
 def stof_mha_plan(fmt: stof_format, B: int, H: int, L: int, d: int, which: int) -> stof_plan:
