@@ -53,14 +53,23 @@ def load_peaks():
 HOST_CODE_MARK = b"// ---------------------------------------------------------------- host side"
 
 
+def _code_only(text: bytes) -> bytes:
+    """C++ source without its comments and blank-line or trailing-space
+    differences (string literals in these files hold no comment markers)."""
+    text = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)
+    text = re.sub(rb"//[^\n]*", b"", text)
+    return b"\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the block-wise kernel's device code: blockwise.cu up to its
-    host-side launch code, and the headers of device code it includes."""
+    """Hash of the block-wise kernel's device code, comments left out:
+    blockwise.cu up to its host-side launch code, and the headers of device
+    code it includes."""
     h = hashlib.sha256()
     for f in ("blockwise.cu", "blockwise_common.cuh", "sm100_ptx.cuh"):
         with open(os.path.join(ROOT, "sparse_mask_transformer_gb300", "csrc", f), "rb") as fh:
             text = fh.read()
-        h.update(text.split(HOST_CODE_MARK)[0] if f == "blockwise.cu" else text)
+        h.update(_code_only(text.split(HOST_CODE_MARK)[0] if f == "blockwise.cu" else text))
     return h.hexdigest()[:16]
 
 

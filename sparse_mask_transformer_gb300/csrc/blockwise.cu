@@ -11,10 +11,11 @@
 // One CTA computes one 128-row query tile (b, h, OT row I) over the n OTs
 // listed for its row (full OTs first):
 //   warp 0      TMA producer: the Q tile once, then the K tile of every
-//               listed OT into a three-stage ring (stage t % 3 is refilled
-//               once S = Q K_{t-3}^T is done);
-//   warp 1      TMA producer: the V tiles into a three-stage ring (refilled
-//               once O += P_{t-3} V_{t-3} is done);
+//               listed OT into a ring of ST stages (3 by default; the tuner
+//               also samples 2, and 4 at d = 64; stage t % ST is refilled
+//               once S = Q K_{t-ST}^T is done);
+//   warp 1      TMA producer: the V tiles into a ring of ST stages
+//               (refilled once O += P_{t-ST} V_{t-ST} is done);
 //   warp 2      allocates TMEM and issues the score MMAs S = Q K_t^T;
 //   warp 3      issues the PV MMAs O_g += P_t V_t, P read from TMEM.
 //               (Every role has a warp of its own: divergent lanes of one
@@ -38,6 +39,10 @@
 // 0 for a row without valid keys.
 // TMEM columns: S [0,BN) P_0 [128,128+BN/2) P_1 [192,192+BN/2)
 // O_0 [256,256+d) O_1 [256+d,256+2d).
+// Q, K and V are read through per-head 3-D tensor maps ([B*H][L or Lk][d]):
+// a tile that runs past a length that is not a whole number of tiles reads
+// zeros there, and O rows past L are not stored.  ESPLIT instances (a tuner
+// candidate) take one key pair in eight of the exponentials on the FMA pipe.
 // Every pipeline wait is bounded; on timeout the CTA raises
 // STOF_DEVERR_PIPE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>

@@ -39,9 +39,16 @@
 // take the same rescale decision, write their halves of P, rescale their
 // halves of O and keep their own partial sums, which the epilogue adds.
 // Same TMEM columns; 640 threads at 96 registers, split 32 / 112.
+// The exp split (ESPLIT, another candidate) changes only the softmax's
+// exponentials: one key pair in eight on the FMA pipe.
+//
+// Q, K and V are read through per-head 3-D tensor maps ([B*H][L or Lk][64]):
+// a tile that runs past a length that is not a whole number of tiles reads
+// zeros there, and O rows past L are not stored.
 // The work counter lives in the format's workspace (zeroed by the encoders)
-// and is zeroed again by the last CTA to finish, ready for the next launch.  Every wait is bounded; on timeout the CTA raises
-// STOF_DEVERR_PIPE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+// and is zeroed again by the last CTA to finish, ready for the next launch.
+// Every wait is bounded; on timeout the CTA raises STOF_DEVERR_PIPE_TIMEOUT,
+// drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

@@ -78,9 +78,13 @@ def test_traffic_is_reported_only_for_the_profiled_kernel_source(tmp_path, monke
     with open(csrc / "blockwise.cu", "a") as fh:
         fh.write("\n// host-side note\n")
     assert bench.profiled("wl", "traffic_bytes_per_launch") == 1.5e9
+    # nor does a comment in the device code
+    src = (csrc / "blockwise_common.cuh").read_text()
+    (csrc / "blockwise_common.cuh").write_text(src + "\n// a note\n/* another */\n")
+    assert bench.profiled("wl", "traffic_bytes_per_launch") == 1.5e9
     # a change to the device code does
     src = (csrc / "blockwise_common.cuh").read_text()
-    (csrc / "blockwise_common.cuh").write_text(src + "\n// device-side change\n")
+    (csrc / "blockwise_common.cuh").write_text(src + "\nconstexpr int kDeviceSideChange = 1;\n")
     assert bench.profiled("wl", "traffic_bytes_per_launch") is None
 
 
