@@ -34,10 +34,10 @@ struct EncodeGeom {
   int n_tr, n_tc, ct, cpr;      // cpr = chunks per OT row
   int64_t n_rows, n_chunks, n_tiles;
   int words_per_tile;           // (bm/8) * (bn/8)
-  size_t smem_bytes;            // dynamic shared memory of one encoder CTA
+  size_t smem_bytes;            // one chunk's IT words (a CTA's dynamic shared memory per chunk buffer)
 };
-// chunk_cols: mask columns per chunk (rounded to whole OTs); 0 = the width
-// the encoder uses for a dense (bits = false) or bit-packed mask.
+// False for sizes the encoder does not take.  A chunk is about 1024 mask
+// columns of one OT row band (whole OTs).
 bool encode_geometry(int n_masks, int lq, int lk, int bm, int bn, EncodeGeom* g);
 
 // Workspace carve-up (byte offsets, 256-byte aligned sections).
