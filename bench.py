@@ -790,8 +790,10 @@ def run_rules(args, w, q, k, v, ws, scale, stream, device, dist):
 
 def run_e2e(args, w, mask, q, k, v, ws, fmt, scale, stream, device, dist):
     """Same metric through the public API from pinned host buffers: each
-    step copies mask, Q, K, V host->device, runs the hot path and reads O
-    back to the host."""
+    step moves mask, Q, K, V host->device, runs the hot path and reads O
+    back to the host.  The encoder reads the mask straight from pinned host
+    memory (every byte once, over the host link, which bounds the step);
+    Q, K and V are copied."""
     import torch
     from sparse_mask_transformer_gb300 import stof
     hm = torch.empty(mask.shape, dtype=mask.dtype, pin_memory=True)
@@ -802,11 +804,10 @@ def run_e2e(args, w, mask, q, k, v, ws, fmt, scale, stream, device, dist):
     steps = max(1, min(args.steps, args.e2e_steps))
 
     def step():
-        mask.copy_(hm, non_blocking=True)
         q.copy_(hq, non_blocking=True)
         k.copy_(hk, non_blocking=True)
         v.copy_(hv, non_blocking=True)
-        stof.stof_encode_mask(mask, 128, 128, ws, fmt)
+        stof.stof_encode_mask(hm, 128, 128, ws, fmt)
         stof.stof_format_sync(fmt)
         stof.stof_mha_fwd(q, k, v, fmt, scale, w.stride_b, w.stride_h, stof.STOF_KERNEL_AUTO, o)
         ho.copy_(o, non_blocking=True)
@@ -828,7 +829,8 @@ def run_e2e(args, w, mask, q, k, v, ws, fmt, scale, stream, device, dist):
     h2d = hm.numel() + 3 * hq.numel() * hq.element_size()
     d2h = ho.numel() * ho.element_size()
     return {"value": round(total / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
-            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "mask_input": "pinned host memory, read by the encoder over the host link (no device copy)"}
 
 
 # ---------------------------------------------------------------- CPU oracle

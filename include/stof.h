@@ -125,7 +125,13 @@ size_t stof_encode_workspace_bytes(int n_masks, int lq, int lk, int bm, int bn);
  * Encodes a dense mask into the two-level format [FMT]: classifies every OT
  * as empty / full / partial, builds the two CSR pointer arrays by a prefix
  * sum, and packs the IT bitmaps of partial OTs, in one pass over the mask.
- *   mask       device, uint8 [n_masks][lq][lk]; 8-byte aligned.
+ *   mask       uint8 [n_masks][lq][lk], 8-byte aligned, readable by the
+ *              device: device memory, or page-locked host memory mapped into
+ *              the device's address space (cudaHostAlloc, or
+ *              cudaHostRegister with mapping; with unified addressing the
+ *              host pointer itself).  Every byte is read once, so a mask
+ *              in mapped host memory is encoded at the host link's rate
+ *              with no device copy of it (the format is the same).
  *   bm, bn     OT size: multiples of 8 in [8, 256].  lq and lk need not be
  *              multiples of bm and bn: a side that is not a whole number of
  *              OTs is encoded as padded to one with invalid elements, so
@@ -169,8 +175,9 @@ stof_status stof_encode_mask_bits(const uint8_t* mask_bits, int n_masks, int lq,
  *     libstof.so, 1 MiB + 8 bytes, held by every GPU that loads the
  *     library until the process exits.
  *   - Size limit: at most 131072 chunks, a chunk being one OT row band of
- *     W mask columns: chunks = n_masks * (lq / bm) * ceil(lk / W) with
- *     W = bn * min(lk / bn, max(1, 1024 / bn)) (W = 1024 for bn = 128).
+ *     W mask columns: chunks = n_masks * ceil(lq / bm) * ceil(n_tc / w)
+ *     with n_tc = ceil(lk / bn) and w = min(n_tc, max(1, 1024 / bn)) OTs
+ *     (W = w * bn = 1024 columns for bn = 128).
  *     Larger masks return STOF_ERR_SHAPE before any launch.  The
  *     16384 x 16384, 32-mask workload needs 65536 chunks.
  *   - The workspace (same size as for stof_encode_mask) receives the

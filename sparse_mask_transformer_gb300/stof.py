@@ -216,9 +216,13 @@ def stof_encode_workspace_bytes(n_masks: int, lq: int, lk: int, bm: int, bn: int
 
 def stof_encode_mask(mask: torch.Tensor, bm: int, bn: int, workspace: torch.Tensor,
                      fmt: stof_format | None = None, stream=None) -> stof_format:
-    """mask: device uint8/bool [n_masks, lq, lk]; workspace: device uint8 tensor."""
+    """mask: uint8/bool [n_masks, lq, lk] on the device, or in pinned host
+    memory (the encoder then reads it over the host link); workspace:
+    device uint8 tensor."""
     if mask.dim() != 3 or not mask.is_contiguous() or mask.element_size() != 1:
         raise StofError(STOF_ERR_SHAPE, "stof_encode_mask: mask must be contiguous 1-byte [n_masks, lq, lk]")
+    if not mask.is_cuda and not mask.is_pinned():
+        raise StofError(STOF_ERR_INVALID_ARG, "stof_encode_mask: a host mask must be in pinned memory")
     fmt = fmt if fmt is not None else stof_format()
     n_masks, lq, lk = mask.shape
     _check(load_library().stof_encode_mask(
@@ -356,16 +360,25 @@ class MaskedAttention:
         self.workspace = None
         self.fmt = None
 
-    def encode(self, mask: torch.Tensor, stream=None) -> stof_format:
-        """mask: device [n_masks, Lq, Lk], nonzero = valid."""
+    def encode(self, mask: torch.Tensor, stream=None, device=None) -> stof_format:
+        """mask: [n_masks, Lq, Lk], nonzero = valid, on the device or in
+        pinned host memory (read by the encoder over the host link, with no
+        device copy); the workspace goes on `device` (default: the mask's,
+        or the current CUDA device for a host mask)."""
         n_masks, lq, lk = mask.shape
         need = stof_encode_workspace_bytes(n_masks, lq, lk, self.bm, self.bn)
         if need == 0:
             raise StofError(STOF_ERR_SHAPE, "MaskedAttention: bad mask or tile sizes")
-        if self.workspace is None or self.workspace.numel() < need or self.workspace.device != mask.device:
-            self.workspace = torch.empty(need, dtype=torch.uint8, device=mask.device)
-        m = mask if mask.dtype in (torch.uint8, torch.bool) and mask.is_contiguous() else \
-            mask.to(torch.uint8).contiguous()
+        if device is None:
+            device = mask.device if mask.is_cuda else torch.device("cuda", torch.cuda.current_device())
+        if self.workspace is None or self.workspace.numel() < need or self.workspace.device != device:
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=device)
+        if mask.dtype in (torch.uint8, torch.bool) and mask.is_contiguous():
+            m = mask
+        elif mask.is_cuda:
+            m = mask.to(torch.uint8).contiguous()
+        else:
+            raise StofError(STOF_ERR_SHAPE, "MaskedAttention: a host mask must be contiguous uint8 or bool")
         self.fmt = stof_encode_mask(m, self.bm, self.bn, self.workspace, stream=stream)
         return stof_format_sync(self.fmt, stream)
 
@@ -378,7 +391,7 @@ class MaskedAttention:
         (b, h) if there are B * H, one per head if H, one for all if 1.
         scale defaults to 1 / sqrt(d)."""
         if mask is not None:
-            self.encode(mask, stream)
+            self.encode(mask, stream, q.device)
         if self.fmt is None:
             raise StofError(STOF_ERR_INVALID_ARG, "MaskedAttention: no mask encoded")
         B, H, _, d = q.shape

@@ -460,3 +460,14 @@ def test_head_dims_outside_the_block_wise_kernels_plan_row_wise(lib):
         assert e.value.status == stof.STOF_ERR_UNSUPPORTED
     few = stof.stof_mha_plan(_plan_format(L=1024, nnz=20 * 1024), 1, 64, 1024, 256, stof.STOF_KERNEL_AUTO)
     assert few.rows_per_warp <= 2
+
+
+def test_binding_refuses_a_host_mask_that_is_not_pinned():
+    """A host mask is only readable by the device from pinned memory; the
+    binding refuses any other before it calls the library."""
+    import torch
+    mask = torch.zeros(1, 128, 128, dtype=torch.uint8)
+    ws = torch.zeros(1024, dtype=torch.uint8)
+    with pytest.raises(stof.StofError) as e:
+        stof.stof_encode_mask(mask, 128, 128, ws)
+    assert e.value.status == stof.STOF_ERR_INVALID_ARG
