@@ -363,14 +363,16 @@ class MaskedAttention:
     def encode(self, mask: torch.Tensor, stream=None, device=None) -> stof_format:
         """mask: [n_masks, Lq, Lk], nonzero = valid, on the device or in
         pinned host memory (read by the encoder over the host link, with no
-        device copy); the workspace goes on `device` (default: the mask's,
-        or the current CUDA device for a host mask)."""
+        device copy).  The workspace goes on the mask's device; for a host
+        mask on `device` (default: the current CUDA device)."""
         n_masks, lq, lk = mask.shape
         need = stof_encode_workspace_bytes(n_masks, lq, lk, self.bm, self.bn)
         if need == 0:
             raise StofError(STOF_ERR_SHAPE, "MaskedAttention: bad mask or tile sizes")
-        if device is None:
-            device = mask.device if mask.is_cuda else torch.device("cuda", torch.cuda.current_device())
+        if mask.is_cuda:
+            device = mask.device
+        elif device is None:
+            device = torch.device("cuda", torch.cuda.current_device())
         if self.workspace is None or self.workspace.numel() < need or self.workspace.device != device:
             self.workspace = torch.empty(need, dtype=torch.uint8, device=device)
         if mask.dtype in (torch.uint8, torch.bool) and mask.is_contiguous():
