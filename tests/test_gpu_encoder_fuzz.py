@@ -3,10 +3,10 @@ brute-force encoder: mask counts, lengths (whole tiles or not, Lq != Lk),
 OT shapes from 8 to 256, densities from empty to full with full rows and
 columns mixed in, and every input path -- the dense mask in device memory,
 in pinned host memory, through the no-allocation entry point, and
-bit-packed when Lk is a multiple of 8.  Each format must equal the oracle's
-bit for bit ("Accelerating Sparse Transformer Inference on GPU",
-gist.science technical summary, Methodology 1, two-level storage
-format)."""
+bit-packed when Lk is a multiple of 8 -- and random parametric rules on
+such lengths.  Each format must equal the oracle's bit for bit
+("Accelerating Sparse Transformer Inference on GPU", gist.science
+technical summary, Methodology 1, two-level storage format)."""
 import ctypes
 
 import numpy as np
@@ -83,3 +83,45 @@ def test_random_encoder_configuration(gpu_lib, seed):
             assert_format_equal(fmt, arrs, want)
         except AssertionError as e:
             raise AssertionError(f"{name} path, mask {mask.shape}, OT {bm}x{bn}: {e}") from e
+
+
+N_RULE_CASES = 24
+
+
+def _rule_case(seed):
+    """Random rules (band, global rows and columns, and a block pattern when a
+    block edge divides both lengths) on lengths that need not be whole OTs."""
+    rng = np.random.default_rng(7000 + seed)
+    n = int(rng.integers(1, 4))
+    lq, lk = int(rng.integers(1, 900)), int(rng.integers(1, 900))
+    if rng.random() < 0.4:
+        lq, lk = 8 * max(1, lq // 8), 8 * max(1, lk // 8)
+    bm, bn = int(rng.choice(SIDES)), int(rng.choice(SIDES))
+    blocks = [b for b in (8, 16, 24, 32, 64) if lq % b == 0 and lk % b == 0]
+    rules = []
+    for _ in range(n):
+        lo = int(rng.integers(-lk, lq))
+        r = {"band_lo": lo, "band_hi": lo + int(rng.integers(-3, 300)), "global_rows": None, "global_cols": None,
+             "blocks": None, "block": 0}
+        if rng.random() < 0.5:
+            r["global_rows"] = rng.random(lq) < 0.03
+        if rng.random() < 0.5:
+            r["global_cols"] = rng.random(lk) < 0.03
+        if blocks and rng.random() < 0.5:
+            blk = int(rng.choice(blocks))
+            r["blocks"], r["block"] = rng.random((lq // blk, lk // blk)) < 0.15, blk
+        rules.append(r)
+    return rules, lq, lk, bm, bn
+
+
+@pytest.mark.parametrize("seed", range(N_RULE_CASES))
+def test_random_rule_configuration(gpu_lib, seed):
+    rules, lq, lk, bm, bn = _rule_case(seed)
+    bits = lambda a: None if a is None else stof.bitset_words(a)  # noqa: E731
+    dev = [stof.MaskRule(r["band_lo"], r["band_hi"], bits(r["global_rows"]), bits(r["global_cols"]),
+                         bits(r["blocks"]), r["block"]) for r in rules]
+    ws = torch.full((stof.stof_encode_workspace_bytes(len(rules), lq, lk, bm, bn),), 0x5A, dtype=torch.uint8,
+                    device="cuda")
+    fmt = stof.stof_encode_rules(dev, lq, lk, bm, bn, ws)
+    masks = np.stack([oracle.rule_mask(lq, lk, **r) for r in rules])
+    assert_format_equal(fmt, _arrays(fmt, ws), oracle.encode(masks, bm, bn))
