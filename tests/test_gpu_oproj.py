@@ -177,3 +177,20 @@ def test_ln_argument_errors(gpu_lib):
         with pytest.raises(stof.StofError) as e:
             stof.stof_oproj_ln_fwd(o, w, None, None, None, None, eps, y, wsp)
         assert e.value.status == status
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_shapes(gpu_lib, seed):
+    """Seeded random batch sizes, head counts, lengths (whole token tiles or
+    not), head sizes, widths, dtypes and epilogue parts, with and without
+    the LayerNorm, each within the error bound of its case above."""
+    rng = np.random.default_rng(9000 + seed)
+    B, H, L = int(rng.integers(1, 4)), int(rng.integers(1, 17)), int(rng.integers(1, 700))
+    d, N = int(rng.choice([64, 128])), 256 * int(rng.integers(1, 9))
+    dtype = str(rng.choice(["bf16", "fp16"]))
+    bias, residual = bool(rng.random() < 0.7), bool(rng.random() < 0.7)
+    if rng.random() < 0.5:
+        _case(B, H, L, d, N, dtype, bias=bias, residual=residual, seed=seed)
+    else:
+        _ln_case(B, H, L, d, N, dtype, affine=bool(rng.random() < 0.7), offset=float(rng.choice([0.0, 30.0])),
+                 seed=seed)
