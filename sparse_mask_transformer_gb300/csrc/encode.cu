@@ -83,20 +83,34 @@ struct ChunkState {
 struct ChunkGeom {
   long long row;
   int cc, m, I, J0, nt, itc, itcols, bands, wpt;
+  uint64_t rcp_itc, rcp_wpt;  // ceil(2^32 / itc), ceil(2^32 / wpt): see qdiv
 };
+
+// e / d for the reciprocal rcp = ceil(2^32 / d): exact while e * d < 2^32
+// (with rcp = (2^32 + k) / d, 0 <= k < d, the product overshoots e / d by
+// e k / (d 2^32) < 1 / d).  The encoder's divisors are at most 1024 and its
+// dividends below 2^17.
+__device__ __forceinline__ int qdiv(int e, uint64_t rcp) {
+  return static_cast<int>((static_cast<uint64_t>(e) * rcp) >> 32);
+}
+__host__ __device__ __forceinline__ uint64_t reciprocal(uint32_t d) { return 0xFFFFFFFFull / d + 1; }
 
 __device__ __forceinline__ ChunkGeom chunk_geom(const EncodeParams& p, long long chunk) {
   ChunkGeom g;
-  g.row = chunk / p.cpr;
-  g.cc = static_cast<int>(chunk % p.cpr);
-  g.m = static_cast<int>(g.row / p.n_tr);
-  g.I = static_cast<int>(g.row % p.n_tr);
+  const uint32_t c = static_cast<uint32_t>(chunk);  // chunk < n_chunks < 2^31
+  const uint32_t row = c / static_cast<uint32_t>(p.cpr);
+  g.row = row;
+  g.cc = static_cast<int>(c - row * static_cast<uint32_t>(p.cpr));
+  g.m = static_cast<int>(row / static_cast<uint32_t>(p.n_tr));
+  g.I = static_cast<int>(row - static_cast<uint32_t>(g.m) * static_cast<uint32_t>(p.n_tr));
   g.J0 = g.cc * p.ct;
   g.nt = min(p.ct, p.n_tc - g.J0);
   g.itc = p.bn >> 3;
   g.itcols = g.nt * g.itc;
   g.bands = p.bm >> 3;
   g.wpt = g.bands * g.itc;
+  g.rcp_itc = p.rcp_itc;
+  g.rcp_wpt = p.rcp_wpt;
   return g;
 }
 
@@ -107,7 +121,7 @@ __device__ __forceinline__ void classify(const uint64_t* words, const ChunkGeom&
   for (int t = warp; t < g.nt; t += nwarps) {
     uint64_t any = 0, all = ~0ull;
     for (int e = lane; e < g.wpt; e += 32) {
-      const int pb = e / g.itc, qq = e - pb * g.itc;
+      const int pb = qdiv(e, g.rcp_itc), qq = e - pb * g.itc;
       const uint64_t w = words[pb * g.itcols + t * g.itc + qq];
       any |= w;
       all &= w;
@@ -202,9 +216,9 @@ __device__ __forceinline__ void write_outputs(const EncodeParams& p, long long c
   }
   const int total = np * g.wpt;
   for (int e = tid; e < total; e += nthreads) {
-    const int r = e / g.wpt, x = e - r * g.wpt;
+    const int r = qdiv(e, g.rcp_wpt), x = e - r * g.wpt;
     const int t = cs.plist[r];
-    const int pb = x / g.itc, qq = x - pb * g.itc;
+    const int pb = qdiv(x, g.rcp_itc), qq = x - pb * g.itc;
     p.bitmaps[(ep + r) * g.wpt + x] = words[pb * g.itcols + t * g.itc + qq];
   }
   if (chunk == p.n_chunks - 1 && tid == 0) {
@@ -330,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
   constexpr int WPU = VEC / 8;                 // IT words per unit
   constexpr int kUnroll = VEC == 16 ? 1 : 2;   // units in flight per thread (128 B)
   const int upr = g.itcols / WPU;              // units per band
+  const uint64_t rcp_upr = reciprocal(static_cast<uint32_t>(upr));
   const int nunits = g.bands * upr;
   for (int u0 = tid; u0 < nunits; u0 += kThreads * kUnroll) {
     uint4 v[kUnroll][8];
@@ -337,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
     for (int u = 0; u < kUnroll; ++u) {
       const int w = u0 + u * kThreads;
       if (w < nunits) {
-        const int pb = w / upr, qu = w - pb * upr;
+        const int pb = qdiv(w, rcp_upr), qu = w - pb * upr;
         const uint8_t* src = base + static_cast<long long>(8 * pb) * p.lk + VEC * qu;
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
@@ -354,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 7) encode_kernel(const EncodeParams 
     for (int u = 0; u < kUnroll; ++u) {
       const int w = u0 + u * kThreads;
       if (w < nunits) {
-        const int pb = w / upr, qu = w - pb * upr;
+        const int pb = qdiv(w, rcp_upr), qu = w - pb * upr;
 #pragma unroll
         for (int h = 0; h < WPU; ++h) {
           uint64_t word = 0;
@@ -738,7 +753,17 @@ WorkspaceLayout workspace_layout(const EncodeGeom& g) {
   return w;
 }
 
-cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s) {
+// The reciprocals the kernels divide by (qdiv).
+static EncodeParams with_reciprocals(const EncodeParams& p) {
+  EncodeParams q = p;
+  const int itc = p.bn >> 3;
+  q.rcp_itc = reciprocal(static_cast<uint32_t>(itc));
+  q.rcp_wpt = reciprocal(static_cast<uint32_t>((p.bm >> 3) * itc));
+  return q;
+}
+
+cudaError_t launch_encode(const EncodeParams& p_in, const EncodeGeom& g, cudaStream_t s) {
+  const EncodeParams p = with_reciprocals(p_in);
   // shared memory per CTA: (bm / 8) * (chunk columns / 8) words
   const unsigned grid = static_cast<unsigned>(g.n_chunks);
   const uintptr_t a = reinterpret_cast<uintptr_t>(p.mask);
@@ -769,7 +794,8 @@ cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream
   return cudaGetLastError();
 }
 
-cudaError_t launch_encode_rules(const EncodeParams& p, const EncodeGeom& g, const RuleSet& rs, cudaStream_t s) {
+cudaError_t launch_encode_rules(const EncodeParams& p_in, const EncodeGeom& g, const RuleSet& rs, cudaStream_t s) {
+  const EncodeParams p = with_reciprocals(p_in);
   if (g.smem_bytes > 48 * 1024 &&
       cudaFuncSetAttribute(encode_rules_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(g.smem_bytes)) != cudaSuccess)

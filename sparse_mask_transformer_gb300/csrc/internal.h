@@ -63,6 +63,7 @@ struct EncodeParams {
   unsigned long long* status;      // scratch [n_chunks], zero at launch
   uint8_t* cls;                    // bit-packed encoder: class of every OT [n_rows][n_tc]
   int32_t* rowcnt;                 // bit-packed encoder: full, then partial OT counts per row, zero at launch
+  uint64_t rcp_itc, rcp_wpt;       // set by the launchers: ceil(2^32 / (bn / 8)), ceil(2^32 / IT words per OT)
 };
 cudaError_t launch_encode(const EncodeParams& p, const EncodeGeom& g, cudaStream_t s);
 
